@@ -1,0 +1,138 @@
+"""fp64 CPU oracle for attention over a paged KV cache.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference arm are the only callers.  The product
+path (``paged_kv_cache_174_gb300``) never imports this package, and this
+package never imports the product.  Arrays are numpy; bfloat16 tensors are
+passed as their raw 16-bit patterns (``np.uint16``), which the C code decodes
+itself.
+
+What it computes, and which page passage each function follows, is stated in
+``oracle.c``.  Every function here is a thin ctypes marshaller over it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    global _LIB
+    if _LIB is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        i32, i64, dbl, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
+        L.oracle_num_threads.restype = ctypes.c_int
+        L.oracle_slot_of.argtypes = [vp, i32, i32]
+        L.oracle_slot_of.restype = i64
+        L.oracle_reshape_and_cache.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, i32, vp]
+        L.oracle_reshape_and_cache.restype = ctypes.c_int
+        L.oracle_copy_blocks.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32]
+        L.oracle_copy_blocks.restype = ctypes.c_int
+        L.oracle_paged_attention.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32,
+                                             vp, i32, vp, vp, i32, dbl, vp, i32]
+        L.oracle_paged_attention.restype = ctypes.c_int
+        L.oracle_paged_attention_rows.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32,
+                                                  vp, i32, vp, vp, i32, dbl, vp, i32,
+                                                  vp, i32]
+        L.oracle_paged_attention_rows.restype = ctypes.c_int
+        _LIB = L
+    return _LIB
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _c(a, dtype) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+def num_threads() -> int:
+    return int(lib().oracle_num_threads())
+
+
+def slot_of(block_table_row, pos: int, block_size: int) -> int:
+    row = _c(block_table_row, np.int32)
+    return int(lib().oracle_slot_of(_ptr(row), int(pos), int(block_size)))
+
+
+def reshape_and_cache(k, v, k_cache: np.ndarray, v_cache: np.ndarray, slot_mapping) -> None:
+    """In place on k_cache / v_cache ([num_blocks, block_size, n_kv, d] uint16)."""
+    assert k_cache.dtype == np.uint16 and k_cache.flags.c_contiguous
+    assert v_cache.dtype == np.uint16 and v_cache.flags.c_contiguous
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    sm = _c(slot_mapping, np.int32)
+    nb, bs, nkv, d = k_cache.shape
+    st = lib().oracle_reshape_and_cache(_ptr(k), _ptr(v), int(sm.shape[0]), _ptr(k_cache),
+                                        _ptr(v_cache), nb, bs, nkv, d, _ptr(sm))
+    if st:
+        raise OracleError(f"oracle_reshape_and_cache status {st}")
+
+
+def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, pairs) -> None:
+    """In place; pairs is [n, 2] int (src, dst)."""
+    assert k_cache.dtype == np.uint16 and k_cache.flags.c_contiguous
+    p = _c(pairs, np.int32).reshape(-1, 2)
+    nb, bs, nkv, d = k_cache.shape
+    st = lib().oracle_copy_blocks(_ptr(k_cache), _ptr(v_cache), nb, bs, nkv, d, _ptr(p),
+                                  int(p.shape[0]))
+    if st:
+        raise OracleError(f"oracle_copy_blocks status {st}")
+
+
+def paged_attention(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc,
+                    scale: float, threads: int = 0) -> np.ndarray:
+    """Returns fp64 out [num_tokens, n_q, d]; rows owned by no sequence are NaN."""
+    q = _c(q, np.uint16)
+    kc = _c(k_cache, np.uint16)
+    vc = _c(v_cache, np.uint16)
+    bt = _c(block_tables, np.int32)
+    sl = _c(seq_lens, np.int32)
+    qsl = _c(query_start_loc, np.int32)
+    T, nq, d = q.shape
+    nb, bs, nkv, d2 = kc.shape
+    assert d == d2
+    S = int(sl.shape[0])
+    maxb = int(bt.shape[1]) if bt.ndim == 2 else 0
+    out = np.full((T, nq, d), np.nan, dtype=np.float64)
+    st = lib().oracle_paged_attention(_ptr(q), _ptr(kc), _ptr(vc), nb, bs, nq, nkv, d,
+                                      _ptr(bt), maxb, _ptr(sl), _ptr(qsl), S, float(scale),
+                                      _ptr(out), int(threads))
+    if st:
+        raise OracleError(f"oracle_paged_attention status {st}")
+    return out
+
+
+def paged_attention_rows(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc,
+                         scale: float, samples, threads: int = 0) -> np.ndarray:
+    """samples: [n, 3] (sequence, row within the sequence, q head) -> fp64 [n, d]."""
+    q = _c(q, np.uint16)
+    kc = _c(k_cache, np.uint16)
+    vc = _c(v_cache, np.uint16)
+    bt = _c(block_tables, np.int32)
+    sl = _c(seq_lens, np.int32)
+    qsl = _c(query_start_loc, np.int32)
+    smp = _c(samples, np.int32).reshape(-1, 3)
+    T, nq, d = q.shape
+    nb, bs, nkv, _ = kc.shape
+    out = np.full((smp.shape[0], d), np.nan, dtype=np.float64)
+    st = lib().oracle_paged_attention_rows(_ptr(q), _ptr(kc), _ptr(vc), nb, bs, nq, nkv, d,
+                                           _ptr(bt), int(bt.shape[1]), _ptr(sl), _ptr(qsl),
+                                           int(sl.shape[0]), float(scale), _ptr(smp),
+                                           int(smp.shape[0]), _ptr(out), int(threads))
+    if st:
+        raise OracleError(f"oracle_paged_attention_rows status {st}")
+    return out
