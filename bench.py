@@ -1,0 +1,387 @@
+"""Benchmark: attention over a paged KV cache on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode_batch|long_decode|mixed_step|tiny_decode]
+
+One step is one pass of the whole hot path over one batch of the workload:
+the slot scatter of the step's new K/V, then paged attention over every
+request (split-KV decode kernel + merge, and the tensor-core prefill kernel
+for chunked-prefill rows), through the C ABI.  Inputs are synthetic and
+seeded; the KV cache (hundreds of MB to GB) is far larger than the 129 MB L2,
+so no explicit L2 flush is done between steps.
+
+Prints one JSON line (rank 0).  With N > 1 (torchrun, one process per GPU)
+every rank runs its own replica of the batch and `value` is the bytes all
+ranks processed divided by the slowest rank's time (weak scaling).
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (there is no other implementation of this method to run).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-attn decode HBM GB/s (% of peak); mixed-batch tokens/s per step"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            j = json.load(f)
+        return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j["bf16_tflops"]),
+                "bf16_tflops_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _make(workload: str, rank: int):
+    from paged_kv_cache_174_gb300 import workloads as W
+    b = W.by_name(workload, poison=False)
+    return b
+
+
+def _launch_count(b) -> int:
+    n = 1 if b.num_tokens else 0        # scatter
+    n += 2                              # decode + merge
+    if b.max_q_len >= 2:
+        n += 1                          # prefill
+    if b.copy_pairs.size:
+        n += 1
+    return n
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from paged_kv_cache_174_gb300 import ops
+    from paged_kv_cache_174_gb300 import workloads as W
+
+    world, rank, local = _dist()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = _peaks()
+
+    b = _make(args.workload, rank)
+    d = W.to_device(b, dev)
+    alg = W.algorithmic_bytes(b)
+    flops = W.causal_flops(b)
+    step_bytes = alg["total"]
+    ws = ops.alloc_workspace(b.num_seqs, b.num_tokens, b.num_q_heads, b.num_kv_heads,
+                             b.head_dim, b.max_q_len, b.max_seq_len, dev)
+    out = torch.empty_like(d.q)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        if d.copy_pairs.numel():
+            ops.copy_blocks(d.k_cache, d.v_cache, d.copy_pairs)
+        ops.reshape_and_cache(d.k_new, d.v_new, d.k_cache, d.v_cache, d.slot_mapping)
+        ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens,
+                            d.query_start_loc, b.scale, max_q_len=b.max_q_len,
+                            max_seq_len=b.max_seq_len, out=out, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    ops.check_device_errors()
+    torch.cuda.synchronize()
+
+    # ---- device-resident timed region
+    ev_attn = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        if d.copy_pairs.numel():
+            ops.copy_blocks(d.k_cache, d.v_cache, d.copy_pairs)
+        ops.reshape_and_cache(d.k_new, d.v_new, d.k_cache, d.v_cache, d.slot_mapping)
+        ev_attn[i][0].record(stream)
+        ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens,
+                            d.query_start_loc, b.scale, max_q_len=b.max_q_len,
+                            max_seq_len=b.max_seq_len, out=out, workspace=ws)
+        ev_attn[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ops.check_device_errors()
+    ms = t0.elapsed_time(t1) / args.steps
+    attn_ms = statistics.mean(a.elapsed_time(e) for a, e in ev_attn)
+    if world > 1:
+        tt = torch.tensor([ms, attn_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms, attn_ms = float(tt[0]), float(tt[1])
+
+    # ---- end to end through the public API from pinned host buffers
+    host = {k: getattr(d, k).cpu().pin_memory() for k in
+            ("q", "k_new", "v_new", "block_tables", "seq_lens", "query_start_loc",
+             "slot_mapping", "copy_pairs")}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    dev_in = {k: torch.empty_like(getattr(d, k)) for k in host}
+
+    def e2e_step():
+        for k, t in host.items():
+            dev_in[k].copy_(t, non_blocking=True)
+        if dev_in["copy_pairs"].numel():
+            ops.copy_blocks(d.k_cache, d.v_cache, dev_in["copy_pairs"])
+        ops.reshape_and_cache(dev_in["k_new"], dev_in["v_new"], d.k_cache, d.v_cache,
+                              dev_in["slot_mapping"])
+        ops.paged_attention(dev_in["q"], d.k_cache, d.v_cache, dev_in["block_tables"],
+                            dev_in["seq_lens"], dev_in["query_start_loc"], b.scale,
+                            max_q_len=b.max_q_len, max_seq_len=b.max_seq_len, out=out,
+                            workspace=ws)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt[0])
+        dist.barrier()
+
+    gbs = step_bytes * world / (ms * 1e-3) / 1e9
+    attn_gbs = alg["attention"] / (attn_ms * 1e-3) / 1e9
+    tokens_per_s = b.num_tokens * world / (ms * 1e-3)
+    line = {
+        "metric": METRIC,
+        "value": round(gbs, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, shuffled physical blocks)",
+        "config": {"workload": b.name, "description": W.WORKLOADS[b.name].description,
+                   "num_seqs": b.num_seqs, "num_tokens": b.num_tokens,
+                   "kv_tokens": int(b.seq_lens.sum()), "block_size": b.block_size,
+                   "algorithmic_bytes_per_step": step_bytes,
+                   "l2": "inputs larger than L2 (KV read per step >> 129 MB); no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "tokens_per_s": round(tokens_per_s, 1),
+        "pct_of_hbm_peak": round(100.0 * gbs / world / peaks["hbm_gbs"], 2),
+        "roofline": {"bound": "hbm", "kernel": "pa_paged_attention (split-KV decode + merge)",
+                     "achieved": round(attn_gbs, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(attn_gbs / peaks["hbm_gbs"], 4),
+                     "peak_source": peaks["source"], "traffic": None,
+                     "algorithmic_bytes_per_launch": alg["attention"],
+                     "avg_launch_ms": round(attn_ms, 5)},
+        "e2e": {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": _launch_count(b) * args.steps,
+        "clocks": clk,
+    }
+    if flops:
+        line["prefill_tflops"] = round(flops / (attn_ms * 1e-3) / 1e12, 2)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(b, args.cpu_seconds)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def _oracle_sample_step(b, n_seqs, rng):
+    """One oracle pass over a sample of n_seqs requests of batch b (scatter of
+    their new tokens + attention); returns (seconds, algorithmic bytes)."""
+    import oracle
+    from paged_kv_cache_174_gb300 import workloads as W
+
+    idx = np.sort(rng.choice(b.num_seqs, size=min(n_seqs, b.num_seqs), replace=False))
+    ql = b.q_lens[idx]
+    qsl = np.zeros(len(idx) + 1, np.int32)
+    qsl[1:] = np.cumsum(ql)
+    rows = np.concatenate([np.arange(b.query_start_loc[s], b.query_start_loc[s + 1])
+                           for s in idx]).astype(np.int64)
+    sub = W.PagedBatch(name=b.name, q=b.q[rows], k_new=b.k_new[rows], v_new=b.v_new[rows],
+                       k_cache=b.k_cache, v_cache=b.v_cache, block_tables=b.block_tables[idx],
+                       seq_lens=b.seq_lens[idx], query_start_loc=qsl,
+                       slot_mapping=b.slot_mapping[rows], scale=b.scale,
+                       block_size=b.block_size, seed=b.seed)
+    t = time.perf_counter()
+    oracle.reshape_and_cache(sub.k_new, sub.v_new, b.k_cache, b.v_cache, sub.slot_mapping)
+    oracle.paged_attention(sub.q, b.k_cache, b.v_cache, sub.block_tables, sub.seq_lens,
+                           sub.query_start_loc, sub.scale)
+    dt = time.perf_counter() - t
+    return dt, W.algorithmic_bytes(sub)["total"], len(idx)
+
+
+def cpu_baseline(b, seconds: float):
+    """The oracle, as it stands, on the host cores: repeated passes over
+    random samples of the batch's requests until ~`seconds` of CPU time."""
+    import oracle
+    rng = np.random.default_rng(0)
+    n_seqs = max(1, min(b.num_seqs, 8))
+    total_t, total_b, passes = 0.0, 0, 0
+    while total_t < seconds and passes < 1000:
+        dt, nb, _ = _oracle_sample_step(b, n_seqs, rng)
+        total_t += dt
+        total_b += nb
+        passes += 1
+    return {"value": round(total_b / total_t / 1e9, 4), "unit": "GB/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{passes} passes, each over {n_seqs} random requests of the batch "
+                      f"(scatter + attention), {total_t:.1f} s total"}
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+    from paged_kv_cache_174_gb300 import workloads as W
+
+    b = _make(args.workload, rank)
+    rng = np.random.default_rng(1)
+    n_seqs = max(1, min(b.num_seqs, 8))
+    for _ in range(args.warmup):
+        _oracle_sample_step(b, n_seqs, rng)
+    ts, bs = [], []
+    for _ in range(args.steps):
+        dt, nb, _ = _oracle_sample_step(b, n_seqs, rng)
+        ts.append(dt)
+        bs.append(nb)
+    value = sum(bs) / sum(ts) / 1e9
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * sum(ts) / len(ts), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16, shuffled physical blocks)",
+        "config": {"workload": b.name, "description": W.WORKLOADS[b.name].description,
+                   "sample_requests_per_step": n_seqs},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"each step: {n_seqs} random requests of the batch"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_batch",
+                    choices=["tiny_decode", "decode_batch", "long_decode", "mixed_step"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

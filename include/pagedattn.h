@@ -1,0 +1,161 @@
+/*
+ * pagedattn.h -- C ABI of libpagedattn.so: attention over a paged KV cache on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The cache is a pool of fixed-size physical blocks; each request reaches its
+ * tokens through a Block Table row that maps logical block b (tokens
+ * b*block_size .. b*block_size + block_size - 1) to a physical block id
+ * ("PagedAttention 显存分页与连续批处理(Continuous Batching)实战",
+ * "PagedAttention 核心机理" part 1; "连续批处理：推理吞吐的范式革命",
+ * section 2.2).
+ *
+ * Conventions for every call:
+ *  - pa_bf16 is a raw bfloat16 bit pattern.  Every array pointer is a DEVICE
+ *    pointer owned by the caller, C-contiguous, 16-byte aligned; the library
+ *    never frees or keeps it.
+ *  - KV cache layout: [num_blocks, block_size, num_kv_heads, head_dim].
+ *  - Calls are asynchronous on `stream` (0 = legacy default stream).  The
+ *    returned status covers argument checks and launch errors only.  Index
+ *    errors found on the device (a slot, block id or length out of range)
+ *    make the kernel skip that work item and set a device error word, which
+ *    pa_check_device_errors() reads back.
+ *  - The library allocates no device memory.  pa_paged_attention takes a
+ *    caller-provided workspace of pa_workspace_size() bytes.
+ *  - Supported: block_size 16; head_dim 64 or 128; num_q_heads a multiple of
+ *    num_kv_heads with group size num_q_heads / num_kv_heads in {1, 2, 4, 8};
+ *    num_kv_heads in {1, 2, 4, 8, 16} and num_kv_heads * head_dim <= 1024.
+ *    Anything else returns PA_ERR_UNSUPPORTED.
+ *  - On error the call returns a non-zero status and pa_get_last_error()
+ *    returns a message (per thread, valid until the next call on the thread).
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t pa_bf16;
+
+enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,   /* bad size, null or misaligned pointer         */
+  PA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (shape, block size) */
+  PA_ERR_CUDA = 3,          /* a CUDA runtime call or a launch failed       */
+  PA_ERR_DEVICE_BOUNDS = 4, /* a kernel found an index out of range         */
+  PA_ERR_TIMEOUT = 5,       /* a kernel gave up a bounded wait              */
+  PA_ERR_WORKSPACE = 6      /* workspace missing, too small or misaligned   */
+};
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pa_version(void);
+
+/* Message for the last non-zero status returned on this thread. */
+const char *pa_get_last_error(void);
+
+/*
+ * Slot scatter.  For each new token t in [0, num_tokens) with
+ * s = slot_mapping[t] >= 0, copy k[t, :, :] to k_cache[s / block_size,
+ * s % block_size, :, :] and v[t] to v_cache likewise (a bit copy).  A negative
+ * slot skips the token.  Slots must be distinct within one call.  This is how
+ * a step's new tokens reach their on-demand allocated physical slots
+ * ("PagedAttention 显存分页与连续批处理实战", comparison table: blocks are
+ * allocated on demand as a block fills; TypeScript Block Manager appendToken).
+ *
+ *   k, v          [num_tokens, num_kv_heads, head_dim]  bf16, read
+ *   k_cache, v_cache  [num_blocks, block_size, num_kv_heads, head_dim], written
+ *   slot_mapping  [num_tokens] int32, read
+ * A slot >= num_blocks * block_size is skipped and flags PA_ERR_DEVICE_BOUNDS.
+ */
+int pa_reshape_and_cache(const pa_bf16 *k, const pa_bf16 *v, int32_t num_tokens,
+                         pa_bf16 *k_cache, pa_bf16 *v_cache, int32_t num_blocks,
+                         int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                         const int32_t *slot_mapping, cudaStream_t stream);
+
+/*
+ * Workspace bytes pa_paged_attention needs on the current device for a call
+ * with these sizes (0 is never returned; the size depends only on the
+ * arguments and on the device's SM count).  Returns 0 if an argument is
+ * invalid.
+ */
+size_t pa_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t max_q_len,
+                         int32_t max_seq_len);
+
+/*
+ * Causal, GQA-aware, variable-length attention over the paged cache
+ * ("连续批处理：推理吞吐的范式革命", section 4.1: walk the request's Block
+ * Table, score q.k scaled, softmax, weighted sum of v, normalise; chunked
+ * prefill mixes prompt slices and decode tokens in one batch:
+ * "PagedAttention 显存分页与连续批处理实战", Chunked Prefill section).
+ *
+ * Request s owns query tokens query_start_loc[s] .. query_start_loc[s+1]-1
+ * (q_len = their count, 0 allowed) and seq_lens[s] cached tokens, which
+ * include those q_len tokens (write them with pa_reshape_and_cache first).
+ * Query row i of request s is at position p = seq_lens[s] - q_len + i and
+ * attends to positions 0..p; q head h reads kv head h / (num_q_heads /
+ * num_kv_heads):
+ *   out[t, h, :] = sum_j softmax_j(scale * q[t,h,:] . K[s,j,g,:]) V[s,j,g,:]
+ * where K[s, j] = k_cache[block_tables[s, j / block_size], j % block_size].
+ *
+ *   q             [num_tokens, num_q_heads, head_dim] bf16, read
+ *   k_cache, v_cache  [num_blocks, block_size, num_kv_heads, head_dim], read
+ *   block_tables  [num_seqs, max_blocks] int32, read; only entries
+ *                 0 .. ceil(seq_lens[s] / block_size) - 1 are read
+ *   seq_lens      [num_seqs] int32, read
+ *   query_start_loc [num_seqs + 1] int32, read, non-decreasing, last entry
+ *                 <= num_tokens
+ *   max_q_len, max_seq_len  host-side upper bounds of q_len and seq_lens
+ *                 (size the launch; a request beyond them flags
+ *                 PA_ERR_DEVICE_BOUNDS and its rows are not written)
+ *   out           [num_tokens, num_q_heads, head_dim] bf16, written for every
+ *                 token that belongs to a request; other rows are untouched
+ *   workspace     device buffer of >= pa_workspace_size(...) bytes,
+ *                 256-byte aligned; its contents on entry do not matter and
+ *                 it must not be used by another call running concurrently
+ * Accumulation is fp32; out is rounded to nearest even.  Rows with q_len == 1
+ * run on the split-KV decode kernel, rows of requests with q_len >= 2 on the
+ * tensor-core prefill kernel.  A request with q_len > seq_len, seq_len >
+ * max_blocks * block_size or a block id outside [0, num_blocks) flags
+ * PA_ERR_DEVICE_BOUNDS.
+ */
+int pa_paged_attention(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
+                       int32_t num_blocks, int32_t block_size, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_dim, const int32_t *block_tables,
+                       int32_t max_blocks, const int32_t *seq_lens,
+                       const int32_t *query_start_loc, int32_t num_seqs, int32_t num_tokens,
+                       int32_t max_q_len, int32_t max_seq_len, float scale, pa_bf16 *out,
+                       void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Copy-on-write block copy: for each pair i, physical block
+ * src_dst_pairs[2i+1] of both caches becomes a bit copy of block
+ * src_dst_pairs[2i] ("PagedAttention 显存分页与连续批处理实战", comparison
+ * table, Copy-on-Write sharing of prompt blocks; "连续批处理：推理吞吐的范式革命",
+ * section 4.2, prefix sharing).  Destinations must be distinct and no
+ * destination may be a source of the same call (pairs are then independent
+ * and run in parallel).  An id outside [0, num_blocks) skips the pair and
+ * flags PA_ERR_DEVICE_BOUNDS.
+ *
+ *   src_dst_pairs [num_pairs, 2] int32 device array, read
+ */
+int pa_copy_blocks(pa_bf16 *k_cache, pa_bf16 *v_cache, int32_t num_blocks, int32_t block_size,
+                   int32_t num_kv_heads, int32_t head_dim, const int32_t *src_dst_pairs,
+                   int32_t num_pairs, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word that
+ * the kernels of this library set on the current device.  Returns PA_OK,
+ * PA_ERR_DEVICE_BOUNDS, PA_ERR_TIMEOUT or PA_ERR_CUDA.
+ */
+int pa_check_device_errors(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

@@ -1,0 +1,245 @@
+// pa_api.cu -- the C ABI of libpagedattn (declared in include/pagedattn.h):
+// argument validation, error reporting, workspace carving and dispatch to
+// the kernels.  No device memory is allocated here.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "pagedattn.h"
+#include "pa_internal.h"
+
+namespace {
+
+// Device error word, one per device that loads the library.  Kernels OR
+// pa::DEVERR_* bits into it; pa_check_device_errors reads and clears it.
+__device__ unsigned g_pa_error_word = 0;
+
+thread_local std::string t_last_error;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned* g_err_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+int fail(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(PA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Per-device state: address of the error word and the SM count.
+int device_state(unsigned** err, int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PA_ERR_UNSUPPORTED, "device id %d", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_pa_error_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    g_err_ptr[dev] = static_cast<unsigned*>(p);
+    g_sm_count[dev] = n;
+  }
+  if (err) *err = g_err_ptr[dev];
+  if (sms) *sms = g_sm_count[dev];
+  return PA_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_cache_geometry(int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                         int32_t head_dim) {
+  if (num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return fail(PA_ERR_INVALID_ARG,
+                "cache geometry must be positive (num_blocks=%d block_size=%d "
+                "num_kv_heads=%d head_dim=%d)",
+                num_blocks, block_size, num_kv_heads, head_dim);
+  if (((int64_t)num_kv_heads * head_dim * 2) % 16 != 0)
+    return fail(PA_ERR_UNSUPPORTED, "a token row (num_kv_heads*head_dim*2 bytes) must be a "
+                                    "multiple of 16 bytes");
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_version(void) { return 100; }
+
+const char* pa_get_last_error(void) { return t_last_error.c_str(); }
+
+int pa_reshape_and_cache(const pa_bf16* k, const pa_bf16* v, int32_t num_tokens,
+                         pa_bf16* k_cache, pa_bf16* v_cache, int32_t num_blocks,
+                         int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                         const int32_t* slot_mapping, cudaStream_t stream) {
+  if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens %d < 0", num_tokens);
+  int st = check_cache_geometry(num_blocks, block_size, num_kv_heads, head_dim);
+  if (st) return st;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping)
+    return fail(PA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 4))
+    return fail(PA_ERR_INVALID_ARG, "bf16 arrays must be 16-byte aligned, slot_mapping 4-byte");
+  unsigned* err = nullptr;
+  st = device_state(&err, nullptr);
+  if (st) return st;
+  cudaError_t e = pa::launch_reshape_and_cache(
+      k, v, num_tokens, k_cache, v_cache, (int64_t)num_blocks * block_size,
+      num_kv_heads * head_dim, slot_mapping, err, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
+  return PA_OK;
+}
+
+int pa_copy_blocks(pa_bf16* k_cache, pa_bf16* v_cache, int32_t num_blocks, int32_t block_size,
+                   int32_t num_kv_heads, int32_t head_dim, const int32_t* src_dst_pairs,
+                   int32_t num_pairs, cudaStream_t stream) {
+  if (num_pairs < 0) return fail(PA_ERR_INVALID_ARG, "num_pairs %d < 0", num_pairs);
+  int st = check_cache_geometry(num_blocks, block_size, num_kv_heads, head_dim);
+  if (st) return st;
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !src_dst_pairs)
+    return fail(PA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(src_dst_pairs, 4))
+    return fail(PA_ERR_INVALID_ARG, "caches must be 16-byte aligned, pairs 4-byte");
+  if (num_pairs > 0x7fffffff / 2) return fail(PA_ERR_INVALID_ARG, "too many pairs");
+  unsigned* err = nullptr;
+  st = device_state(&err, nullptr);
+  if (st) return st;
+  cudaError_t e = pa::launch_copy_blocks(k_cache, v_cache, num_blocks,
+                                         (int64_t)block_size * num_kv_heads * head_dim,
+                                         src_dst_pairs, num_pairs, err, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
+  return PA_OK;
+}
+
+size_t pa_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t max_q_len,
+                         int32_t max_seq_len) {
+  if (num_seqs < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      head_dim <= 0 || max_q_len < 0 || max_seq_len < 0)
+    return 0;
+  int sms = 0;
+  if (device_state(nullptr, &sms)) return 0;
+  const int ctas = pa::decode_ctas(sms);
+  size_t bytes = pa::decode_workspace_bytes(ctas, num_seqs, num_q_heads, head_dim);
+  bytes += pa::prefill_workspace_bytes(num_seqs, num_tokens, num_q_heads, head_dim, max_q_len);
+  return bytes;
+}
+
+int pa_paged_attention(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
+                       int32_t num_blocks, int32_t block_size, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_dim, const int32_t* block_tables,
+                       int32_t max_blocks, const int32_t* seq_lens,
+                       const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens,
+                       int32_t max_q_len, int32_t max_seq_len, float scale, pa_bf16* out,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  int st = check_cache_geometry(num_blocks, block_size, num_kv_heads, head_dim);
+  if (st) return st;
+  if (num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return fail(PA_ERR_INVALID_ARG, "num_q_heads %d must be a positive multiple of "
+                "num_kv_heads %d", num_q_heads, num_kv_heads);
+  if (num_seqs < 0 || num_tokens < 0 || max_blocks < 0 || max_q_len < 0 || max_seq_len < 0)
+    return fail(PA_ERR_INVALID_ARG, "negative size argument");
+  if (max_q_len > max_seq_len)
+    return fail(PA_ERR_INVALID_ARG, "max_q_len %d > max_seq_len %d", max_q_len, max_seq_len);
+  if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "scale is NaN");
+  if (block_size != 16)
+    return fail(PA_ERR_UNSUPPORTED, "block_size %d (only 16 is implemented)", block_size);
+  const int group = num_q_heads / num_kv_heads;
+  if (!pa::decode_supported(head_dim, group, num_kv_heads))
+    return fail(PA_ERR_UNSUPPORTED, "shape head_dim=%d group=%d num_kv_heads=%d", head_dim,
+                group, num_kv_heads);
+  if (num_seqs == 0 || num_tokens == 0 || max_seq_len == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start_loc || !out)
+    return fail(PA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(query_start_loc, 4))
+    return fail(PA_ERR_INVALID_ARG, "bf16 arrays must be 16-byte aligned, int32 arrays 4-byte");
+  if ((int64_t)max_blocks * block_size < max_seq_len)
+    return fail(PA_ERR_INVALID_ARG, "max_blocks %d * block_size cannot hold max_seq_len %d",
+                max_blocks, max_seq_len);
+  if (max_q_len >= 2 && !pa::prefill_supported(head_dim, group, num_kv_heads))
+    return fail(PA_ERR_UNSUPPORTED, "prefill rows (q_len >= 2) for head_dim=%d group=%d",
+                head_dim, group);
+
+  unsigned* err = nullptr;
+  int sms = 0;
+  st = device_state(&err, &sms);
+  if (st) return st;
+  const int ctas = pa::decode_ctas(sms);
+  const size_t need_decode = pa::decode_workspace_bytes(ctas, num_seqs, num_q_heads, head_dim);
+  const size_t need_prefill =
+      pa::prefill_workspace_bytes(num_seqs, num_tokens, num_q_heads, head_dim, max_q_len);
+  if (!workspace || !aligned(workspace, 256))
+    return fail(PA_ERR_WORKSPACE, "workspace must be a non-null 256-byte aligned pointer");
+  if (workspace_bytes < need_decode + need_prefill)
+    return fail(PA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", workspace_bytes,
+                need_decode + need_prefill);
+
+  pa::AttnArgs a;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.num_blocks = num_blocks;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_tables = block_tables;
+  a.max_blocks = max_blocks;
+  a.seq_lens = seq_lens;
+  a.query_start_loc = query_start_loc;
+  a.num_seqs = num_seqs;
+  a.num_tokens = num_tokens;
+  a.max_q_len = max_q_len;
+  a.max_seq_len = max_seq_len;
+  a.scale = scale;
+  a.out = out;
+  a.err = err;
+
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  if (max_q_len >= 2) {
+    cudaError_t e = pa::launch_prefill(a, ws + need_decode, need_prefill, sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  }
+  pa::DecodeWorkspace dws = pa::decode_workspace(ws, ctas, num_seqs, num_q_heads, head_dim);
+  cudaError_t e = pa::launch_decode(a, dws, ctas, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return PA_OK;
+}
+
+int pa_check_device_errors(cudaStream_t stream) {
+  unsigned* err = nullptr;
+  int st = device_state(&err, nullptr);
+  if (st) return st;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned word = 0;
+  e = cudaMemcpy(&word, err, sizeof word, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+  const unsigned zero = 0;
+  e = cudaMemcpy(err, &zero, sizeof zero, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+  if (word & pa::DEVERR_TIMEOUT)
+    return fail(PA_ERR_TIMEOUT, "a kernel gave up a bounded wait (device word 0x%x)", word);
+  if (word & pa::DEVERR_BOUNDS)
+    return fail(PA_ERR_DEVICE_BOUNDS,
+                "a kernel found an index or length out of range (device word 0x%x)", word);
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,100 @@
+// pa_cache.cu -- the two cache-maintenance kernels: the slot scatter that
+// writes a step's new K/V rows into their physical slots, and the
+// copy-on-write block copy.  Both are pure bit copies with 16-byte vectors;
+// HBM-bound.
+//
+// Slot scatter: "PagedAttention 显存分页与连续批处理(Continuous Batching)实战",
+//   comparison table (blocks allocated on demand as a block fills) and the
+//   TypeScript Block Manager's appendToken (a new token lands in the last
+//   block of the request's Block Table).
+// Copy-on-write: same page, comparison table ("Copy-on-Write ... shared
+//   blocks"); "连续批处理：推理吞吐的范式革命", section 4.2 (prefix sharing).
+#include <cstdint>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr int kScatterWarps = 8;
+
+// One warp per new token: copy its K row and V row (num_kv_heads * head_dim
+// bf16 each, row_vec 16-byte vectors) to slot slot_mapping[t].
+__global__ void __launch_bounds__(kScatterWarps * 32)
+    reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                             int32_t num_tokens, uint4* __restrict__ k_cache,
+                             uint4* __restrict__ v_cache, int64_t num_slots, int32_t row_vec,
+                             const int32_t* __restrict__ slot_mapping, unsigned* err) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * kScatterWarps + warp;
+  if (t >= num_tokens) return;
+  const int64_t slot = slot_mapping[t];
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (lane == 0) flag_error(err, DEVERR_BOUNDS);
+    return;
+  }
+  const uint4* ks = k + t * row_vec;
+  const uint4* vs = v + t * row_vec;
+  uint4* kd = k_cache + slot * row_vec;
+  uint4* vd = v_cache + slot * row_vec;
+  for (int i = lane; i < row_vec; i += 32) {
+    const uint4 a = __ldg(ks + i);
+    const uint4 b = __ldg(vs + i);
+    kd[i] = a;
+    vd[i] = b;
+  }
+}
+
+constexpr int kCopyThreads = 256;
+
+// One CTA per (src, dst) pair: copy the K block and the V block.
+__global__ void __launch_bounds__(kCopyThreads)
+    copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                       int32_t num_blocks, int64_t block_vec, const int32_t* __restrict__ pairs,
+                       unsigned* err) {
+  const int64_t src = pairs[2 * (int64_t)blockIdx.x];
+  const int64_t dst = pairs[2 * (int64_t)blockIdx.x + 1];
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (threadIdx.x == 0) flag_error(err, DEVERR_BOUNDS);
+    return;
+  }
+  const uint4* ks = k_cache + src * block_vec;
+  const uint4* vs = v_cache + src * block_vec;
+  uint4* kd = k_cache + dst * block_vec;
+  uint4* vd = v_cache + dst * block_vec;
+  for (int64_t i = threadIdx.x; i < block_vec; i += kCopyThreads) {
+    const uint4 a = ks[i];
+    const uint4 b = vs[i];
+    kd[i] = a;
+    vd[i] = b;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_reshape_and_cache(const uint16_t* k, const uint16_t* v, int32_t num_tokens,
+                                     uint16_t* k_cache, uint16_t* v_cache, int64_t num_slots,
+                                     int32_t row_elems, const int32_t* slot_mapping,
+                                     unsigned* err, cudaStream_t stream) {
+  if (num_tokens == 0) return cudaSuccess;
+  const int grid = (num_tokens + kScatterWarps - 1) / kScatterWarps;
+  reshape_and_cache_kernel<<<grid, kScatterWarps * 32, 0, stream>>>(
+      reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v), num_tokens,
+      reinterpret_cast<uint4*>(k_cache), reinterpret_cast<uint4*>(v_cache), num_slots,
+      row_elems / 8, slot_mapping, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, int32_t num_blocks,
+                               int64_t block_elems, const int32_t* pairs, int32_t num_pairs,
+                               unsigned* err, cudaStream_t stream) {
+  if (num_pairs == 0) return cudaSuccess;
+  copy_blocks_kernel<<<num_pairs, kCopyThreads, 0, stream>>>(
+      reinterpret_cast<uint4*>(k_cache), reinterpret_cast<uint4*>(v_cache), num_blocks,
+      block_elems / 8, pairs, err);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,72 @@
+// pa_internal.h -- host-side interfaces between the C-ABI layer (pa_api.cu)
+// and the kernel translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pa {
+
+// Bits of the device error word (read back by pa_check_device_errors).
+enum : unsigned {
+  DEVERR_BOUNDS = 1u,   // an index / length was out of range; work skipped
+  DEVERR_TIMEOUT = 2u,  // a bounded wait gave up
+};
+
+// Geometry and pointers of one paged-attention call, already validated.
+struct AttnArgs {
+  const uint16_t* q;
+  const uint16_t* k_cache;
+  const uint16_t* v_cache;
+  int32_t num_blocks;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  const int32_t* block_tables;
+  int32_t max_blocks;
+  const int32_t* seq_lens;
+  const int32_t* query_start_loc;
+  int32_t num_seqs;
+  int32_t num_tokens;
+  int32_t max_q_len;
+  int32_t max_seq_len;
+  float scale;
+  uint16_t* out;
+  unsigned* err;  // device error word
+};
+
+// Workspace carve-up shared by the launchers (sizes in bytes, 256-aligned).
+struct DecodeWorkspace {
+  float* part_o;    // [ctas * 2, num_q_heads, head_dim]
+  float* part_ml;   // [ctas * 2, num_q_heads, 2]  (running max in log2 units, sum)
+  int4* seq_rec;    // [num_seqs]
+};
+
+size_t decode_workspace_bytes(int ctas, int num_seqs, int num_q_heads, int head_dim);
+DecodeWorkspace decode_workspace(void* base, int ctas, int num_seqs, int num_q_heads,
+                                 int head_dim);
+int decode_ctas(int sm_count);
+
+// Each launcher returns cudaSuccess or the launch error.  Unsupported shapes
+// are rejected by the API layer before these are called.
+bool decode_supported(int head_dim, int group, int num_kv_heads);
+cudaError_t launch_decode(const AttnArgs& a, const DecodeWorkspace& ws, int ctas,
+                          cudaStream_t stream);
+
+bool prefill_supported(int head_dim, int group, int num_kv_heads);
+size_t prefill_workspace_bytes(int num_seqs, int num_tokens, int num_q_heads, int head_dim,
+                               int max_q_len);
+cudaError_t launch_prefill(const AttnArgs& a, void* ws, size_t ws_bytes, int sm_count,
+                           cudaStream_t stream);
+
+cudaError_t launch_reshape_and_cache(const uint16_t* k, const uint16_t* v, int32_t num_tokens,
+                                     uint16_t* k_cache, uint16_t* v_cache, int64_t num_slots,
+                                     int32_t row_elems, const int32_t* slot_mapping,
+                                     unsigned* err, cudaStream_t stream);
+
+cudaError_t launch_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, int32_t num_blocks,
+                               int64_t block_elems, const int32_t* pairs, int32_t num_pairs,
+                               unsigned* err, cudaStream_t stream);
+
+}  // namespace pa

@@ -304,3 +304,47 @@ def causal_flops(b: PagedBatch, min_q_len: int = 2) -> int:
         pairs = ql * (L - ql) + ql * (ql + 1) // 2
         total += pairs * b.num_q_heads * b.head_dim * 4
     return total
+
+
+@dataclass
+class DeviceBatch:
+    """torch tensors of a PagedBatch on one device (bf16 / int32)."""
+
+    q: "object"
+    k_new: "object"
+    v_new: "object"
+    k_cache: "object"
+    v_cache: "object"
+    block_tables: "object"
+    seq_lens: "object"
+    query_start_loc: "object"
+    slot_mapping: "object"
+    copy_pairs: "object"
+
+
+def bf16_tensor(bits: np.ndarray, device):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.to(device)
+
+
+def int32_tensor(a: np.ndarray, device):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+
+def to_device(b: PagedBatch, device="cuda") -> DeviceBatch:
+    return DeviceBatch(q=bf16_tensor(b.q, device), k_new=bf16_tensor(b.k_new, device),
+                       v_new=bf16_tensor(b.v_new, device), k_cache=bf16_tensor(b.k_cache, device),
+                       v_cache=bf16_tensor(b.v_cache, device),
+                       block_tables=int32_tensor(b.block_tables, device),
+                       seq_lens=int32_tensor(b.seq_lens, device),
+                       query_start_loc=int32_tensor(b.query_start_loc, device),
+                       slot_mapping=int32_tensor(b.slot_mapping, device),
+                       copy_pairs=int32_tensor(b.copy_pairs.reshape(-1, 2), device))
+
+
+def bits_of(t) -> np.ndarray:
+    """bf16 torch tensor (any device) -> uint16 numpy bits."""
+    import torch
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)

@@ -1,0 +1,79 @@
+"""The C ABI library builds, loads without a GPU, exports every symbol the
+header declares, and rejects bad arguments on the host before touching CUDA.
+CPU only."""
+import ctypes
+
+import pytest
+
+from paged_kv_cache_174_gb300 import build as pkg_build
+from paged_kv_cache_174_gb300 import ops
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkg_build.build()
+    return ops.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = ops.declared_symbols()
+    assert {"pa_reshape_and_cache", "pa_paged_attention", "pa_copy_blocks",
+            "pa_workspace_size", "pa_check_device_errors", "pa_get_last_error",
+            "pa_version"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version(lib):
+    assert ops.version() >= 100
+
+
+def _status(code):
+    return ops.STATUS_NAMES[code]
+
+
+def test_host_side_argument_checks(lib):
+    L = lib
+    vp = ctypes.c_void_p
+    # negative sizes are rejected before any CUDA call
+    assert _status(L.pa_reshape_and_cache(None, None, -1, None, None, 4, 16, 2, 64, None, None)) \
+        == "PA_ERR_INVALID_ARG"
+    assert b"num_tokens" in L.pa_get_last_error()
+    # an empty call is a no-op
+    assert L.pa_reshape_and_cache(None, None, 0, None, None, 4, 16, 2, 64, None, None) == 0
+    assert _status(L.pa_copy_blocks(None, None, 0, 16, 2, 64, None, 0, None)) \
+        == "PA_ERR_INVALID_ARG"
+    assert L.pa_copy_blocks(None, None, 4, 16, 2, 64, None, 0, None) == 0
+    assert _status(L.pa_copy_blocks(None, None, 4, 16, 2, 64, None, 3, None)) \
+        == "PA_ERR_INVALID_ARG"
+    # a token row must be a whole number of 16-byte vectors
+    assert _status(L.pa_reshape_and_cache(None, None, 1, None, None, 4, 16, 1, 3, None, None)) \
+        == "PA_ERR_UNSUPPORTED"
+    args = dict(q=None, k=None, v=None, nb=32, bs=16, nq=4, nkv=2, d=64, bt=None, maxb=3,
+                sl=None, qsl=None, S=4, T=4, mq=1, ms=48, scale=0.125, out=None, ws=None,
+                wsb=0, st=None)
+
+    def attn(**kw):
+        a = {**args, **kw}
+        return _status(L.pa_paged_attention(a["q"], a["k"], a["v"], a["nb"], a["bs"], a["nq"],
+                                            a["nkv"], a["d"], a["bt"], a["maxb"], a["sl"],
+                                            a["qsl"], a["S"], a["T"], a["mq"], a["ms"],
+                                            ctypes.c_float(a["scale"]), a["out"], a["ws"],
+                                            a["wsb"], a["st"]))
+    assert attn(bs=32) == "PA_ERR_UNSUPPORTED"
+    assert attn(d=96) == "PA_ERR_UNSUPPORTED"
+    assert attn(nq=6, nkv=4) == "PA_ERR_INVALID_ARG"
+    assert attn(nq=48, nkv=2) == "PA_ERR_UNSUPPORTED"  # group 24
+    assert attn(mq=5, ms=4) == "PA_ERR_INVALID_ARG"
+    assert attn(scale=float("nan")) == "PA_ERR_INVALID_ARG"
+    assert attn(S=0) == "PA_OK"   # nothing to do
+    assert attn() == "PA_ERR_INVALID_ARG"  # null pointers
+    assert vp  # keep the import used
+
+
+def test_torch_side_checks_without_gpu():
+    import torch
+    with pytest.raises((TypeError, ValueError)):
+        ops.reshape_and_cache(torch.zeros(1, 2, 64), torch.zeros(1, 2, 64),
+                              torch.zeros(4, 16, 2, 64), torch.zeros(4, 16, 2, 64),
+                              torch.zeros(1, dtype=torch.int32))
