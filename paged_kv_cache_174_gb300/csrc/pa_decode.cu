@@ -75,15 +75,23 @@ __device__ __forceinline__ int64_t slice_begin(int64_t c, int64_t F, int64_t C) 
   return c * F / C;
 }
 
-// Shared-memory layout after the stage ring (dynamic shared memory).
-template <int D, int G, int NW>
+// Shared-memory state after the stage ring (dynamic shared memory).
+template <int G>
+struct PBuf {          // hand-off from the QK warp to the PV warp of one kv head
+  float p[kBlock][G];  // exp2(score - m) of the page's tokens
+  float alpha[G];      // rescale of the running output for this page
+  float m[G];          // running max after this page (segment end only)
+  float l[G];          // running sum after this page (segment end only)
+};
+
+template <int G, int NKV>
 struct DecodeSmem {
-  uint64_t full[8];      // stage holds its page (bulk-copy transaction count)
-  int released[8];       // warps done with the page in the stage
-  int last_issued[8];    // last page whose copies went into the stage (-1: none)
-  float p_s[NW][kBlock][G];
-  float alpha_s[NW][G];
-  float seg_ml[NW][G][2];
+  uint64_t full[8];           // stage holds its page (bulk-copy transaction count)
+  uint64_t p_full[NKV][2];    // QK warp -> PV warp: page's p is ready
+  uint64_t p_empty[NKV][2];   // PV warp -> QK warp: buffer may be rewritten
+  int released[8];            // warps done with the page in the stage
+  int last_issued[8];         // last page whose copies went into the stage (-1: none)
+  PBuf<G> pb[NKV][2];
   int plan[2];
   int abort_flag;
 };
@@ -101,7 +109,7 @@ struct PageCursor {
   }
 };
 
-// Issue the bulk copies of page (c.s, c.j) into stage st.
+// Issue the bulk copies of page (c.s, c.j) into a stage.
 __device__ __forceinline__ void fetch_page(const DecodeParams& p, const PageCursor& c,
                                            uint32_t stage_smem, uint32_t full_bar) {
   const int L = __ldg(p.seq_lens + c.s);
@@ -120,30 +128,151 @@ __device__ __forceinline__ void fetch_page(const DecodeParams& p, const PageCurs
            bytes, full_bar);
 }
 
-// D: head_dim; G: q heads per kv head; NW: warps; NSUB: warps per kv head
-// (each takes 16 / NSUB tokens of every page), so num_kv_heads = NW / NSUB.
-template <int D, int G, int NW, int NSUB>
-__global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p) {
-  constexpr int LPT = D / 8;          // lanes per token: each holds 8 elements = 16 bytes
-  constexpr int TPI = 32 / LPT;       // tokens per warp iteration
-  constexpr int TPS = kBlock / NSUB;  // tokens of a page per warp
-  constexpr int NIT = (TPS + TPI - 1) / TPI;
-  constexpr int REP = LPT / G;        // lanes that end up holding the same score
-  static_assert(LPT >= G && LPT % G == 0, "group too large for the lane split");
-  static_assert(NW % NSUB == 0, "warps must split evenly over kv heads");
+template <int N>
+__device__ __forceinline__ void lds_floats(uint32_t addr, float (&v)[N]) {
+  if constexpr (N % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < N; i += 4) {
+      const float4 x = lds128f(addr + 4 * i);
+      v[i] = x.x, v[i + 1] = x.y, v[i + 2] = x.z, v[i + 3] = x.w;
+    }
+  } else if constexpr (N == 2) {
+    float2 x;
+    asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(x.x), "=f"(x.y) : "r"(addr));
+    v[0] = x.x, v[1] = x.y;
+  } else {
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v[0]) : "r"(addr));
+  }
+}
+
+// Sum over the LPT lanes of one token, handing out the G values: after the
+// call, lane holds the total of value index (lane % LPT) / (LPT / G).
+template <int G, int LPT>
+__device__ __forceinline__ float reduce_scatter(float (&part)[G], int lane) {
+  int cnt = G;
+#pragma unroll
+  for (int m = LPT / 2; m >= 1; m >>= 1) {
+    if (cnt > 1) {
+      const int half = cnt / 2;
+      const bool upper = (lane & m) != 0;
+#pragma unroll
+      for (int x = 0; x < G / 2; ++x) {
+        if (x < half) {
+          const float send = upper ? part[x] : part[x + half];
+          const float keep = upper ? part[x + half] : part[x];
+          part[x] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+      }
+      cnt = half;
+    } else {
+      part[0] += __shfl_xor_sync(0xffffffffu, part[0], m);
+    }
+  }
+  return part[0];
+}
+
+// Scores of one page for one QK warp.  kb points at this lane's 16-byte piece
+// of its first token's key row in the stage; FULL pages need no per-token
+// predicate.  sc[it] is the base-2 score of token it * TPI + tok_lane for the
+// head this lane holds after the reduce-scatter (-inf past the page's end).
+template <int D, int G, int E_QK, int LPT, uint32_t ROW, bool FULL>
+__device__ __forceinline__ void qk_scores(const unsigned char* kb, int ntok, int tok_lane,
+                                          const float2 (&qf)[G][E_QK / 2],
+                                          float (&sc)[kBlock / (32 / LPT)], int lane) {
+  constexpr int TPI = 32 / LPT;
+  constexpr int NIT = kBlock / TPI;
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
+    const bool valid = FULL || (it * TPI + tok_lane < ntok);
+    float2 a2[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) a2[h] = make_float2(0.f, 0.f);
+    if (valid) {
+#pragma unroll
+      for (int piece = 0; piece < E_QK / 8; ++piece) {
+        const uint4 kw = *reinterpret_cast<const uint4*>(kb + it * TPI * ROW + piece * D);
+        const uint32_t ks[4] = {kw.x, kw.y, kw.z, kw.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 k2 = bf16x2_to_float2(ks[e]);
+#pragma unroll
+          for (int h = 0; h < G; ++h) a2[h] = __ffma2_rn(qf[h][piece * 4 + e], k2, a2[h]);
+        }
+      }
+    }
+    float part[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) part[h] = a2[h].x + a2[h].y;
+    const float s = reduce_scatter<G, LPT>(part, lane);
+    sc[it] = valid ? s : kNegInf;
+  }
+}
+
+// p * V of one page for one PV warp: vb points at this lane's 16-byte piece of
+// its first token's value row, pp at p[tok_lane][0] of the page's hand-off.
+template <int D, int G, int LPT, uint32_t ROW, bool FULL>
+__device__ __forceinline__ void pv_accumulate(const unsigned char* vb, const float* pp, int ntok,
+                                              int tok_lane, float2 (&acc)[G][4]) {
+  constexpr int TPI = 32 / LPT;
+  constexpr int NIT = kBlock / TPI;
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
+    if (FULL || it * TPI + tok_lane < ntok) {
+      const uint4 vw = *reinterpret_cast<const uint4*>(vb + it * TPI * ROW);
+      const uint32_t vs[4] = {vw.x, vw.y, vw.z, vw.w};
+      float pr[G];
+      if constexpr (G % 4 == 0) {
+#pragma unroll
+        for (int h = 0; h < G; h += 4) {
+          const float4 x = *reinterpret_cast<const float4*>(pp + it * TPI * G + h);
+          pr[h] = x.x, pr[h + 1] = x.y, pr[h + 2] = x.z, pr[h + 3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < G; ++h) pr[h] = pp[it * TPI * G + h];
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 v2 = bf16x2_to_float2(vs[e]);
+#pragma unroll
+        for (int h = 0; h < G; ++h) acc[h][e] = __ffma2_rn(v2, make_float2(pr[h], pr[h]), acc[h][e]);
+      }
+    }
+  }
+}
+
+// D: head_dim; G: q heads per kv head; NKV: kv heads (= warps of each role).
+// Warps 0..NKV-1 compute scores and the softmax (QK warps), warps
+// NKV..2*NKV-1 accumulate p * V (PV warps); warp g and warp NKV + g serve kv
+// head g and hand over p through a double-buffered slot in shared memory.
+template <int D, int G, int NKV>
+__global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodeParams p) {
+  constexpr int NW = 2 * NKV;
+  // QK lanes: E_QK head_dim elements each (two 16-byte pieces when 16)
+  constexpr int E_QK = (G <= 4 && D == 128) ? 16 : 8;
+  constexpr int LPT_QK = D / E_QK;
+  constexpr int TPI_QK = 32 / LPT_QK;
+  constexpr int NIT_QK = kBlock / TPI_QK;
+  constexpr int REP_QK = LPT_QK / G;
+  // PV lanes: 8 elements (16 bytes) each
+  constexpr int LPT_PV = D / 8;
+  constexpr int TPI_PV = 32 / LPT_PV;
+  constexpr int NIT_PV = kBlock / TPI_PV;
+  constexpr uint32_t ROW = NKV * D * 2;  // bytes of one token row in a page
+  static_assert(LPT_QK >= G && LPT_QK % G == 0, "group too large for the lane split");
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  using Smem = DecodeSmem<D, G, NW>;
+  using Smem = DecodeSmem<G, NKV>;
   unsigned char* stages = smem_raw;
   Smem& S = *reinterpret_cast<Smem*>(smem_raw + (size_t)p.nstages * p.stage_bytes);
-  // cross-warp buffer for the o of subsets 1.. of each kv head
-  float* seg_o = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(&S) + sizeof(Smem));
   __shared__ long long red[NW];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = p.ctas;
   const int c = blockIdx.x;
   const int NST = p.nstages;
+  // the merge kernel waits for this whole grid anyway; let it be scheduled
+  asm volatile("griddepcontrol.launch_dependents;");
 
   // ---------------------------------------------------------------- plan
   // pass 1: total decode pages F (all threads)
@@ -193,6 +322,11 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
         S.released[i] = 0;
         S.last_issued[i] = -1;
       }
+      for (int g = 0; g < NKV; ++g)
+        for (int b = 0; b < 2; ++b) {
+          mbar_init(smem_addr(&S.p_full[g][b]), 1);
+          mbar_init(smem_addr(&S.p_empty[g][b]), 1);
+        }
       fence_mbar_init();
       if (found_s >= 0) {
         PageCursor fc{found_s, found_j, decode_pages(p, found_s, false)};
@@ -211,280 +345,225 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
   if (s_begin < 0) return;  // cannot happen when n_pages > 0
   volatile int* abort_flag = &S.abort_flag;
 
-  // ---------------------------------------------------------------- main loop
-  const int n_kv = NW / NSUB;
-  const int g = warp % n_kv;   // kv head
-  const int sub = warp / n_kv; // token subset of the page
-  const int tok_lane = lane / LPT;
-  const int dl = lane % LPT;
-  const int my_h = dl / REP;   // head whose score this lane holds after the reduce-scatter
-  const int rep = dl % REP;
-
-  float2 qf[G][4];
-  float2 acc[G][4];
-  float m_run = kNegInf, l_run = 0.f;
-
+  const bool is_qk = warp < NKV;
+  const int g = is_qk ? warp : warp - NKV;  // kv head served by this warp
   PageCursor cur{s_begin, j_begin, decode_pages(p, s_begin, false)};
   PageCursor fc = cur;  // page to fetch when this warp is the last to release a stage
   for (int i = 0; i < NST; ++i) fc.next(p);
+
+  int L = __ldg(p.seq_lens + cur.s);
   int seg_j0 = j_begin;
 
-  auto load_q = [&](int seq) {
-    const int tok = __ldg(p.qsl + seq);
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const uint4 w = __ldg(reinterpret_cast<const uint4*>(
-          p.q + ((int64_t)tok * p.n_q + g * G + h) * D + dl * 8));
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = bf16x2_to_float2(ws[e]);
-        qf[h][e] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
-        acc[h][e] = make_float2(0.f, 0.f);
-      }
-    }
-    m_run = kNegInf;
-    l_run = 0.f;
-  };
-
-  load_q(cur.s);
-  const uint32_t stage0 = smem_addr(stages);
-  const uint32_t gh_off = (uint32_t)(g * D * 2 + dl * 16);
-
-  for (int i = 0; i < n_pages; ++i) {
-    const int st = i % NST;
-    // A failed wait leaves the page's contents meaningless (the error word
-    // says so) but the page is still processed: control flow must stay the
-    // same in every warp because of the CTA barriers at segment ends.
-    mbar_wait(smem_addr(&S.full[st]), (i / NST) & 1, p.err, abort_flag);
-    const int L = __ldg(p.seq_lens + cur.s);
-    const int ntok = min(kBlock, L - cur.j * kBlock);
-    const uint32_t kst = stage0 + (uint32_t)st * p.stage_bytes;
-    const uint32_t vst = kst + p.page_bytes;
-
-    // ---- scores of this warp's tokens, one (token, head) per lane
-    float sc[NIT];
-#pragma unroll
-    for (int it = 0; it < NIT; ++it) {
-      const int tl = it * TPI + tok_lane;  // token index within the subset
-      const int t = sub * TPS + tl;
-      const bool valid = tl < TPS && t < ntok;
-      uint4 kw = make_uint4(0, 0, 0, 0);
-      if (valid) kw = lds128(kst + (uint32_t)t * p.row_bytes + gh_off);
-      const uint32_t ks[4] = {kw.x, kw.y, kw.z, kw.w};
-      float part[G];
+  if (is_qk) {
+    // ================================================================ QK warp
+    const int tok_lane = lane / LPT_QK;
+    const int dl = lane % LPT_QK;
+    const int my_h = dl / REP_QK;
+    const int rep = dl % REP_QK;
+    float2 qf[G][E_QK / 2];
+    float m_run = kNegInf, l_lane = 0.f;
+    auto load_q = [&](int seq) {
+      const int tok = __ldg(p.qsl + seq);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        float2 a = make_float2(0.f, 0.f);
+        const uint16_t* qrow = p.q + ((int64_t)tok * p.n_q + g * G + h) * D;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) a = __ffma2_rn(qf[h][e], bf16x2_to_float2(ks[e]), a);
-        part[h] = a.x + a.y;
-      }
-      // reduce-scatter over the LPT lanes of the token: each halving step
-      // hands half of the remaining heads to the partner lane
-      int cnt = G;
-#pragma unroll
-      for (int m = LPT / 2; m >= 1; m >>= 1) {
-        if (cnt > 1) {
-          const int half = cnt / 2;
-          const bool upper = (lane & m) != 0;
-#pragma unroll
-          for (int x = 0; x < G / 2; ++x) {
-            if (x < half) {
-              const float send = upper ? part[x] : part[x + half];
-              const float keep = upper ? part[x + half] : part[x];
-              part[x] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-            }
-          }
-          cnt = half;
-        } else {
-          part[0] += __shfl_xor_sync(0xffffffffu, part[0], m);
-        }
-      }
-      sc[it] = valid ? part[0] : kNegInf;
-    }
-    // ---- online softmax update (base 2) for head my_h
-    float mx = kNegInf;
-#pragma unroll
-    for (int it = 0; it < NIT; ++it) mx = fmaxf(mx, sc[it]);
-#pragma unroll
-    for (int m = LPT; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-    const float m_new = fmaxf(m_run, mx);
-    const float m_use = (m_new == kNegInf) ? 0.f : m_new;
-    const float alpha = fast_exp2(m_run - m_use);
-    float lsum = 0.f;
-#pragma unroll
-    for (int it = 0; it < NIT; ++it) {
-      const float pr = fast_exp2(sc[it] - m_use);
-      lsum += pr;
-      const int tl = it * TPI + tok_lane;
-      if (rep == 0 && tl < TPS) S.p_s[warp][tl][my_h] = pr;
-    }
-    l_run = l_run * alpha + lsum;
-    m_run = m_new;
-    if (tok_lane == 0 && rep == 0) S.alpha_s[warp][my_h] = alpha;
-    __syncwarp();
-
-    // ---- rescale, then accumulate p * v
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float a = S.alpha_s[warp][h];
-      const float2 a2 = make_float2(a, a);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[h][e] = __fmul2_rn(acc[h][e], a2);
-    }
-#pragma unroll
-    for (int it = 0; it < NIT; ++it) {
-      const int tl = it * TPI + tok_lane;
-      const int t = sub * TPS + tl;
-      if (tl < TPS && t < ntok) {
-        const uint4 vw = lds128(vst + (uint32_t)t * p.row_bytes + gh_off);
-        const uint32_t vs[4] = {vw.x, vw.y, vw.z, vw.w};
-        float pr[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) pr[h] = S.p_s[warp][tl][h];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 v2 = bf16x2_to_float2(vs[e]);
-#pragma unroll
-          for (int h = 0; h < G; ++h)
-            acc[h][e] = __ffma2_rn(v2, make_float2(pr[h], pr[h]), acc[h][e]);
-        }
-      }
-    }
-    __syncwarp();
-    // ---- release the stage; the last warp out refills it NST pages ahead
-    if (lane == 0) {
-      const int before = atomicAdd(&S.released[st], 1);
-      if (before == NW - 1) {
-        S.released[st] = 0;
-        // after a failed wait nothing more is issued: the stage's previous
-        // copy may still be landing
-        if (i + NST < n_pages && !*abort_flag) {
-          fetch_page(p, fc, kst, smem_addr(&S.full[st]));
-          S.last_issued[st] = i + NST;
-        }
-      }
-      fc.next(p);
-    }
-
-    // ---- end of a segment: the request is finished, or this CTA's slice ends
-    const bool seq_done = (cur.j + 1 == cur.np);
-    const bool slice_done = (i + 1 == n_pages);
-    if (seq_done || slice_done) {
-      // sum over the token lanes of the warp
-#pragma unroll
-      for (int m = LPT; m < 32; m <<= 1) {
-        l_run += __shfl_xor_sync(0xffffffffu, l_run, m);
-#pragma unroll
-        for (int h = 0; h < G; ++h)
+        for (int piece = 0; piece < E_QK / 8; ++piece) {
+          const uint4 w = __ldg(reinterpret_cast<const uint4*>(qrow + piece * (D / 2) + dl * 8));
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, m);
-            acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, m);
+            const float2 f = bf16x2_to_float2(ws[e]);
+            qf[h][piece * 4 + e] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
           }
-      }
-      float m_fin[G], l_fin[G];
-      if constexpr (NSUB > 1) {
-        // combine the warps of each kv head through shared memory
-        if (tok_lane == 0 && rep == 0) {
-          S.seg_ml[warp][my_h][0] = m_run;
-          S.seg_ml[warp][my_h][1] = l_run;
         }
-        if (sub > 0 && tok_lane == 0) {
-          float* dst = seg_o + ((size_t)(warp - n_kv) * G) * D + dl * 8;
+      }
+      m_run = kNegInf;
+      l_lane = 0.f;
+    };
+    load_q(cur.s);
+    // this lane's piece of its first token's key row, relative to a stage
+    const uint32_t k_off = (uint32_t)(g * D * 2 + dl * 16) + (uint32_t)tok_lane * ROW;
+    int st = 0, st_phase = 0;
+    const unsigned char* stage = stages;
+    for (int i = 0; i < n_pages; ++i) {
+      const int b = i & 1;
+      if (i >= 2) mbar_wait(smem_addr(&S.p_empty[g][b]), ((i >> 1) - 1) & 1, p.err, abort_flag);
+      mbar_wait(smem_addr(&S.full[st]), st_phase, p.err, abort_flag);
+      const int ntok = min(kBlock, L - cur.j * kBlock);
+      float sc[NIT_QK];
+      if (ntok == kBlock)
+        qk_scores<D, G, E_QK, LPT_QK, ROW, true>(stage + k_off, ntok, tok_lane, qf, sc, lane);
+      else
+        qk_scores<D, G, E_QK, LPT_QK, ROW, false>(stage + k_off, ntok, tok_lane, qf, sc, lane);
+      // online softmax (base 2) for head my_h over the page's 16 tokens
+      float mx = sc[0];
+#pragma unroll
+      for (int it = 1; it < NIT_QK; ++it) mx = fmaxf(mx, sc[it]);
+#pragma unroll
+      for (int m = LPT_QK; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+      const float m_new = fmaxf(m_run, mx);
+      const float m_use = (m_new == kNegInf) ? 0.f : m_new;
+      const float alpha = fast_exp2(m_run - m_use);
+      PBuf<G>& pb = S.pb[g][b];
+      float* pw = &pb.p[tok_lane][my_h];
+      float lsum = 0.f;
+#pragma unroll
+      for (int it = 0; it < NIT_QK; ++it) {
+        const float pr = fast_exp2(sc[it] - m_use);
+        lsum += pr;
+        if (rep == 0) pw[it * TPI_QK * G] = pr;
+      }
+      l_lane = l_lane * alpha + lsum;
+      m_run = m_new;
+      if (tok_lane == 0 && rep == 0) pb.alpha[my_h] = alpha;
+      const bool seq_done = (cur.j + 1 == cur.np);
+      const bool seg_end = seq_done || (i + 1 == n_pages);
+      if (seg_end) {
+        float lt = l_lane;
+#pragma unroll
+        for (int m = LPT_QK; m < 32; m <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, m);
+        if (tok_lane == 0 && rep == 0) {
+          pb.m[my_h] = m_run;
+          pb.l[my_h] = lt;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_addr(&S.p_full[g][b]));
+        // release the stage; the last warp out refills it NST pages ahead
+        if (atomicAdd(&S.released[st], 1) == NW - 1) {
+          S.released[st] = 0;
+          if (i + NST < n_pages && !*abort_flag) {
+            fetch_page(p, fc, smem_addr(stage), smem_addr(&S.full[st]));
+            S.last_issued[st] = i + NST;
+          }
+        }
+        fc.next(p);
+      }
+      stage += p.stage_bytes;
+      if (++st == NST) st = 0, st_phase ^= 1, stage = stages;
+      const int prev_s = cur.s;
+      cur.next(p);
+      if (seg_end && cur.s != prev_s && i + 1 < n_pages) {
+        L = __ldg(p.seq_lens + cur.s);
+        load_q(cur.s);
+      }
+    }
+  } else {
+    // ================================================================ PV warp
+    const int tok_lane = lane / LPT_PV;
+    const int dl = lane % LPT_PV;
+    float2 acc[G][4];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[h][e] = make_float2(0.f, 0.f);
+    // this lane's piece of its first token's value row, relative to a stage
+    const uint32_t v_off = p.page_bytes + (uint32_t)(g * D * 2 + dl * 16) + (uint32_t)tok_lane * ROW;
+    int st = 0, st_phase = 0;
+    const unsigned char* stage = stages;
+    for (int i = 0; i < n_pages; ++i) {
+      const int b = i & 1;
+      mbar_wait(smem_addr(&S.full[st]), st_phase, p.err, abort_flag);
+      mbar_wait(smem_addr(&S.p_full[g][b]), (i >> 1) & 1, p.err, abort_flag);
+      const int ntok = min(kBlock, L - cur.j * kBlock);
+      const PBuf<G>& pb = S.pb[g][b];
+      const uint32_t pb_addr = smem_addr(&pb);
+      float al[G];
+      lds_floats<G>(pb_addr + offsetof(PBuf<G>, alpha), al);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float2 a2 = make_float2(al[h], al[h]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[h][e] = __fmul2_rn(acc[h][e], a2);
+      }
+      const float* pp = &pb.p[tok_lane][0];
+      if (ntok == kBlock)
+        pv_accumulate<D, G, LPT_PV, ROW, true>(stage + v_off, pp, ntok, tok_lane, acc);
+      else
+        pv_accumulate<D, G, LPT_PV, ROW, false>(stage + v_off, pp, ntok, tok_lane, acc);
+      const bool seq_done = (cur.j + 1 == cur.np);
+      const bool seg_end = seq_done || (i + 1 == n_pages);
+      float m_fin[G], l_fin[G];
+      if (seg_end) {
+        lds_floats<G>(pb_addr + offsetof(PBuf<G>, m), m_fin);
+        lds_floats<G>(pb_addr + offsetof(PBuf<G>, l), l_fin);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_addr(&S.p_empty[g][b]));
+        if (atomicAdd(&S.released[st], 1) == NW - 1) {
+          S.released[st] = 0;
+          if (i + NST < n_pages && !*abort_flag) {
+            fetch_page(p, fc, smem_addr(stage), smem_addr(&S.full[st]));
+            S.last_issued[st] = i + NST;
+          }
+        }
+        fc.next(p);
+      }
+      stage += p.stage_bytes;
+      if (++st == NST) st = 0, st_phase ^= 1, stage = stages;
+      if (seg_end) {
+        // sum over the token lanes of the warp
+#pragma unroll
+        for (int m = LPT_PV; m < 32; m <<= 1)
 #pragma unroll
           for (int h = 0; h < G; ++h)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              dst[h * D + 2 * e] = acc[h][e].x;
-              dst[h * D + 2 * e + 1] = acc[h][e].y;
+              acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, m);
+              acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, m);
             }
-        }
-        __syncthreads();
-        if (sub == 0) {
+        if (tok_lane == 0) {
+          const int tok = __ldg(p.qsl + cur.s);
+          const bool whole = (seg_j0 == 0) && seq_done;
+          const int slot = 2 * c + (cur.s == s_begin ? 0 : 1);
 #pragma unroll
           for (int h = 0; h < G; ++h) {
-            float mm = kNegInf;
-#pragma unroll
-            for (int u = 0; u < NSUB; ++u) mm = fmaxf(mm, S.seg_ml[u * n_kv + g][h][0]);
-            const float mu = (mm == kNegInf) ? 0.f : mm;
-            float ll = 0.f;
-#pragma unroll
-            for (int u = 0; u < NSUB; ++u)
-              ll += S.seg_ml[u * n_kv + g][h][1] * fast_exp2(S.seg_ml[u * n_kv + g][h][0] - mu);
-            const float w0s = fast_exp2(S.seg_ml[g][h][0] - mu);
-            const float2 w0 = make_float2(w0s, w0s);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[h][e] = __fmul2_rn(acc[h][e], w0);
-#pragma unroll
-            for (int u = 1; u < NSUB; ++u) {
-              const float* src = seg_o + ((size_t)((u - 1) * n_kv + g) * G + h) * D + dl * 8;
-              const float w = fast_exp2(S.seg_ml[u * n_kv + g][h][0] - mu);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                acc[h][e].x += src[2 * e] * w;
-                acc[h][e].y += src[2 * e + 1] * w;
+            const int qh = g * G + h;
+            if (whole) {
+              const float inv = 1.f / l_fin[h];
+              uint4 w;
+              w.x = pack_bf16x2(acc[h][0].x * inv, acc[h][0].y * inv);
+              w.y = pack_bf16x2(acc[h][1].x * inv, acc[h][1].y * inv);
+              w.z = pack_bf16x2(acc[h][2].x * inv, acc[h][2].y * inv);
+              w.w = pack_bf16x2(acc[h][3].x * inv, acc[h][3].y * inv);
+              *reinterpret_cast<uint4*>(p.out + ((int64_t)tok * p.n_q + qh) * D + dl * 8) = w;
+            } else {
+              float4* dst = reinterpret_cast<float4*>(
+                  p.part_o + ((int64_t)slot * p.n_q + qh) * D + dl * 8);
+              dst[0] = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
+              dst[1] = make_float4(acc[h][2].x, acc[h][2].y, acc[h][3].x, acc[h][3].y);
+              if (dl == 0) {
+                p.part_ml[((int64_t)slot * p.n_q + qh) * 2 + 0] = m_fin[h];
+                p.part_ml[((int64_t)slot * p.n_q + qh) * 2 + 1] = l_fin[h];
               }
             }
-            m_fin[h] = mm;
-            l_fin[h] = ll;
           }
-        }
-        __syncthreads();
-      } else {
-        // one warp per kv head: gather each head's (m, l) from its lanes
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          m_fin[h] = __shfl_sync(0xffffffffu, m_run, h * REP);
-          l_fin[h] = __shfl_sync(0xffffffffu, l_run, h * REP);
-        }
-      }
-      if (sub == 0 && tok_lane == 0) {
-        const int tok = __ldg(p.qsl + cur.s);
-        const bool whole = (seg_j0 == 0) && seq_done;
-        const int slot = 2 * c + (cur.s == s_begin ? 0 : 1);
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const int qh = g * G + h;
-          if (whole) {
-            const float inv = 1.f / l_fin[h];
-            uint4 w;
-            w.x = pack_bf16x2(acc[h][0].x * inv, acc[h][0].y * inv);
-            w.y = pack_bf16x2(acc[h][1].x * inv, acc[h][1].y * inv);
-            w.z = pack_bf16x2(acc[h][2].x * inv, acc[h][2].y * inv);
-            w.w = pack_bf16x2(acc[h][3].x * inv, acc[h][3].y * inv);
-            *reinterpret_cast<uint4*>(p.out + ((int64_t)tok * p.n_q + qh) * D + dl * 8) = w;
-          } else {
-            float4* dst = reinterpret_cast<float4*>(
-                p.part_o + ((int64_t)slot * p.n_q + qh) * D + dl * 8);
-            dst[0] = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
-            dst[1] = make_float4(acc[h][2].x, acc[h][2].y, acc[h][3].x, acc[h][3].y);
-            if (dl == 0) {
-              p.part_ml[((int64_t)slot * p.n_q + qh) * 2 + 0] = m_fin[h];
-              p.part_ml[((int64_t)slot * p.n_q + qh) * 2 + 1] = l_fin[h];
+          if (g == 0 && lane == 0 && seg_j0 == 0) {
+            // this CTA owns the request's first page: record where its pieces are
+            int c_last = c;
+            if (!seq_done) {
+              const int64_t f_last = f0 + i + (cur.np - 1 - cur.j);
+              const int64_t cl = ((f_last + 1) * C + F - 1) / F - 1;
+              c_last = (int)(cl < C - 1 ? cl : C - 1);
             }
+            p.seq_rec[cur.s] = make_int4(c, c_last, slot, (int)F);
           }
         }
-        if (warp == 0 && lane == 0 && seg_j0 == 0) {
-          // this CTA owns the request's first page: record where its pieces are
-          int c_last = c;
-          if (!seq_done) {
-            const int64_t f_last = f0 + i + (cur.np - 1 - cur.j);
-            const int64_t cl = ((f_last + 1) * C + F - 1) / F - 1;
-            c_last = (int)(cl < C - 1 ? cl : C - 1);
-          }
-          p.seq_rec[cur.s] = make_int4(c, c_last, slot, (int)F);
-        }
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[h][e] = make_float2(0.f, 0.f);
       }
-      if (seq_done && !slice_done) {
-        cur.next(p);
+      const int prev_s = cur.s;
+      cur.next(p);
+      if (seg_end && cur.s != prev_s && i + 1 < n_pages) {
+        L = __ldg(p.seq_lens + cur.s);
         seg_j0 = 0;
-        load_q(cur.s);
-        continue;
       }
     }
-    cur.next(p);
   }
 
   // never hand back shared memory with a copy still landing in it
@@ -505,55 +584,68 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
   }
 }
 
-// Combine the pieces of every decode request that spans several CTAs.
+// Combine the pieces of every decode request that spans several CTAs.  One
+// warp per (request, q head); lanes own 4 consecutive elements of head_dim.
+// Launched as a programmatic dependent of the decode kernel: it may start
+// while the decode grid drains and waits for it before reading partials.
+constexpr int kMergeWarps = 8;
+
 template <int D>
-__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const DecodeParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s = blockIdx.x;
-  const int a = __ldg(p.qsl + s);
+  const int h = blockIdx.y * kMergeWarps + warp;
+  if (h >= p.n_q) return;
   if (decode_pages(p, s, false) == 0) return;  // not a (valid) decode request
   const int4 rec = p.seq_rec[s];
   const int C = p.ctas;
   const int c_first = rec.x, c_last = rec.y, first_slot = rec.z;
   const int64_t F = rec.w;
-  if (c_first == c_last) return;
+  if (c_first == c_last) return;  // written directly by the decode kernel
   if (c_first < 0 || c_last >= C || c_first > c_last || first_slot < 0 || first_slot >= 2 * C ||
       F <= 0) {
-    if (threadIdx.x == 0) flag_error(p.err, DEVERR_BOUNDS);
+    if (lane == 0) flag_error(p.err, DEVERR_BOUNDS);
     return;
   }
-  for (int idx = threadIdx.x; idx < p.n_q * D; idx += blockDim.x) {
-    const int h = idx / D, e = idx % D;
-    float M = kNegInf;
-    for (int cc = c_first; cc <= c_last; ++cc) {
-      if (slice_begin(cc, F, C) == slice_begin(cc + 1, F, C)) continue;
-      const int slot = (cc == c_first) ? first_slot : 2 * cc;
-      M = fmaxf(M, p.part_ml[((int64_t)slot * p.n_q + h) * 2]);
+  float M = kNegInf;
+  for (int cc = c_first; cc <= c_last; ++cc) {
+    if (slice_begin(cc, F, C) == slice_begin(cc + 1, F, C)) continue;
+    const int slot = (cc == c_first) ? first_slot : 2 * cc;
+    M = fmaxf(M, __ldg(p.part_ml + ((int64_t)slot * p.n_q + h) * 2));
+  }
+  const float mu = (M == kNegInf) ? 0.f : M;
+  float Lsum = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  const bool active = lane * 4 < D;
+  for (int cc = c_first; cc <= c_last; ++cc) {
+    if (slice_begin(cc, F, C) == slice_begin(cc + 1, F, C)) continue;
+    const int slot = (cc == c_first) ? first_slot : 2 * cc;
+    const float2 ml = __ldg(reinterpret_cast<const float2*>(p.part_ml) + (int64_t)slot * p.n_q + h);
+    const float w = fast_exp2(ml.x - mu);
+    Lsum += ml.y * w;
+    if (active) {
+      const float4 o = __ldg(reinterpret_cast<const float4*>(
+          p.part_o + ((int64_t)slot * p.n_q + h) * D + lane * 4));
+      O.x += o.x * w;
+      O.y += o.y * w;
+      O.z += o.z * w;
+      O.w += o.w * w;
     }
-    const float mu = (M == kNegInf) ? 0.f : M;
-    float Lsum = 0.f, O = 0.f;
-    for (int cc = c_first; cc <= c_last; ++cc) {
-      if (slice_begin(cc, F, C) == slice_begin(cc + 1, F, C)) continue;
-      const int slot = (cc == c_first) ? first_slot : 2 * cc;
-      const float w = fast_exp2(p.part_ml[((int64_t)slot * p.n_q + h) * 2] - mu);
-      Lsum += p.part_ml[((int64_t)slot * p.n_q + h) * 2 + 1] * w;
-      O += p.part_o[((int64_t)slot * p.n_q + h) * D + e] * w;
-    }
-    p.out[((int64_t)a * p.n_q + h) * D + e] = float_to_bf16_rn(O / Lsum);
+  }
+  if (active) {
+    const float inv = 1.f / Lsum;
+    uint2 w;
+    w.x = pack_bf16x2(O.x * inv, O.y * inv);
+    w.y = pack_bf16x2(O.z * inv, O.w * inv);
+    const int a = __ldg(p.qsl + s);
+    *reinterpret_cast<uint2*>(p.out + ((int64_t)a * p.n_q + h) * D + lane * 4) = w;
   }
 }
-
-template <int D, int G, int NW>
-size_t decode_smem_bytes(int nstages, uint32_t stage_bytes, int n_kv) {
-  const int nsub = NW / n_kv;
-  return (size_t)nstages * stage_bytes + sizeof(DecodeSmem<D, G, NW>) +
-         (size_t)(nsub - 1) * n_kv * G * D * sizeof(float);
-}
-
-constexpr int warps_for_group(int g) { return g <= 4 ? 16 : 8; }
 
 constexpr size_t kSmemBudget = 220 * 1024;
 
-template <int D, int G, int NW, int NSUB>
+template <int D, int G, int NKV>
 cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ctas,
                             cudaStream_t stream) {
   DecodeParams p;
@@ -577,24 +669,39 @@ cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ct
   p.max_seq_len = a.max_seq_len;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.ctas = ctas;
-  p.row_bytes = (uint32_t)a.num_kv_heads * D * 2;
+  p.row_bytes = (uint32_t)NKV * D * 2;
   p.page_bytes = kBlock * p.row_bytes;
   p.stage_bytes = 2 * p.page_bytes;
-  const size_t fixed = decode_smem_bytes<D, G, NW>(0, p.stage_bytes, a.num_kv_heads);
+  const size_t fixed = sizeof(DecodeSmem<G, NKV>);
   int nst = (int)((kSmemBudget - fixed) / p.stage_bytes);
   nst = nst > 8 ? 8 : nst;
   if (nst < 2) return cudaErrorInvalidConfiguration;
   p.nstages = nst;
-  const size_t smem = decode_smem_bytes<D, G, NW>(nst, p.stage_bytes, a.num_kv_heads);
-  auto kern = decode_kernel<D, G, NW, NSUB>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  const size_t smem = (size_t)nst * p.stage_bytes + fixed;
+  auto kern = decode_kernel<D, G, NKV>;
+  static int configured_device = -1;  // one attribute set per process and device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(kSmemBudget + 4096));
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  kern<<<ctas, 2 * NKV * 32, smem, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  kern<<<ctas, NW * 32, smem, stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  decode_merge_kernel<D><<<a.num_seqs, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_seqs, (a.num_q_heads + kMergeWarps - 1) / kMergeWarps, 1);
+  cfg.blockDim = dim3(kMergeWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, p);
 }
 
 }  // namespace
@@ -625,23 +732,17 @@ DecodeWorkspace decode_workspace(void* base, int ctas, int num_seqs, int num_q_h
 bool decode_supported(int head_dim, int group, int num_kv_heads) {
   if (head_dim != 64 && head_dim != 128) return false;
   if (group != 1 && group != 2 && group != 4 && group != 8) return false;
-  if (num_kv_heads != 1 && num_kv_heads != 2 && num_kv_heads != 4 && num_kv_heads != 8)
-    return false;
-  return num_kv_heads * head_dim <= 1024;
+  return num_kv_heads == 1 || num_kv_heads == 2 || num_kv_heads == 4 || num_kv_heads == 8;
 }
 
 template <int D, int G>
 static cudaError_t launch_decode_dg(const AttnArgs& a, const DecodeWorkspace& ws, int ctas,
                                     cudaStream_t stream) {
-  constexpr int NW = warps_for_group(G);
-  switch (NW / a.num_kv_heads) {
-    case 1: return launch_decode_t<D, G, NW, 1>(a, ws, ctas, stream);
-    case 2: return launch_decode_t<D, G, NW, 2>(a, ws, ctas, stream);
-    case 4: return launch_decode_t<D, G, NW, 4>(a, ws, ctas, stream);
-    case 8: return launch_decode_t<D, G, NW, 8>(a, ws, ctas, stream);
-    case 16:
-      if constexpr (NW == 16) return launch_decode_t<D, G, NW, 16>(a, ws, ctas, stream);
-      break;
+  switch (a.num_kv_heads) {
+    case 1: return launch_decode_t<D, G, 1>(a, ws, ctas, stream);
+    case 2: return launch_decode_t<D, G, 2>(a, ws, ctas, stream);
+    case 4: return launch_decode_t<D, G, 4>(a, ws, ctas, stream);
+    case 8: return launch_decode_t<D, G, 8>(a, ws, ctas, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -133,9 +133,10 @@ def test_invalid_block_id_is_flagged():
 def test_seq_len_beyond_table_is_flagged():
     b = _decode([40, 40], seed=11)
     d = W.to_device(b, "cuda")
-    d.seq_lens[1] = 16 * b.block_tables.shape[1] + 1
+    d.seq_lens[1] = 16 * b.block_tables.shape[1] + 1  # one past what the table can hold
     ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens,
-                        d.query_start_loc, b.scale, max_q_len=1, max_seq_len=10000)
+                        d.query_start_loc, b.scale, max_q_len=1,
+                        max_seq_len=16 * b.block_tables.shape[1])
     with pytest.raises(ops.PagedAttnError) as ei:
         ops.check_device_errors()
     assert ei.value.code == 4
