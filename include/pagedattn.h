@@ -154,6 +154,33 @@ int pa_copy_blocks(pa_bf16 *k_cache, pa_bf16 *v_cache, int32_t num_blocks, int32
  */
 int pa_check_device_errors(cudaStream_t stream);
 
+/*
+ * Allocation-free form of pa_paged_attention.  The pages have no counterpart
+ * for it; it exists for callers that cannot allocate device memory where they
+ * run attention: code running while a stream is captured into a CUDA graph,
+ * plugins whose host owns all device memory, serving loops that must not
+ * allocate after start-up.
+ *
+ * Same arguments, layout and results as pa_paged_attention, minus the
+ * workspace: scratch comes from an array built into the library
+ * (pa_noalloc_scratch_bytes() bytes, 8 MiB, held on every device that loads
+ * the library until the process exits).  A call needing more scratch than
+ * that (see pa_workspace_size) returns PA_ERR_WORKSPACE.  Allocates nothing.
+ * The first call on a device looks up the array's device address (make it
+ * before any stream capture).  Calls share the array, so calls whose
+ * executions overlap on the GPU race and must be serialised by the caller.
+ */
+size_t pa_noalloc_scratch_bytes(void);
+
+int pa_paged_attention_noalloc(const pa_bf16 *q, const pa_bf16 *k_cache,
+                               const pa_bf16 *v_cache, int32_t num_blocks, int32_t block_size,
+                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                               const int32_t *block_tables, int32_t max_blocks,
+                               const int32_t *seq_lens, const int32_t *query_start_loc,
+                               int32_t num_seqs, int32_t num_tokens, int32_t max_q_len,
+                               int32_t max_seq_len, float scale, pa_bf16 *out,
+                               cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -243,3 +243,79 @@ int pa_check_device_errors(cudaStream_t stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of pa_paged_attention.
+//
+// Some callers cannot call cudaMalloc (or any allocating routine) at the
+// point where they run attention: code that executes while a stream is being
+// captured into a CUDA graph, plugins whose host application owns every
+// device allocation and only hands out pointers, or latency-critical serving
+// loops that forbid allocation after start-up.  For them this entry point
+// uses a fixed scratch array that lives in the library itself instead of a
+// caller-provided workspace.  The array is a file-scope __device__ object, so
+// every GPU that loads the library holds it until the process exits.
+//
+// Its device address is looked up once per device, on the first call made on
+// that device (with the device current); make that first call before any
+// stream capture begins.  All calls share the array and it keeps whatever the
+// last call left there: nothing in it needs to start at zero, but calls whose
+// executions overlap on the GPU (different streams, or different threads on
+// one device) race on it and must be serialised by the caller.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char g_pa_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PA_ERR_UNSUPPORTED, "device id %d", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_pa_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pa_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+int pa_paged_attention_noalloc(const pa_bf16* q, const pa_bf16* k_cache,
+                               const pa_bf16* v_cache, int32_t num_blocks, int32_t block_size,
+                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                               const int32_t* block_tables, int32_t max_blocks,
+                               const int32_t* seq_lens, const int32_t* query_start_loc,
+                               int32_t num_seqs, int32_t num_tokens, int32_t max_q_len,
+                               int32_t max_seq_len, float scale, pa_bf16* out,
+                               cudaStream_t stream) {
+  const size_t need = pa_workspace_size(num_seqs, num_tokens, num_q_heads, num_kv_heads,
+                                        head_dim, max_q_len, max_seq_len);
+  if (need == 0)
+    return fail(PA_ERR_INVALID_ARG, "invalid sizes, or no CUDA device for the scratch size");
+  if (need > kNoAllocScratchBytes)
+    return fail(PA_ERR_WORKSPACE,
+                "this call needs %zu bytes of scratch, more than the %zu-byte built-in array "
+                "of the allocation-free entry point; use pa_paged_attention with a workspace",
+                need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  int st = noalloc_scratch(&scratch);
+  if (st) return st;
+  return pa_paged_attention(q, k_cache, v_cache, num_blocks, block_size, num_q_heads,
+                            num_kv_heads, head_dim, block_tables, max_blocks, seq_lens,
+                            query_start_loc, num_seqs, num_tokens, max_q_len, max_seq_len, scale,
+                            out, scratch, kNoAllocScratchBytes, stream);
+}
+
+}  // extern "C"
