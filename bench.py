@@ -129,6 +129,98 @@ def _launch_count(b) -> int:
     return n
 
 
+def _time_steps(b, d, ws, out, steps, warmup, stream, ops):
+    """Device-resident steps (scatter + attention); returns per-step and
+    per-attention-call milliseconds (CUDA events on the launching stream)."""
+    import torch
+
+    def step(ev=None):
+        if d.copy_pairs.numel():
+            ops.copy_blocks(d.k_cache, d.v_cache, d.copy_pairs)
+        ops.reshape_and_cache(d.k_new, d.v_new, d.k_cache, d.v_cache, d.slot_mapping)
+        if ev is not None:
+            ev[0].record(stream)
+        ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens,
+                            d.query_start_loc, b.scale, max_q_len=b.max_q_len,
+                            max_seq_len=b.max_seq_len, out=out, workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(warmup):
+        step()
+    ops.check_device_errors()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ops.check_device_errors()
+    return (t0.elapsed_time(t1) / steps,
+            statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs))
+
+
+def _prefill_only(b, d):
+    """The requests of b with q_len >= 2, as their own batch (same device
+    K/V cache and q rows)."""
+    import torch
+    from paged_kv_cache_174_gb300 import workloads as W
+    idx = [s for s in range(b.num_seqs) if b.q_lens[s] >= 2]
+    if not idx:
+        return None
+    rows = np.concatenate([np.arange(b.query_start_loc[s], b.query_start_loc[s + 1])
+                           for s in idx])
+    ql = b.q_lens[idx]
+    qsl = np.zeros(len(idx) + 1, np.int32)
+    qsl[1:] = np.cumsum(ql)
+    sub = W.PagedBatch(name=b.name + "/prefill", q=b.q[rows], k_new=b.k_new[rows],
+                       v_new=b.v_new[rows], k_cache=b.k_cache[:1], v_cache=b.v_cache[:1],
+                       block_tables=b.block_tables[idx], seq_lens=b.seq_lens[idx],
+                       query_start_loc=qsl, slot_mapping=b.slot_mapping[rows], scale=b.scale,
+                       block_size=b.block_size, seed=b.seed)
+    dev = d.q.device
+    rows_t = torch.from_numpy(rows).to(dev)
+    return sub, dict(q=d.q.index_select(0, rows_t).contiguous(),
+                     block_tables=W.int32_tensor(sub.block_tables, dev),
+                     seq_lens=W.int32_tensor(sub.seq_lens, dev),
+                     query_start_loc=W.int32_tensor(qsl, dev))
+
+
+def _time_prefill(b, d, steps, warmup, stream, ops):
+    import torch
+    from paged_kv_cache_174_gb300 import workloads as W
+    po = _prefill_only(b, d)
+    if po is None:
+        return None
+    sub, t = po
+    out = torch.empty_like(t["q"])
+    ws = ops.alloc_workspace(sub.num_seqs, sub.num_tokens, sub.num_q_heads, sub.num_kv_heads,
+                             sub.head_dim, sub.max_q_len, sub.max_seq_len, d.q.device)
+
+    def call():
+        ops.paged_attention(t["q"], d.k_cache, d.v_cache, t["block_tables"], t["seq_lens"],
+                            t["query_start_loc"], sub.scale, max_q_len=sub.max_q_len,
+                            max_seq_len=sub.max_seq_len, out=out, workspace=ws)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ops.check_device_errors()
+    ms = e0.elapsed_time(e1) / steps
+    flops = W.causal_flops(sub)
+    return {"ms": round(ms, 5), "flops": flops, "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+            "tokens": sub.num_tokens}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -142,58 +234,27 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks = _peaks()
+    stream = torch.cuda.current_stream(dev)
 
     b = _make(args.workload, rank)
     d = W.to_device(b, dev)
     alg = W.algorithmic_bytes(b)
-    flops = W.causal_flops(b)
     step_bytes = alg["total"]
     ws = ops.alloc_workspace(b.num_seqs, b.num_tokens, b.num_q_heads, b.num_kv_heads,
                              b.head_dim, b.max_q_len, b.max_seq_len, dev)
     out = torch.empty_like(d.q)
-    stream = torch.cuda.current_stream(dev)
 
-    def step():
-        if d.copy_pairs.numel():
-            ops.copy_blocks(d.k_cache, d.v_cache, d.copy_pairs)
-        ops.reshape_and_cache(d.k_new, d.v_new, d.k_cache, d.v_cache, d.slot_mapping)
-        ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens,
-                            d.query_start_loc, b.scale, max_q_len=b.max_q_len,
-                            max_seq_len=b.max_seq_len, out=out, workspace=ws)
-
-    for _ in range(args.warmup):
-        step()
-    ops.check_device_errors()
-    torch.cuda.synchronize()
-
-    # ---- device-resident timed region
-    ev_attn = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # ---- device-resident timed region (clocks sampled meanwhile)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    t0.record(stream)
-    for i in range(args.steps):
-        if d.copy_pairs.numel():
-            ops.copy_blocks(d.k_cache, d.v_cache, d.copy_pairs)
-        ops.reshape_and_cache(d.k_new, d.v_new, d.k_cache, d.v_cache, d.slot_mapping)
-        ev_attn[i][0].record(stream)
-        ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens,
-                            d.query_start_loc, b.scale, max_q_len=b.max_q_len,
-                            max_seq_len=b.max_seq_len, out=out, workspace=ws)
-        ev_attn[i][1].record(stream)
-    t1.record(stream)
-    torch.cuda.synchronize()
+    ms, attn_ms = _time_steps(b, d, ws, out, args.steps, args.warmup, stream, ops)
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    ops.check_device_errors()
-    ms = t0.elapsed_time(t1) / args.steps
-    attn_ms = statistics.mean(a.elapsed_time(e) for a, e in ev_attn)
     if world > 1:
         tt = torch.tensor([ms, attn_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -241,7 +302,6 @@ def run_ours(args):
 
     gbs = step_bytes * world / (ms * 1e-3) / 1e9
     attn_gbs = alg["attention"] / (attn_ms * 1e-3) / 1e9
-    tokens_per_s = b.num_tokens * world / (ms * 1e-3)
     line = {
         "metric": METRIC,
         "value": round(gbs, 1),
@@ -261,12 +321,12 @@ def run_ours(args):
                    "algorithmic_bytes_per_step": step_bytes,
                    "l2": "inputs larger than L2 (KV read per step >> 129 MB); no flush",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "tokens_per_s": round(tokens_per_s, 1),
+        "tokens_per_s": round(b.num_tokens * world / (ms * 1e-3), 1),
         "pct_of_hbm_peak": round(100.0 * gbs / world / peaks["hbm_gbs"], 2),
         "roofline": {"bound": "hbm", "kernel": "pa_paged_attention (split-KV decode + merge)",
                      "achieved": round(attn_gbs, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(attn_gbs / peaks["hbm_gbs"], 4),
-                     "peak_source": peaks["source"], "traffic": None,
+                     "peak_source": peaks["source"] + " (hbm_gbs)", "traffic": None,
                      "algorithmic_bytes_per_launch": alg["attention"],
                      "avg_launch_ms": round(attn_ms, 5)},
         "e2e": {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
@@ -275,8 +335,28 @@ def run_ours(args):
         "gpu_launches": _launch_count(b) * args.steps,
         "clocks": clk,
     }
-    if flops:
-        line["prefill_tflops"] = round(flops / (attn_ms * 1e-3) / 1e12, 2)
+    # ---- the mixed chunked-prefill step (second half of the metric)
+    if not args.no_mixed and args.workload != "mixed_step":
+        mb = _make("mixed_step", rank)
+        md = W.to_device(mb, dev)
+        mws = ops.alloc_workspace(mb.num_seqs, mb.num_tokens, mb.num_q_heads, mb.num_kv_heads,
+                                  mb.head_dim, mb.max_q_len, mb.max_seq_len, dev)
+        mout = torch.empty_like(md.q)
+        mms, mattn = _time_steps(mb, md, mws, mout, args.steps, args.warmup, stream, ops)
+        pre = _time_prefill(mb, md, args.steps, args.warmup, stream, ops)
+        line["mixed_batch"] = {
+            "workload": mb.name, "description": W.WORKLOADS[mb.name].description,
+            "tokens_per_s": round(mb.num_tokens * world / (mms * 1e-3), 1),
+            "ms_per_step": round(mms, 5), "attention_ms": round(mattn, 5),
+            "gpu_launches": _launch_count(mb) * args.steps}
+        if pre:
+            line["roofline_prefill"] = {
+                "bound": "tensor", "kernel": "prefill chunk alone (tcgen05)",
+                "achieved": pre["tflops"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(pre["tflops"] / peaks["bf16_tflops"], 4),
+                "peak_source": peaks["source"] + " (bf16_tflops, burst)", "traffic": None,
+                "algorithmic_flops_per_launch": pre["flops"], "avg_launch_ms": pre["ms"]}
+        del md, mws, mout
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(b, args.cpu_seconds)
     if world > 1:
@@ -374,6 +454,8 @@ def main():
                     choices=["tiny_decode", "decode_batch", "long_decode", "mixed_step"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-mixed", action="store_true",
+                    help="skip the mixed chunked-prefill step measurement")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -257,7 +257,6 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
   // PV lanes: 8 elements (16 bytes) each
   constexpr int LPT_PV = D / 8;
   constexpr int TPI_PV = 32 / LPT_PV;
-  constexpr int NIT_PV = kBlock / TPI_PV;
   constexpr uint32_t ROW = NKV * D * 2;  // bytes of one token row in a page
   static_assert(LPT_QK >= G && LPT_QK % G == 0, "group too large for the lane split");
 

@@ -1,0 +1,95 @@
+"""Chunked-prefill attention (q_len >= 2) on the tcgen05 path against the
+fp64 oracle: the mixed chunked-prefill step and edge cases."""
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_174_gb300 import ops
+from paged_kv_cache_174_gb300 import workloads as W
+
+from gpu_util import assert_attn_close, run_gpu_step, run_oracle_step, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def test_mixed_step_workload():
+    b = W.mixed_step()
+    d, out = run_gpu_step(b)
+    kc, vc, ref = run_oracle_step(b)
+    assert np.array_equal(W.bits_of(d.k_cache), kc), "scatter not bit-exact"
+    assert np.array_equal(W.bits_of(d.v_cache), vc), "scatter not bit-exact"
+    got = to_f64(out)
+    assert_attn_close(got, ref, "mixed step (all rows)")
+    chunk = slice(b.query_start_loc[-2], b.query_start_loc[-1])
+    assert_attn_close(got[chunk], ref[chunk], "mixed step (prefill chunk rows)")
+
+
+def _batch(lens, q_lens, nq=32, nkv=8, d=128, seed=0, extra_blocks=9):
+    nb = sum(-(-L // 16) for L in lens) + extra_blocks
+    return W.make_batch("prefill-edge", lens, q_lens, num_q_heads=nq, num_kv_heads=nkv,
+                        head_dim=d, block_size=16, num_blocks=nb, seed=seed)
+
+
+@pytest.mark.parametrize("lens,q_lens,nq,nkv,d", [
+    ([2], [2], 32, 8, 128),                       # smallest prefill
+    ([37], [37], 32, 8, 128),                     # fresh prompt, one ragged tile
+    ([300], [77], 32, 8, 128),                    # chunk at an offset, ragged tiles
+    ([128, 129, 255, 256, 257], [128, 2, 100, 33, 257], 32, 8, 128),  # tile edges
+    ([1000, 50, 700], [512, 1, 40], 32, 8, 128),  # prefill + decode mixed
+    ([513], [513], 8, 8, 128),                    # group 1: 128 tokens per tile
+    ([400, 90], [131, 90], 16, 8, 128),           # group 2
+    ([600], [200], 64, 8, 128),                   # group 8: 16 tokens per tile
+    ([333, 41], [150, 41], 8, 2, 64),             # head_dim 64
+    ([250], [250], 4, 1, 64),                     # multi-query, head_dim 64
+])
+def test_prefill_edge_shapes(lens, q_lens, nq, nkv, d):
+    b = _batch(lens, q_lens, nq, nkv, d, seed=sum(lens) % 97)
+    _, out = run_gpu_step(b)
+    _, _, ref = run_oracle_step(b)
+    assert_attn_close(to_f64(out), ref, f"lens={lens} q_lens={q_lens} nq={nq} nkv={nkv} d={d}")
+
+
+def test_many_prefill_requests():
+    rng = np.random.default_rng(5)
+    lens = list(rng.integers(2, 600, size=40))
+    q_lens = [int(rng.integers(2, L + 1)) for L in lens]
+    b = _batch(lens, q_lens, seed=11)
+    _, out = run_gpu_step(b)
+    _, _, ref = run_oracle_step(b)
+    assert_attn_close(to_f64(out), ref, "40 prefill requests")
+
+
+def test_prefill_physical_permutation_gives_identical_bits():
+    b = _batch([700, 260], [300, 260], seed=6, extra_blocks=40)
+    _, out1 = run_gpu_step(b)
+    pi = np.random.default_rng(3).permutation(b.num_blocks).astype(np.int32)
+    b2 = W.PagedBatch(**{**b.__dict__})
+    b2.k_cache = np.empty_like(b.k_cache)
+    b2.v_cache = np.empty_like(b.v_cache)
+    b2.k_cache[pi] = b.k_cache
+    b2.v_cache[pi] = b.v_cache
+    b2.block_tables = np.where(b.block_tables >= 0, pi[np.maximum(b.block_tables, 0)],
+                               -1).astype(np.int32)
+    b2.slot_mapping = (pi[b.slot_mapping // 16] * 16 + b.slot_mapping % 16).astype(np.int32)
+    _, out2 = run_gpu_step(b2)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def test_prefill_chunk_equals_rows_of_full_prompt():
+    """Chunked prefill: the last 64 rows computed as a chunk at offset 256
+    equal those rows of the whole 320-token prompt computed at once."""
+    full = _batch([320], [320], seed=8)
+    _, out_full = run_gpu_step(full)
+    chunk = W.PagedBatch(**{**full.__dict__})
+    chunk.q = full.q[256:]
+    chunk.k_new = full.k_new[256:]
+    chunk.v_new = full.v_new[256:]
+    chunk.slot_mapping = full.slot_mapping[256:]
+    chunk.query_start_loc = np.array([0, 64], np.int32)
+    # the cache already holds positions 0..255 (written by the full step's scatter)
+    kc, vc, _ = run_oracle_step(full, attention=False)
+    chunk.k_cache, chunk.v_cache = kc, vc
+    _, out_chunk = run_gpu_step(chunk)
+    a = to_f64(out_full)[256:]
+    c = to_f64(out_chunk)
+    assert_attn_close(c, a, "chunk vs full prompt")
