@@ -12,9 +12,10 @@
 //  * An item is (request, tile of 128/G query tokens, kv head g).  Its 128 MMA
 //    rows are the tile's tokens x the G q heads that share kv head g, so every
 //    K/V tile is loaded once for the whole GQA group.
-//  * Warp 0 streams Q and K/V tiles of 128 keys (8 pages of 16 tokens, one
-//    TMA box per page and 64-element half of head_dim, 128-byte swizzle) into
-//    a ring of shared-memory stages.
+//  * Warp 0 streams Q and K tiles, warp 6 V tiles, of 128 keys (8 pages of 16
+//    tokens, one TMA box per page and 64-element half of head_dim, 128-byte
+//    swizzle) into rings of shared-memory stages; separate K and V producers
+//    let the next K tiles load while the V of earlier tiles is still in use.
 //  * Warp 1 (one thread) issues tcgen05.mma: S = Q K^T into one of two TMEM
 //    buffers, then O += P V into a TMEM accumulator.
 //  * Warps 2-5 own one MMA row each: they read S from TMEM, apply the causal
@@ -36,10 +37,11 @@ namespace {
 constexpr int kBlock = 16;        // tokens per physical block
 constexpr int kKeysPerTile = 128; // keys per K/V tile (8 blocks)
 constexpr int kRows = 128;        // MMA rows (tokens x group heads)
-constexpr int kStages = 2;        // K and V stages each
+constexpr int kStagesK = 2;       // K tile stages
+constexpr int kStagesV = 2;       // V tile stages
 constexpr float kNegInf = -INFINITY;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;  // K/Q producer, MMA, 4 softmax, V producer
 
 struct PrefillParams {
   const int32_t* block_tables;
@@ -109,8 +111,8 @@ struct ItemCursor {
 
 struct PrefillBarriers {
   uint64_t q_full, q_empty;
-  uint64_t k_full[kStages], k_empty[kStages];
-  uint64_t v_full[kStages], v_empty[kStages];
+  uint64_t k_full[kStagesK], k_empty[kStagesK];
+  uint64_t v_full[kStagesV], v_empty[kStagesV];
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full[2], pv_done[2];
   uint64_t o_full, o_empty;
@@ -136,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t HALF = kRows * 128;  // bytes of one [128 rows][64] block
   constexpr uint32_t Q_BYTES = NH * HALF;
   constexpr uint32_t KV_BYTES = NH * HALF;  // 128 keys
-  constexpr uint32_t P_BYTES = 2 * HALF;    // 128 rows x 128 keys
+  constexpr uint32_t P_BYTES = 2 * HALF;    // 128 rows x 128 keys (two buffers)
   constexpr uint32_t TMEM_COLS = 512;
   constexpr uint32_t S_COL0 = 0, O_COL = 256;
   constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(kRows, kKeysPerTile, 0, 0);
@@ -147,8 +149,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   unsigned char* q_s = base;
   unsigned char* k_s = q_s + Q_BYTES;
-  unsigned char* v_s = k_s + kStages * KV_BYTES;
-  unsigned char* p_s = v_s + kStages * KV_BYTES;
+  unsigned char* v_s = k_s + kStagesK * KV_BYTES;
+  unsigned char* p_s = v_s + kStagesV * KV_BYTES;
   PrefillBarriers& B = *reinterpret_cast<PrefillBarriers*>(p_s + 2 * P_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -158,15 +160,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(smem_addr(&B.q_full), 1);
     mbar_init(smem_addr(&B.q_empty), 1);
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kStagesK; ++i) {
       mbar_init(smem_addr(&B.k_full[i]), 1);
       mbar_init(smem_addr(&B.k_empty[i]), 1);
+    }
+    for (int i = 0; i < kStagesV; ++i) {
       mbar_init(smem_addr(&B.v_full[i]), 1);
       mbar_init(smem_addr(&B.v_empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&B.s_full[i]), 1);
       mbar_init(smem_addr(&B.s_empty[i]), 4);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&B.p_full[i]), 4);
       mbar_init(smem_addr(&B.pv_done[i]), 1);
     }
@@ -190,25 +196,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long total_items = B.total_items;
   volatile int* abort_flag = &B.abort_flag;
 
-  if (warp == 0) {
-    // ============================================================ producer
+  if (warp == 0 || warp == 6) {
+    // ============================================================ producers
     if (lane == 0) {
+      const bool is_k = (warp == 0);  // warp 0: Q and K, warp 6: V
+      const CUtensorMap* map = is_k ? &kmap : &vmap;
+      unsigned char* ring = is_k ? k_s : v_s;
+      uint64_t* full = is_k ? B.k_full : B.v_full;
+      uint64_t* empty = is_k ? B.k_empty : B.v_empty;
+      const int nst = is_k ? kStagesK : kStagesV;
       ItemCursor<TM> cur;
       cur.init(p);
-      int n_item = 0, kc = 0, vc = 0;
+      int n_item = 0, c = 0;
       for (long long item = blockIdx.x; item < total_items; item += gridDim.x, ++n_item) {
         Item it;
         if (!cur.locate(p, item, it)) break;
-        if (n_item > 0) mbar_wait(smem_addr(&B.q_empty), (n_item - 1) & 1, p.err, abort_flag);
-        if (*abort_flag) break;
-        mbar_arrive_expect_tx(smem_addr(&B.q_full), Q_BYTES);
+        if (is_k) {
+          if (n_item > 0) mbar_wait(smem_addr(&B.q_empty), (n_item - 1) & 1, p.err, abort_flag);
+          mbar_arrive_expect_tx(smem_addr(&B.q_full), Q_BYTES);
 #pragma unroll
-        for (int h = 0; h < NH; ++h)
-          tc::tma_load_3d(smem_addr(q_s + h * HALF), &qmap, h * 64, it.g * G, it.q0,
-                          smem_addr(&B.q_full));
+          for (int h = 0; h < NH; ++h)
+            tc::tma_load_3d(smem_addr(q_s + h * HALF), &qmap, h * 64, it.g * G, it.q0,
+                            smem_addr(&B.q_full));
+        }
         const int pages = (it.kv_end + kBlock - 1) / kBlock;
         const int32_t* table = p.block_tables + (int64_t)it.s * p.max_blocks;
-        for (int kt = 0; kt < it.nkt; ++kt) {
+        for (int kt = 0; kt < it.nkt; ++kt, ++c) {
           const int p0 = kt * (kKeysPerTile / kBlock);
           const int npg = min(kKeysPerTile / kBlock, pages - p0);
           int phys[kKeysPerTile / kBlock];
@@ -222,47 +235,24 @@ __global__ void __launch_bounds__(kThreads, 1)
               ++nvalid;
             }
           }
-          const uint32_t bytes = (uint32_t)nvalid * NH * (kBlock * 128);
-          // K
-          {
-            const int st = kc % kStages;
-            if (kc >= kStages)
-              mbar_wait(smem_addr(&B.k_empty[st]), ((kc / kStages) - 1) & 1, p.err, abort_flag);
-            mbar_arrive_expect_tx(smem_addr(&B.k_full[st]), bytes);
-            for (int i = 0; i < npg; ++i) {
-              if (phys[i] < 0) continue;
+          const int st = c % nst;
+          if (c >= nst)
+            mbar_wait(smem_addr(&empty[st]), ((c / nst) - 1) & 1, p.err, abort_flag);
+          mbar_arrive_expect_tx(smem_addr(&full[st]),
+                                (uint32_t)nvalid * NH * (kBlock * 128));
+          for (int i = 0; i < npg; ++i) {
+            if (phys[i] < 0) continue;
 #pragma unroll
-              for (int h = 0; h < NH; ++h)
-                tc::tma_load_3d(smem_addr(k_s + st * KV_BYTES + h * HALF + i * (kBlock * 128)),
-                                &kmap, h * 64, it.g, phys[i] * kBlock,
-                                smem_addr(&B.k_full[st]));
-            }
-            ++kc;
-          }
-          // V
-          {
-            const int st = vc % kStages;
-            if (vc >= kStages)
-              mbar_wait(smem_addr(&B.v_empty[st]), ((vc / kStages) - 1) & 1, p.err, abort_flag);
-            mbar_arrive_expect_tx(smem_addr(&B.v_full[st]), bytes);
-            for (int i = 0; i < npg; ++i) {
-              if (phys[i] < 0) continue;
-#pragma unroll
-              for (int h = 0; h < NH; ++h)
-                tc::tma_load_3d(smem_addr(v_s + st * KV_BYTES + h * HALF + i * (kBlock * 128)),
-                                &vmap, h * 64, it.g, phys[i] * kBlock,
-                                smem_addr(&B.v_full[st]));
-            }
-            ++vc;
+            for (int h = 0; h < NH; ++h)
+              tc::tma_load_3d(smem_addr(ring + st * KV_BYTES + h * HALF + i * (kBlock * 128)),
+                              map, h * 64, it.g, phys[i] * kBlock, smem_addr(&full[st]));
           }
         }
       }
       // never hand back shared memory with a TMA copy still landing in it
-      for (int i = max(0, kc - kStages); i < kc; ++i)
-        mbar_wait(smem_addr(&B.k_full[i % kStages]), (i / kStages) & 1, p.err, abort_flag);
-      for (int i = max(0, vc - kStages); i < vc; ++i)
-        mbar_wait(smem_addr(&B.v_full[i % kStages]), (i / kStages) & 1, p.err, abort_flag);
-      if (n_item > 0)
+      for (int i = max(0, c - nst); i < c; ++i)
+        mbar_wait(smem_addr(&full[i % nst]), (i / nst) & 1, p.err, abort_flag);
+      if (is_k && n_item > 0)
         mbar_wait(smem_addr(&B.q_full), (n_item - 1) & 1, p.err, abort_flag);
     }
   } else if (warp == 1) {
@@ -281,30 +271,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto issue_pv = [&](long long t, bool first) {
           const int b = (int)(t & 1);
           mbar_wait(smem_addr(&B.p_full[b]), (int)((t >> 1) & 1), p.err, abort_flag);
-          mbar_wait(smem_addr(&B.v_full[t % kStages]), (int)((t / kStages) & 1), p.err,
+          mbar_wait(smem_addr(&B.v_full[t % kStagesV]), (int)((t / kStagesV) & 1), p.err,
                     abort_flag);
           if (first && n_item > 0)
             mbar_wait(smem_addr(&B.o_empty), (n_item - 1) & 1, p.err, abort_flag);
           tc::fence_after_sync();
           const uint32_t pa = smem_addr(p_s + b * P_BYTES);
-          const uint32_t va = smem_addr(v_s + (t % kStages) * KV_BYTES);
+          const uint32_t va = smem_addr(v_s + (t % kStagesV) * KV_BYTES);
 #pragma unroll
           for (int kk = 0; kk < kKeysPerTile / 16; ++kk) {
             const uint64_t ad = tc::sw128_desc(pa + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024);
             const uint64_t bd = tc::sw128_desc(va + kk * 2048, HALF, 1024);
             tc::mma_bf16(tmem + O_COL, ad, bd, IDESC_O, (first && kk == 0) ? 0u : 1u);
           }
-          tc::commit(smem_addr(&B.v_empty[t % kStages]));
+          tc::commit(smem_addr(&B.v_empty[t % kStagesV]));
           tc::commit(smem_addr(&B.pv_done[b]));
         };
         for (int kt = 0; kt < it.nkt; ++kt, ++T) {
           const int sb = (int)(T & 1);
-          mbar_wait(smem_addr(&B.k_full[T % kStages]), (int)((T / kStages) & 1), p.err,
+          mbar_wait(smem_addr(&B.k_full[T % kStagesK]), (int)((T / kStagesK) & 1), p.err,
                     abort_flag);
           if (T >= 2)
             mbar_wait(smem_addr(&B.s_empty[sb]), (int)(((T - 2) >> 1) & 1), p.err, abort_flag);
           tc::fence_after_sync();
-          const uint32_t ka = smem_addr(k_s + (T % kStages) * KV_BYTES);
+          const uint32_t ka = smem_addr(k_s + (T % kStagesK) * KV_BYTES);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t ad =
@@ -313,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_bf16(tmem + S_COL0 + sb * kKeysPerTile, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
           }
           tc::commit(smem_addr(&B.s_full[sb]));
-          tc::commit(smem_addr(&B.k_empty[T % kStages]));
+          tc::commit(smem_addr(&B.k_empty[T % kStagesK]));
           if (kt == it.nkt - 1) tc::commit(smem_addr(&B.q_empty));
           if (kt > 0) issue_pv(T - 1, kt == 1);
           issued = true;
@@ -356,16 +346,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&B.s_empty[sb]));
 
-        // causal mask + scale (base 2), tile max
+        // causal mask, tile max (8 independent chains).  With a positive
+        // scale the max of the raw scores gives the max of the scaled ones,
+        // and the scale folds into the exponent's FMA below.
         const int k0 = kt * kKeysPerTile;
         const int lim = p_row - k0;  // keys c <= lim are visible
-        float mx = kNegInf;
+        const float sl2 = p.scale_log2;
+        const bool pos_scale = sl2 > 0.f;
+        const float mul = pos_scale ? 1.f : sl2;  // applied now; sl2 is applied in the exp
+        const float emul = pos_scale ? sl2 : 1.f;
+        float m8[8];
 #pragma unroll
-        for (int c = 0; c < kKeysPerTile; ++c) {
-          const float s = (c <= lim) ? __uint_as_float(sr[c]) * p.scale_log2 : kNegInf;
-          sr[c] = __float_as_uint(s);
-          mx = fmaxf(mx, s);
+        for (int j = 0; j < 8; ++j) m8[j] = kNegInf;
+        if (__all_sync(0xffffffffu, lim >= kKeysPerTile - 1)) {
+          if (!pos_scale) {
+#pragma unroll
+            for (int c = 0; c < kKeysPerTile; ++c)
+              sr[c] = __float_as_uint(__uint_as_float(sr[c]) * mul);
+          }
+#pragma unroll
+          for (int c = 0; c < kKeysPerTile; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sr[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < kKeysPerTile; ++c) {
+            const float s = (c <= lim) ? __uint_as_float(sr[c]) * mul : kNegInf;
+            sr[c] = __float_as_uint(s);
+            m8[c & 7] = fmaxf(m8[c & 7], s);
+          }
         }
+        float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        mx = (mx == kNegInf) ? kNegInf : mx * emul;  // now in scaled base-2 units
         float alpha = 1.f;
         if (m_ref == kNegInf) {
           m_ref = mx;  // first tile: O not yet written
@@ -378,7 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (T >= 2)
           mbar_wait(smem_addr(&B.pv_done[sb]), (int)(((T - 2) >> 1) & 1), p.err, abort_flag);
         unsigned char* pb = p_s + sb * P_BYTES;
-        float lsum = 0.f;
+        // p = 2^(emul * s - m_ref)
+        const float nm = -m_ref;
+        float l8[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) l8[j] = 0.f;
 #pragma unroll
         for (int kh = 0; kh < 2; ++kh) {
 #pragma unroll
@@ -387,16 +402,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int c = kh * 64 + c8 * 8 + 2 * e;
-              const float p0 = fast_exp2(__uint_as_float(sr[c]) - m_ref);
-              const float p1 = fast_exp2(__uint_as_float(sr[c + 1]) - m_ref);
-              lsum += p0 + p1;
+              const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), emul, nm));
+              const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), emul, nm));
+              l8[(2 * e) & 7] += p0;
+              l8[(2 * e + 1) & 7] += p1;
               w[e] = pack_bf16x2(p0, p1);
             }
             *reinterpret_cast<uint4*>(pb + kh * HALF + sw128_chunk(r, c8)) =
                 make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
-        l += lsum;
+        l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
         // rescale the running output when the reference max moved (rare)
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
           mbar_wait(smem_addr(&B.pv_done[(T - 1) & 1]), (int)(((T - 1) >> 1) & 1), p.err,
@@ -417,10 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // poisoned data; zero them so that P = 0 times V stays 0
         const int kv_local = it.kv_end - k0;
         if (kv_local < kKeysPerTile) {
-          mbar_wait(smem_addr(&B.v_full[T % kStages]), (int)((T / kStages) & 1), p.err,
+          mbar_wait(smem_addr(&B.v_full[T % kStagesV]), (int)((T / kStagesV) & 1), p.err,
                     abort_flag);
           if (r >= kv_local) {
-            unsigned char* vrow = v_s + (T % kStages) * KV_BYTES;
+            unsigned char* vrow = v_s + (T % kStagesV) * KV_BYTES;
 #pragma unroll
             for (int h = 0; h < NH; ++h)
 #pragma unroll
@@ -510,7 +526,7 @@ cudaError_t make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t m
 template <int D, int G>
 size_t prefill_smem_bytes() {
   constexpr size_t half = kRows * 128;
-  return 1024 + (size_t)(D / 64) * half * (1 + 2 * kStages) + 2 * 2 * half +
+  return 1024 + (size_t)(D / 64) * half * (1 + kStagesK + kStagesV) + 2 * 2 * half +
          sizeof(PrefillBarriers);
 }
 
