@@ -221,6 +221,88 @@ def _time_prefill(b, d, steps, warmup, stream, ops):
             "tokens": sub.num_tokens}
 
 
+def _run_trace(dev, stream, ops, warmup):
+    """The continuous-batching trace: every step's CoW copies, scatter and
+    attention timed with CUDA events (schedule precomputed on the host,
+    inputs generated on the device before each step's events)."""
+    import torch
+    from paged_kv_cache_174_gb300 import workloads as W
+    from paged_kv_cache_174_gb300.host import CONTINUOUS_BATCHING_TRACE, ContinuousBatchingTrace
+
+    cfg = CONTINUOUS_BATCHING_TRACE
+    tr = ContinuousBatchingTrace(cfg)
+    plans = [tr.step() for _ in range(cfg.steps)]
+    shape = (cfg.num_blocks, cfg.block_size, cfg.num_kv_heads, cfg.head_dim)
+    gen = torch.Generator(device=dev)
+
+    def fresh_cache():
+        kc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+        vc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+        pos = torch.arange(cfg.prefix, device=dev)
+        blocks = torch.tensor(tr.prefix_blocks, device=dev)
+        slots = blocks[pos // cfg.block_size] * cfg.block_size + pos % cfg.block_size
+        gen.manual_seed(cfg.seed)
+        kc.view(-1, cfg.num_kv_heads, cfg.head_dim)[slots] = torch.randn(
+            cfg.prefix, cfg.num_kv_heads, cfg.head_dim, generator=gen, device=dev).bfloat16()
+        vc.view(-1, cfg.num_kv_heads, cfg.head_dim)[slots] = torch.randn(
+            cfg.prefix, cfg.num_kv_heads, cfg.head_dim, generator=gen, device=dev).bfloat16()
+        return kc, vc
+
+    S = max(len(pl.rids) for pl in plans)
+    T = max(pl.num_tokens for pl in plans)
+    ws = ops.alloc_workspace(S, T, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim,
+                             max(pl.max_q_len for pl in plans),
+                             max(pl.max_seq_len for pl in plans), dev)
+    scale = 1.0 / (cfg.head_dim ** 0.5)
+
+    def run(kc, vc, plan_list, record):
+        times = []
+        for pl in plan_list:
+            if pl.num_tokens == 0:
+                continue
+            meta = {k: W.int32_tensor(getattr(pl, k), dev) for k in
+                    ("copy_pairs", "slot_mapping", "block_tables", "seq_lens", "query_start_loc")}
+            q = torch.randn(pl.num_tokens, cfg.num_q_heads, cfg.head_dim, generator=gen,
+                            device=dev).bfloat16()
+            k = torch.randn(pl.num_tokens, cfg.num_kv_heads, cfg.head_dim, generator=gen,
+                            device=dev).bfloat16()
+            v = torch.randn(pl.num_tokens, cfg.num_kv_heads, cfg.head_dim, generator=gen,
+                            device=dev).bfloat16()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            if len(pl.copy_pairs):
+                ops.copy_blocks(kc, vc, meta["copy_pairs"])
+            ops.reshape_and_cache(k, v, kc, vc, meta["slot_mapping"])
+            ops.paged_attention(q, kc, vc, meta["block_tables"], meta["seq_lens"],
+                                meta["query_start_loc"], scale, max_q_len=pl.max_q_len,
+                                max_seq_len=pl.max_seq_len, workspace=ws)
+            e1.record(stream)
+            if record:
+                times.append((pl, e0, e1))
+        torch.cuda.synchronize()
+        ops.check_device_errors()
+        return [(pl, a.elapsed_time(b)) for pl, a, b in times]
+
+    kc, vc = fresh_cache()
+    run(kc, vc, plans[:warmup], False)
+    kc, vc = fresh_cache()
+    res = run(kc, vc, plans, True)
+    ms = np.array([t for _, t in res])
+    toks = sum(pl.num_tokens for pl, _ in res)
+    launches = sum(3 + (pl.max_q_len >= 2) + (len(pl.copy_pairs) > 0) for pl, _ in res)
+    return {"workload": "continuous-batching trace", "steps": len(res),
+            "description": "200 steps, Poisson 8 arrivals/step, lognormal prompts (median 600, "
+                           "sigma 1, clamp 64-8192), geometric outputs (mean 200), 500-token "
+                           "shared prefix with copy-on-write, 512-token chunks, 2048-token "
+                           "budget, max 256 running, 40000-block pool, 32/8 heads, d 128",
+            "tokens": int(toks), "tokens_per_s": round(toks / (ms.sum() * 1e-3), 1),
+            "gpu_ms_total": round(float(ms.sum()), 3),
+            "step_ms_p50": round(float(np.percentile(ms, 50)), 5),
+            "step_ms_p99": round(float(np.percentile(ms, 99)), 5),
+            "cow_copies": int(tr.total_copies), "finished_requests": len(tr.finished),
+            "gpu_launches": int(launches)}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -357,6 +439,8 @@ def run_ours(args):
                 "peak_source": peaks["source"] + " (bf16_tflops, burst)", "traffic": None,
                 "algorithmic_flops_per_launch": pre["flops"], "avg_launch_ms": pre["ms"]}
         del md, mws, mout
+    if not args.no_trace:
+        line["trace"] = _run_trace(dev, stream, ops, args.warmup)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(b, args.cpu_seconds)
     if world > 1:
@@ -456,6 +540,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-mixed", action="store_true",
                     help="skip the mixed chunked-prefill step measurement")
+    ap.add_argument("--no-trace", action="store_true",
+                    help="skip the continuous-batching trace measurement")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

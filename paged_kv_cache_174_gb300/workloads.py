@@ -348,3 +348,34 @@ def bits_of(t) -> np.ndarray:
     """bf16 torch tensor (any device) -> uint16 numpy bits."""
     import torch
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# Continuous-batching trace inputs (the schedule comes from host.trace)
+# ---------------------------------------------------------------------------
+
+def trace_initial_cache(cfg, prefix_blocks, poison: bool = True):
+    """Pool for the trace: the shared prefix's K/V written into its blocks,
+    every other slot poisoned (or zero)."""
+    rng = np.random.default_rng(cfg.seed + 1)
+    fill = BF16_NAN if poison else np.uint16(0)
+    shape = (cfg.num_blocks, cfg.block_size, cfg.num_kv_heads, cfg.head_dim)
+    kc = np.full(shape, fill, dtype=np.uint16)
+    vc = np.full(shape, fill, dtype=np.uint16)
+    kf = kc.reshape(-1, cfg.num_kv_heads, cfg.head_dim)
+    vf = vc.reshape(-1, cfg.num_kv_heads, cfg.head_dim)
+    pos = np.arange(cfg.prefix)
+    slots = np.asarray(prefix_blocks, np.int64)[pos // cfg.block_size] * cfg.block_size + \
+        pos % cfg.block_size
+    kf[slots] = randn_bf16(rng, (cfg.prefix, cfg.num_kv_heads, cfg.head_dim))
+    vf[slots] = randn_bf16(rng, (cfg.prefix, cfg.num_kv_heads, cfg.head_dim))
+    return kc, vc
+
+
+def trace_step_inputs(cfg, step_index: int, num_tokens: int):
+    """q, k_new, v_new (bf16 bits) for one trace step, N(0, 1)."""
+    rng = np.random.default_rng([cfg.seed, 7, step_index])
+    q = randn_bf16(rng, (num_tokens, cfg.num_q_heads, cfg.head_dim))
+    k = randn_bf16(rng, (num_tokens, cfg.num_kv_heads, cfg.head_dim))
+    v = randn_bf16(rng, (num_tokens, cfg.num_kv_heads, cfg.head_dim))
+    return q, k, v

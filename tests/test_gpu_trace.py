@@ -1,0 +1,92 @@
+"""The continuous-batching trace on the GPU: every step's copy-on-write block
+copies, slot scatter and mixed decode / chunked-prefill attention, replayed on
+the fp64 oracle from the same step plans."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_174_gb300 import ops
+from paged_kv_cache_174_gb300 import workloads as W
+from paged_kv_cache_174_gb300.host import CONTINUOUS_BATCHING_TRACE, ContinuousBatchingTrace, \
+    TraceConfig
+
+from gpu_util import MAX_ABS, REL_L2, attn_errors, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _replay(cfg, steps, full_rows, sample_rows=24, seed=0):
+    tr = ContinuousBatchingTrace(cfg)
+    kc, vc = W.trace_initial_cache(cfg, tr.prefix_blocks)
+    dk, dv = W.bf16_tensor(kc, "cuda"), W.bf16_tensor(vc, "cuda")
+    scale = 1.0 / np.sqrt(cfg.head_dim)
+    rng = np.random.default_rng(seed)
+    worst = (0.0, 0.0)
+    checked = 0
+    for _ in range(steps):
+        plan = tr.step()
+        if plan.num_tokens == 0:
+            continue
+        q, k, v = W.trace_step_inputs(cfg, plan.index, plan.num_tokens)
+        if len(plan.copy_pairs):
+            ops.copy_blocks(dk, dv, W.int32_tensor(plan.copy_pairs, "cuda"))
+            oracle.copy_blocks(kc, vc, plan.copy_pairs)
+        ops.reshape_and_cache(W.bf16_tensor(k, "cuda"), W.bf16_tensor(v, "cuda"), dk, dv,
+                              W.int32_tensor(plan.slot_mapping, "cuda"))
+        oracle.reshape_and_cache(k, v, kc, vc, plan.slot_mapping)
+        dq = W.bf16_tensor(q, "cuda")
+        out = ops.paged_attention(dq, dk, dv, W.int32_tensor(plan.block_tables, "cuda"),
+                                  W.int32_tensor(plan.seq_lens, "cuda"),
+                                  W.int32_tensor(plan.query_start_loc, "cuda"), scale,
+                                  max_q_len=plan.max_q_len, max_seq_len=plan.max_seq_len)
+        ops.check_device_errors()
+        got = to_f64(out)
+        if full_rows:
+            ref = oracle.paged_attention(q, kc, vc, plan.block_tables, plan.seq_lens,
+                                         plan.query_start_loc, scale)
+            g, r = got, ref
+        else:
+            # sampled rows: always one decode row and one prefill row when present
+            ql = np.diff(plan.query_start_loc)
+            cand = list(rng.integers(0, len(plan.rids), size=sample_rows))
+            if plan.num_decode:
+                cand[0] = 0
+            if (ql > 1).any():
+                cand[1 % len(cand)] = int(np.flatnonzero(ql > 1)[0])
+            samples = []
+            for s in cand:
+                i = int(rng.integers(0, ql[s]))
+                samples.append((s, i, int(rng.integers(0, cfg.num_q_heads))))
+            samples = np.array(samples, np.int32)
+            r = oracle.paged_attention_rows(q, kc, vc, plan.block_tables, plan.seq_lens,
+                                            plan.query_start_loc, scale, samples)
+            tok = plan.query_start_loc[samples[:, 0]] + samples[:, 1]
+            g = got[tok, samples[:, 2]]
+        mx, rel = attn_errors(g, r)
+        assert np.isfinite(g).all(), f"step {plan.index}: non-finite output"
+        assert mx <= MAX_ABS and rel <= REL_L2, f"step {plan.index}: max {mx:.3e} rel {rel:.3e}"
+        worst = (max(worst[0], mx), max(worst[1], rel))
+        checked += 1
+    assert checked > 0
+    # the whole pool, bit for bit, after all the copies and scatters
+    assert np.array_equal(W.bits_of(dk), kc), "K cache differs from the oracle"
+    assert np.array_equal(W.bits_of(dv), vc), "V cache differs from the oracle"
+    return tr, worst
+
+
+def test_trace_full_configuration_sampled_rows():
+    """The 40000-block, 32/8-head trace configuration: 60 steps (decodes and
+    512-token chunks, copy-on-write of the shared 500-token prefix), sampled
+    output rows every step, the whole pool compared at the end."""
+    tr, worst = _replay(CONTINUOUS_BATCHING_TRACE, steps=60, full_rows=False)
+    assert tr.total_copies > 0
+
+
+def test_trace_small_heads_all_rows():
+    cfg = TraceConfig(steps=40, arrival_rate=4.0, prompt_median=150.0, prompt_min=8,
+                      prompt_max=700, output_mean=20.0, prefix=60, chunk=64, budget=256,
+                      max_num_seqs=32, num_blocks=1200, num_q_heads=8, num_kv_heads=2,
+                      head_dim=64, seed=21)
+    tr, worst = _replay(cfg, steps=40, full_rows=True)
+    assert tr.total_copies > 0 and len(tr.finished) > 0
