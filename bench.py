@@ -106,11 +106,50 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def _profiled_traffic(profile: str, sources, workload: str, want_workload: str):
+    """DRAM bytes per launch recorded by an ncu capture under profiles/, or
+    None when the workload differs or the kernel sources changed since."""
+    import hashlib
+    if workload != want_workload:
+        return None
+    path = os.path.join(ROOT, "profiles", profile)
+    if not os.path.exists(path):
+        return None
+    h = hashlib.sha256()
+    for src in sources:
+        with open(os.path.join(ROOT, "paged_kv_cache_174_gb300", "csrc", src), "rb") as f:
+            h.update(f.read())
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().split(":")[0] in (
+                    "kernel_source_sha256_16", "traffic_bytes_per_launch"):
+                k, v = line.strip().split(":", 1)
+                fields[k] = v.strip()
+    if fields.get("kernel_source_sha256_16") != h.hexdigest()[:16]:
+        return None
+    try:
+        return int(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def reduce_max(values, dist, device):
+    """Element-wise max of a list of floats over all ranks (identity for one
+    process): the slowest rank's time is the job's time."""
+    import torch
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
 
 
 def _make(workload: str, rank: int):
@@ -337,10 +376,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    if world > 1:
-        tt = torch.tensor([ms, attn_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms, attn_ms = float(tt[0]), float(tt[1])
+    ms, attn_ms = reduce_max([ms, attn_ms], dist if world > 1 else None, dev)
 
     # ---- end to end through the public API from pinned host buffers
     host = {k: getattr(d, k).cpu().pin_memory() for k in
@@ -376,10 +412,8 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
+    (e2e_ms,) = reduce_max([e2e_ms], dist if world > 1 else None, dev)
     if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt[0])
         dist.barrier()
 
     gbs = step_bytes * world / (ms * 1e-3) / 1e9
@@ -408,7 +442,10 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "kernel": "pa_paged_attention (split-KV decode + merge)",
                      "achieved": round(attn_gbs, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(attn_gbs / peaks["hbm_gbs"], 4),
-                     "peak_source": peaks["source"] + " (hbm_gbs)", "traffic": None,
+                     "peak_source": peaks["source"] + " (hbm_gbs)",
+                     "traffic": _profiled_traffic("decode_kernel_decode_batch.md",
+                                                  ["pa_decode.cu", "pa_common.cuh"], b.name,
+                                                  "decode_batch"),
                      "algorithmic_bytes_per_launch": alg["attention"],
                      "avg_launch_ms": round(attn_ms, 5)},
         "e2e": {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",

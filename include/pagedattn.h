@@ -19,12 +19,13 @@
  *    errors found on the device (a slot, block id or length out of range)
  *    make the kernel skip that work item and set a device error word, which
  *    pa_check_device_errors() reads back.
- *  - The library allocates no device memory.  pa_paged_attention takes a
- *    caller-provided workspace of pa_workspace_size() bytes.
+ *  - The library allocates no device memory at run time.  pa_paged_attention
+ *    takes a caller-provided workspace of pa_workspace_size() bytes (the
+ *    allocation-free variant at the end of this header uses a fixed array
+ *    built into the library instead).
  *  - Supported: block_size 16; head_dim 64 or 128; num_q_heads a multiple of
  *    num_kv_heads with group size num_q_heads / num_kv_heads in {1, 2, 4, 8};
- *    num_kv_heads in {1, 2, 4, 8, 16} and num_kv_heads * head_dim <= 1024.
- *    Anything else returns PA_ERR_UNSUPPORTED.
+ *    num_kv_heads in {1, 2, 4, 8}.  Anything else returns PA_ERR_UNSUPPORTED.
  *  - On error the call returns a non-zero status and pa_get_last_error()
  *    returns a message (per thread, valid until the next call on the thread).
  */
