@@ -160,7 +160,7 @@ def _make(workload: str, rank: int):
 
 def _launch_count(b) -> int:
     n = 1 if b.num_tokens else 0        # scatter
-    n += 2                              # decode + merge
+    n += 2                              # split-KV decode + merge
     if b.max_q_len >= 2:
         n += 1                          # prefill
     if b.copy_pairs.size:

@@ -607,30 +607,42 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
     if (lane == 0) flag_error(p.err, DEVERR_BOUNDS);
     return;
   }
-  float M = kNegInf;
-  for (int cc = c_first; cc <= c_last; ++cc) {
-    if (slice_begin(cc, F, C) == slice_begin(cc + 1, F, C)) continue;
-    const int slot = (cc == c_first) ? first_slot : 2 * cc;
-    M = fmaxf(M, __ldg(p.part_ml + ((int64_t)slot * p.n_q + h) * 2));
-  }
-  const float mu = (M == kNegInf) ? 0.f : M;
-  float Lsum = 0.f;
-  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  // online merge over the pieces, eight at a time so that their loads are in
+  // flight together (a long request can span tens of CTAs)
   const bool active = lane * 4 < D;
-  for (int cc = c_first; cc <= c_last; ++cc) {
-    if (slice_begin(cc, F, C) == slice_begin(cc + 1, F, C)) continue;
-    const int slot = (cc == c_first) ? first_slot : 2 * cc;
-    const float2 ml = __ldg(reinterpret_cast<const float2*>(p.part_ml) + (int64_t)slot * p.n_q + h);
-    const float w = fast_exp2(ml.x - mu);
-    Lsum += ml.y * w;
-    if (active) {
-      const float4 o = __ldg(reinterpret_cast<const float4*>(
-          p.part_o + ((int64_t)slot * p.n_q + h) * D + lane * 4));
-      O.x += o.x * w;
-      O.y += o.y * w;
-      O.z += o.z * w;
-      O.w += o.w * w;
+  float M = kNegInf, Lsum = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int cc0 = c_first; cc0 <= c_last; cc0 += 8) {
+    float2 ml[8];
+    float4 o[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int cc = cc0 + k;
+      const bool v = cc <= c_last && slice_begin(cc, F, C) != slice_begin(cc + 1, F, C);
+      const int slot = (cc == c_first) ? first_slot : 2 * cc;
+      ml[k] = make_float2(kNegInf, 0.f);
+      o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (v) {
+        ml[k] = __ldg(reinterpret_cast<const float2*>(p.part_ml) + (int64_t)slot * p.n_q + h);
+        if (active)
+          o[k] = __ldg(reinterpret_cast<const float4*>(
+              p.part_o + ((int64_t)slot * p.n_q + h) * D + lane * 4));
+      }
     }
+    float bm = M;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) bm = fmaxf(bm, ml[k].x);
+    const float mu = (bm == kNegInf) ? 0.f : bm;
+    const float f = fast_exp2(M - mu);
+    Lsum *= f;
+    O.x *= f, O.y *= f, O.z *= f, O.w *= f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float w = fast_exp2(ml[k].x - mu);
+      Lsum += ml[k].y * w;
+      O.x += o[k].x * w, O.y += o[k].y * w, O.z += o[k].z * w, O.w += o[k].w * w;
+    }
+    M = bm;
   }
   if (active) {
     const float inv = 1.f / Lsum;
