@@ -19,10 +19,11 @@
 //  * Warp 1 (one thread) issues tcgen05.mma: S = Q K^T into one of two TMEM
 //    buffers, then O += P V into a TMEM accumulator.
 //  * Warps 2-5 own one MMA row each: they read S from TMEM, apply the causal
-//    mask and scale, keep the running max / sum (base 2), write P (bf16) into
-//    shared memory for the next MMA, and rescale O in TMEM only when the max
-//    grows by more than 2^8 (exact: the same reference max scales the numerator
-//    and the denominator).  At the end they normalise O and store bf16 rows.
+//    mask and scale, keep the running max / sum (base 2), write P (bf16) back
+//    over the S buffer in TMEM, where the P V MMA reads it as its A operand,
+//    and rescale O in TMEM only when the max grows by more than 2^8 (exact: the
+//    same reference max scales the numerator and the denominator).  At the end
+//    they normalise O and store bf16 rows.
 //  * Persistent CTAs (at most one per SM) walk the item list.
 #include <cstdint>
 #include <mutex>
@@ -37,8 +38,8 @@ namespace {
 constexpr int kBlock = 16;        // tokens per physical block
 constexpr int kKeysPerTile = 128; // keys per K/V tile (8 blocks)
 constexpr int kRows = 128;        // MMA rows (tokens x group heads)
-constexpr int kStagesK = 2;       // K tile stages
-constexpr int kStagesV = 2;       // V tile stages
+constexpr int kStagesK = 3;       // K tile stages
+constexpr int kStagesV = 3;       // V tile stages
 constexpr float kNegInf = -INFINITY;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kThreads = 224;  // K/Q producer, MMA, 4 softmax, V producer
@@ -113,7 +114,7 @@ struct PrefillBarriers {
   uint64_t q_full, q_empty;
   uint64_t k_full[kStagesK], k_empty[kStagesK];
   uint64_t v_full[kStagesV], v_empty[kStagesV];
-  uint64_t s_full[2], s_empty[2];
+  uint64_t s_full[2];
   uint64_t p_full[2], pv_done[2];
   uint64_t o_full, o_empty;
   uint64_t mma_done;
@@ -138,7 +139,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t HALF = kRows * 128;  // bytes of one [128 rows][64] block
   constexpr uint32_t Q_BYTES = NH * HALF;
   constexpr uint32_t KV_BYTES = NH * HALF;  // 128 keys
-  constexpr uint32_t P_BYTES = 2 * HALF;    // 128 rows x 128 keys (two buffers)
   constexpr uint32_t TMEM_COLS = 512;
   constexpr uint32_t S_COL0 = 0, O_COL = 256;
   constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(kRows, kKeysPerTile, 0, 0);
@@ -150,8 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* q_s = base;
   unsigned char* k_s = q_s + Q_BYTES;
   unsigned char* v_s = k_s + kStagesK * KV_BYTES;
-  unsigned char* p_s = v_s + kStagesV * KV_BYTES;
-  PrefillBarriers& B = *reinterpret_cast<PrefillBarriers*>(p_s + 2 * P_BYTES);
+  PrefillBarriers& B = *reinterpret_cast<PrefillBarriers*>(v_s + kStagesV * KV_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // decode rows of the same step may use the SMs this grid leaves free
@@ -170,7 +169,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&B.s_full[i]), 1);
-      mbar_init(smem_addr(&B.s_empty[i]), 4);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&B.p_full[i]), 4);
@@ -276,13 +274,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (first && n_item > 0)
             mbar_wait(smem_addr(&B.o_empty), (n_item - 1) & 1, p.err, abort_flag);
           tc::fence_after_sync();
-          const uint32_t pa = smem_addr(p_s + b * P_BYTES);
+          // P (bf16, 64 packed columns) sits in the S buffer it came from
+          const uint32_t pt = tmem + S_COL0 + b * kKeysPerTile;
           const uint32_t va = smem_addr(v_s + (t % kStagesV) * KV_BYTES);
 #pragma unroll
           for (int kk = 0; kk < kKeysPerTile / 16; ++kk) {
-            const uint64_t ad = tc::sw128_desc(pa + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024);
             const uint64_t bd = tc::sw128_desc(va + kk * 2048, HALF, 1024);
-            tc::mma_bf16(tmem + O_COL, ad, bd, IDESC_O, (first && kk == 0) ? 0u : 1u);
+            tc::mma_bf16_tmem_a(tmem + O_COL, pt + kk * 8, bd, IDESC_O,
+                                (first && kk == 0) ? 0u : 1u);
           }
           tc::commit(smem_addr(&B.v_empty[t % kStagesV]));
           tc::commit(smem_addr(&B.pv_done[b]));
@@ -291,8 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int sb = (int)(T & 1);
           mbar_wait(smem_addr(&B.k_full[T % kStagesK]), (int)((T / kStagesK) & 1), p.err,
                     abort_flag);
+          // buffer sb holds P of tile T - 2 until its PV has run
           if (T >= 2)
-            mbar_wait(smem_addr(&B.s_empty[sb]), (int)(((T - 2) >> 1) & 1), p.err, abort_flag);
+            mbar_wait(smem_addr(&B.pv_done[sb]), (int)(((T - 2) >> 1) & 1), p.err, abort_flag);
           tc::fence_after_sync();
           const uint32_t ka = smem_addr(k_s + (T % kStagesK) * KV_BYTES);
 #pragma unroll
@@ -342,9 +342,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_ld32(tmem + lane_addr + S_COL0 + sb * kKeysPerTile + c * 32,
                         *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
         tc::tmem_wait_ld();
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&B.s_empty[sb]));
 
         // causal mask, tile max (8 independent chains).  With a positive
         // scale the max of the raw scores gives the max of the scaled ones,
@@ -385,33 +382,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           l *= alpha;
           m_ref = mx;
         }
-        // P buffer sb was last read by the PV of tile T - 2
-        if (T >= 2)
-          mbar_wait(smem_addr(&B.pv_done[sb]), (int)(((T - 2) >> 1) & 1), p.err, abort_flag);
-        unsigned char* pb = p_s + sb * P_BYTES;
-        // p = 2^(emul * s - m_ref)
+        // p = 2^(emul * s - m_ref), packed in bf16 pairs in place (sr[j] holds
+        // keys 2j, 2j+1), then stored over the S buffer's first 64 columns
         const float nm = -m_ref;
         float l8[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) l8[j] = 0.f;
 #pragma unroll
-        for (int kh = 0; kh < 2; ++kh) {
-#pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = kh * 64 + c8 * 8 + 2 * e;
-              const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), emul, nm));
-              const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), emul, nm));
-              l8[(2 * e) & 7] += p0;
-              l8[(2 * e + 1) & 7] += p1;
-              w[e] = pack_bf16x2(p0, p1);
-            }
-            *reinterpret_cast<uint4*>(pb + kh * HALF + sw128_chunk(r, c8)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
-          }
+        for (int j = 0; j < kKeysPerTile / 2; ++j) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * j]), emul, nm));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * j + 1]), emul, nm));
+          l8[(2 * j) & 7] += p0;
+          l8[(2 * j + 1) & 7] += p1;
+          sr[j] = pack_bf16x2(p0, p1);
         }
+        tc::tmem_st32(tmem + lane_addr + S_COL0 + sb * kKeysPerTile,
+                      *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tc::tmem_st32(tmem + lane_addr + S_COL0 + sb * kKeysPerTile + 32,
+                      *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
         // rescale the running output when the reference max moved (rare)
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
@@ -445,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     make_uint4(0, 0, 0, 0);
           }
         }
+        tc::tmem_wait_st();
         tc::fence_proxy_async_smem();
         tc::fence_before_sync();
         __syncwarp();
@@ -526,7 +515,7 @@ cudaError_t make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t m
 template <int D, int G>
 size_t prefill_smem_bytes() {
   constexpr size_t half = kRows * 128;
-  return 1024 + (size_t)(D / 64) * half * (1 + kStagesK + kStagesV) + 2 * 2 * half +
+  return 1024 + (size_t)(D / 64) * half * (1 + kStagesK + kStagesV) +
          sizeof(PrefillBarriers);
 }
 
