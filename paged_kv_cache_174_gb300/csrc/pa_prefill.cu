@@ -12,18 +12,22 @@
 //  * An item is (request, tile of 128/G query tokens, kv head g).  Its 128 MMA
 //    rows are the tile's tokens x the G q heads that share kv head g, so every
 //    K/V tile is loaded once for the whole GQA group.
-//  * Warp 0 streams Q and K tiles, warp 6 V tiles, of 128 keys (8 pages of 16
+//  * Warp 0 streams Q and K tiles, warp 10 V tiles, of 128 keys (8 pages of 16
 //    tokens, one TMA box per page and 64-element half of head_dim, 128-byte
 //    swizzle) into rings of shared-memory stages; separate K and V producers
 //    let the next K tiles load while the V of earlier tiles is still in use.
-//  * Warp 1 (one thread) issues tcgen05.mma: S = Q K^T into one of two TMEM
-//    buffers, then O += P V into a TMEM accumulator.
-//  * Warps 2-5 own one MMA row each: they read S from TMEM, apply the causal
+//  * Warp 1 (one thread) issues tcgen05.mma: S = Q K^T into one of three
+//    TMEM buffers, then O += P V into a TMEM accumulator.  S of the next tile
+//    is queued before the P V of the current one, so the tensor pipe works on
+//    one tile while the softmax warps work on the other.
+//  * Warps 2-9 run the softmax, two warps per MMA row: the warp pair that
+//    shares a TMEM lane quarter splits the 128 keys of a tile in halves and
+//    swaps partial row maxima through shared memory.  They apply the causal
 //    mask and scale, keep the running max / sum (base 2), write P (bf16) back
-//    over the S buffer in TMEM, where the P V MMA reads it as its A operand,
-//    and rescale O in TMEM only when the max grows by more than 2^8 (exact: the
-//    same reference max scales the numerator and the denominator).  At the end
-//    they normalise O and store bf16 rows.
+//    over their half of the S buffer in TMEM, where the P V MMA reads it as its
+//    A operand, and rescale O in TMEM only when the max grows by more than 2^8
+//    (exact: the same reference max scales the numerator and the denominator).
+//    At the end they normalise O and store bf16 rows.
 //  * Persistent CTAs (at most one per SM) walk the item list.
 #include <cstdint>
 #include <mutex>
@@ -38,11 +42,14 @@ namespace {
 constexpr int kBlock = 16;        // tokens per physical block
 constexpr int kKeysPerTile = 128; // keys per K/V tile (8 blocks)
 constexpr int kRows = 128;        // MMA rows (tokens x group heads)
-constexpr int kStagesK = 3;       // K tile stages
-constexpr int kStagesV = 3;       // V tile stages
+constexpr int kStagesK = 2;       // K tile stages
+constexpr int kStagesV = 3;       // V tile stages (held from the S to the P V product)
+constexpr int kSBufs = 3;         // S / P buffers in TMEM
+constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quarter
 constexpr float kNegInf = -INFINITY;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kThreads = 224;  // K/Q producer, MMA, 4 softmax, V producer
+constexpr int kWarpV = 2 + kSoftmaxWarps;    // V producer
+constexpr int kThreads = 32 * (kWarpV + 1);  // Q/K producer, MMA, softmax, V producer
 
 struct PrefillParams {
   const int32_t* block_tables;
@@ -114,13 +121,14 @@ struct PrefillBarriers {
   uint64_t q_full, q_empty;
   uint64_t k_full[kStagesK], k_empty[kStagesK];
   uint64_t v_full[kStagesV], v_empty[kStagesV];
-  uint64_t s_full[2];
-  uint64_t p_full[2], pv_done[2];
+  uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
   uint64_t o_full, o_empty;
   uint64_t mma_done;
   uint32_t tmem_slot;
   int abort_flag;
   long long total_items;
+  float xmax[2][2][kRows];  // partial row maxima: [tile parity][key half][row]
+  float xsum[2][kRows];     // partial row sums at the end of an item: [key half][row]
 };
 
 // Byte offset of 16-byte chunk c (0..7) of row r inside a [rows][64 x bf16]
@@ -128,6 +136,18 @@ struct PrefillBarriers {
 __device__ __forceinline__ uint32_t sw128_chunk(int r, int c) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
+
+// Position in a ring of pipeline stages: the stage and the parity of its
+// current use, which flips each time the ring wraps around.
+struct Ring {
+  uint32_t stage = 0, phase = 0;
+  __device__ __forceinline__ void next(uint32_t n) {
+    if (++stage == n) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+};
 
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -140,7 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t Q_BYTES = NH * HALF;
   constexpr uint32_t KV_BYTES = NH * HALF;  // 128 keys
   constexpr uint32_t TMEM_COLS = 512;
-  constexpr uint32_t S_COL0 = 0, O_COL = 256;
+  constexpr uint32_t S_COL0 = 0, O_COL = kSBufs * kKeysPerTile;
+  static_assert(O_COL + D <= TMEM_COLS, "TMEM columns");
   constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(kRows, kKeysPerTile, 0, 0);
   constexpr uint32_t IDESC_O = tc::idesc_bf16_f32(kRows, D, 0, 1);
 
@@ -167,15 +188,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&B.v_full[i]), 1);
       mbar_init(smem_addr(&B.v_empty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(smem_addr(&B.s_full[i]), 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_addr(&B.p_full[i]), 4);
+      mbar_init(smem_addr(&B.p_full[i]), kSoftmaxWarps);
       mbar_init(smem_addr(&B.pv_done[i]), 1);
     }
     mbar_init(smem_addr(&B.o_full), 1);
-    mbar_init(smem_addr(&B.o_empty), 4);
+    mbar_init(smem_addr(&B.o_empty), kSoftmaxWarps);
     mbar_init(smem_addr(&B.mma_done), 1);
     B.abort_flag = 0;
     fence_mbar_init();
@@ -194,18 +213,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long total_items = B.total_items;
   volatile int* abort_flag = &B.abort_flag;
 
-  if (warp == 0 || warp == 6) {
+  if (warp == 0 || warp == kWarpV) {
     // ============================================================ producers
     if (lane == 0) {
-      const bool is_k = (warp == 0);  // warp 0: Q and K, warp 6: V
+      const bool is_k = (warp == 0);  // warp 0: Q and K, the last warp: V
       const CUtensorMap* map = is_k ? &kmap : &vmap;
       unsigned char* ring = is_k ? k_s : v_s;
       uint64_t* full = is_k ? B.k_full : B.v_full;
       uint64_t* empty = is_k ? B.k_empty : B.v_empty;
-      const int nst = is_k ? kStagesK : kStagesV;
+      const uint32_t nst = is_k ? kStagesK : kStagesV;
       ItemCursor<TM> cur;
       cur.init(p);
       int n_item = 0, c = 0;
+      Ring pos;
       for (long long item = blockIdx.x; item < total_items; item += gridDim.x, ++n_item) {
         Item it;
         if (!cur.locate(p, item, it)) break;
@@ -233,9 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               ++nvalid;
             }
           }
-          const int st = c % nst;
-          if (c >= nst)
-            mbar_wait(smem_addr(&empty[st]), ((c / nst) - 1) & 1, p.err, abort_flag);
+          const uint32_t st = pos.stage;
+          if (c >= (int)nst) mbar_wait(smem_addr(&empty[st]), pos.phase ^ 1u, p.err, abort_flag);
           mbar_arrive_expect_tx(smem_addr(&full[st]),
                                 (uint32_t)nvalid * NH * (kBlock * 128));
           for (int i = 0; i < npg; ++i) {
@@ -245,10 +264,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc::tma_load_3d(smem_addr(ring + st * KV_BYTES + h * HALF + i * (kBlock * 128)),
                               map, h * 64, it.g, phys[i] * kBlock, smem_addr(&full[st]));
           }
+          pos.next(nst);
         }
       }
       // never hand back shared memory with a TMA copy still landing in it
-      for (int i = max(0, c - nst); i < c; ++i)
+      for (int i = max(0, c - (int)nst); i < c; ++i)
         mbar_wait(smem_addr(&full[i % nst]), (i / nst) & 1, p.err, abort_flag);
       if (is_k && n_item > 0)
         mbar_wait(smem_addr(&B.q_full), (n_item - 1) & 1, p.err, abort_flag);
@@ -259,56 +279,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       ItemCursor<TM> cur;
       cur.init(p);
       int n_item = 0;
-      long long T = 0;  // K/V tiles so far (all items)
+      uint32_t ntiles = 0;  // K/V tiles so far (all items)
+      Ring kr, vr, sbr, prev;  // K stages, V stages, S buffers, S buffer of the last tile
       const uint32_t q_addr = smem_addr(q_s);
       bool issued = false;
       for (long long item = blockIdx.x; item < total_items; item += gridDim.x, ++n_item) {
         Item it;
         if (!cur.locate(p, item, it)) break;
         mbar_wait(smem_addr(&B.q_full), n_item & 1, p.err, abort_flag);
-        auto issue_pv = [&](long long t, bool first) {
-          const int b = (int)(t & 1);
-          mbar_wait(smem_addr(&B.p_full[b]), (int)((t >> 1) & 1), p.err, abort_flag);
-          mbar_wait(smem_addr(&B.v_full[t % kStagesV]), (int)((t / kStagesV) & 1), p.err,
-                    abort_flag);
+        auto issue_pv = [&](const Ring& pb, bool first) {
+          mbar_wait(smem_addr(&B.p_full[pb.stage]), pb.phase, p.err, abort_flag);
+          mbar_wait(smem_addr(&B.v_full[vr.stage]), vr.phase, p.err, abort_flag);
           if (first && n_item > 0)
             mbar_wait(smem_addr(&B.o_empty), (n_item - 1) & 1, p.err, abort_flag);
           tc::fence_after_sync();
-          // P (bf16, 64 packed columns) sits in the S buffer it came from
-          const uint32_t pt = tmem + S_COL0 + b * kKeysPerTile;
-          const uint32_t va = smem_addr(v_s + (t % kStagesV) * KV_BYTES);
+          // P (bf16 pairs) of keys 64h .. 64h + 63 sits in columns 64h .. 64h + 31
+          // of the S buffer it came from
+          const uint32_t pt = tmem + S_COL0 + pb.stage * kKeysPerTile;
+          const uint32_t va = smem_addr(v_s + vr.stage * KV_BYTES);
 #pragma unroll
           for (int kk = 0; kk < kKeysPerTile / 16; ++kk) {
             const uint64_t bd = tc::sw128_desc(va + kk * 2048, HALF, 1024);
-            tc::mma_bf16_tmem_a(tmem + O_COL, pt + kk * 8, bd, IDESC_O,
+            tc::mma_bf16_tmem_a(tmem + O_COL, pt + (kk >> 2) * 64 + (kk & 3) * 8, bd, IDESC_O,
                                 (first && kk == 0) ? 0u : 1u);
           }
-          tc::commit(smem_addr(&B.v_empty[t % kStagesV]));
-          tc::commit(smem_addr(&B.pv_done[b]));
+          tc::commit(smem_addr(&B.v_empty[vr.stage]));
+          tc::commit(smem_addr(&B.pv_done[pb.stage]));
+          vr.next(kStagesV);
         };
-        for (int kt = 0; kt < it.nkt; ++kt, ++T) {
-          const int sb = (int)(T & 1);
-          mbar_wait(smem_addr(&B.k_full[T % kStagesK]), (int)((T / kStagesK) & 1), p.err,
-                    abort_flag);
-          // buffer sb holds P of tile T - 2 until its PV has run
-          if (T >= 2)
-            mbar_wait(smem_addr(&B.pv_done[sb]), (int)(((T - 2) >> 1) & 1), p.err, abort_flag);
+        for (int kt = 0; kt < it.nkt; ++kt, ++ntiles) {
+          mbar_wait(smem_addr(&B.k_full[kr.stage]), kr.phase, p.err, abort_flag);
+          // the S buffer holds P of the tile kSBufs back until its PV has run
+          if (ntiles >= kSBufs)
+            mbar_wait(smem_addr(&B.pv_done[sbr.stage]), sbr.phase ^ 1u, p.err, abort_flag);
           tc::fence_after_sync();
-          const uint32_t ka = smem_addr(k_s + (T % kStagesK) * KV_BYTES);
+          const uint32_t ka = smem_addr(k_s + kr.stage * KV_BYTES);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t ad =
                 tc::sw128_desc(q_addr + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024);
             const uint64_t bd = tc::sw128_desc(ka + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024);
-            tc::mma_bf16(tmem + S_COL0 + sb * kKeysPerTile, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
+            tc::mma_bf16(tmem + S_COL0 + sbr.stage * kKeysPerTile, ad, bd, IDESC_S,
+                         kk > 0 ? 1u : 0u);
           }
-          tc::commit(smem_addr(&B.s_full[sb]));
-          tc::commit(smem_addr(&B.k_empty[T % kStagesK]));
+          tc::commit(smem_addr(&B.s_full[sbr.stage]));
+          tc::commit(smem_addr(&B.k_empty[kr.stage]));
+          kr.next(kStagesK);
           if (kt == it.nkt - 1) tc::commit(smem_addr(&B.q_empty));
-          if (kt > 0) issue_pv(T - 1, kt == 1);
+          if (kt > 0) issue_pv(prev, kt == 1);
+          prev = sbr;
+          sbr.next(kSBufs);
           issued = true;
         }
-        issue_pv(T - 1, it.nkt == 1);
+        issue_pv(prev, it.nkt == 1);
         tc::commit(smem_addr(&B.o_full));
       }
       if (issued) {
@@ -319,61 +342,71 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ============================================================ softmax
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int kh = (warp - 2) >> 2;  // key half of each tile: 64*kh .. 64*kh + 63
     const int r = quarter * 32 + lane;
+    const int pair_bar = 1 + quarter;  // named barrier of the two warps on these rows
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const int tl = r / G, hl = r % G;
+    const float sl2 = p.scale_log2;
+    // With a positive scale the max of the raw scores gives the max of the
+    // scaled ones and the scale folds into the exponent's FMA; otherwise the
+    // scores are scaled first.
+    const bool pos_scale = sl2 > 0.f;
+    const float mul = pos_scale ? 1.f : sl2;
+    const float emul = pos_scale ? sl2 : 1.f;
     ItemCursor<TM> cur;
     cur.init(p);
     int n_item = 0;
-    long long T = 0;
+    Ring sbr, prev, vr;  // S buffer of this tile and of the last one, V stage
+    uint32_t xpar = 0;   // exchange slot parity
     for (long long item = blockIdx.x; item < total_items; item += gridDim.x, ++n_item) {
       Item it;
       if (!cur.locate(p, item, it)) break;
       const bool row_valid = tl < it.ntok;
       const int p_row = row_valid ? it.p_first + tl : it.kv_end - 1;
       float m_ref = kNegInf, l = 0.f;
-      for (int kt = 0; kt < it.nkt; ++kt, ++T) {
-        const int sb = (int)(T & 1);
-        mbar_wait(smem_addr(&B.s_full[sb]), (int)((T >> 1) & 1), p.err, abort_flag);
+      for (int kt = 0; kt < it.nkt; ++kt) {
+        const uint32_t s_cols = tmem + lane_addr + S_COL0 + sbr.stage * kKeysPerTile + kh * 64;
+        mbar_wait(smem_addr(&B.s_full[sbr.stage]), sbr.phase, p.err, abort_flag);
         tc::fence_after_sync();
-        uint32_t sr[kKeysPerTile];
-#pragma unroll
-        for (int c = 0; c < kKeysPerTile / 32; ++c)
-          tc::tmem_ld32(tmem + lane_addr + S_COL0 + sb * kKeysPerTile + c * 32,
-                        *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+        uint32_t sr[64];
+        tc::tmem_ld32(s_cols, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tc::tmem_ld32(s_cols + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         tc::tmem_wait_ld();
 
-        // causal mask, tile max (8 independent chains).  With a positive
-        // scale the max of the raw scores gives the max of the scaled ones,
-        // and the scale folds into the exponent's FMA below.
-        const int k0 = kt * kKeysPerTile;
-        const int lim = p_row - k0;  // keys c <= lim are visible
-        const float sl2 = p.scale_log2;
-        const bool pos_scale = sl2 > 0.f;
-        const float mul = pos_scale ? 1.f : sl2;  // applied now; sl2 is applied in the exp
-        const float emul = pos_scale ? sl2 : 1.f;
-        float m8[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) m8[j] = kNegInf;
-        if (__all_sync(0xffffffffu, lim >= kKeysPerTile - 1)) {
+        // causal mask and the max of this half (three-input max, 4 chains)
+        const int k0 = kt * kKeysPerTile + kh * 64;
+        const int lim = p_row - k0;  // keys c <= lim of this half are visible
+        float m4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+        if (__all_sync(0xffffffffu, lim >= 63)) {
           if (!pos_scale) {
 #pragma unroll
-            for (int c = 0; c < kKeysPerTile; ++c)
-              sr[c] = __float_as_uint(__uint_as_float(sr[c]) * mul);
+            for (int c = 0; c < 64; ++c) sr[c] = __float_as_uint(__uint_as_float(sr[c]) * mul);
           }
-#pragma unroll
-          for (int c = 0; c < kKeysPerTile; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sr[c]));
         } else {
 #pragma unroll
-          for (int c = 0; c < kKeysPerTile; ++c) {
-            const float s = (c <= lim) ? __uint_as_float(sr[c]) * mul : kNegInf;
-            sr[c] = __float_as_uint(s);
-            m8[c & 7] = fmaxf(m8[c & 7], s);
-          }
+          for (int c = 0; c < 64; ++c)
+            sr[c] = __float_as_uint((c <= lim) ? __uint_as_float(sr[c]) * mul : kNegInf);
         }
-        float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+#pragma unroll
+        for (int c = 0; c < 64; c += 8) {
+          m4[(c >> 3) & 3] = fmax3(m4[(c >> 3) & 3], __uint_as_float(sr[c]),
+                                   __uint_as_float(sr[c + 1]));
+          m4[(c >> 3) & 3] = fmax3(m4[(c >> 3) & 3], __uint_as_float(sr[c + 2]),
+                                   __uint_as_float(sr[c + 3]));
+          m4[(c >> 3) & 3] = fmax3(m4[(c >> 3) & 3], __uint_as_float(sr[c + 4]),
+                                   __uint_as_float(sr[c + 5]));
+          m4[(c >> 3) & 3] = fmax3(m4[(c >> 3) & 3], __uint_as_float(sr[c + 6]),
+                                   __uint_as_float(sr[c + 7]));
+        }
+        const float mh = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        // swap the half maxima with the other warp on these rows (slots alternate
+        // with the tile parity, so a slot is rewritten only after a later barrier)
+        B.xmax[xpar][kh][r] = mh;
+        named_barrier(pair_bar, 64);
+        float mx = fmaxf(mh, B.xmax[xpar][kh ^ 1][r]);
         mx = (mx == kNegInf) ? kNegInf : mx * emul;  // now in scaled base-2 units
+        // both warps of the pair see the same maxima and take the same branch
         float alpha = 1.f;
         if (m_ref == kNegInf) {
           m_ref = mx;  // first tile: O not yet written
@@ -383,52 +416,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = mx;
         }
         // p = 2^(emul * s - m_ref), packed in bf16 pairs in place (sr[j] holds
-        // keys 2j, 2j+1), then stored over the S buffer's first 64 columns
-        const float nm = -m_ref;
-        float l8[8];
+        // keys 2j, 2j+1 of this half), stored over the first 32 columns of the half
+        const float2 e2 = make_float2(emul, emul);
+        const float2 nm2 = make_float2(-m_ref, -m_ref);
+        float2 l4[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) l8[j] = 0.f;
+        for (int j = 0; j < 4; ++j) l4[j] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < kKeysPerTile / 2; ++j) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * j]), emul, nm));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * j + 1]), emul, nm));
-          l8[(2 * j) & 7] += p0;
-          l8[(2 * j + 1) & 7] += p1;
-          sr[j] = pack_bf16x2(p0, p1);
+        for (int j = 0; j < 32; ++j) {
+          const float2 x = __ffma2_rn(
+              make_float2(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])), e2, nm2);
+          const float2 pj = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          l4[j & 3] = __fadd2_rn(l4[j & 3], pj);
+          sr[j] = pack_bf16x2(pj.x, pj.y);
         }
-        tc::tmem_st32(tmem + lane_addr + S_COL0 + sb * kKeysPerTile,
-                      *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        tc::tmem_st32(tmem + lane_addr + S_COL0 + sb * kKeysPerTile + 32,
-                      *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-        l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
-        // rescale the running output when the reference max moved (rare)
+        tc::tmem_st32(s_cols, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        l += ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
+        // rescale this half of the running output when the reference max moved (rare)
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          mbar_wait(smem_addr(&B.pv_done[(T - 1) & 1]), (int)(((T - 1) >> 1) & 1), p.err,
-                    abort_flag);
+          mbar_wait(smem_addr(&B.pv_done[prev.stage]), prev.phase, p.err, abort_flag);
           tc::fence_after_sync();
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < D / 64; ++c) {
+            const uint32_t oc = tmem + lane_addr + O_COL + kh * (D / 2) + c * 32;
             uint32_t o[32];
-            tc::tmem_ld32(tmem + lane_addr + O_COL + c * 32, o);
+            tc::tmem_ld32(oc, o);
             tc::tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-            tc::tmem_st32(tmem + lane_addr + O_COL + c * 32, o);
+            tc::tmem_st32(oc, o);
           }
-          tc::tmem_wait_st();
         }
         // keys past the last needed one: V rows there may hold stale or
-        // poisoned data; zero them so that P = 0 times V stays 0
-        const int kv_local = it.kv_end - k0;
+        // poisoned data; zero them so that P = 0 times V stays 0 (each warp of
+        // the pair clears half of the row's 16-byte chunks)
+        const int kv_local = it.kv_end - kt * kKeysPerTile;
         if (kv_local < kKeysPerTile) {
-          mbar_wait(smem_addr(&B.v_full[T % kStagesV]), (int)((T / kStagesV) & 1), p.err,
-                    abort_flag);
+          mbar_wait(smem_addr(&B.v_full[vr.stage]), vr.phase, p.err, abort_flag);
           if (r >= kv_local) {
-            unsigned char* vrow = v_s + (T % kStagesV) * KV_BYTES;
+            unsigned char* vrow = v_s + vr.stage * KV_BYTES;
 #pragma unroll
             for (int h = 0; h < NH; ++h)
 #pragma unroll
-              for (int c8 = 0; c8 < 8; ++c8)
+              for (int c8 = 4 * kh; c8 < 4 * kh + 4; ++c8)
                 *reinterpret_cast<uint4*>(vrow + h * HALF + sw128_chunk(r, c8)) =
                     make_uint4(0, 0, 0, 0);
           }
@@ -437,17 +467,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_proxy_async_smem();
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&B.p_full[sb]));
+        if (lane == 0) mbar_arrive(smem_addr(&B.p_full[sbr.stage]));
+        prev = sbr;
+        sbr.next(kSBufs);
+        vr.next(kStagesV);
+        xpar ^= 1u;
       }
-      // epilogue: O / l -> bf16 rows
+      // epilogue: O / l -> bf16 rows; each warp of the pair writes half of d
+      B.xsum[kh][r] = l;
+      named_barrier(pair_bar, 64);
+      const float inv = 1.f / (l + B.xsum[kh ^ 1][r]);
       mbar_wait(smem_addr(&B.o_full), n_item & 1, p.err, abort_flag);
       tc::fence_after_sync();
-      const float inv = 1.f / l;
-      uint16_t* orow = p.out + ((int64_t)(it.q0 + tl) * p.n_q + it.g * G + hl) * D;
+      uint16_t* orow = p.out + ((int64_t)(it.q0 + tl) * p.n_q + it.g * G + hl) * D + kh * (D / 2);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t o[32];
-        tc::tmem_ld32(tmem + lane_addr + O_COL + c * 32, o);
+        tc::tmem_ld32(tmem + lane_addr + O_COL + kh * (D / 2) + c * 32, o);
         tc::tmem_wait_ld();
         if (row_valid) {
 #pragma unroll
