@@ -158,11 +158,19 @@ def _make(workload: str, rank: int):
     return b
 
 
+def ops_splits(b) -> int:
+    from paged_kv_cache_174_gb300 import ops
+    return ops.prefill_splits(b.num_tokens, b.num_q_heads, b.num_kv_heads, b.head_dim,
+                              b.max_q_len, b.max_seq_len)
+
+
 def _launch_count(b) -> int:
     n = 1 if b.num_tokens else 0        # scatter
     n += 2                              # split-KV decode + merge
     if b.max_q_len >= 2:
         n += 1                          # prefill
+        if ops_splits(b) > 1:
+            n += 1                      # merge of the prefill key pieces
     if b.copy_pairs.size:
         n += 1
     return n

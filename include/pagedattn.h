@@ -88,6 +88,17 @@ size_t pa_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t num_q_hea
                          int32_t max_seq_len);
 
 /*
+ * Number of pieces the tensor-core prefill kernel splits each request's keys
+ * into for a pa_paged_attention call with these sizes on the current device
+ * (informational; 1 means no split).  With more than one piece, every prefill
+ * row is written as per-piece partial results into the workspace and a second
+ * kernel combines them with log-sum-exp weights, so the call launches one
+ * kernel more.  Returns 0 if an argument is invalid.
+ */
+int pa_prefill_splits(int32_t num_tokens, int32_t num_q_heads, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t max_q_len, int32_t max_seq_len);
+
+/*
  * Causal, GQA-aware, variable-length attention over the paged cache
  * ("连续批处理：推理吞吐的范式革命", section 4.1: walk the request's Block
  * Table, score q.k scaled, softmax, weighted sum of v, normalise; chunked

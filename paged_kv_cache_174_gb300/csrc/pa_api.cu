@@ -137,9 +137,42 @@ size_t pa_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t num_q_hea
   if (device_state(nullptr, &sms)) return 0;
   const int ctas = pa::decode_ctas(sms);
   size_t bytes = pa::decode_workspace_bytes(ctas, num_seqs, num_q_heads, head_dim);
-  bytes += pa::prefill_workspace_bytes(num_seqs, num_tokens, num_q_heads, head_dim, max_q_len);
+  bytes += pa::prefill_plan(num_tokens, num_q_heads, num_kv_heads, head_dim, max_q_len,
+                            max_seq_len, sms, ~size_t(0))
+               .bytes;
   return bytes;
 }
+
+int pa_prefill_splits(int32_t num_tokens, int32_t num_q_heads, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t max_q_len, int32_t max_seq_len) {
+  if (num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      max_q_len < 0 || max_seq_len < 0 || num_q_heads % num_kv_heads != 0)
+    return 0;
+  int sms = 0;
+  if (device_state(nullptr, &sms)) return 0;
+  return pa::prefill_plan(num_tokens, num_q_heads, num_kv_heads, head_dim, max_q_len,
+                          max_seq_len, sms, ~size_t(0))
+      .nsplit;
+}
+
+}  // extern "C"
+
+namespace {
+
+// pa_paged_attention with a cap on the workspace the prefill key split may
+// take (the allocation-free entry point has a fixed array).
+int paged_attention_impl(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
+                         int32_t num_blocks, int32_t block_size, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, const int32_t* block_tables,
+                         int32_t max_blocks, const int32_t* seq_lens,
+                         const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens,
+                         int32_t max_q_len, int32_t max_seq_len, float scale, pa_bf16* out,
+                         void* workspace, size_t workspace_bytes, size_t split_cap,
+                         cudaStream_t stream);
+
+}  // namespace
+
+extern "C" {
 
 int pa_paged_attention(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
                        int32_t num_blocks, int32_t block_size, int32_t num_q_heads,
@@ -148,6 +181,24 @@ int pa_paged_attention(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* 
                        const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens,
                        int32_t max_q_len, int32_t max_seq_len, float scale, pa_bf16* out,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return paged_attention_impl(q, k_cache, v_cache, num_blocks, block_size, num_q_heads,
+                              num_kv_heads, head_dim, block_tables, max_blocks, seq_lens,
+                              query_start_loc, num_seqs, num_tokens, max_q_len, max_seq_len,
+                              scale, out, workspace, workspace_bytes, ~size_t(0), stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+int paged_attention_impl(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
+                         int32_t num_blocks, int32_t block_size, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, const int32_t* block_tables,
+                         int32_t max_blocks, const int32_t* seq_lens,
+                         const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens,
+                         int32_t max_q_len, int32_t max_seq_len, float scale, pa_bf16* out,
+                         void* workspace, size_t workspace_bytes, size_t split_cap,
+                         cudaStream_t stream) {
   int st = check_cache_geometry(num_blocks, block_size, num_kv_heads, head_dim);
   if (st) return st;
   if (num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
@@ -183,8 +234,9 @@ int pa_paged_attention(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* 
   if (st) return st;
   const int ctas = pa::decode_ctas(sms);
   const size_t need_decode = pa::decode_workspace_bytes(ctas, num_seqs, num_q_heads, head_dim);
-  const size_t need_prefill =
-      pa::prefill_workspace_bytes(num_seqs, num_tokens, num_q_heads, head_dim, max_q_len);
+  const pa::PrefillPlan plan = pa::prefill_plan(num_tokens, num_q_heads, num_kv_heads, head_dim,
+                                                max_q_len, max_seq_len, sms, split_cap);
+  const size_t need_prefill = plan.bytes;
   if (!workspace || !aligned(workspace, 256))
     return fail(PA_ERR_WORKSPACE, "workspace must be a non-null 256-byte aligned pointer");
   if (workspace_bytes < need_decode + need_prefill)
@@ -213,7 +265,7 @@ int pa_paged_attention(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* 
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   if (max_q_len >= 2) {
-    cudaError_t e = pa::launch_prefill(a, ws + need_decode, need_prefill, sms, stream);
+    cudaError_t e = pa::launch_prefill(a, plan, ws + need_decode, sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
   pa::DecodeWorkspace dws = pa::decode_workspace(ws, ctas, num_seqs, num_q_heads, head_dim);
@@ -221,6 +273,10 @@ int pa_paged_attention(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* 
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return PA_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 int pa_check_device_errors(cudaStream_t stream) {
   unsigned* err = nullptr;
@@ -300,8 +356,9 @@ int pa_paged_attention_noalloc(const pa_bf16* q, const pa_bf16* k_cache,
                                int32_t num_seqs, int32_t num_tokens, int32_t max_q_len,
                                int32_t max_seq_len, float scale, pa_bf16* out,
                                cudaStream_t stream) {
+  // the split-KV decode part must fit; the prefill key split takes what is left
   const size_t need = pa_workspace_size(num_seqs, num_tokens, num_q_heads, num_kv_heads,
-                                        head_dim, max_q_len, max_seq_len);
+                                        head_dim, max_q_len < 1 ? max_q_len : 1, max_seq_len);
   if (need == 0)
     return fail(PA_ERR_INVALID_ARG, "invalid sizes, or no CUDA device for the scratch size");
   if (need > kNoAllocScratchBytes)
@@ -312,10 +369,11 @@ int pa_paged_attention_noalloc(const pa_bf16* q, const pa_bf16* k_cache,
   void* scratch = nullptr;
   int st = noalloc_scratch(&scratch);
   if (st) return st;
-  return pa_paged_attention(q, k_cache, v_cache, num_blocks, block_size, num_q_heads,
-                            num_kv_heads, head_dim, block_tables, max_blocks, seq_lens,
-                            query_start_loc, num_seqs, num_tokens, max_q_len, max_seq_len, scale,
-                            out, scratch, kNoAllocScratchBytes, stream);
+  return paged_attention_impl(q, k_cache, v_cache, num_blocks, block_size, num_q_heads,
+                              num_kv_heads, head_dim, block_tables, max_blocks, seq_lens,
+                              query_start_loc, num_seqs, num_tokens, max_q_len, max_seq_len,
+                              scale, out, scratch, kNoAllocScratchBytes,
+                              kNoAllocScratchBytes - need, stream);
 }
 
 }  // extern "C"

@@ -55,9 +55,15 @@ cudaError_t launch_decode(const AttnArgs& a, const DecodeWorkspace& ws, int ctas
                           cudaStream_t stream);
 
 bool prefill_supported(int head_dim, int group, int num_kv_heads);
-size_t prefill_workspace_bytes(int num_seqs, int num_tokens, int num_q_heads, int head_dim,
-                               int max_q_len);
-cudaError_t launch_prefill(const AttnArgs& a, void* ws, size_t ws_bytes, int sm_count,
+// How the prefill kernel splits the keys of each query-tile pair, and the
+// workspace bytes the pieces take (0 when nsplit == 1).
+struct PrefillPlan {
+  int nsplit;
+  size_t bytes;
+};
+PrefillPlan prefill_plan(int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+                         int max_q_len, int max_seq_len, int sm_count, size_t max_bytes);
+cudaError_t launch_prefill(const AttnArgs& a, const PrefillPlan& plan, void* ws, int sm_count,
                            cudaStream_t stream);
 
 cudaError_t launch_reshape_and_cache(const uint16_t* k, const uint16_t* v, int32_t num_tokens,

@@ -9,26 +9,29 @@
 // p = seq_len - q_len + i and attends to keys 0..p of its Block Table.
 //
 // Layout of the work (GB300 design, not the pages' scalar kernel):
-//  * An item is (request, tile of 128/G query tokens, kv head g).  Its 128 MMA
-//    rows are the tile's tokens x the G q heads that share kv head g, so every
-//    K/V tile is loaded once for the whole GQA group.
-//  * Warp 0 streams Q and K tiles, warp 10 V tiles, of 128 keys (8 pages of 16
-//    tokens, one TMA box per page and 64-element half of head_dim, 128-byte
-//    swizzle) into rings of shared-memory stages; separate K and V producers
-//    let the next K tiles load while the V of earlier tiles is still in use.
-//  * Warp 1 (one thread) issues tcgen05.mma: S = Q K^T into one of three
-//    TMEM buffers, then O += P V into a TMEM accumulator.  S of the next tile
-//    is queued before the P V of the current one, so the tensor pipe works on
-//    one tile while the softmax warps work on the other.
+//  * A query tile is 128/G tokens x the G q heads that share kv head g: the
+//    128 rows of one MMA, so every K/V tile is loaded once for the whole GQA
+//    group.  A unit is (request, query tile, kv head, key split).
+//  * K/V tiles hold 128 keys (8 pages).  K lands as 16 TMA boxes (one per page
+//    and 64-column half, 128-byte swizzle: the layout the S = Q K^T MMA reads
+//    as 128 rows); V as 8 boxes of one page and both halves each (the P V MMA
+//    consumes one page per instruction).  A single thread issues TMA boxes
+//    slowly, so seven producer warps share them.
+//  * Warp 1 (one thread) issues S = Q K^T into one of three TMEM buffers and
+//    O += P V into a TMEM accumulator; S runs two tiles ahead of P V, so the
+//    tensor pipe works on later tiles while the softmax warps work on one.  Descriptors are built once and advanced
+//    by constants: a 64-cycle MMA leaves the issuing thread little time.
 //  * Warps 2-9 run the softmax, two warps per MMA row: the warp pair that
 //    shares a TMEM lane quarter splits the 128 keys of a tile in halves and
 //    swaps partial row maxima through shared memory.  They apply the causal
 //    mask and scale, keep the running max / sum (base 2), write P (bf16) back
-//    over their half of the S buffer in TMEM, where the P V MMA reads it as its
-//    A operand, and rescale O in TMEM only when the max grows by more than 2^8
-//    (exact: the same reference max scales the numerator and the denominator).
-//    At the end they normalise O and store bf16 rows.
-//  * Persistent CTAs (at most one per SM) walk the item list.
+//    over their half of the S buffer, where the P V MMA reads it as its A
+//    operand, and rescale O in TMEM only when the max grows by more than 2^8
+//    (exact: the same reference max scales numerator and denominator).
+//  * When the query tiles alone would leave SMs idle, the keys of each tile
+//    are split over several units; each writes (O / l, m, l) per row and a
+//    merge kernel combines the pieces with log-sum-exp weights.
+//  * Persistent CTAs (at most one per SM) walk the unit list.
 #include <cstdint>
 #include <mutex>
 
@@ -39,85 +42,105 @@
 namespace pa {
 namespace {
 
-constexpr int kBlock = 16;        // tokens per physical block
-constexpr int kKeysPerTile = 128; // keys per K/V tile (8 blocks)
-constexpr int kRows = 128;        // MMA rows (tokens x group heads)
-constexpr int kStagesK = 2;       // K tile stages
-constexpr int kStagesV = 3;       // V tile stages (held from the S to the P V product)
-constexpr int kSBufs = 3;         // S / P buffers in TMEM
-constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quarter
+constexpr int kBlock = 16;         // tokens per physical block
+constexpr int kKeysPerTile = 128;  // keys per K/V tile (8 blocks)
+constexpr int kPagesPerTile = kKeysPerTile / kBlock;
+constexpr int kRows = 128;         // MMA rows of a query tile
+constexpr int kStagesK = 3;        // K tile stages
+constexpr int kStagesV = 2;        // V tile stages
+constexpr int kSBufs = 3;          // S / P buffers in TMEM
+constexpr int kSoftmaxWarps = 8;   // two per TMEM lane quarter
+constexpr int kKWarps = 4;         // warp 0 (which also loads Q) and warps 10-12
+constexpr int kVWarps = 3;         // warps 13-15
+constexpr int kWarpK1 = 10, kWarpV0 = 13;
+constexpr int kThreads = 512;
 constexpr float kNegInf = -INFINITY;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kWarpV = 2 + kSoftmaxWarps;    // V producer
-constexpr int kThreads = 32 * (kWarpV + 1);  // Q/K producer, MMA, softmax, V producer
+constexpr int kMaxSplit = 4;
 
 struct PrefillParams {
   const int32_t* block_tables;
   const int32_t* seq_lens;
   const int32_t* qsl;
   uint16_t* out;
+  float* part_o;   // [num_tokens * n_q * nsplit, D] (nsplit > 1)
+  float* part_ml;  // [num_tokens * n_q * nsplit, 2]
   unsigned* err;
-  int32_t num_blocks, max_blocks, num_seqs, num_tokens, n_q, n_kv, max_seq_len;
+  int32_t num_blocks, max_blocks, num_seqs, num_tokens, n_q, n_kv, max_seq_len, nsplit;
   float scale_log2;
 };
 
-// Query tiles of request s (0 unless it has q_len >= 2 and is valid).
-template <int TM>
-__device__ __forceinline__ int prefill_tiles(const PrefillParams& p, int s, bool report) {
-  const int a = __ldg(p.qsl + s), b = __ldg(p.qsl + s + 1);
-  const int ql = b - a;
-  if (ql < 2) return 0;
-  const int L = __ldg(p.seq_lens + s);
+// Whether request s runs here (q_len >= 2) and its lengths are valid.
+__device__ __forceinline__ bool prefill_request(const PrefillParams& p, int s, int& a, int& ql,
+                                                int& L, bool report) {
+  a = __ldg(p.qsl + s);
+  const int b = __ldg(p.qsl + s + 1);
+  ql = b - a;
+  if (ql < 2) return false;
+  L = __ldg(p.seq_lens + s);
   if (L < ql || L > p.max_seq_len || L > p.max_blocks * kBlock || a < 0 || b > p.num_tokens) {
     if (report) flag_error(p.err, DEVERR_BOUNDS);
-    return 0;
+    return false;
   }
+  return true;
+}
+
+// Query tiles of request s.
+template <int TM>
+__device__ __forceinline__ int prefill_tiles(const PrefillParams& p, int s, bool report) {
+  int a, ql, L;
+  if (!prefill_request(p, s, a, ql, L, report)) return 0;
   return (ql + TM - 1) / TM;
 }
 
-// Geometry of one item.
-struct Item {
-  int s, mt, g;
-  int q0;         // first query token of the tile
-  int ntok;       // valid query tokens in the tile
-  int p_first;    // position of the first query token
-  int kv_end;     // keys needed: 0 .. kv_end - 1
-  int nkt;        // K/V tiles
+// Geometry of one unit.
+struct Unit {
+  int s, g, ks;
+  int q0;       // first query token of the tile
+  int ntok;     // valid query tokens of the tile
+  int p_first;  // position of token q0
+  int kv_end;   // keys the tile needs: 0 .. kv_end - 1
+  int kt0, kt1; // K/V tiles of this unit (of ceil(kv_end / 128))
 };
 
-// Walks the item list (request-major, then query tile, then kv head).
+// Walks the unit list: request-major, then query tile, kv head, key split.
 template <int TM>
-struct ItemCursor {
-  int s = 0, tile_base = 0, tiles = 0;
-  __device__ __forceinline__ bool locate(const PrefillParams& p, long long item, Item& it) {
-    const long long tile = item / p.n_kv;
-    const int g = (int)(item % p.n_kv);
-    while (s < p.num_seqs && tile >= (long long)tile_base + tiles) {
-      tile_base += tiles;
+struct UnitCursor {
+  int s = 0, base = 0, tiles = 0;
+  __device__ __forceinline__ void init(const PrefillParams& p) {
+    s = 0;
+    base = 0;
+    tiles = p.num_seqs > 0 ? prefill_tiles<TM>(p, 0, false) : 0;
+  }
+  __device__ __forceinline__ bool locate(const PrefillParams& p, long long u, Unit& U) {
+    const long long per = (long long)p.n_kv * p.nsplit;
+    const long long tile = u / per;
+    const int rem = (int)(u % per);
+    while (s < p.num_seqs && tile >= (long long)base + tiles) {
+      base += tiles;
       ++s;
       tiles = s < p.num_seqs ? prefill_tiles<TM>(p, s, false) : 0;
     }
     if (s >= p.num_seqs) return false;
     const int a = __ldg(p.qsl + s), b = __ldg(p.qsl + s + 1);
     const int L = __ldg(p.seq_lens + s);
-    it.s = s;
-    it.mt = (int)(tile - tile_base);
-    it.g = g;
-    it.q0 = a + it.mt * TM;
-    it.ntok = min(TM, (b - a) - it.mt * TM);
-    it.p_first = L - (b - a) + it.mt * TM;
-    it.kv_end = it.p_first + it.ntok;
-    it.nkt = (it.kv_end + kKeysPerTile - 1) / kKeysPerTile;
+    const int ql = b - a;
+    const int first = (int)(tile - base) * TM;
+    U.s = s;
+    U.g = rem / p.nsplit;
+    U.ks = rem % p.nsplit;
+    U.q0 = a + first;
+    U.ntok = min(TM, ql - first);
+    U.p_first = L - ql + first;
+    U.kv_end = U.p_first + U.ntok;
+    const int nkt = (U.kv_end + kKeysPerTile - 1) / kKeysPerTile;
+    U.kt0 = U.ks * nkt / p.nsplit;
+    U.kt1 = (U.ks + 1) * nkt / p.nsplit;
     return true;
-  }
-  __device__ __forceinline__ void init(const PrefillParams& p) {
-    s = 0;
-    tile_base = 0;
-    tiles = p.num_seqs > 0 ? prefill_tiles<TM>(p, 0, false) : 0;
   }
 };
 
-struct PrefillBarriers {
+struct PrefillShared {
   uint64_t q_full, q_empty;
   uint64_t k_full[kStagesK], k_empty[kStagesK];
   uint64_t v_full[kStagesV], v_empty[kStagesV];
@@ -126,9 +149,9 @@ struct PrefillBarriers {
   uint64_t mma_done;
   uint32_t tmem_slot;
   int abort_flag;
-  long long total_items;
+  long long total_units;
   float xmax[2][2][kRows];  // partial row maxima: [tile parity][key half][row]
-  float xsum[2][kRows];     // partial row sums at the end of an item: [key half][row]
+  float xsum[2][2][kRows];  // partial row sums: [unit parity][key half][row]
 };
 
 // Byte offset of 16-byte chunk c (0..7) of row r inside a [rows][64 x bf16]
@@ -149,21 +172,64 @@ struct Ring {
   }
 };
 
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, int w, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(mbar)
+      : "memory");
+}
+
+// S = Q K^T for the query tile and a K tile (128 x 128 x D), issued by one
+// thread.  a, b: descriptors of the Q tile and the K tile; each K = 16 step
+// advances both start addresses by a compile-time offset.
+template <int D>
+__device__ __forceinline__ void issue_s_mma(uint32_t d_tmem, tc::Desc a, tc::Desc b) {
+  constexpr uint32_t HALF = kRows * 128;
+  constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(kRows, kKeysPerTile, 0, 0);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = ((kk >> 2) * HALF + (kk & 3) * 32) >> 4;
+    if (kk == 0)
+      tc::mma_bf16_pair<false>(d_tmem, a, off, b, off, IDESC_S);
+    else
+      tc::mma_bf16_pair<true>(d_tmem, a, off, b, off, IDESC_S);
+  }
+}
+
+// O += P V: P (bf16 pairs) of keys 64h .. 64h + 63 sits in columns
+// 64h .. 64h + 31 of the S buffer at p_tmem; V page kk of the tile
+// (descriptor b) is one K = 16 step.
+template <int D>
+__device__ __forceinline__ void issue_pv_mma(uint32_t o_tmem, uint32_t p_tmem, tc::Desc b,
+                                             bool first) {
+  constexpr uint32_t V_PAGE = (D / 64) * kBlock * 128;
+  constexpr uint32_t IDESC_O = tc::idesc_bf16_f32(kRows, D, 0, 1);
+  if (first)
+    tc::mma_bf16_tmem_a_pair<false>(o_tmem, p_tmem, b, 0, IDESC_O);
+  else
+    tc::mma_bf16_tmem_a_pair<true>(o_tmem, p_tmem, b, 0, IDESC_O);
+#pragma unroll
+  for (int kk = 1; kk < kPagesPerTile; ++kk)
+    tc::mma_bf16_tmem_a_pair<true>(o_tmem, p_tmem + (kk >> 2) * 64 + (kk & 3) * 8, b,
+                                   (kk * V_PAGE) >> 4, IDESC_O);
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap) {
-  constexpr int TM = kRows / G;       // query tokens per tile
-  constexpr int NH = D / 64;          // 64-element halves of head_dim
-  constexpr uint32_t HALF = kRows * 128;  // bytes of one [128 rows][64] block
-  constexpr uint32_t Q_BYTES = NH * HALF;
-  constexpr uint32_t KV_BYTES = NH * HALF;  // 128 keys
+  constexpr int TM = kRows / G;            // query tokens per tile
+  constexpr int NH = D / 64;               // 64-element halves of head_dim
+  constexpr uint32_t HALF = kRows * 128;   // bytes of one [128 rows][64] block
+  constexpr uint32_t Q_BYTES = NH * HALF;  // the query tile
+  constexpr uint32_t KV_BYTES = NH * HALF; // one K or V tile (128 keys)
+  constexpr uint32_t V_PAGE = NH * kBlock * 128;  // V tile: [page][half][16][64]
   constexpr uint32_t TMEM_COLS = 512;
-  constexpr uint32_t S_COL0 = 0, O_COL = kSBufs * kKeysPerTile;
+  constexpr uint32_t O_COL = kSBufs * kKeysPerTile;  // S buffers, then O
   static_assert(O_COL + D <= TMEM_COLS, "TMEM columns");
-  constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(kRows, kKeysPerTile, 0, 0);
-  constexpr uint32_t IDESC_O = tc::idesc_bf16_f32(kRows, D, 0, 1);
 
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
@@ -171,21 +237,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* q_s = base;
   unsigned char* k_s = q_s + Q_BYTES;
   unsigned char* v_s = k_s + kStagesK * KV_BYTES;
-  PrefillBarriers& B = *reinterpret_cast<PrefillBarriers*>(v_s + kStagesV * KV_BYTES);
+  PrefillShared& B = *reinterpret_cast<PrefillShared*>(v_s + kStagesV * KV_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // decode rows of the same step may use the SMs this grid leaves free
+  // the merge grid of split keys may start launching now
   asm volatile("griddepcontrol.launch_dependents;");
 
   if (threadIdx.x == 0) {
     mbar_init(smem_addr(&B.q_full), 1);
     mbar_init(smem_addr(&B.q_empty), 1);
     for (int i = 0; i < kStagesK; ++i) {
-      mbar_init(smem_addr(&B.k_full[i]), 1);
+      mbar_init(smem_addr(&B.k_full[i]), kKWarps);
       mbar_init(smem_addr(&B.k_empty[i]), 1);
     }
     for (int i = 0; i < kStagesV; ++i) {
-      mbar_init(smem_addr(&B.v_full[i]), 1);
+      mbar_init(smem_addr(&B.v_full[i]), kVWarps);
       mbar_init(smem_addr(&B.v_empty[i]), 1);
     }
     for (int i = 0; i < kSBufs; ++i) {
@@ -200,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     long long total = 0;
     for (int s = 0; s < p.num_seqs; ++s) total += prefill_tiles<TM>(p, s, blockIdx.x == 0);
-    B.total_items = total * p.n_kv;
+    B.total_units = total * p.n_kv * p.nsplit;
   }
   if (warp == 1) {
     tc::tmem_alloc(smem_addr(&B.tmem_slot), TMEM_COLS);
@@ -210,59 +276,79 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = B.tmem_slot;
-  const long long total_items = B.total_items;
+  const long long total_units = B.total_units;
   volatile int* abort_flag = &B.abort_flag;
 
-  if (warp == 0 || warp == kWarpV) {
+  const bool k_warp = warp == 0 || (warp >= kWarpK1 && warp < kWarpK1 + kKWarps - 1);
+  const bool v_warp = warp >= kWarpV0 && warp < kWarpV0 + kVWarps;
+  if (k_warp || v_warp) {
     // ============================================================ producers
     if (lane == 0) {
-      const bool is_k = (warp == 0);  // warp 0: Q and K, the last warp: V
-      const CUtensorMap* map = is_k ? &kmap : &vmap;
-      unsigned char* ring = is_k ? k_s : v_s;
-      uint64_t* full = is_k ? B.k_full : B.v_full;
-      uint64_t* empty = is_k ? B.k_empty : B.v_empty;
-      const uint32_t nst = is_k ? kStagesK : kStagesV;
-      ItemCursor<TM> cur;
+      // K warp k loads pages 2k, 2k+1 of each tile; V warp v pages 3v .. 3v+2
+      const int kidx = warp == 0 ? 0 : warp - kWarpK1 + 1;
+      const int pg_lo = k_warp ? 2 * kidx : 3 * (warp - kWarpV0);
+      const int pg_hi = k_warp ? pg_lo + 2 : min(pg_lo + 3, kPagesPerTile);
+      const CUtensorMap* map = k_warp ? &kmap : &vmap;
+      unsigned char* ring = k_warp ? k_s : v_s;
+      uint64_t* full = k_warp ? B.k_full : B.v_full;
+      uint64_t* empty = k_warp ? B.k_empty : B.v_empty;
+      const uint32_t nst = k_warp ? kStagesK : kStagesV;
+      UnitCursor<TM> cur;
       cur.init(p);
-      int n_item = 0, c = 0;
+      int n_out = 0, c = 0;
       Ring pos;
-      for (long long item = blockIdx.x; item < total_items; item += gridDim.x, ++n_item) {
-        Item it;
-        if (!cur.locate(p, item, it)) break;
-        if (is_k) {
-          if (n_item > 0) mbar_wait(smem_addr(&B.q_empty), (n_item - 1) & 1, p.err, abort_flag);
+      for (long long u = blockIdx.x; u < total_units; u += gridDim.x) {
+        Unit U;
+        if (!cur.locate(p, u, U)) break;
+        if (U.kt0 == U.kt1) continue;
+        if (warp == 0) {
+          if (n_out > 0) mbar_wait(smem_addr(&B.q_empty), (n_out - 1) & 1, p.err, abort_flag);
           mbar_arrive_expect_tx(smem_addr(&B.q_full), Q_BYTES);
 #pragma unroll
           for (int h = 0; h < NH; ++h)
-            tc::tma_load_3d(smem_addr(q_s + h * HALF), &qmap, h * 64, it.g * G, it.q0,
+            tc::tma_load_3d(smem_addr(q_s + h * HALF), &qmap, h * 64, U.g * G, U.q0,
                             smem_addr(&B.q_full));
         }
-        const int pages = (it.kv_end + kBlock - 1) / kBlock;
-        const int32_t* table = p.block_tables + (int64_t)it.s * p.max_blocks;
-        for (int kt = 0; kt < it.nkt; ++kt, ++c) {
-          const int p0 = kt * (kKeysPerTile / kBlock);
-          const int npg = min(kKeysPerTile / kBlock, pages - p0);
-          int phys[kKeysPerTile / kBlock];
+        ++n_out;
+        const int pages = (U.kv_end + kBlock - 1) / kBlock;
+        const int32_t* table = p.block_tables + (int64_t)U.s * p.max_blocks;
+        for (int kt = U.kt0; kt < U.kt1; ++kt, ++c) {
+          int phys[3];
           int nvalid = 0;
-          for (int i = 0; i < npg; ++i) {
-            phys[i] = __ldg(table + p0 + i);
-            if (phys[i] < 0 || phys[i] >= p.num_blocks) {
-              flag_error(p.err, DEVERR_BOUNDS);
-              phys[i] = -1;
-            } else {
-              ++nvalid;
+#pragma unroll
+          for (int i = 0; i < 3; ++i) {
+            const int lp = kt * kPagesPerTile + pg_lo + i;  // logical page
+            phys[i] = -1;
+            if (pg_lo + i < pg_hi && lp < pages) {
+              const int b = __ldg(table + lp);
+              if (b < 0 || b >= p.num_blocks) {
+                flag_error(p.err, DEVERR_BOUNDS);
+              } else {
+                phys[i] = b;
+                ++nvalid;
+              }
             }
           }
           const uint32_t st = pos.stage;
           if (c >= (int)nst) mbar_wait(smem_addr(&empty[st]), pos.phase ^ 1u, p.err, abort_flag);
-          mbar_arrive_expect_tx(smem_addr(&full[st]),
-                                (uint32_t)nvalid * NH * (kBlock * 128));
-          for (int i = 0; i < npg; ++i) {
-            if (phys[i] < 0) continue;
+          mbar_arrive_expect_tx(smem_addr(&full[st]), (uint32_t)nvalid * NH * (kBlock * 128));
+          unsigned char* stage = ring + st * KV_BYTES;
 #pragma unroll
-            for (int h = 0; h < NH; ++h)
-              tc::tma_load_3d(smem_addr(ring + st * KV_BYTES + h * HALF + i * (kBlock * 128)),
-                              map, h * 64, it.g, phys[i] * kBlock, smem_addr(&full[st]));
+          for (int i = 0; i < 3; ++i) {
+            if (phys[i] < 0) continue;
+            const int pg = pg_lo + i;
+            if (k_warp) {
+#pragma unroll
+              for (int h = 0; h < NH; ++h)
+                tc::tma_load_3d(smem_addr(stage + h * HALF + pg * (kBlock * 128)), map, h * 64,
+                                U.g, phys[i] * kBlock, smem_addr(&full[st]));
+            } else if (NH == 2) {
+              tma_load_4d(smem_addr(stage + pg * V_PAGE), map, 0, U.g, phys[i] * kBlock, 0,
+                          smem_addr(&full[st]));
+            } else {
+              tc::tma_load_3d(smem_addr(stage + pg * V_PAGE), map, 0, U.g, phys[i] * kBlock,
+                              smem_addr(&full[st]));
+            }
           }
           pos.next(nst);
         }
@@ -270,78 +356,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       // never hand back shared memory with a TMA copy still landing in it
       for (int i = max(0, c - (int)nst); i < c; ++i)
         mbar_wait(smem_addr(&full[i % nst]), (i / nst) & 1, p.err, abort_flag);
-      if (is_k && n_item > 0)
-        mbar_wait(smem_addr(&B.q_full), (n_item - 1) & 1, p.err, abort_flag);
+      if (warp == 0 && n_out > 0)
+        mbar_wait(smem_addr(&B.q_full), (n_out - 1) & 1, p.err, abort_flag);
     }
   } else if (warp == 1) {
     // ============================================================ MMA issuer
+    // (waits spin without the suspend hint: this thread's latency is the
+    // tensor pipe's)
     if (lane == 0) {
-      ItemCursor<TM> cur;
+      static_assert(kStagesK == 3 && kStagesV == 2, "descriptor selection below");
+      const tc::Desc qd = tc::sw128_desc_pair(smem_addr(q_s), 16, 1024);
+      const tc::Desc kd0 = tc::sw128_desc_pair(smem_addr(k_s), 16, 1024);
+      const tc::Desc kd1 = tc::sw128_desc_pair(smem_addr(k_s + KV_BYTES), 16, 1024);
+      const tc::Desc kd2 = tc::sw128_desc_pair(smem_addr(k_s + 2 * KV_BYTES), 16, 1024);
+      const tc::Desc vd0 = tc::sw128_desc_pair(smem_addr(v_s), kBlock * 128, 1024);
+      const tc::Desc vd1 = tc::sw128_desc_pair(smem_addr(v_s + KV_BYTES), kBlock * 128, 1024);
+      UnitCursor<TM> cur;
       cur.init(p);
-      int n_item = 0;
-      uint32_t ntiles = 0;  // K/V tiles so far (all items)
-      Ring kr, vr, sbr, prev;  // K stages, V stages, S buffers, S buffer of the last tile
-      const uint32_t q_addr = smem_addr(q_s);
-      bool issued = false;
-      for (long long item = blockIdx.x; item < total_items; item += gridDim.x, ++n_item) {
-        Item it;
-        if (!cur.locate(p, item, it)) break;
-        mbar_wait(smem_addr(&B.q_full), n_item & 1, p.err, abort_flag);
-        auto issue_pv = [&](const Ring& pb, bool first) {
-          mbar_wait(smem_addr(&B.p_full[pb.stage]), pb.phase, p.err, abort_flag);
-          mbar_wait(smem_addr(&B.v_full[vr.stage]), vr.phase, p.err, abort_flag);
-          if (first && n_item > 0)
-            mbar_wait(smem_addr(&B.o_empty), (n_item - 1) & 1, p.err, abort_flag);
-          tc::fence_after_sync();
-          // P (bf16 pairs) of keys 64h .. 64h + 63 sits in columns 64h .. 64h + 31
-          // of the S buffer it came from
-          const uint32_t pt = tmem + S_COL0 + pb.stage * kKeysPerTile;
-          const uint32_t va = smem_addr(v_s + vr.stage * KV_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < kKeysPerTile / 16; ++kk) {
-            const uint64_t bd = tc::sw128_desc(va + kk * 2048, HALF, 1024);
-            tc::mma_bf16_tmem_a(tmem + O_COL, pt + (kk >> 2) * 64 + (kk & 3) * 8, bd, IDESC_O,
-                                (first && kk == 0) ? 0u : 1u);
-          }
-          tc::commit(smem_addr(&B.v_empty[vr.stage]));
-          tc::commit(smem_addr(&B.pv_done[pb.stage]));
-          vr.next(kStagesV);
-        };
-        for (int kt = 0; kt < it.nkt; ++kt, ++ntiles) {
-          mbar_wait(smem_addr(&B.k_full[kr.stage]), kr.phase, p.err, abort_flag);
-          // the S buffer holds P of the tile kSBufs back until its PV has run
-          if (ntiles >= kSBufs)
-            mbar_wait(smem_addr(&B.pv_done[sbr.stage]), sbr.phase ^ 1u, p.err, abort_flag);
-          tc::fence_after_sync();
-          const uint32_t ka = smem_addr(k_s + kr.stage * KV_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t ad =
-                tc::sw128_desc(q_addr + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = tc::sw128_desc(ka + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024);
-            tc::mma_bf16(tmem + S_COL0 + sbr.stage * kKeysPerTile, ad, bd, IDESC_S,
-                         kk > 0 ? 1u : 0u);
-          }
-          tc::commit(smem_addr(&B.s_full[sbr.stage]));
-          tc::commit(smem_addr(&B.k_empty[kr.stage]));
-          kr.next(kStagesK);
-          if (kt == it.nkt - 1) tc::commit(smem_addr(&B.q_empty));
-          if (kt > 0) issue_pv(prev, kt == 1);
-          prev = sbr;
-          sbr.next(kSBufs);
-          issued = true;
+      int n_out = 0;
+      uint32_t ntiles = 0;  // S products issued so far (all units)
+      Ring kr, vr, sr_, pr;  // K stages, V stages, S buffer of the next S / of the next P V
+      // S of the next tile into the S buffer at sr_ (which held P three tiles
+      // back: its P V must have run)
+      auto issue_s = [&](bool last) {
+        mbar_wait_spin(smem_addr(&B.k_full[kr.stage]), kr.phase, p.err, abort_flag);
+        if (ntiles >= kSBufs)
+          mbar_wait_spin(smem_addr(&B.pv_done[sr_.stage]), sr_.phase ^ 1u, p.err, abort_flag);
+        tc::fence_after_sync();
+        issue_s_mma<D>(tmem + sr_.stage * kKeysPerTile, qd,
+                       kr.stage == 0 ? kd0 : (kr.stage == 1 ? kd1 : kd2));
+        tc::commit(smem_addr(&B.s_full[sr_.stage]));
+        tc::commit(smem_addr(&B.k_empty[kr.stage]));
+        if (last) tc::commit(smem_addr(&B.q_empty));
+        kr.next(kStagesK);
+        sr_.next(kSBufs);
+        ++ntiles;
+      };
+      // O += P V for the next tile (P in the S buffer at pr, V at vr)
+      auto issue_pv = [&](bool first) {
+        mbar_wait_spin(smem_addr(&B.p_full[pr.stage]), pr.phase, p.err, abort_flag);
+        mbar_wait_spin(smem_addr(&B.v_full[vr.stage]), vr.phase, p.err, abort_flag);
+        if (first && n_out > 0)
+          mbar_wait_spin(smem_addr(&B.o_empty), (n_out - 1) & 1, p.err, abort_flag);
+        tc::fence_after_sync();
+        issue_pv_mma<D>(tmem + O_COL, tmem + pr.stage * kKeysPerTile, vr.stage ? vd1 : vd0,
+                        first);
+        tc::commit(smem_addr(&B.v_empty[vr.stage]));
+        tc::commit(smem_addr(&B.pv_done[pr.stage]));
+        vr.next(kStagesV);
+        pr.next(kSBufs);
+      };
+      for (long long u = blockIdx.x; u < total_units; u += gridDim.x) {
+        Unit U;
+        if (!cur.locate(p, u, U)) break;
+        if (U.kt0 == U.kt1) continue;
+        const int n = U.kt1 - U.kt0;
+        mbar_wait_spin(smem_addr(&B.q_full), n_out & 1, p.err, abort_flag);
+        // S runs two tiles ahead of P V, so the softmax of a tile never waits
+        // for the P V of the one before it to be issued
+        issue_s(n == 1);
+        if (n > 1) issue_s(n == 2);
+        for (int j = 0; j < n; ++j) {
+          if (j + 2 < n) issue_s(j + 3 == n);
+          issue_pv(j == 0);
         }
-        issue_pv(prev, it.nkt == 1);
         tc::commit(smem_addr(&B.o_full));
+        ++n_out;
       }
-      if (issued) {
+      if (ntiles > 0) {
         tc::commit(smem_addr(&B.mma_done));
-        mbar_wait(smem_addr(&B.mma_done), 0, p.err, abort_flag);
+        mbar_wait_spin(smem_addr(&B.mma_done), 0, p.err, abort_flag);
       }
     }
   } else {
     // ============================================================ softmax
-    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int quarter = warp & 3;    // TMEM lanes 32*quarter .. +31
     const int kh = (warp - 2) >> 2;  // key half of each tile: 64*kh .. 64*kh + 63
     const int r = quarter * 32 + lane;
     const int pair_bar = 1 + quarter;  // named barrier of the two warps on these rows
@@ -354,19 +443,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool pos_scale = sl2 > 0.f;
     const float mul = pos_scale ? 1.f : sl2;
     const float emul = pos_scale ? sl2 : 1.f;
-    ItemCursor<TM> cur;
+    UnitCursor<TM> cur;
     cur.init(p);
-    int n_item = 0;
+    int n_out = 0;
     Ring sbr, prev, vr;  // S buffer of this tile and of the last one, V stage
     uint32_t xpar = 0;   // exchange slot parity
-    for (long long item = blockIdx.x; item < total_items; item += gridDim.x, ++n_item) {
-      Item it;
-      if (!cur.locate(p, item, it)) break;
-      const bool row_valid = tl < it.ntok;
-      const int p_row = row_valid ? it.p_first + tl : it.kv_end - 1;
+    for (long long u = blockIdx.x; u < total_units; u += gridDim.x) {
+      Unit U;
+      if (!cur.locate(p, u, U)) break;
+      const bool row_valid = tl < U.ntok;
+      const int64_t row = (int64_t)(U.q0 + tl) * p.n_q + U.g * G + hl;
+      if (U.kt0 == U.kt1) {
+        // a key split with no tile (fewer tiles than splits): an empty piece
+        if (kh == 0 && row_valid)
+          *reinterpret_cast<float2*>(p.part_ml + (row * p.nsplit + U.ks) * 2) =
+              make_float2(kNegInf, 0.f);
+        continue;
+      }
+      const int p_row = row_valid ? U.p_first + tl : U.kv_end - 1;
       float m_ref = kNegInf, l = 0.f;
-      for (int kt = 0; kt < it.nkt; ++kt) {
-        const uint32_t s_cols = tmem + lane_addr + S_COL0 + sbr.stage * kKeysPerTile + kh * 64;
+      for (int kt = U.kt0; kt < U.kt1; ++kt) {
+        const uint32_t s_cols = tmem + lane_addr + sbr.stage * kKeysPerTile + kh * 64;
         mbar_wait(smem_addr(&B.s_full[sbr.stage]), sbr.phase, p.err, abort_flag);
         tc::fence_after_sync();
         uint32_t sr[64];
@@ -375,9 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_wait_ld();
 
         // causal mask and the max of this half (three-input max, 4 chains)
-        const int k0 = kt * kKeysPerTile + kh * 64;
-        const int lim = p_row - k0;  // keys c <= lim of this half are visible
-        float m4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+        const int lim = p_row - (kt * kKeysPerTile + kh * 64);  // keys c <= lim visible
         if (__all_sync(0xffffffffu, lim >= 63)) {
           if (!pos_scale) {
 #pragma unroll
@@ -388,20 +483,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 64; ++c)
             sr[c] = __float_as_uint((c <= lim) ? __uint_as_float(sr[c]) * mul : kNegInf);
         }
+        float m4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
 #pragma unroll
         for (int c = 0; c < 64; c += 8) {
-          m4[(c >> 3) & 3] = fmax3(m4[(c >> 3) & 3], __uint_as_float(sr[c]),
-                                   __uint_as_float(sr[c + 1]));
-          m4[(c >> 3) & 3] = fmax3(m4[(c >> 3) & 3], __uint_as_float(sr[c + 2]),
-                                   __uint_as_float(sr[c + 3]));
-          m4[(c >> 3) & 3] = fmax3(m4[(c >> 3) & 3], __uint_as_float(sr[c + 4]),
-                                   __uint_as_float(sr[c + 5]));
-          m4[(c >> 3) & 3] = fmax3(m4[(c >> 3) & 3], __uint_as_float(sr[c + 6]),
-                                   __uint_as_float(sr[c + 7]));
+          const int q = (c >> 3) & 3;
+          m4[q] = fmax3(m4[q], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+          m4[q] = fmax3(m4[q], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+          m4[q] = fmax3(m4[q], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+          m4[q] = fmax3(m4[q], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
         }
         const float mh = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-        // swap the half maxima with the other warp on these rows (slots alternate
-        // with the tile parity, so a slot is rewritten only after a later barrier)
+        // swap the half maxima with the other warp on these rows (slots
+        // alternate with the tile parity, so a slot is rewritten only after a
+        // later barrier)
         B.xmax[xpar][kh][r] = mh;
         named_barrier(pair_bar, 64);
         float mx = fmaxf(mh, B.xmax[xpar][kh ^ 1][r]);
@@ -409,16 +503,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // both warps of the pair see the same maxima and take the same branch
         float alpha = 1.f;
         if (m_ref == kNegInf) {
-          m_ref = mx;  // first tile: O not yet written
+          m_ref = mx;  // first tile with a visible key: O holds zeros so far
         } else if (mx > m_ref + kRescaleThreshold) {
           alpha = fast_exp2(m_ref - mx);
           l *= alpha;
           m_ref = mx;
         }
         // p = 2^(emul * s - m_ref), packed in bf16 pairs in place (sr[j] holds
-        // keys 2j, 2j+1 of this half), stored over the first 32 columns of the half
+        // keys 2j, 2j+1 of this half), stored over the first 32 columns of the
+        // half; a row with no visible key so far gets p = 0
+        const float mu = (m_ref == kNegInf) ? 0.f : m_ref;
         const float2 e2 = make_float2(emul, emul);
-        const float2 nm2 = make_float2(-m_ref, -m_ref);
+        const float2 nm2 = make_float2(-mu, -mu);
         float2 l4[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) l4[j] = make_float2(0.f, 0.f);
@@ -431,8 +527,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           sr[j] = pack_bf16x2(pj.x, pj.y);
         }
         tc::tmem_st32(s_cols, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        l += ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
-        // rescale this half of the running output when the reference max moved (rare)
+        l += ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) +
+             ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
+        // rescale this half of the running output when the reference max moved
+        // (rare); the P V product of the last tile must have landed first
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
           mbar_wait(smem_addr(&B.pv_done[prev.stage]), prev.phase, p.err, abort_flag);
           tc::fence_after_sync();
@@ -448,18 +546,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // keys past the last needed one: V rows there may hold stale or
-        // poisoned data; zero them so that P = 0 times V stays 0 (each warp of
-        // the pair clears half of the row's 16-byte chunks)
-        const int kv_local = it.kv_end - kt * kKeysPerTile;
+        // poisoned data; zero them so that P = 0 times V stays 0.  Thread r
+        // clears half of the 16-byte chunks of V row 64 kh + r / 2.
+        const int kv_local = U.kv_end - kt * kKeysPerTile;
         if (kv_local < kKeysPerTile) {
           mbar_wait(smem_addr(&B.v_full[vr.stage]), vr.phase, p.err, abort_flag);
-          if (r >= kv_local) {
-            unsigned char* vrow = v_s + vr.stage * KV_BYTES;
+          const int key = kh * 64 + (r >> 1);
+          if (key >= kv_local) {
+            unsigned char* vpage = v_s + vr.stage * KV_BYTES + (key >> 4) * V_PAGE;
 #pragma unroll
             for (int h = 0; h < NH; ++h)
 #pragma unroll
-              for (int c8 = 4 * kh; c8 < 4 * kh + 4; ++c8)
-                *reinterpret_cast<uint4*>(vrow + h * HALF + sw128_chunk(r, c8)) =
+              for (int c8 = 4 * (r & 1); c8 < 4 * (r & 1) + 4; ++c8)
+                *reinterpret_cast<uint4*>(vpage + h * (kBlock * 128) + sw128_chunk(key & 15, c8)) =
                     make_uint4(0, 0, 0, 0);
           }
         }
@@ -473,19 +572,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         vr.next(kStagesV);
         xpar ^= 1u;
       }
-      // epilogue: O / l -> bf16 rows; each warp of the pair writes half of d
-      B.xsum[kh][r] = l;
+      // epilogue: each warp of the pair handles half of d
+      const uint32_t upar = n_out & 1;
+      B.xsum[upar][kh][r] = l;
       named_barrier(pair_bar, 64);
-      const float inv = 1.f / (l + B.xsum[kh ^ 1][r]);
-      mbar_wait(smem_addr(&B.o_full), n_item & 1, p.err, abort_flag);
+      const float ltot = l + B.xsum[upar][kh ^ 1][r];
+      const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
+      mbar_wait(smem_addr(&B.o_full), upar, p.err, abort_flag);
       tc::fence_after_sync();
-      uint16_t* orow = p.out + ((int64_t)(it.q0 + tl) * p.n_q + it.g * G + hl) * D + kh * (D / 2);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         uint32_t o[32];
         tc::tmem_ld32(tmem + lane_addr + O_COL + kh * (D / 2) + c * 32, o);
         tc::tmem_wait_ld();
-        if (row_valid) {
+        if (!row_valid) continue;
+        if (p.nsplit == 1) {
+          uint16_t* orow = p.out + row * D + kh * (D / 2) + c * 32;
 #pragma unroll
           for (int j = 0; j < 32; j += 8) {
             uint4 w;
@@ -493,13 +595,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             w.y = pack_bf16x2(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
             w.z = pack_bf16x2(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv);
             w.w = pack_bf16x2(__uint_as_float(o[j + 6]) * inv, __uint_as_float(o[j + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + c * 32 + j) = w;
+            *reinterpret_cast<uint4*>(orow + j) = w;
           }
+        } else {
+          float* prow = p.part_o + (row * p.nsplit + U.ks) * D + kh * (D / 2) + c * 32;
+#pragma unroll
+          for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4*>(prow + j) =
+                make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
+                            __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
         }
       }
+      if (p.nsplit > 1 && kh == 0 && row_valid)
+        *reinterpret_cast<float2*>(p.part_ml + (row * p.nsplit + U.ks) * 2) =
+            make_float2(ltot > 0.f ? m_ref : kNegInf, ltot);
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&B.o_empty));
+      ++n_out;
     }
   }
 
@@ -509,6 +622,76 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// Combines the key-split pieces of the prefill rows: one warp per (token, q
+// head) of a request with q_len >= 2; out = sum_i w_i (O_i / l_i) / sum_i w_i
+// with w_i = l_i 2^(m_i - max m).  Pieces with l = 0 saw no key.
+template <int D>
+__global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int E = D / 32;  // columns per lane
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= (long long)p.num_tokens * p.n_q) return;
+  const int token = (int)(row / p.n_q);
+  if (token < __ldg(p.qsl) || token >= __ldg(p.qsl + p.num_seqs)) return;
+  // the request of this token: the last s with qsl[s] <= token
+  int lo = 0, hi = p.num_seqs;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(p.qsl + mid) <= token)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  int a, ql, L;
+  if (!prefill_request(p, lo, a, ql, L, false)) return;
+  const int ns = p.nsplit;
+  float m[kMaxSplit], w[kMaxSplit];
+  float mmax = kNegInf;
+#pragma unroll
+  for (int i = 0; i < kMaxSplit; ++i) {
+    m[i] = kNegInf;
+    w[i] = 0.f;
+    if (i < ns) {
+      const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (row * ns + i) * 2);
+      if (ml.y > 0.f) {
+        m[i] = ml.x;
+        w[i] = ml.y;
+        mmax = fmaxf(mmax, ml.x);
+      }
+    }
+  }
+  float wsum = 0.f;
+#pragma unroll
+  for (int i = 0; i < kMaxSplit; ++i) {
+    w[i] = w[i] > 0.f ? w[i] * fast_exp2(m[i] - mmax) : 0.f;
+    wsum += w[i];
+  }
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll
+  for (int i = 0; i < kMaxSplit; ++i) {
+    if (w[i] > 0.f) {
+      const float* o = p.part_o + (row * ns + i) * D + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; e += 2) {
+        const float2 v = *reinterpret_cast<const float2*>(o + e);
+        acc[e] = fmaf(w[i], v.x, acc[e]);
+        acc[e + 1] = fmaf(w[i], v.y, acc[e + 1]);
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  uint16_t* orow = p.out + row * D + lane * E;
+  if constexpr (E == 4) {
+    *reinterpret_cast<uint2*>(orow) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                                 pack_bf16x2(acc[2] * inv, acc[3] * inv));
+  } else {
+    *reinterpret_cast<uint32_t*>(orow) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
   }
 }
 
@@ -531,17 +714,13 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D bf16 map {inner, mid, outer} with a {64, box_mid, box_outer} box and
-// the 128-byte swizzle.
-cudaError_t make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t mid,
-                     uint64_t outer, uint32_t box_mid, uint32_t box_outer) {
+// bf16 tensor map with the 128-byte swizzle (the box's inner extent is 64).
+cudaError_t make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
+                     const cuuint64_t* strides, const cuuint32_t* box) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  const cuuint64_t dims[3] = {inner, mid, outer};
-  const cuuint64_t strides[2] = {inner * 2, inner * mid * 2};
-  const cuuint32_t box[3] = {64, box_mid, box_outer};
-  const cuuint32_t es[3] = {1, 1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims,
                          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -551,18 +730,27 @@ cudaError_t make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t m
 template <int D, int G>
 size_t prefill_smem_bytes() {
   constexpr size_t half = kRows * 128;
-  return 1024 + (size_t)(D / 64) * half * (1 + kStagesK + kStagesV) +
-         sizeof(PrefillBarriers);
+  return 1024 + (size_t)(D / 64) * half * (1 + kStagesK + kStagesV) + sizeof(PrefillShared);
+}
+
+size_t split_bytes(int num_tokens, int num_q_heads, int head_dim, int nsplit) {
+  if (nsplit <= 1) return 0;
+  const size_t rows = (size_t)num_tokens * num_q_heads * nsplit;
+  return ((rows * head_dim * sizeof(float) + 255) & ~size_t(255)) +
+         ((rows * 2 * sizeof(float) + 255) & ~size_t(255));
 }
 
 template <int D, int G>
-cudaError_t launch_prefill_t(const AttnArgs& a, int sm_count, cudaStream_t stream) {
+cudaError_t launch_prefill_t(const AttnArgs& a, const PrefillPlan& plan, void* ws, int sm_count,
+                             cudaStream_t stream) {
   constexpr int TM = kRows / G;
   PrefillParams p;
   p.block_tables = a.block_tables;
   p.seq_lens = a.seq_lens;
   p.qsl = a.query_start_loc;
   p.out = a.out;
+  p.part_o = nullptr;
+  p.part_ml = nullptr;
   p.err = a.err;
   p.num_blocks = a.num_blocks;
   p.max_blocks = a.max_blocks;
@@ -571,18 +759,48 @@ cudaError_t launch_prefill_t(const AttnArgs& a, int sm_count, cudaStream_t strea
   p.n_q = a.num_q_heads;
   p.n_kv = a.num_kv_heads;
   p.max_seq_len = a.max_seq_len;
+  p.nsplit = plan.nsplit;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  if (plan.nsplit > 1) {
+    const size_t rows = (size_t)a.num_tokens * a.num_q_heads * plan.nsplit;
+    p.part_o = static_cast<float*>(ws);
+    p.part_ml = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) +
+                                         ((rows * D * sizeof(float) + 255) & ~size_t(255)));
+  }
+  const cuuint64_t nkv = (cuuint64_t)a.num_kv_heads;
+  const cuuint64_t rows = (cuuint64_t)a.num_blocks * kBlock;
   CUtensorMap qm, km, vm;
-  cudaError_t e = make_map(&qm, a.q, D, a.num_q_heads, a.num_tokens, G, TM);
-  if (e != cudaSuccess) return e;
-  e = make_map(&km, a.k_cache, D, a.num_kv_heads, (uint64_t)a.num_blocks * kBlock, 1, kBlock);
-  if (e != cudaSuccess) return e;
-  e = make_map(&vm, a.v_cache, D, a.num_kv_heads, (uint64_t)a.num_blocks * kBlock, 1, kBlock);
-  if (e != cudaSuccess) return e;
-  // upper bound of the number of items; the kernel reads the exact count
+  {
+    const cuuint64_t dims[3] = {D, (cuuint64_t)a.num_q_heads, (cuuint64_t)a.num_tokens};
+    const cuuint64_t strides[2] = {D * 2, (cuuint64_t)a.num_q_heads * D * 2};
+    const cuuint32_t box[3] = {64, G, TM};
+    cudaError_t e = make_map(&qm, a.q, 3, dims, strides, box);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const cuuint64_t dims[3] = {D, nkv, rows};
+    const cuuint64_t strides[2] = {D * 2, nkv * D * 2};
+    const cuuint32_t box[3] = {64, 1, kBlock};
+    cudaError_t e = make_map(&km, a.k_cache, 3, dims, strides, box);
+    if (e != cudaSuccess) return e;
+    if (D == 64) {
+      e = make_map(&vm, a.v_cache, 3, dims, strides, box);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  if (D == 128) {
+    // one box per page with both 64-column halves, the half as the outermost
+    // box dimension: shared-memory layout [half][16 tokens][64]
+    const cuuint64_t dims[4] = {64, nkv, rows, 2};
+    const cuuint64_t strides[3] = {D * 2, nkv * D * 2, 128};
+    const cuuint32_t box[4] = {64, 1, kBlock, 2};
+    cudaError_t e = make_map(&vm, a.v_cache, 4, dims, strides, box);
+    if (e != cudaSuccess) return e;
+  }
+  // upper bound of the number of units; the kernel reads the exact count
   const long long tiles_bound = (long long)a.num_tokens / TM + a.num_seqs;
-  long long items_bound = tiles_bound * a.num_kv_heads;
-  const int grid = (int)(items_bound < sm_count ? items_bound : sm_count);
+  const long long units_bound = tiles_bound * a.num_kv_heads * plan.nsplit;
+  const int grid = (int)(units_bound < sm_count ? units_bound : sm_count);
   if (grid <= 0) return cudaSuccess;
   const size_t smem = prefill_smem_bytes<D, G>();
   auto kern = prefill_kernel<D, G>;
@@ -590,12 +808,27 @@ cudaError_t launch_prefill_t(const AttnArgs& a, int sm_count, cudaStream_t strea
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   kern<<<grid, kThreads, smem, stream>>>(p, qm, km, vm);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || plan.nsplit == 1) return e;
+  // the merge may launch while the prefill grid runs; it waits for that grid
+  // with griddepcontrol.wait before reading a piece
+  const long long mrows = (long long)a.num_tokens * a.num_q_heads;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((mrows + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_merge_kernel<D>, p);
 }
 
 }  // namespace
@@ -605,12 +838,35 @@ bool prefill_supported(int head_dim, int group, int num_kv_heads) {
          (group == 1 || group == 2 || group == 4 || group == 8) && num_kv_heads >= 1;
 }
 
-size_t prefill_workspace_bytes(int, int, int, int, int) { return 0; }
+// Key splits: enough units to fill about 70% of the SMs when the query tiles
+// alone would not (every token counted as a prefill row), at least four K/V
+// tiles per piece of the longest request, at most kMaxSplit, and no more
+// pieces than max_bytes of workspace hold.
+PrefillPlan prefill_plan(int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+                         int max_q_len, int max_seq_len, int sm_count, size_t max_bytes) {
+  PrefillPlan plan;
+  plan.nsplit = 1;
+  plan.bytes = 0;
+  if (max_q_len < 2 || num_kv_heads <= 0 || num_q_heads < num_kv_heads || head_dim <= 0)
+    return plan;
+  const int tm = kRows / (num_q_heads / num_kv_heads);
+  const long long units = (long long)((num_tokens + tm - 1) / tm) * num_kv_heads;
+  const int tiles = (max_seq_len + kKeysPerTile - 1) / kKeysPerTile;
+  int ns = 1;
+  while (ns < kMaxSplit && units * ns * 10 < (long long)sm_count * 7 && tiles >= 4 * (ns + 1))
+    ++ns;
+  while (ns > 1 && split_bytes(num_tokens, num_q_heads, head_dim, ns) > max_bytes) --ns;
+  plan.nsplit = ns;
+  plan.bytes = split_bytes(num_tokens, num_q_heads, head_dim, ns);
+  return plan;
+}
 
-cudaError_t launch_prefill(const AttnArgs& a, void*, size_t, int sm_count, cudaStream_t stream) {
+cudaError_t launch_prefill(const AttnArgs& a, const PrefillPlan& plan, void* ws, int sm_count,
+                           cudaStream_t stream) {
   const int group = a.num_q_heads / a.num_kv_heads;
-#define PA_PREFILL_CASE(D_, G_) \
-  if (a.head_dim == D_ && group == G_) return launch_prefill_t<D_, G_>(a, sm_count, stream);
+#define PA_PREFILL_CASE(D_, G_)     \
+  if (a.head_dim == D_ && group == G_) \
+    return launch_prefill_t<D_, G_>(a, plan, ws, sm_count, stream);
   PA_PREFILL_CASE(128, 1)
   PA_PREFILL_CASE(128, 2)
   PA_PREFILL_CASE(128, 4)

@@ -83,6 +83,18 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo, uint
   return d;
 }
 
+// The same descriptor as two 32-bit words.  The start address sits in the
+// low 14 bits of the low word (16-byte units; shared memory is below 256 KB,
+// so it never carries), so a descriptor for an address `off` bytes further is
+// lo + (off >> 4): one add per MMA instead of rebuilding 64 bits.
+struct Desc {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ Desc sw128_desc_pair(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  const uint64_t d = sw128_desc(addr, lbo, sbo);
+  return Desc{(uint32_t)d, (uint32_t)(d >> 32)};
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B and an fp32
 // accumulator: D format F32 (1) at [4,6), A format BF16 (1) at [7,10),
 // B format BF16 (1) at [10,13), A / B major (0 = K, 1 = MN) at bits 15 / 16,
@@ -100,6 +112,32 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// mma_bf16 with descriptors given as word pairs advanced by a_off / b_off
+// 16-byte units, and a compile-time accumulate flag.
+template <bool ACC>
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, Desc a, uint32_t a_off, Desc b,
+                                              uint32_t b_off, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .b64 da, db;\n\t.reg .pred p;\n\t"
+      "mov.b64 da, {%1, %2};\n\t"
+      "mov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a.lo + a_off), "r"(a.hi), "r"(b.lo + b_off), "r"(b.hi), "r"(idesc), "n"(ACC ? 1 : 0)
+      : "memory");
+}
+template <bool ACC>
+__device__ __forceinline__ void mma_bf16_tmem_a_pair(uint32_t d_tmem, uint32_t a_tmem, Desc b,
+                                                     uint32_t b_off, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .b64 db;\n\t.reg .pred p;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b.lo + b_off), "r"(b.hi), "r"(idesc), "n"(ACC ? 1 : 0)
       : "memory");
 }
 

@@ -53,6 +53,8 @@ def _load() -> ctypes.CDLL:
     L.pa_reshape_and_cache.restype = ctypes.c_int
     L.pa_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     L.pa_workspace_size.restype = sz
+    L.pa_prefill_splits.argtypes = [i32, i32, i32, i32, i32, i32]
+    L.pa_prefill_splits.restype = ctypes.c_int
     L.pa_paged_attention.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, vp, vp, i32,
                                      i32, i32, i32, f32, vp, vp, sz, vp]
     L.pa_paged_attention.restype = ctypes.c_int
@@ -132,6 +134,16 @@ def workspace_size(num_seqs: int, num_tokens: int, num_q_heads: int, num_kv_head
                                       max_q_len, max_seq_len))
     if n == 0:
         raise PagedAttnError(1, "pa_workspace_size rejected the arguments or found no device")
+    return n
+
+
+def prefill_splits(num_tokens: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                   max_q_len: int, max_seq_len: int) -> int:
+    """Key pieces the prefill kernel uses for these sizes (1 = no split)."""
+    n = int(_load().pa_prefill_splits(num_tokens, num_q_heads, num_kv_heads, head_dim,
+                                      max_q_len, max_seq_len))
+    if n == 0:
+        raise PagedAttnError(1, "pa_prefill_splits rejected the arguments or found no device")
     return n
 
 

@@ -41,6 +41,10 @@ def _batch(lens, q_lens, nq=32, nkv=8, d=128, seed=0, extra_blocks=9):
     ([600], [200], 64, 8, 128),                   # group 8: 16 tokens per tile
     ([333, 41], [150, 41], 8, 2, 64),             # head_dim 64
     ([250], [250], 4, 1, 64),                     # multi-query, head_dim 64
+    ([4096], [64], 32, 8, 128),                   # two query tiles: keys in 4 pieces + merge
+    ([4096, 100], [64, 100], 32, 8, 128),         # short request: pieces with no key tile
+    ([1100], [1024], 8, 8, 128),                  # rows that see no key of a piece
+    ([3000], [40], 8, 2, 64),                     # head_dim 64, keys in pieces
 ])
 def test_prefill_edge_shapes(lens, q_lens, nq, nkv, d):
     b = _batch(lens, q_lens, nq, nkv, d, seed=sum(lens) % 97)
@@ -93,3 +97,19 @@ def test_prefill_chunk_equals_rows_of_full_prompt():
     a = to_f64(out_full)[256:]
     c = to_f64(out_chunk)
     assert_attn_close(c, a, "chunk vs full prompt")
+
+
+@pytest.mark.parametrize("lens,q_lens,nq,nkv,d,pieces", [
+    ([4096], [64], 32, 8, 128, 4),
+    ([4096, 100], [64, 100], 32, 8, 128, 3),
+    ([1100], [1024], 8, 8, 128, 2),
+    ([3000], [40], 8, 2, 64, 4),
+    ([300], [77], 32, 8, 128, 1),
+    ([4096], [512], 32, 8, 128, 1),               # the mixed step's chunk alone
+])
+def test_prefill_key_split_plan(lens, q_lens, nq, nkv, d, pieces):
+    """The cases above that are meant to split the keys really do (on a
+    152-SM GB300; other SM counts may choose differently)."""
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("plan thresholds depend on the SM count")
+    assert ops.prefill_splits(sum(q_lens), nq, nkv, d, max(q_lens), max(lens)) == pieces
