@@ -16,10 +16,13 @@
 //    and 64-column half, 128-byte swizzle: the layout the S = Q K^T MMA reads
 //    as 128 rows); V as 8 boxes of one page and both halves each (the P V MMA
 //    consumes one page per instruction).  A single thread issues TMA boxes
-//    slowly, so seven producer warps share them.
-//  * Warp 1 (one thread) issues S = Q K^T into one of three TMEM buffers and
-//    O += P V into a TMEM accumulator; S runs two tiles ahead of P V, so the
-//    tensor pipe works on later tiles while the softmax warps work on one.  Descriptors are built once and advanced
+//    slowly, so six producer warps share them, 96 rows of 128 bytes each
+//    per tile.
+//  * One thread of warp 1 issues S = Q K^T into one of three TMEM buffers and
+//    one thread of warp 15 issues O += P V into a TMEM accumulator.  The
+//    tensor pipe queues only a few MMAs, so a single issuing thread that
+//    waits and commits between products leaves it idle; with two, one
+//    thread's waits overlap the other's MMAs, and S runs ahead of P V.  Descriptors are built once and advanced
 //    by constants: a 64-cycle MMA leaves the issuing thread little time.
 //  * Warps 2-9 run the softmax, two warps per MMA row: the warp pair that
 //    shares a TMEM lane quarter splits the 128 keys of a tile in halves and
@@ -50,9 +53,10 @@ constexpr int kStagesK = 3;        // K tile stages
 constexpr int kStagesV = 2;        // V tile stages
 constexpr int kSBufs = 3;          // S / P buffers in TMEM
 constexpr int kSoftmaxWarps = 8;   // two per TMEM lane quarter
-constexpr int kKWarps = 4;         // warp 0 (which also loads Q) and warps 10-12
-constexpr int kVWarps = 3;         // warps 13-15
-constexpr int kWarpK1 = 10, kWarpV0 = 13;
+constexpr int kKWarps = 3;         // warp 0 (which also loads Q) and warps 10-11
+constexpr int kVWarps = 3;         // warps 12-14
+constexpr int kWarpK1 = 10, kWarpV0 = 12;
+constexpr int kWarpPV = 15;        // issues the P V products
 constexpr int kThreads = 512;
 constexpr float kNegInf = -INFINITY;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -146,7 +150,7 @@ struct PrefillShared {
   uint64_t v_full[kStagesV], v_empty[kStagesV];
   uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
   uint64_t o_full, o_empty;
-  uint64_t mma_done;
+  uint64_t s_done, pv_done_all;  // each issuer's last products, before TMEM is freed
   uint32_t tmem_slot;
   int abort_flag;
   long long total_units;
@@ -261,7 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_addr(&B.o_full), 1);
     mbar_init(smem_addr(&B.o_empty), kSoftmaxWarps);
-    mbar_init(smem_addr(&B.mma_done), 1);
+    mbar_init(smem_addr(&B.s_done), 1);
+    mbar_init(smem_addr(&B.pv_done_all), 1);
     B.abort_flag = 0;
     fence_mbar_init();
     long long total = 0;
@@ -284,10 +289,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (k_warp || v_warp) {
     // ============================================================ producers
     if (lane == 0) {
-      // K warp k loads pages 2k, 2k+1 of each tile; V warp v pages 3v .. 3v+2
-      const int kidx = warp == 0 ? 0 : warp - kWarpK1 + 1;
-      const int pg_lo = k_warp ? 2 * kidx : 3 * (warp - kWarpV0);
-      const int pg_hi = k_warp ? pg_lo + 2 : min(pg_lo + 3, kPagesPerTile);
+      // K warp k and V warp k load pages 3k .. 3k+2 of each tile (the last
+      // two): 96 rows of 128 bytes per warp and tile either way
+      const int idx = k_warp ? (warp == 0 ? 0 : warp - kWarpK1 + 1) : warp - kWarpV0;
+      const int pg_lo = 3 * idx;
+      const int pg_hi = min(pg_lo + 3, kPagesPerTile);
       const CUtensorMap* map = k_warp ? &kmap : &vmap;
       unsigned char* ring = k_warp ? k_s : v_s;
       uint64_t* full = k_warp ? B.k_full : B.v_full;
@@ -313,10 +319,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pages = (U.kv_end + kBlock - 1) / kBlock;
         const int32_t* table = p.block_tables + (int64_t)U.s * p.max_blocks;
         for (int kt = U.kt0; kt < U.kt1; ++kt, ++c) {
-          int phys[3];
+          int phys[4];
           int nvalid = 0;
 #pragma unroll
-          for (int i = 0; i < 3; ++i) {
+          for (int i = 0; i < 4; ++i) {
             const int lp = kt * kPagesPerTile + pg_lo + i;  // logical page
             phys[i] = -1;
             if (pg_lo + i < pg_hi && lp < pages) {
@@ -334,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(smem_addr(&full[st]), (uint32_t)nvalid * NH * (kBlock * 128));
           unsigned char* stage = ring + st * KV_BYTES;
 #pragma unroll
-          for (int i = 0; i < 3; ++i) {
+          for (int i = 0; i < 4; ++i) {
             if (phys[i] < 0) continue;
             const int pg = pg_lo + i;
             if (k_warp) {
@@ -359,73 +365,78 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp == 0 && n_out > 0)
         mbar_wait(smem_addr(&B.q_full), (n_out - 1) & 1, p.err, abort_flag);
     }
-  } else if (warp == 1) {
-    // ============================================================ MMA issuer
-    // (waits spin without the suspend hint: this thread's latency is the
+  } else if (warp == 1 || warp == kWarpPV) {
+    // ============================================================ MMA issuers
+    // (waits spin without the suspend hint: these threads' latency is the
     // tensor pipe's)
     if (lane == 0) {
       static_assert(kStagesK == 3 && kStagesV == 2, "descriptor selection below");
-      const tc::Desc qd = tc::sw128_desc_pair(smem_addr(q_s), 16, 1024);
-      const tc::Desc kd0 = tc::sw128_desc_pair(smem_addr(k_s), 16, 1024);
-      const tc::Desc kd1 = tc::sw128_desc_pair(smem_addr(k_s + KV_BYTES), 16, 1024);
-      const tc::Desc kd2 = tc::sw128_desc_pair(smem_addr(k_s + 2 * KV_BYTES), 16, 1024);
-      const tc::Desc vd0 = tc::sw128_desc_pair(smem_addr(v_s), kBlock * 128, 1024);
-      const tc::Desc vd1 = tc::sw128_desc_pair(smem_addr(v_s + KV_BYTES), kBlock * 128, 1024);
       UnitCursor<TM> cur;
       cur.init(p);
       int n_out = 0;
-      uint32_t ntiles = 0;  // S products issued so far (all units)
-      Ring kr, vr, sr_, pr;  // K stages, V stages, S buffer of the next S / of the next P V
-      // S of the next tile into the S buffer at sr_ (which held P three tiles
-      // back: its P V must have run)
-      auto issue_s = [&](bool last) {
-        mbar_wait_spin(smem_addr(&B.k_full[kr.stage]), kr.phase, p.err, abort_flag);
-        if (ntiles >= kSBufs)
-          mbar_wait_spin(smem_addr(&B.pv_done[sr_.stage]), sr_.phase ^ 1u, p.err, abort_flag);
-        tc::fence_after_sync();
-        issue_s_mma<D>(tmem + sr_.stage * kKeysPerTile, qd,
-                       kr.stage == 0 ? kd0 : (kr.stage == 1 ? kd1 : kd2));
-        tc::commit(smem_addr(&B.s_full[sr_.stage]));
-        tc::commit(smem_addr(&B.k_empty[kr.stage]));
-        if (last) tc::commit(smem_addr(&B.q_empty));
-        kr.next(kStagesK);
-        sr_.next(kSBufs);
-        ++ntiles;
-      };
-      // O += P V for the next tile (P in the S buffer at pr, V at vr)
-      auto issue_pv = [&](bool first) {
-        mbar_wait_spin(smem_addr(&B.p_full[pr.stage]), pr.phase, p.err, abort_flag);
-        mbar_wait_spin(smem_addr(&B.v_full[vr.stage]), vr.phase, p.err, abort_flag);
-        if (first && n_out > 0)
-          mbar_wait_spin(smem_addr(&B.o_empty), (n_out - 1) & 1, p.err, abort_flag);
-        tc::fence_after_sync();
-        issue_pv_mma<D>(tmem + O_COL, tmem + pr.stage * kKeysPerTile, vr.stage ? vd1 : vd0,
-                        first);
-        tc::commit(smem_addr(&B.v_empty[vr.stage]));
-        tc::commit(smem_addr(&B.pv_done[pr.stage]));
-        vr.next(kStagesV);
-        pr.next(kSBufs);
-      };
-      for (long long u = blockIdx.x; u < total_units; u += gridDim.x) {
-        Unit U;
-        if (!cur.locate(p, u, U)) break;
-        if (U.kt0 == U.kt1) continue;
-        const int n = U.kt1 - U.kt0;
-        mbar_wait_spin(smem_addr(&B.q_full), n_out & 1, p.err, abort_flag);
-        // S runs two tiles ahead of P V, so the softmax of a tile never waits
-        // for the P V of the one before it to be issued
-        issue_s(n == 1);
-        if (n > 1) issue_s(n == 2);
-        for (int j = 0; j < n; ++j) {
-          if (j + 2 < n) issue_s(j + 3 == n);
-          issue_pv(j == 0);
+      uint32_t ntiles = 0;  // tiles of S (or P V) issued so far, all units
+      Ring kv, sb;          // K (or V) stage; S buffer of the next S (or P V)
+      if (warp == 1) {
+        // S = Q K^T into the S buffer at sb, which held P three tiles back:
+        // the P V of that tile must have run
+        const tc::Desc qd = tc::sw128_desc_pair(smem_addr(q_s), 16, 1024);
+        const tc::Desc kd0 = tc::sw128_desc_pair(smem_addr(k_s), 16, 1024);
+        const tc::Desc kd1 = tc::sw128_desc_pair(smem_addr(k_s + KV_BYTES), 16, 1024);
+        const tc::Desc kd2 = tc::sw128_desc_pair(smem_addr(k_s + 2 * KV_BYTES), 16, 1024);
+        for (long long u = blockIdx.x; u < total_units; u += gridDim.x) {
+          Unit U;
+          if (!cur.locate(p, u, U)) break;
+          if (U.kt0 == U.kt1) continue;
+          mbar_wait_spin(smem_addr(&B.q_full), n_out & 1, p.err, abort_flag);
+          for (int kt = U.kt0; kt < U.kt1; ++kt, ++ntiles) {
+            mbar_wait_spin(smem_addr(&B.k_full[kv.stage]), kv.phase, p.err, abort_flag);
+            if (ntiles >= kSBufs)
+              mbar_wait_spin(smem_addr(&B.pv_done[sb.stage]), sb.phase ^ 1u, p.err, abort_flag);
+            tc::fence_after_sync();
+            issue_s_mma<D>(tmem + sb.stage * kKeysPerTile, qd,
+                           kv.stage == 0 ? kd0 : (kv.stage == 1 ? kd1 : kd2));
+            tc::commit(smem_addr(&B.s_full[sb.stage]));
+            tc::commit(smem_addr(&B.k_empty[kv.stage]));
+            if (kt == U.kt1 - 1) tc::commit(smem_addr(&B.q_empty));
+            kv.next(kStagesK);
+            sb.next(kSBufs);
+          }
+          ++n_out;
         }
-        tc::commit(smem_addr(&B.o_full));
-        ++n_out;
-      }
-      if (ntiles > 0) {
-        tc::commit(smem_addr(&B.mma_done));
-        mbar_wait_spin(smem_addr(&B.mma_done), 0, p.err, abort_flag);
+        if (ntiles > 0) {
+          tc::commit(smem_addr(&B.s_done));
+          mbar_wait_spin(smem_addr(&B.s_done), 0, p.err, abort_flag);
+        }
+      } else {
+        // O += P V with P in the S buffer at sb and V at kv; the first tile of
+        // a unit overwrites O once the previous unit's epilogue has read it
+        const tc::Desc vd0 = tc::sw128_desc_pair(smem_addr(v_s), kBlock * 128, 1024);
+        const tc::Desc vd1 = tc::sw128_desc_pair(smem_addr(v_s + KV_BYTES), kBlock * 128, 1024);
+        for (long long u = blockIdx.x; u < total_units; u += gridDim.x) {
+          Unit U;
+          if (!cur.locate(p, u, U)) break;
+          if (U.kt0 == U.kt1) continue;
+          for (int kt = U.kt0; kt < U.kt1; ++kt, ++ntiles) {
+            const bool first = kt == U.kt0;
+            mbar_wait_spin(smem_addr(&B.p_full[sb.stage]), sb.phase, p.err, abort_flag);
+            mbar_wait_spin(smem_addr(&B.v_full[kv.stage]), kv.phase, p.err, abort_flag);
+            if (first && n_out > 0)
+              mbar_wait_spin(smem_addr(&B.o_empty), (n_out - 1) & 1, p.err, abort_flag);
+            tc::fence_after_sync();
+            issue_pv_mma<D>(tmem + O_COL, tmem + sb.stage * kKeysPerTile, kv.stage ? vd1 : vd0,
+                            first);
+            tc::commit(smem_addr(&B.v_empty[kv.stage]));
+            tc::commit(smem_addr(&B.pv_done[sb.stage]));
+            kv.next(kStagesV);
+            sb.next(kSBufs);
+          }
+          tc::commit(smem_addr(&B.o_full));
+          ++n_out;
+        }
+        if (ntiles > 0) {
+          tc::commit(smem_addr(&B.pv_done_all));
+          mbar_wait_spin(smem_addr(&B.pv_done_all), 0, p.err, abort_flag);
+        }
       }
     }
   } else {
