@@ -262,11 +262,14 @@ int paged_attention_impl(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16
   a.scale = scale;
   a.out = out;
   a.err = err;
+  a.after_prefill = false;
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   if (max_q_len >= 2) {
     cudaError_t e = pa::launch_prefill(a, plan, ws + need_decode, sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    // with key pieces the merge kernel comes last and must not be overtaken
+    a.after_prefill = plan.nsplit == 1;
   }
   pa::DecodeWorkspace dws = pa::decode_workspace(ws, ctas, num_seqs, num_q_heads, head_dim);
   cudaError_t e = pa::launch_decode(a, dws, ctas, stream);

@@ -699,8 +699,25 @@ cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ct
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  kern<<<ctas, 2 * NKV * 32, smem, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e;
+  if (a.after_prefill) {
+    // overlaps the prefill grid (no data dependence: different output rows,
+    // and the cache writes of the step finished before the prefill started)
+    cudaLaunchConfig_t pcfg = {};
+    pcfg.gridDim = dim3(ctas);
+    pcfg.blockDim = dim3(2 * NKV * 32);
+    pcfg.dynamicSmemBytes = smem;
+    pcfg.stream = stream;
+    cudaLaunchAttribute pattr[1];
+    pattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pattr[0].val.programmaticStreamSerializationAllowed = 1;
+    pcfg.attrs = pattr;
+    pcfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&pcfg, kern, p);
+  } else {
+    kern<<<ctas, 2 * NKV * 32, smem, stream>>>(p);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.num_seqs, (a.num_q_heads + kMergeWarps - 1) / kMergeWarps, 1);

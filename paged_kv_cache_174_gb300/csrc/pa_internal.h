@@ -34,6 +34,10 @@ struct AttnArgs {
   float scale;
   uint16_t* out;
   unsigned* err;  // device error word
+  // The kernel launched just before on the stream is the prefill kernel
+  // (which triggers its dependents at once and writes only prefill rows):
+  // the decode kernel may then start on SMs it leaves free.
+  bool after_prefill;
 };
 
 // Workspace carve-up shared by the launchers (sizes in bytes, 256-aligned).
