@@ -61,6 +61,7 @@ constexpr int kThreads = 512;
 constexpr float kNegInf = -INFINITY;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kMaxSplit = 4;
+constexpr int kMaxListed = 1024;   // prefill requests the shared-memory unit list holds
 
 struct PrefillParams {
   const int32_t* block_tables;
@@ -108,24 +109,44 @@ struct Unit {
 };
 
 // Walks the unit list: request-major, then query tile, kv head, key split.
+// Requests are found through the block's list of prefill requests (sequence
+// ids and first tile indices, built once per CTA); when a batch holds more
+// than kMaxListed of them the cursor walks the sequences instead.
 template <int TM>
 struct UnitCursor {
-  int s = 0, base = 0, tiles = 0;
-  __device__ __forceinline__ void init(const PrefillParams& p) {
-    s = 0;
+  const int* seq;   // listed requests, or nullptr
+  const int* tbase; // first tile of each listed request; tbase[n] = all tiles
+  int n;
+  int i = 0;        // list position, or sequence when walking
+  int base = 0, tiles = 0;
+  __device__ __forceinline__ void init(const PrefillParams& p, const int* list_seq,
+                                       const int* list_base, int listed) {
+    seq = listed <= kMaxListed ? list_seq : nullptr;
+    tbase = list_base;
+    n = listed;
+    i = 0;
     base = 0;
-    tiles = p.num_seqs > 0 ? prefill_tiles<TM>(p, 0, false) : 0;
+    tiles = (!seq && p.num_seqs > 0) ? prefill_tiles<TM>(p, 0, false) : 0;
   }
   __device__ __forceinline__ bool locate(const PrefillParams& p, long long u, Unit& U) {
     const long long per = (long long)p.n_kv * p.nsplit;
     const long long tile = u / per;
     const int rem = (int)(u % per);
-    while (s < p.num_seqs && tile >= (long long)base + tiles) {
-      base += tiles;
-      ++s;
-      tiles = s < p.num_seqs ? prefill_tiles<TM>(p, s, false) : 0;
+    int s;
+    if (seq) {
+      while (i < n && tile >= tbase[i + 1]) ++i;
+      if (i >= n) return false;
+      s = seq[i];
+      base = tbase[i];
+    } else {
+      while (i < p.num_seqs && tile >= (long long)base + tiles) {
+        base += tiles;
+        ++i;
+        tiles = i < p.num_seqs ? prefill_tiles<TM>(p, i, false) : 0;
+      }
+      if (i >= p.num_seqs) return false;
+      s = i;
     }
-    if (s >= p.num_seqs) return false;
     const int a = __ldg(p.qsl + s), b = __ldg(p.qsl + s + 1);
     const int L = __ldg(p.seq_lens + s);
     const int ql = b - a;
@@ -156,6 +177,10 @@ struct PrefillShared {
   long long total_units;
   float xmax[2][2][kRows];  // partial row maxima: [tile parity][key half][row]
   float xsum[2][2][kRows];  // partial row sums: [unit parity][key half][row]
+  int list_seq[kMaxListed];       // prefill requests in order
+  int list_base[kMaxListed + 1];  // their first tile indices, then the tile count
+  int listed;
+  int warp_n[kThreads / 32], warp_tiles[kThreads / 32];
 };
 
 // Byte offset of 16-byte chunk c (0..7) of row r inside a [rows][64 x bf16]
@@ -269,9 +294,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_addr(&B.pv_done_all), 1);
     B.abort_flag = 0;
     fence_mbar_init();
-    long long total = 0;
-    for (int s = 0; s < p.num_seqs; ++s) total += prefill_tiles<TM>(p, s, blockIdx.x == 0);
-    B.total_units = total * p.n_kv * p.nsplit;
+  }
+  {
+    // list the requests with prefill rows (and their first tile index): one
+    // pass over the sequences by the whole block, in order
+    int listed = 0, tiles_so_far = 0;
+    for (int s0 = 0; s0 < p.num_seqs; s0 += kThreads) {
+      const int s = s0 + (int)threadIdx.x;
+      const int t = s < p.num_seqs ? prefill_tiles<TM>(p, s, blockIdx.x == 0) : 0;
+      const unsigned has = __ballot_sync(0xffffffffu, t > 0);
+      int incl = t;  // inclusive scan of tiles over the warp
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (lane == 31) {
+        B.warp_n[warp] = __popc(has);
+        B.warp_tiles[warp] = incl;
+      }
+      __syncthreads();
+      int n_before = 0, t_before = 0, n_all = 0, t_all = 0;
+      for (int w = 0; w < kThreads / 32; ++w) {
+        if (w < warp) {
+          n_before += B.warp_n[w];
+          t_before += B.warp_tiles[w];
+        }
+        n_all += B.warp_n[w];
+        t_all += B.warp_tiles[w];
+      }
+      if (t > 0) {
+        const int idx = listed + n_before + __popc(has & ((1u << lane) - 1u));
+        if (idx < kMaxListed) {
+          B.list_seq[idx] = s;
+          B.list_base[idx] = tiles_so_far + t_before + incl - t;
+        }
+      }
+      listed += n_all;
+      tiles_so_far += t_all;
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+      B.listed = listed;
+      if (listed <= kMaxListed) B.list_base[listed] = tiles_so_far;
+      B.total_units = (long long)tiles_so_far * p.n_kv * p.nsplit;
+    }
   }
   if (warp == 1) {
     tc::tmem_alloc(smem_addr(&B.tmem_slot), TMEM_COLS);
@@ -300,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t* empty = k_warp ? B.k_empty : B.v_empty;
       const uint32_t nst = k_warp ? kStagesK : kStagesV;
       UnitCursor<TM> cur;
-      cur.init(p);
+      cur.init(p, B.list_seq, B.list_base, B.listed);
       int n_out = 0, c = 0;
       Ring pos;
       for (long long u = blockIdx.x; u < total_units; u += gridDim.x) {
@@ -372,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       static_assert(kStagesK == 3 && kStagesV == 2, "descriptor selection below");
       UnitCursor<TM> cur;
-      cur.init(p);
+      cur.init(p, B.list_seq, B.list_base, B.listed);
       int n_out = 0;
       uint32_t ntiles = 0;  // tiles of S (or P V) issued so far, all units
       Ring kv, sb;          // K (or V) stage; S buffer of the next S (or P V)
@@ -455,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float mul = pos_scale ? 1.f : sl2;
     const float emul = pos_scale ? sl2 : 1.f;
     UnitCursor<TM> cur;
-    cur.init(p);
+    cur.init(p, B.list_seq, B.list_base, B.listed);
     int n_out = 0;
     Ring sbr, prev, vr;  // S buffer of this tile and of the last one, V stage
     uint32_t xpar = 0;   // exchange slot parity

@@ -63,6 +63,21 @@ def test_many_prefill_requests():
     assert_attn_close(to_f64(out), ref, "40 prefill requests")
 
 
+def test_more_prefill_requests_than_the_listed_maximum():
+    """Over 1024 requests with prefill rows: the kernel walks the sequences
+    instead of its per-CTA request list; decode rows interleaved."""
+    rng = np.random.default_rng(9)
+    lens, q_lens = [], []
+    for i in range(1100):
+        L = int(rng.integers(48, 97))
+        lens.append(L)
+        q_lens.append(1 if i % 7 == 3 else int(rng.integers(2, 7)))
+    b = _batch(lens, q_lens, nq=4, nkv=2, d=64, seed=12)
+    _, out = run_gpu_step(b)
+    _, _, ref = run_oracle_step(b)
+    assert_attn_close(to_f64(out), ref, "1100 requests")
+
+
 def test_prefill_physical_permutation_gives_identical_bits():
     b = _batch([700, 260], [300, 260], seed=6, extra_blocks=40)
     _, out1 = run_gpu_step(b)
