@@ -35,6 +35,10 @@ def lib() -> ctypes.CDLL:
         L.oracle_reshape_and_cache.restype = ctypes.c_int
         L.oracle_copy_blocks.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32]
         L.oracle_copy_blocks.restype = ctypes.c_int
+        L.oracle_swap_out.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, vp, vp]
+        L.oracle_swap_out.restype = ctypes.c_int
+        L.oracle_swap_in.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, vp, vp]
+        L.oracle_swap_in.restype = ctypes.c_int
         L.oracle_paged_attention.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32,
                                              vp, i32, vp, vp, i32, dbl, vp, i32]
         L.oracle_paged_attention.restype = ctypes.c_int
@@ -91,6 +95,37 @@ def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, pairs) -> None:
                                   int(p.shape[0]))
     if st:
         raise OracleError(f"oracle_copy_blocks status {st}")
+
+
+def swap_out(k_cache: np.ndarray, v_cache: np.ndarray, block_ids):
+    """Returns (host_k, host_v), each [n, block_size, n_kv, d] uint16: the blocks
+    block_ids[i] of the caches, in list order."""
+    kc = _c(k_cache, np.uint16)
+    vc = _c(v_cache, np.uint16)
+    ids = _c(block_ids, np.int32).reshape(-1)
+    nb, bs, nkv, d = kc.shape
+    hk = np.empty((ids.shape[0], bs, nkv, d), np.uint16)
+    hv = np.empty_like(hk)
+    st = lib().oracle_swap_out(_ptr(kc), _ptr(vc), nb, bs, nkv, d, _ptr(ids), int(ids.shape[0]),
+                               _ptr(hk), _ptr(hv))
+    if st:
+        raise OracleError(f"oracle_swap_out status {st}")
+    return hk, hv
+
+
+def swap_in(k_cache: np.ndarray, v_cache: np.ndarray, block_ids, host_k, host_v) -> None:
+    """In place: block block_ids[i] of the caches <- host_k[i], host_v[i]."""
+    assert k_cache.dtype == np.uint16 and k_cache.flags.c_contiguous
+    assert v_cache.dtype == np.uint16 and v_cache.flags.c_contiguous
+    ids = _c(block_ids, np.int32).reshape(-1)
+    hk = _c(host_k, np.uint16)
+    hv = _c(host_v, np.uint16)
+    nb, bs, nkv, d = k_cache.shape
+    assert hk.shape == (ids.shape[0], bs, nkv, d) and hv.shape == hk.shape
+    st = lib().oracle_swap_in(_ptr(k_cache), _ptr(v_cache), nb, bs, nkv, d, _ptr(ids),
+                              int(ids.shape[0]), _ptr(hk), _ptr(hv))
+    if st:
+        raise OracleError(f"oracle_swap_in status {st}")
 
 
 def paged_attention(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc,

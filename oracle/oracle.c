@@ -16,7 +16,9 @@
  *            part 2 (the kernel reads the Block Table and turns a logical
  *            index into a physical block pointer), and the comparison table
  *            there (on-demand block allocation, copy-on-write sharing).
- *  [guijiagi] "连续批处理：推理吞吐的范式革命", section 4.1 (the paged
+ *  [guijiagi] "连续批处理：推理吞吐的范式革命", section 3.3 (preemption by
+ *            swapping: a request's KV cache moves to CPU memory and comes back
+ *            without recomputation), section 4.1 (the paged
  *            attention kernel: q [num_tokens, d], key/value caches
  *            [num_blocks, block_size, d], block_tables
  *            [num_requests, max_blocks], seq_lens [num_requests]; walk the
@@ -36,6 +38,10 @@
  *    p = seq_len - q_len + i and attends to keys 0..p (bottom-right causal);
  *  - a negative slot in slot_mapping means "skip this token";
  *  - copy_blocks applies its (src, dst) pairs one after the other.
+ *  - swap works on whole blocks ("vLLM中的PagedAttention机制与显存优化实践",
+ *    section 2.1: swap is block-grained): swap-out packs the listed blocks,
+ *    in list order, into host arrays [n, block_size, num_kv_heads, head_dim];
+ *    swap-in writes the host arrays' blocks back at the listed block ids.
  */
 #include <math.h>
 #include <stdint.h>
@@ -123,6 +129,48 @@ int oracle_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, int32_t num_blocks,
     for (int64_t c = 0; c < blk; ++c) {
       k_cache[dst * blk + c] = k_cache[src * blk + c];
       v_cache[dst * blk + c] = v_cache[src * blk + c];
+    }
+  }
+  return ORACLE_OK;
+}
+
+/* Swap-out: host_k[i], host_v[i] <- K and V of block ids[i], for i < n (a
+ * bit copy of each block; ids may repeat). */
+int oracle_swap_out(const uint16_t *k_cache, const uint16_t *v_cache, int32_t num_blocks,
+                    int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                    const int32_t *ids, int32_t n, uint16_t *host_k, uint16_t *host_v) {
+  if (n < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return ORACLE_ERR_ARG;
+  const int64_t blk = (int64_t)block_size * num_kv_heads * head_dim;
+  for (int32_t i = 0; i < n; ++i) {
+    const int64_t b = ids[i];
+    if (b < 0 || b >= num_blocks) return ORACLE_ERR_INDEX;
+    for (int64_t c = 0; c < blk; ++c) {
+      host_k[i * blk + c] = k_cache[b * blk + c];
+      host_v[i * blk + c] = v_cache[b * blk + c];
+    }
+  }
+  return ORACLE_OK;
+}
+
+/* Swap-in: K and V of block ids[i] <- host_k[i], host_v[i], for i < n in
+ * order (ids should be distinct; with repeats the last one wins). */
+int oracle_swap_in(uint16_t *k_cache, uint16_t *v_cache, int32_t num_blocks,
+                   int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                   const int32_t *ids, int32_t n, const uint16_t *host_k,
+                   const uint16_t *host_v) {
+  if (n < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return ORACLE_ERR_ARG;
+  const int64_t blk = (int64_t)block_size * num_kv_heads * head_dim;
+  for (int32_t i = 0; i < n; ++i) {
+    const int64_t b = ids[i];
+    if (b < 0 || b >= num_blocks) return ORACLE_ERR_INDEX;
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    const int64_t b = ids[i];
+    for (int64_t c = 0; c < blk; ++c) {
+      k_cache[b * blk + c] = host_k[i * blk + c];
+      v_cache[b * blk + c] = host_v[i * blk + c];
     }
   }
   return ORACLE_OK;

@@ -330,3 +330,29 @@ def test_oracle_rejects_bad_lengths():
     with pytest.raises(oracle.OracleError):
         oracle.paged_attention(b.q, b.k_cache, b.v_cache, b.block_tables,
                                np.array([0, 17, 33, 48], np.int32), b.query_start_loc, b.scale)
+
+
+def test_pin_swap_round_trip_and_library_gather():
+    """Swap is a block-grained bit copy ("vLLM中的PagedAttention机制与显存优化实践",
+    section 2.1): swap-out equals numpy's take along the block axis; swapping
+    the blocks back in at other ids moves them there bit for bit and leaves
+    every other block alone."""
+    rng = np.random.default_rng(21)
+    nb, bs, nkv, d = 12, 16, 2, 64
+    kc = rng.integers(0, 65536, size=(nb, bs, nkv, d), dtype=np.uint16)
+    vc = rng.integers(0, 65536, size=(nb, bs, nkv, d), dtype=np.uint16)
+    ids = np.array([7, 2, 9, 2], np.int32)  # repeats allowed on swap-out
+    hk, hv = oracle.swap_out(kc, vc, ids)
+    assert np.array_equal(hk, np.take(kc, ids, axis=0))
+    assert np.array_equal(hv, np.take(vc, ids, axis=0))
+    k2, v2 = kc.copy(), vc.copy()
+    dst = np.array([0, 11, 4, 5], np.int32)
+    oracle.swap_in(k2, v2, dst, hk, hv)
+    for i, b in enumerate(dst):
+        assert np.array_equal(k2[b], kc[ids[i]]) and np.array_equal(v2[b], vc[ids[i]])
+    others = np.setdiff1d(np.arange(nb), dst)
+    assert np.array_equal(k2[others], kc[others]) and np.array_equal(v2[others], vc[others])
+    with pytest.raises(oracle.OracleError):
+        oracle.swap_out(kc, vc, np.array([nb], np.int32))
+    with pytest.raises(oracle.OracleError):
+        oracle.swap_in(k2, v2, np.array([-1], np.int32), hk[:1], hv[:1])
