@@ -160,6 +160,42 @@ int pa_copy_blocks(pa_bf16 *k_cache, pa_bf16 *v_cache, int32_t num_blocks, int32
                    int32_t num_pairs, cudaStream_t stream);
 
 /*
+ * Block swap for preemption by swapping instead of recomputing
+ * ("连续批处理：推理吞吐的范式革命", section 3.3: a preempted request's KV
+ * cache moves to CPU memory and comes back without recomputation;
+ * "vLLM中的PagedAttention机制与显存优化实践", section 2.1: swap is
+ * block-grained and runs asynchronously on its own CUDA streams, so pass a
+ * side stream to overlap it with attention on another).
+ *
+ * pa_swap_out copies blocks block_ids[0..n) of both caches to the host:
+ * host_k[i] and host_v[i] ([n, block_size, num_kv_heads, head_dim] bf16
+ * each, in list order) become bit copies of block block_ids[i].  A kernel
+ * first packs the blocks into `staging`, then two cudaMemcpyAsync calls copy
+ * it to the host (use pinned host memory for the copies to be asynchronous).
+ * pa_swap_in is the reverse: block block_ids[i] of both caches becomes a bit
+ * copy of host_k[i] / host_v[i]; ids must then be distinct.
+ *
+ *   block_ids  [n] int32 device array, read; an id outside [0, num_blocks)
+ *              skips that block and flags PA_ERR_DEVICE_BOUNDS
+ *   staging    device buffer of pa_swap_staging_bytes(n, ...) bytes,
+ *              16-byte aligned, owned by the caller, not used by another call
+ *              meanwhile; its contents on entry do not matter
+ *   host_k/v   host buffers of n * block_size * num_kv_heads * head_dim bf16
+ * Asynchronous on `stream`: host_k / host_v hold the blocks after the stream
+ * has synchronised (swap-out), and may be reused once it has (swap-in).
+ */
+size_t pa_swap_staging_bytes(int32_t n, int32_t block_size, int32_t num_kv_heads,
+                             int32_t head_dim);
+int pa_swap_out(const pa_bf16 *k_cache, const pa_bf16 *v_cache, int32_t num_blocks,
+                int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                const int32_t *block_ids, int32_t n, pa_bf16 *staging, pa_bf16 *host_k,
+                pa_bf16 *host_v, cudaStream_t stream);
+int pa_swap_in(pa_bf16 *k_cache, pa_bf16 *v_cache, int32_t num_blocks, int32_t block_size,
+               int32_t num_kv_heads, int32_t head_dim, const int32_t *block_ids, int32_t n,
+               pa_bf16 *staging, const pa_bf16 *host_k, const pa_bf16 *host_v,
+               cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word that
  * the kernels of this library set on the current device.  Returns PA_OK,
  * PA_ERR_DEVICE_BOUNDS, PA_ERR_TIMEOUT or PA_ERR_CUDA.

@@ -127,6 +127,61 @@ int pa_copy_blocks(pa_bf16* k_cache, pa_bf16* v_cache, int32_t num_blocks, int32
   return PA_OK;
 }
 
+size_t pa_swap_staging_bytes(int32_t n, int32_t block_size, int32_t num_kv_heads,
+                             int32_t head_dim) {
+  if (n < 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
+  return (size_t)2 * n * block_size * num_kv_heads * head_dim * sizeof(pa_bf16);
+}
+
+}  // extern "C"
+
+namespace {
+
+int swap_blocks(pa_bf16* k_cache, pa_bf16* v_cache, int32_t num_blocks, int32_t block_size,
+                int32_t num_kv_heads, int32_t head_dim, const int32_t* block_ids, int32_t n,
+                pa_bf16* staging, pa_bf16* host_k, pa_bf16* host_v, bool out,
+                cudaStream_t stream) {
+  if (n < 0) return fail(PA_ERR_INVALID_ARG, "n %d < 0", n);
+  int st = check_cache_geometry(num_blocks, block_size, num_kv_heads, head_dim);
+  if (st) return st;
+  if (n == 0) return PA_OK;
+  if (!k_cache || !v_cache || !block_ids || !staging || !host_k || !host_v)
+    return fail(PA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(staging, 16) ||
+      !aligned(block_ids, 4))
+    return fail(PA_ERR_INVALID_ARG, "caches and staging must be 16-byte aligned, ids 4-byte");
+  unsigned* err = nullptr;
+  st = device_state(&err, nullptr);
+  if (st) return st;
+  cudaError_t e = pa::launch_swap(k_cache, v_cache, num_blocks,
+                                  (int64_t)block_size * num_kv_heads * head_dim, block_ids, n,
+                                  staging, host_k, host_v, out, err, stream);
+  if (e != cudaSuccess) return cuda_fail(e, out ? "swap_out" : "swap_in");
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_swap_out(const pa_bf16* k_cache, const pa_bf16* v_cache, int32_t num_blocks,
+                int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                const int32_t* block_ids, int32_t n, pa_bf16* staging, pa_bf16* host_k,
+                pa_bf16* host_v, cudaStream_t stream) {
+  return swap_blocks(const_cast<pa_bf16*>(k_cache), const_cast<pa_bf16*>(v_cache), num_blocks,
+                     block_size, num_kv_heads, head_dim, block_ids, n, staging, host_k, host_v,
+                     true, stream);
+}
+
+int pa_swap_in(pa_bf16* k_cache, pa_bf16* v_cache, int32_t num_blocks, int32_t block_size,
+               int32_t num_kv_heads, int32_t head_dim, const int32_t* block_ids, int32_t n,
+               pa_bf16* staging, const pa_bf16* host_k, const pa_bf16* host_v,
+               cudaStream_t stream) {
+  return swap_blocks(k_cache, v_cache, num_blocks, block_size, num_kv_heads, head_dim,
+                     block_ids, n, staging, const_cast<pa_bf16*>(host_k),
+                     const_cast<pa_bf16*>(host_v), false, stream);
+}
+
 size_t pa_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t num_q_heads,
                          int32_t num_kv_heads, int32_t head_dim, int32_t max_q_len,
                          int32_t max_seq_len) {

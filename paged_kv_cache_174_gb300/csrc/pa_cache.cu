@@ -9,6 +9,12 @@
 //   block of the request's Block Table).
 // Copy-on-write: same page, comparison table ("Copy-on-Write ... shared
 //   blocks"); "连续批处理：推理吞吐的范式革命", section 4.2 (prefix sharing).
+// Block swap: "连续批处理：推理吞吐的范式革命", section 3.3 (a preempted
+//   request's KV cache goes to CPU memory and comes back without
+//   recomputation); "vLLM中的PagedAttention机制与显存优化实践", section 2.1
+//   (swap is block-grained and asynchronous on its own streams).  A kernel
+//   packs the listed blocks into a staging buffer (or unpacks them), so the
+//   host transfer is two large copies rather than one per block.
 #include <cstdint>
 
 #include "pa_common.cuh"
@@ -72,7 +78,64 @@ __global__ void __launch_bounds__(kCopyThreads)
   }
 }
 
+// One CTA per listed block: stage[i] <- cache[ids[i]] (to_stage) or
+// cache[ids[i]] <- stage[i], for K and V.
+__global__ void __launch_bounds__(kCopyThreads)
+    swap_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                       uint4* __restrict__ k_stage, uint4* __restrict__ v_stage,
+                       int32_t num_blocks, int64_t block_vec, const int32_t* __restrict__ ids,
+                       bool to_stage, unsigned* err) {
+  const int64_t b = ids[blockIdx.x];
+  if (b < 0 || b >= num_blocks) {
+    if (threadIdx.x == 0) flag_error(err, DEVERR_BOUNDS);
+    return;
+  }
+  uint4* kc = k_cache + b * block_vec;
+  uint4* vc = v_cache + b * block_vec;
+  uint4* ks = k_stage + (int64_t)blockIdx.x * block_vec;
+  uint4* vs = v_stage + (int64_t)blockIdx.x * block_vec;
+  for (int64_t i = threadIdx.x; i < block_vec; i += kCopyThreads) {
+    if (to_stage) {
+      const uint4 a = kc[i];
+      const uint4 c = vc[i];
+      ks[i] = a;
+      vs[i] = c;
+    } else {
+      const uint4 a = ks[i];
+      const uint4 c = vs[i];
+      kc[i] = a;
+      vc[i] = c;
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_swap(uint16_t* k_cache, uint16_t* v_cache, int32_t num_blocks,
+                        int64_t block_elems, const int32_t* ids, int32_t n, uint16_t* staging,
+                        uint16_t* host_k, uint16_t* host_v, bool out, unsigned* err,
+                        cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const size_t bytes = (size_t)n * block_elems * sizeof(uint16_t);
+  uint16_t* k_stage = staging;
+  uint16_t* v_stage = staging + (size_t)n * block_elems;
+  cudaError_t e;
+  if (!out) {
+    e = cudaMemcpyAsync(k_stage, host_k, bytes, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyAsync(v_stage, host_v, bytes, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return e;
+  }
+  swap_blocks_kernel<<<n, kCopyThreads, 0, stream>>>(
+      reinterpret_cast<uint4*>(k_cache), reinterpret_cast<uint4*>(v_cache),
+      reinterpret_cast<uint4*>(k_stage), reinterpret_cast<uint4*>(v_stage), num_blocks,
+      block_elems / 8, ids, out, err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !out) return e;
+  e = cudaMemcpyAsync(host_k, k_stage, bytes, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyAsync(host_v, v_stage, bytes, cudaMemcpyDeviceToHost, stream);
+}
 
 cudaError_t launch_reshape_and_cache(const uint16_t* k, const uint16_t* v, int32_t num_tokens,
                                      uint16_t* k_cache, uint16_t* v_cache, int64_t num_slots,

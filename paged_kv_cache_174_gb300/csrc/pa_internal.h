@@ -79,4 +79,12 @@ cudaError_t launch_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, int32_t num
                                int64_t block_elems, const int32_t* pairs, int32_t num_pairs,
                                unsigned* err, cudaStream_t stream);
 
+// Block swap through a device staging buffer of 2 * n * block_elems values:
+// out = true packs the blocks and copies them to host_k / host_v; out = false
+// copies host_k / host_v in and unpacks them into the cache.
+cudaError_t launch_swap(uint16_t* k_cache, uint16_t* v_cache, int32_t num_blocks,
+                        int64_t block_elems, const int32_t* ids, int32_t n, uint16_t* staging,
+                        uint16_t* host_k, uint16_t* host_v, bool out, unsigned* err,
+                        cudaStream_t stream);
+
 }  // namespace pa

@@ -59,6 +59,10 @@ def _load() -> ctypes.CDLL:
                                      i32, i32, i32, f32, vp, vp, sz, vp]
     L.pa_paged_attention.restype = ctypes.c_int
     L.pa_copy_blocks.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, vp]
+    L.pa_swap_staging_bytes.argtypes = [i32, i32, i32, i32]
+    L.pa_swap_staging_bytes.restype = sz
+    L.pa_swap_out.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, vp, vp, vp, vp]
+    L.pa_swap_in.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, vp, vp, vp, vp]
     L.pa_copy_blocks.restype = ctypes.c_int
     L.pa_check_device_errors.argtypes = [vp]
     L.pa_check_device_errors.restype = ctypes.c_int
@@ -208,6 +212,45 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs: tor
     nb, bs, nkv, d = k_cache.shape
     _check(L.pa_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, nkv, d,
                             src_dst_pairs.data_ptr(), src_dst_pairs.shape[0], _stream(stream)))
+
+
+def _swap(out: bool, k_cache, v_cache, block_ids, host_k, host_v, staging, stream):
+    L = _load()
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_ids, "block_ids", torch.int32, 1)
+    nb, bs, nkv, d = k_cache.shape
+    n = int(block_ids.shape[0])
+    for name, h in (("host_k", host_k), ("host_v", host_v)):
+        if h.device.type != "cpu" or h.dtype != torch.bfloat16 or not h.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous bf16 CPU tensor (pinned for overlap)")
+        if tuple(h.shape) != (n, bs, nkv, d):
+            raise ValueError(f"{name} must be [{n}, {bs}, {nkv}, {d}]")
+    need = int(L.pa_swap_staging_bytes(n, bs, nkv, d))
+    if staging is None:
+        staging = torch.empty(need // 2, dtype=torch.bfloat16, device=k_cache.device)
+    elif staging.numel() * staging.element_size() < need or staging.device != k_cache.device:
+        raise ValueError(f"staging must be a device buffer of >= {need} bytes")
+    fn = L.pa_swap_out if out else L.pa_swap_in
+    _check(fn(k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, nkv, d, block_ids.data_ptr(), n,
+              staging.data_ptr(), host_k.data_ptr(), host_v.data_ptr(), _stream(stream)))
+    return staging
+
+
+def swap_out(k_cache: torch.Tensor, v_cache: torch.Tensor, block_ids: torch.Tensor,
+             host_k: torch.Tensor, host_v: torch.Tensor, staging: Optional[torch.Tensor] = None,
+             stream=None) -> torch.Tensor:
+    """Blocks block_ids of both caches -> host_k / host_v ([n, bs, n_kv, d] bf16 CPU
+    tensors, pinned for the copy to be asynchronous); valid once the stream has
+    synchronised.  Returns the device staging buffer (reusable)."""
+    return _swap(True, k_cache, v_cache, block_ids, host_k, host_v, staging, stream)
+
+
+def swap_in(k_cache: torch.Tensor, v_cache: torch.Tensor, block_ids: torch.Tensor,
+            host_k: torch.Tensor, host_v: torch.Tensor, staging: Optional[torch.Tensor] = None,
+            stream=None) -> torch.Tensor:
+    """host_k / host_v -> blocks block_ids (distinct) of both caches."""
+    return _swap(False, k_cache, v_cache, block_ids, host_k, host_v, staging, stream)
 
 
 def check_device_errors(stream=None) -> None:

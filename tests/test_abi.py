@@ -69,6 +69,15 @@ def test_host_side_argument_checks(lib):
     assert attn(S=0) == "PA_OK"   # nothing to do
     assert attn() == "PA_ERR_INVALID_ARG"  # null pointers
     assert vp  # keep the import used
+    # block swap
+    assert L.pa_swap_staging_bytes(3, 16, 2, 64) == 2 * 3 * 16 * 2 * 64 * 2
+    assert _status(L.pa_swap_out(None, None, 4, 16, 2, 64, None, -1, None, None, None, None)) \
+        == "PA_ERR_INVALID_ARG"
+    assert L.pa_swap_out(None, None, 4, 16, 2, 64, None, 0, None, None, None, None) == 0
+    assert _status(L.pa_swap_in(None, None, 4, 16, 2, 64, None, 2, None, None, None, None)) \
+        == "PA_ERR_INVALID_ARG"
+    assert _status(L.pa_swap_in(None, None, 4, 16, 1, 3, None, 2, None, None, None, None)) \
+        == "PA_ERR_UNSUPPORTED"
 
 
 def test_torch_side_checks_without_gpu():
