@@ -14,6 +14,17 @@ section 3.2 / "vLLM中的PagedAttention机制与显存优化实践", section 1.2
 memory pressure the newest running request is preempted, its blocks freed and
 it goes back to the head of the waiting queue to be recomputed).
 
+Preemption by swapping ("连续批处理：推理吞吐的范式革命", sections 3.2 and 3.3;
+"vLLM中的PagedAttention机制与显存优化实践", sections 1.2 and 2.1): with
+`preempt="swap"` the victim's KV blocks that it alone holds (reference count
+one) are copied block by block to a host swap space and freed, the request
+moves to the swapped queue, and swapped requests are resumed ahead of any new
+admission (they have the highest priority), each into freshly allocated
+blocks.  `preempt="auto"` follows the pages' rule of thumb: swap a victim
+whose cached sequence is at least `swap_min_tokens` long (transfer beats
+recomputation there), recompute a shorter one.  Either swap mode falls back
+to recomputation when the host swap space is full.
+
 Choices where the pages leave the policy open (documented with the build):
   * each step schedules every running decode first (one token each), then
     prefill slices of at most `chunk` tokens, at most one per request, FCFS,
@@ -25,7 +36,16 @@ Choices where the pages leave the policy open (documented with the build):
   * a request with prompt length L decodes positions L, L + 1, ... (q_len 1);
     prompts no longer than the prefix need no prefill;
   * arrivals are Poisson per step; prompt lengths lognormal with the given
-    median and sigma, clamped; output lengths geometric on {1, 2, ...}.
+    median and sigma, clamped; output lengths geometric on {1, 2, ...};
+  * a swapped victim's blocks that are shared prefix blocks are not copied
+    out: the prefix stays cached, and the resumed request shares it again;
+  * swapped requests resume in the order they were swapped out, stopping at
+    the first that does not fit (its private blocks + the 2-block margin);
+    no new request is admitted while one is still swapped out;
+  * the GPU executes a step in this order: swap-in, swap-out, block copies,
+    slot scatter, attention.  A host slot freed by a swap-in may take a
+    swap-out of the same step, and a request resumed and preempted again in
+    one step is copied out from the blocks it was just copied into.
 """
 from __future__ import annotations
 
@@ -58,6 +78,13 @@ class TraceConfig:
     num_kv_heads: int = 8
     head_dim: int = 128
     seed: int = 1005
+    preempt: str = "recompute"       # "recompute" | "swap" | "auto"
+    swap_blocks: int = 65536         # host swap space, in blocks (4 GiB of 8x128 bf16 K+V)
+    swap_min_tokens: int = 2000      # "auto": swap victims with at least this many tokens
+
+    def __post_init__(self):
+        if self.preempt not in ("recompute", "swap", "auto"):
+            raise ValueError(f"preempt must be recompute, swap or auto, not {self.preempt!r}")
 
 
 CONTINUOUS_BATCHING_TRACE = TraceConfig()
@@ -75,6 +102,10 @@ class Request:
     admitted_step: int = -1
     finished_step: int = -1
     preemptions: int = 0
+    swaps: int = 0
+    # while swapped out: per logical block, its host swap slot, or -1 for a
+    # shared prefix block that stays cached on the device
+    host_table: List[int] = field(default_factory=list)
 
     @property
     def in_prefill(self) -> bool:
@@ -83,10 +114,13 @@ class Request:
 
 @dataclass
 class StepPlan:
-    """Everything one GPU step needs, as host arrays (int32)."""
+    """Everything one GPU step needs, as host arrays (int32), executed in
+    field order: swap_in, swap_out, copy_pairs, scatter, attention."""
 
     index: int
-    copy_pairs: np.ndarray        # [n, 2] CoW (src, dst), applied first
+    swap_in: np.ndarray           # [n, 2] (host slot, device block)
+    swap_out: np.ndarray          # [n, 2] (device block, host slot)
+    copy_pairs: np.ndarray        # [n, 2] CoW (src, dst)
     slot_mapping: np.ndarray      # [T]
     block_tables: np.ndarray      # [S, max_blocks], -1 padded
     seq_lens: np.ndarray          # [S]
@@ -121,11 +155,18 @@ class ContinuousBatchingTrace:
         bs = cfg.block_size
         self.prefix_blocks = [self.alloc.allocate() for _ in range(-(-cfg.prefix // bs))]
         self.waiting: Deque[Request] = deque()
+        self.swapped: Deque[Request] = deque()
         self.running: List[Request] = []
         self.finished: List[Request] = []
+        self.host = BlockAllocator(cfg.swap_blocks, bs) if cfg.swap_blocks > 0 else None
         self.next_rid = 0
         self.step_index = 0
         self.total_copies = 0
+        self.total_swap_in = 0
+        self.total_swap_out = 0
+        self.total_preempt = {"recompute": 0, "swap": 0}
+        self._swap_in: List[Tuple[int, int]] = []
+        self._swap_out: List[Tuple[int, int]] = []
 
     # ------------------------------------------------------------- arrivals
     def _arrivals(self) -> None:
@@ -154,20 +195,71 @@ class ContinuousBatchingTrace:
     def _release(self, req: Request) -> None:
         self.alloc.free_all(req.table)
 
-    def _preempt_newest(self, protect: Request) -> bool:
-        """Free the most recently admitted running request other than
-        `protect`; it returns to the head of the waiting queue."""
+    def _swap_victim(self, victim: Request, cow_src: Dict[int, int]) -> bool:
+        """Copy the victim's private blocks out to host slots (False when the
+        swap space cannot take them).  A block made private by this step's
+        copy-on-write still holds nothing, so its logical content is the
+        shared source block's."""
+        n = -(-victim.computed // self.cfg.block_size)
+        logical = []
+        for bi in range(n):
+            src = cow_src.get(victim.table[bi], victim.table[bi])
+            shared = bi < len(self.prefix_blocks) and src == self.prefix_blocks[bi]
+            assert shared or self.alloc.refcount(src) == 1, "only prefix blocks are shared"
+            logical.append(-1 if shared else src)
+        need = sum(1 for b in logical if b >= 0)
+        if self.host is None or self.host.free_count < need:
+            return False
+        victim.host_table = []
+        for b in logical:
+            if b < 0:
+                victim.host_table.append(-1)
+            else:
+                h = self.host.allocate()
+                self._swap_out.append((b, h))
+                victim.host_table.append(h)
+        return True
+
+    def _preempt_newest(self, protect: Request, cow_src: Dict[int, int]) -> bool:
+        """Preempt the most recently admitted running request other than
+        `protect` that holds a block of its own (one that only shares prefix
+        blocks would free nothing): swap it out (swapped queue) or free its
+        blocks for recomputation (head of the waiting queue)."""
+        cfg = self.cfg
         for victim in sorted(self.running, key=lambda r: (r.admitted_step, r.rid), reverse=True):
-            if victim is protect:
+            if victim is protect or all(self.alloc.refcount(b) > 1 for b in victim.table):
                 continue
             self.running.remove(victim)
-            self._release(victim)
-            victim.computed = 0
-            victim.generated = 0
+            swap = cfg.preempt == "swap" or (cfg.preempt == "auto"
+                                             and victim.computed >= cfg.swap_min_tokens)
+            if swap and self._swap_victim(victim, cow_src):
+                self._release(victim)
+                victim.swaps += 1
+                self.swapped.append(victim)
+                self.total_preempt["swap"] += 1
+            else:
+                self._release(victim)
+                victim.computed = 0
+                victim.generated = 0
+                self.waiting.appendleft(victim)
+                self.total_preempt["recompute"] += 1
             victim.preemptions += 1
-            self.waiting.appendleft(victim)
             return True
         return False
+
+    def _resume(self, req: Request) -> None:
+        """Swapped request back onto the device: prefix blocks shared again,
+        every other block freshly allocated and filled from its host slot."""
+        req.table = []
+        for bi, h in enumerate(req.host_table):
+            if h < 0:
+                req.table.append(self.alloc.share(self.prefix_blocks[bi]))
+            else:
+                b = self.alloc.allocate()
+                self._swap_in.append((h, b))
+                self.host.free(h)
+                req.table.append(b)
+        req.host_table = []  # keeps its admission step: its priority does not drop
 
     def _slots(self, req: Request, lo: int, hi: int, copies: List[Tuple[int, int]]) -> List[int]:
         """Make positions lo..hi-1 writable for req (allocate / copy-on-write)
@@ -186,8 +278,19 @@ class ContinuousBatchingTrace:
     def step(self) -> StepPlan:
         cfg = self.cfg
         self._arrivals()
+        self._swap_in, self._swap_out = [], []
+        # swapped requests first, in swap-out order, with the same margin
+        while self.swapped and len(self.running) < cfg.max_num_seqs:
+            cand = self.swapped[0]
+            need = sum(1 for h in cand.host_table if h >= 0)
+            if self.alloc.free_count >= need + 2:
+                self.swapped.popleft()
+                self._resume(cand)
+                self.running.append(cand)
+            else:
+                break
         # admission: FCFS while the pool keeps a 2-block margin
-        while self.waiting and len(self.running) < cfg.max_num_seqs:
+        while not self.swapped and self.waiting and len(self.running) < cfg.max_num_seqs:
             cand = self.waiting[0]
             if self.alloc.free_count >= self._blocks_for(cand.prompt_len) + 2:
                 self.waiting.popleft()
@@ -225,7 +328,7 @@ class ContinuousBatchingTrace:
                 i += 1
             except OutOfBlocks:
                 before = {x.rid for x in self.running}
-                if not self._preempt_newest(protect=r):
+                if not self._preempt_newest(r, {d: s_ for (s_, d) in copies}):
                     raise
                 gone = before - {x.rid for x in self.running}
                 pos = [k for k, (x, _, _) in enumerate(sched) if x.rid in gone]
@@ -270,6 +373,8 @@ class ContinuousBatchingTrace:
                     self.finished.append(r)
                     newly_finished += 1
         self.total_copies += len(copies)
+        self.total_swap_in += len(self._swap_in)
+        self.total_swap_out += len(self._swap_out)
 
         used_slots = sum(r.computed for r in self.running)
         alloc_slots = sum(len(r.table) for r in self.running) * bs
@@ -278,8 +383,13 @@ class ContinuousBatchingTrace:
                  "finished": newly_finished, "tokens": len(slots),
                  "decode_tokens": num_decode, "prefill_tokens": n_prefill,
                  "block_utilisation": self.alloc.used_count / cfg.num_blocks,
-                 "tail_waste_slots": alloc_slots - used_slots}
+                 "tail_waste_slots": alloc_slots - used_slots,
+                 "swapped": len(self.swapped), "swap_in_blocks": len(self._swap_in),
+                 "swap_out_blocks": len(self._swap_out),
+                 "host_free_blocks": self.host.free_count if self.host else 0}
         plan = StepPlan(index=self.step_index,
+                        swap_in=np.array(self._swap_in, np.int32).reshape(-1, 2),
+                        swap_out=np.array(self._swap_out, np.int32).reshape(-1, 2),
                         copy_pairs=np.array(copies, np.int32).reshape(-1, 2),
                         slot_mapping=np.array(slots, np.int32), block_tables=bt,
                         seq_lens=seq_lens, query_start_loc=qsl,
@@ -304,3 +414,24 @@ class ContinuousBatchingTrace:
         for r in self.running:
             assert len(r.table) == -(-r.computed // bs), "a table holds a block past the last token"
             assert len(r.table) * bs - r.computed < bs, "more than the last block is partly empty"
+        host_refs: Dict[int, int] = {}
+        for r in self.swapped:
+            assert not r.table and len(r.host_table) == -(-r.computed // bs)
+            for h in r.host_table:
+                if h >= 0:
+                    host_refs[h] = host_refs.get(h, 0) + 1
+        if self.host is not None:
+            self.host.check()
+            assert host_refs == self.host.refcounts(), "host slots do not match the swapped tables"
+        else:
+            assert not host_refs
+
+    def summary(self) -> Dict[str, float]:
+        """Whole-trace counters: preemptions by kind, blocks moved by swapping,
+        copy-on-write copies, finished requests."""
+        return {"steps": self.step_index, "finished": len(self.finished),
+                "running": len(self.running), "waiting": len(self.waiting),
+                "swapped": len(self.swapped), "copies": self.total_copies,
+                "preempt_recompute": self.total_preempt["recompute"],
+                "preempt_swap": self.total_preempt["swap"],
+                "swap_in_blocks": self.total_swap_in, "swap_out_blocks": self.total_swap_out}

@@ -1,6 +1,7 @@
-"""The continuous-batching trace on the GPU: every step's copy-on-write block
-copies, slot scatter and mixed decode / chunked-prefill attention, replayed on
-the fp64 oracle from the same step plans."""
+"""The continuous-batching trace on the GPU: every step's block swap-in and
+swap-out, copy-on-write block copies, slot scatter and mixed decode /
+chunked-prefill attention, replayed on the fp64 oracle from the same step
+plans."""
 import numpy as np
 import pytest
 import torch
@@ -16,6 +17,28 @@ from gpu_util import MAX_ABS, REL_L2, attn_errors, to_f64
 pytestmark = pytest.mark.gpu
 
 
+def _swaps(plan, dk, dv, kc, vc, host_g, host_o):
+    """The step's swap-in, then its swap-out, through the library and the
+    oracle; each side keeps its own host swap space."""
+    if len(plan.swap_in):
+        hs, db = plan.swap_in[:, 0], plan.swap_in[:, 1]
+        ops.swap_in(dk, dv, W.int32_tensor(db, "cuda"), host_g[0][hs].contiguous(),
+                    host_g[1][hs].contiguous())
+        oracle.swap_in(kc, vc, db, host_o[0][hs], host_o[1][hs])
+    if len(plan.swap_out):
+        db, hs = plan.swap_out[:, 0], plan.swap_out[:, 1]
+        shape = (len(db),) + tuple(host_g[0].shape[1:])
+        tk = torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+        tv = torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+        ops.swap_out(dk, dv, W.int32_tensor(db, "cuda"), tk, tv)
+        ops.check_device_errors()
+        ok, ov = oracle.swap_out(kc, vc, db)
+        assert np.array_equal(W.bits_of(tk), ok) and np.array_equal(W.bits_of(tv), ov), \
+            f"step {plan.index}: swapped-out blocks differ from the oracle"
+        host_g[0][hs], host_g[1][hs] = tk, tv
+        host_o[0][hs], host_o[1][hs] = ok, ov
+
+
 def _replay(cfg, steps, full_rows, sample_rows=24, seed=0):
     tr = ContinuousBatchingTrace(cfg)
     kc, vc = W.trace_initial_cache(cfg, tr.prefix_blocks)
@@ -24,8 +47,12 @@ def _replay(cfg, steps, full_rows, sample_rows=24, seed=0):
     rng = np.random.default_rng(seed)
     worst = (0.0, 0.0)
     checked = 0
+    hshape = (max(cfg.swap_blocks, 1), cfg.block_size, cfg.num_kv_heads, cfg.head_dim)
+    host_o = (np.zeros(hshape, np.uint16), np.zeros(hshape, np.uint16))  # oracle's swap space
+    host_g = (torch.zeros(hshape, dtype=torch.bfloat16), torch.zeros(hshape, dtype=torch.bfloat16))
     for _ in range(steps):
         plan = tr.step()
+        _swaps(plan, dk, dv, kc, vc, host_g, host_o)
         if plan.num_tokens == 0:
             continue
         q, k, v = W.trace_step_inputs(cfg, plan.index, plan.num_tokens)
@@ -90,3 +117,19 @@ def test_trace_small_heads_all_rows():
                       head_dim=64, seed=21)
     tr, worst = _replay(cfg, steps=40, full_rows=True)
     assert tr.total_copies > 0 and len(tr.finished) > 0
+
+
+@pytest.mark.parametrize("preempt", ["swap", "auto"])
+def test_trace_preempting_by_swap_all_rows(preempt):
+    """A pool too small for the load: running requests are swapped out to host
+    memory block by block and later swapped back into other physical blocks
+    (every slot the trace never wrote holds NaN, so a block left behind or
+    restored to the wrong place shows in the output)."""
+    cfg = TraceConfig(steps=80, arrival_rate=1.0, prompt_median=200.0, prompt_min=8,
+                      prompt_max=700, output_mean=60.0, prefix=40, chunk=128, budget=512,
+                      max_num_seqs=64, num_blocks=160, num_q_heads=8, num_kv_heads=2,
+                      head_dim=64, seed=13, preempt=preempt, swap_blocks=2000,
+                      swap_min_tokens=250)
+    tr, worst = _replay(cfg, steps=80, full_rows=True)
+    s = tr.summary()
+    assert s["preempt_swap"] > 0 and s["swap_in_blocks"] > 0

@@ -175,3 +175,109 @@ def test_first_write_after_prefix_copies_the_shared_block():
     assert p.copy_pairs.tolist() == [[tr.prefix_blocks[31], p.block_tables[0, 31]]]
     assert p.block_tables[0, :31].tolist() == tr.prefix_blocks[:31]
     assert p.seq_lens.tolist() == [530] and p.query_start_loc.tolist() == [0, 30]
+
+
+def _token_id_replay(cfg, steps):
+    """Replay every plan on a model of the pool in which each slot holds the
+    identity of the token whose K/V it caches (prefix position i -> i + 1,
+    position p of request r -> (r + 1) * 10**6 + p, never written -> 0),
+    executing the step in its stated order: swap-in, swap-out, block copies,
+    scatter.  Then every scheduled request's block table must read its own
+    tokens at positions 0 .. seq_len - 1: a wrong swap order, a swapped
+    block left out or a copy into a live block shows up here."""
+    tr = ContinuousBatchingTrace(cfg)
+    bs = cfg.block_size
+    pool = np.zeros((cfg.num_blocks, bs), np.int64)
+    for i in range(cfg.prefix):
+        pool[tr.prefix_blocks[i // bs], i % bs] = i + 1
+    host = np.zeros((max(cfg.swap_blocks, 1), bs), np.int64)
+    prompt = {}
+    for _ in range(steps):
+        p = tr.step()
+        tr.check()
+        for r in list(tr.waiting) + list(tr.swapped) + tr.running + tr.finished:
+            prompt[r.rid] = r.prompt_len
+        if len(p.swap_in):
+            pool[p.swap_in[:, 1]] = host[p.swap_in[:, 0]]
+        if len(p.swap_out):
+            host[p.swap_out[:, 1]] = pool[p.swap_out[:, 0]]
+        for src, dst in p.copy_pairs:
+            pool[dst] = pool[src]
+
+        def ident(rid, pos):
+            return pos + 1 if pos < min(prompt[rid], cfg.prefix) else (rid + 1) * 10**6 + pos
+
+        pool.reshape(-1)[p.slot_mapping] = [ident(int(r), int(q))
+                                            for r, q in zip(p.token_rid, p.positions)]
+        for s, rid in enumerate(p.rids):
+            L = int(p.seq_lens[s])
+            pos = np.arange(L)
+            got = pool[p.block_tables[s, pos // bs], pos % bs]
+            want = np.array([ident(rid, int(q)) for q in pos])
+            assert np.array_equal(got, want), f"step {p.index}: request {rid} reads wrong tokens"
+    return tr
+
+
+@pytest.mark.parametrize("preempt", ["recompute", "swap", "auto"])
+def test_preemption_keeps_every_request_reading_its_own_tokens(preempt):
+    cfg = _small(num_blocks=160, arrival_rate=1.0, prompt_median=200.0, prompt_max=700,
+                 output_mean=60.0, prefix=40, chunk=128, budget=512, seed=13, preempt=preempt,
+                 swap_blocks=2000, swap_min_tokens=250)
+    tr = _token_id_replay(cfg, 150)
+    s = tr.summary()
+    assert s["finished"] > 10
+    if preempt == "recompute":
+        assert s["preempt_recompute"] > 0 and s["preempt_swap"] == 0
+    elif preempt == "swap":
+        assert s["preempt_swap"] > 0 and s["preempt_recompute"] == 0
+        assert s["swap_in_blocks"] > 0 and s["swap_out_blocks"] >= s["swap_in_blocks"]
+    else:
+        assert s["preempt_swap"] > 0 and s["preempt_recompute"] > 0
+
+
+def test_swap_falls_back_to_recompute_when_the_host_space_is_full():
+    cfg = _small(num_blocks=160, arrival_rate=1.0, prompt_median=200.0, prompt_max=700,
+                 output_mean=60.0, prefix=40, chunk=128, budget=512, seed=13, preempt="swap",
+                 swap_blocks=12)
+    tr = _token_id_replay(cfg, 150)
+    s = tr.summary()
+    assert s["preempt_swap"] > 0 and s["preempt_recompute"] > 0
+
+
+def test_swapped_request_resumes_with_its_prefix_shared_again():
+    """A victim holding prefix blocks copies out only its private blocks; on
+    resumption it shares the same prefix blocks and gets its own blocks back
+    through swap-in (host slot -> fresh device block)."""
+    cfg = _small(arrival_rate=0.0, num_blocks=36, prefix=100, chunk=512, budget=2048,
+                 preempt="swap", swap_blocks=64)
+    from paged_kv_cache_174_gb300.host.trace import Request
+    tr = ContinuousBatchingTrace(cfg)   # 7 prefix blocks
+    tr.waiting.append(Request(0, 300, 100, 0))   # 19 blocks
+    tr.waiting.append(Request(1, 300, 100, 0))
+    tr.step()
+    tr.step()
+    assert [r.rid for r in tr.running] == [0, 1]
+    # both decode; the pool runs dry when a request crosses into a new block
+    seen_out = None
+    for _ in range(40):
+        p = tr.step()
+        tr.check()
+        if len(p.swap_out):
+            seen_out = p
+            break
+    assert seen_out is not None
+    victim = tr.swapped[0]
+    assert victim.host_table[:6] == [-1] * 6
+    # prefix block 6 (tokens 96..99 of 112) was copied on write: private, swapped out
+    assert all(h >= 0 for h in victim.host_table[6:])
+    assert len(seen_out.swap_out) == len(victim.host_table) - 6
+    assert sorted(seen_out.swap_out[:, 1].tolist()) == sorted(victim.host_table[6:])
+    # once the other request finishes, the victim comes back
+    for _ in range(200):
+        p = tr.step()
+        tr.check()
+        if len(p.swap_in):
+            break
+    assert sorted(p.swap_in[:, 0].tolist()) == sorted(seen_out.swap_out[:, 1].tolist())
+    assert victim in tr.running and victim.table[:6] == tr.prefix_blocks[:6]
+    assert victim.table[6:6 + len(p.swap_in)] == p.swap_in[:, 1].tolist()
