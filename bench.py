@@ -347,7 +347,49 @@ def _run_trace(dev, stream, ops, warmup):
             "step_ms_p50": round(float(np.percentile(ms, 50)), 5),
             "step_ms_p99": round(float(np.percentile(ms, 99)), 5),
             "cow_copies": int(tr.total_copies), "finished_requests": len(tr.finished),
+            "mean_block_utilisation": round(tr.summary()["mean_block_utilisation"], 4),
+            "mean_waste_fraction": round(tr.summary()["mean_waste_fraction"], 4),
             "gpu_launches": int(launches)}
+
+
+def _block32(args, dev, stream, ops, peaks):
+    """32-token blocks against 16: the decode batch and the mixed step with the
+    same token slots in half as many blocks, timed like the main line, and
+    the trace's fragmentation at both block sizes (host-side counters)."""
+    import dataclasses
+
+    import torch
+    from paged_kv_cache_174_gb300 import workloads as W
+    from paged_kv_cache_174_gb300.host import CONTINUOUS_BATCHING_TRACE, ContinuousBatchingTrace
+
+    res = {}
+    for name, make in (("decode_batch", W.decode_batch), ("mixed_step", W.mixed_step)):
+        b = make(poison=False, block_size=32)
+        d = W.to_device(b, dev)
+        ws = ops.alloc_workspace(b.num_seqs, b.num_tokens, b.num_q_heads, b.num_kv_heads,
+                                 b.head_dim, b.max_q_len, b.max_seq_len, dev)
+        out = torch.empty_like(d.q)
+        ms, attn_ms = _time_steps(b, d, ws, out, args.steps, args.warmup, stream, ops)
+        alg = W.algorithmic_bytes(b)
+        res[name] = {"ms_per_step": round(ms, 5), "attention_ms": round(attn_ms, 5),
+                     "GB_per_s": round(alg["total"] / (ms * 1e-3) / 1e9, 1),
+                     "attention_frac_of_hbm": round(
+                         alg["attention"] / (attn_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                     "tokens_per_s": round(b.num_tokens / (ms * 1e-3), 1)}
+        del d, ws, out
+    frag = {}
+    for bs in (16, 32):
+        cfg = dataclasses.replace(CONTINUOUS_BATCHING_TRACE, block_size=bs,
+                                  num_blocks=CONTINUOUS_BATCHING_TRACE.num_blocks * 16 // bs)
+        tr = ContinuousBatchingTrace(cfg)
+        for _ in range(cfg.steps):
+            tr.step()
+        sm = tr.summary()
+        frag[str(bs)] = {"mean_block_utilisation": round(sm["mean_block_utilisation"], 4),
+                         "mean_waste_fraction": round(sm["mean_waste_fraction"], 4),
+                         "cow_copies": sm["copies"]}
+    res["trace_fragmentation"] = frag
+    return res
 
 
 def run_ours(args):
@@ -481,11 +523,16 @@ def run_ours(args):
                 "bound": "tensor", "kernel": "prefill chunk alone (tcgen05)",
                 "achieved": pre["tflops"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(pre["tflops"] / peaks["bf16_tflops"], 4),
-                "peak_source": peaks["source"] + " (bf16_tflops, burst)", "traffic": None,
+                "peak_source": peaks["source"] + " (bf16_tflops, burst)",
+                "traffic": _profiled_traffic("prefill_kernel_mixed_step.md",
+                                             ["pa_prefill.cu", "pa_common.cuh",
+                                              "pa_tcgen05.cuh"], mb.name, "mixed_step"),
                 "algorithmic_flops_per_launch": pre["flops"], "avg_launch_ms": pre["ms"]}
         del md, mws, mout
     if not args.no_trace:
         line["trace"] = _run_trace(dev, stream, ops, args.warmup)
+    if not args.no_block32:
+        line["block_size_32"] = _block32(args, dev, stream, ops, peaks)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(b, args.cpu_seconds)
     if world > 1:
@@ -587,6 +634,8 @@ def main():
                     help="skip the mixed chunked-prefill step measurement")
     ap.add_argument("--no-trace", action="store_true",
                     help="skip the continuous-batching trace measurement")
+    ap.add_argument("--no-block32", action="store_true",
+                    help="skip the 32-token block comparison")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

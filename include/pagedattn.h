@@ -23,9 +23,11 @@
  *    takes a caller-provided workspace of pa_workspace_size() bytes (the
  *    allocation-free variant at the end of this header uses a fixed array
  *    built into the library instead).
- *  - Supported: block_size 16; head_dim 64 or 128; num_q_heads a multiple of
- *    num_kv_heads with group size num_q_heads / num_kv_heads in {1, 2, 4, 8};
- *    num_kv_heads in {1, 2, 4, 8}.  Anything else returns PA_ERR_UNSUPPORTED.
+ *  - Supported: block_size 16 or 32 for attention (the cache writes, block
+ *    copies and swaps take any positive block_size); head_dim 64 or 128;
+ *    num_q_heads a multiple of num_kv_heads with group size num_q_heads /
+ *    num_kv_heads in {1, 2, 4, 8}; num_kv_heads in {1, 2, 4, 8}.  Anything
+ *    else returns PA_ERR_UNSUPPORTED.
  *  - On error the call returns a non-zero status and pa_get_last_error()
  *    returns a message (per thread, valid until the next call on the thread).
  */
@@ -78,10 +80,14 @@ int pa_reshape_and_cache(const pa_bf16 *k, const pa_bf16 *v, int32_t num_tokens,
                          const int32_t *slot_mapping, cudaStream_t stream);
 
 /*
- * Workspace bytes pa_paged_attention needs on the current device for a call
- * with these sizes (0 is never returned; the size depends only on the
- * arguments and on the device's SM count).  Returns 0 if an argument is
- * invalid.
+ * Workspace bytes for pa_paged_attention on the current device: enough for
+ * every call whose num_seqs, num_tokens, max_q_len and max_seq_len are at
+ * most these (so one buffer sized for a serving loop's largest step serves
+ * all its steps).  The size depends only on the arguments and the device's SM
+ * count.  A call needs at least its split-KV decode scratch; the prefill
+ * kernel splits keys only as far as the rest of the workspace allows, so a
+ * smaller workspace is never an error past that, only fewer key pieces.
+ * Returns 0 if an argument is invalid.
  */
 size_t pa_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t num_q_heads,
                          int32_t num_kv_heads, int32_t head_dim, int32_t max_q_len,

@@ -192,9 +192,8 @@ size_t pa_workspace_size(int32_t num_seqs, int32_t num_tokens, int32_t num_q_hea
   if (device_state(nullptr, &sms)) return 0;
   const int ctas = pa::decode_ctas(sms);
   size_t bytes = pa::decode_workspace_bytes(ctas, num_seqs, num_q_heads, head_dim);
-  bytes += pa::prefill_plan(num_tokens, num_q_heads, num_kv_heads, head_dim, max_q_len,
-                            max_seq_len, sms, ~size_t(0))
-               .bytes;
+  bytes += pa::prefill_workspace_bound(num_tokens, num_q_heads, num_kv_heads, head_dim,
+                                       max_q_len, max_seq_len, sms);
   return bytes;
 }
 
@@ -264,8 +263,10 @@ int paged_attention_impl(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16
   if (max_q_len > max_seq_len)
     return fail(PA_ERR_INVALID_ARG, "max_q_len %d > max_seq_len %d", max_q_len, max_seq_len);
   if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "scale is NaN");
-  if (block_size != 16)
-    return fail(PA_ERR_UNSUPPORTED, "block_size %d (only 16 is implemented)", block_size);
+  if (block_size != 16 && block_size != 32)
+    return fail(PA_ERR_UNSUPPORTED, "block_size %d (16 and 32 are implemented)", block_size);
+  if ((int64_t)num_blocks * block_size > INT32_MAX)
+    return fail(PA_ERR_UNSUPPORTED, "num_blocks * block_size above 2^31 - 1 token slots");
   const int group = num_q_heads / num_kv_heads;
   if (!pa::decode_supported(head_dim, group, num_kv_heads))
     return fail(PA_ERR_UNSUPPORTED, "shape head_dim=%d group=%d num_kv_heads=%d", head_dim,
@@ -289,14 +290,16 @@ int paged_attention_impl(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16
   if (st) return st;
   const int ctas = pa::decode_ctas(sms);
   const size_t need_decode = pa::decode_workspace_bytes(ctas, num_seqs, num_q_heads, head_dim);
-  const pa::PrefillPlan plan = pa::prefill_plan(num_tokens, num_q_heads, num_kv_heads, head_dim,
-                                                max_q_len, max_seq_len, sms, split_cap);
-  const size_t need_prefill = plan.bytes;
   if (!workspace || !aligned(workspace, 256))
     return fail(PA_ERR_WORKSPACE, "workspace must be a non-null 256-byte aligned pointer");
-  if (workspace_bytes < need_decode + need_prefill)
+  if (workspace_bytes < need_decode)
     return fail(PA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", workspace_bytes,
-                need_decode + need_prefill);
+                need_decode);
+  // the prefill key split takes only what the workspace has left
+  const size_t left = workspace_bytes - need_decode;
+  const pa::PrefillPlan plan =
+      pa::prefill_plan(num_tokens, num_q_heads, num_kv_heads, head_dim, max_q_len, max_seq_len,
+                       sms, left < split_cap ? left : split_cap);
 
   pa::AttnArgs a;
   a.q = q;
@@ -314,6 +317,7 @@ int paged_attention_impl(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16
   a.num_tokens = num_tokens;
   a.max_q_len = max_q_len;
   a.max_seq_len = max_seq_len;
+  a.block_shift = block_size == 32 ? 1 : 0;
   a.scale = scale;
   a.out = out;
   a.err = err;

@@ -50,11 +50,12 @@ struct DecodeParams {
   int4* seq_rec;
   unsigned* err;
   int32_t num_blocks, max_blocks, num_seqs, num_tokens, n_q, n_kv, max_seq_len;
+  int32_t block_shift;  // log2(block_size / 16)
   float scale_log2;
   int32_t nstages;
   int32_t ctas;
   uint32_t stage_bytes;  // K page + V page
-  uint32_t page_bytes;   // one K (or V) page: 16 * n_kv * head_dim * 2
+  uint32_t page_bytes;   // one K (or V) page of 16 tokens: 16 * n_kv * head_dim * 2
   uint32_t row_bytes;    // one token row of one cache: n_kv * head_dim * 2
 };
 
@@ -64,7 +65,8 @@ __device__ __forceinline__ int decode_pages(const DecodeParams& p, int s, bool r
   const int a = __ldg(p.qsl + s), b = __ldg(p.qsl + s + 1);
   if (b - a != 1) return 0;
   const int L = __ldg(p.seq_lens + s);
-  if (L < 1 || L > p.max_seq_len || L > p.max_blocks * kBlock || a < 0 || a >= p.num_tokens) {
+  if (L < 1 || L > p.max_seq_len || L > (p.max_blocks << p.block_shift) * kBlock || a < 0 ||
+      a >= p.num_tokens) {
     if (report) flag_error(p.err, DEVERR_BOUNDS);
     return 0;
   }
@@ -114,7 +116,8 @@ __device__ __forceinline__ void fetch_page(const DecodeParams& p, const PageCurs
                                            uint32_t stage_smem, uint32_t full_bar) {
   const int L = __ldg(p.seq_lens + c.s);
   const int ntok = min(kBlock, L - c.j * kBlock);
-  const int phys = __ldg(p.block_tables + (int64_t)c.s * p.max_blocks + c.j);
+  const int phys =
+      __ldg(p.block_tables + (int64_t)c.s * p.max_blocks + (c.j >> p.block_shift));
   if (phys < 0 || phys >= p.num_blocks) {
     flag_error(p.err, DEVERR_BOUNDS);
     mbar_arrive_expect_tx(full_bar, 0);  // completes the phase with no data
@@ -122,7 +125,9 @@ __device__ __forceinline__ void fetch_page(const DecodeParams& p, const PageCurs
   }
   const uint32_t bytes = (uint32_t)ntok * p.row_bytes;
   mbar_arrive_expect_tx(full_bar, 2 * bytes);
-  const size_t off = (size_t)phys * p.page_bytes;
+  // 16-token page index in the pool: a block of 32 tokens is two pages
+  const size_t page = ((size_t)phys << p.block_shift) + (c.j & ((1 << p.block_shift) - 1));
+  const size_t off = page * p.page_bytes;
   bulk_g2s(stage_smem, reinterpret_cast<const unsigned char*>(p.k_cache) + off, bytes, full_bar);
   bulk_g2s(stage_smem + p.page_bytes, reinterpret_cast<const unsigned char*>(p.v_cache) + off,
            bytes, full_bar);
@@ -678,6 +683,7 @@ cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ct
   p.n_q = a.num_q_heads;
   p.n_kv = a.num_kv_heads;
   p.max_seq_len = a.max_seq_len;
+  p.block_shift = a.block_shift;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.ctas = ctas;
   p.row_bytes = (uint32_t)NKV * D * 2;

@@ -31,6 +31,10 @@ struct AttnArgs {
   int32_t num_tokens;
   int32_t max_q_len;
   int32_t max_seq_len;
+  // log2(block_size / 16): the kernels walk 16-token pages, and page j of a
+  // request lives in block block_tables[j >> block_shift], 16-token half
+  // (j & ((1 << block_shift) - 1)) of it
+  int32_t block_shift;
   float scale;
   uint16_t* out;
   unsigned* err;  // device error word
@@ -67,6 +71,10 @@ struct PrefillPlan {
 };
 PrefillPlan prefill_plan(int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
                          int max_q_len, int max_seq_len, int sm_count, size_t max_bytes);
+// The most bytes any call with at most num_tokens tokens (and these bounds)
+// would use for key pieces.
+size_t prefill_workspace_bound(int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+                               int max_q_len, int max_seq_len, int sm_count);
 cudaError_t launch_prefill(const AttnArgs& a, const PrefillPlan& plan, void* ws, int sm_count,
                            cudaStream_t stream);
 

@@ -35,6 +35,7 @@
 //    are split over several units; each writes (O / l, m, l) per row and a
 //    merge kernel combines the pieces with log-sum-exp weights.
 //  * Persistent CTAs (at most one per SM) walk the unit list.
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
 
@@ -72,6 +73,7 @@ struct PrefillParams {
   float* part_ml;  // [num_tokens * n_q * nsplit, 2]
   unsigned* err;
   int32_t num_blocks, max_blocks, num_seqs, num_tokens, n_q, n_kv, max_seq_len, nsplit;
+  int32_t block_shift;  // log2(block_size / 16)
   float scale_log2;
 };
 
@@ -83,7 +85,8 @@ __device__ __forceinline__ bool prefill_request(const PrefillParams& p, int s, i
   ql = b - a;
   if (ql < 2) return false;
   L = __ldg(p.seq_lens + s);
-  if (L < ql || L > p.max_seq_len || L > p.max_blocks * kBlock || a < 0 || b > p.num_tokens) {
+  if (L < ql || L > p.max_seq_len || L > (p.max_blocks << p.block_shift) * kBlock || a < 0 ||
+      b > p.num_tokens) {
     if (report) flag_error(p.err, DEVERR_BOUNDS);
     return false;
   }
@@ -386,18 +389,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pages = (U.kv_end + kBlock - 1) / kBlock;
         const int32_t* table = p.block_tables + (int64_t)U.s * p.max_blocks;
         for (int kt = U.kt0; kt < U.kt1; ++kt, ++c) {
-          int phys[4];
+          int phys[4];  // 16-token page index in the pool (a 32-token block is two)
           int nvalid = 0;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int lp = kt * kPagesPerTile + pg_lo + i;  // logical page
             phys[i] = -1;
             if (pg_lo + i < pg_hi && lp < pages) {
-              const int b = __ldg(table + lp);
+              const int b = __ldg(table + (lp >> p.block_shift));
               if (b < 0 || b >= p.num_blocks) {
                 flag_error(p.err, DEVERR_BOUNDS);
               } else {
-                phys[i] = b;
+                phys[i] = (b << p.block_shift) + (lp & ((1 << p.block_shift) - 1));
                 ++nvalid;
               }
             }
@@ -837,6 +840,7 @@ cudaError_t launch_prefill_t(const AttnArgs& a, const PrefillPlan& plan, void* w
   p.n_q = a.num_q_heads;
   p.n_kv = a.num_kv_heads;
   p.max_seq_len = a.max_seq_len;
+  p.block_shift = a.block_shift;
   p.nsplit = plan.nsplit;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   if (plan.nsplit > 1) {
@@ -846,7 +850,7 @@ cudaError_t launch_prefill_t(const AttnArgs& a, const PrefillPlan& plan, void* w
                                          ((rows * D * sizeof(float) + 255) & ~size_t(255)));
   }
   const cuuint64_t nkv = (cuuint64_t)a.num_kv_heads;
-  const cuuint64_t rows = (cuuint64_t)a.num_blocks * kBlock;
+  const cuuint64_t rows = ((cuuint64_t)a.num_blocks << a.block_shift) * kBlock;
   CUtensorMap qm, km, vm;
   {
     const cuuint64_t dims[3] = {D, (cuuint64_t)a.num_q_heads, (cuuint64_t)a.num_tokens};
@@ -937,6 +941,23 @@ PrefillPlan prefill_plan(int num_tokens, int num_q_heads, int num_kv_heads, int 
   plan.nsplit = ns;
   plan.bytes = split_bytes(num_tokens, num_q_heads, head_dim, ns);
   return plan;
+}
+
+size_t prefill_workspace_bound(int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+                               int max_q_len, int max_seq_len, int sm_count) {
+  if (max_q_len < 2 || num_kv_heads <= 0 || num_q_heads < num_kv_heads || head_dim <= 0)
+    return 0;
+  // Fewer tokens can mean more pieces, so take the largest plan of any token
+  // count up to num_tokens.  Past tm * sm_count tokens the query tiles alone
+  // fill the SMs and nothing is split.
+  const int tm = kRows / (num_q_heads / num_kv_heads);
+  const long long last = std::min<long long>(num_tokens, (long long)tm * sm_count);
+  size_t most = 0;
+  for (long long t = 2; t <= last; ++t)
+    most = std::max(most, prefill_plan((int)t, num_q_heads, num_kv_heads, head_dim, max_q_len,
+                                       max_seq_len, sm_count, ~size_t(0))
+                              .bytes);
+  return most;
 }
 
 cudaError_t launch_prefill(const AttnArgs& a, const PrefillPlan& plan, void* ws, int sm_count,

@@ -165,6 +165,8 @@ class ContinuousBatchingTrace:
         self.total_swap_in = 0
         self.total_swap_out = 0
         self.total_preempt = {"recompute": 0, "swap": 0}
+        self._util_sum = 0.0       # sums over steps, for the summary's means
+        self._waste_sum = 0.0
         self._swap_in: List[Tuple[int, int]] = []
         self._swap_out: List[Tuple[int, int]] = []
 
@@ -384,9 +386,12 @@ class ContinuousBatchingTrace:
                  "decode_tokens": num_decode, "prefill_tokens": n_prefill,
                  "block_utilisation": self.alloc.used_count / cfg.num_blocks,
                  "tail_waste_slots": alloc_slots - used_slots,
+                 "waste_fraction": (alloc_slots - used_slots) / alloc_slots if alloc_slots else 0.0,
                  "swapped": len(self.swapped), "swap_in_blocks": len(self._swap_in),
                  "swap_out_blocks": len(self._swap_out),
                  "host_free_blocks": self.host.free_count if self.host else 0}
+        self._util_sum += stats["block_utilisation"]
+        self._waste_sum += stats["waste_fraction"]
         plan = StepPlan(index=self.step_index,
                         swap_in=np.array(self._swap_in, np.int32).reshape(-1, 2),
                         swap_out=np.array(self._swap_out, np.int32).reshape(-1, 2),
@@ -428,8 +433,14 @@ class ContinuousBatchingTrace:
 
     def summary(self) -> Dict[str, float]:
         """Whole-trace counters: preemptions by kind, blocks moved by swapping,
-        copy-on-write copies, finished requests."""
-        return {"steps": self.step_index, "finished": len(self.finished),
+        copy-on-write copies, finished requests; and the per-step means of the
+        pool's block utilisation (used / total blocks) and of the internal
+        fragmentation (slots the running requests hold but have not filled,
+        over the slots they hold: only last blocks are ever partly empty)."""
+        n = max(self.step_index, 1)
+        return {"mean_block_utilisation": self._util_sum / n,
+                "mean_waste_fraction": self._waste_sum / n,
+                "steps": self.step_index, "finished": len(self.finished),
                 "running": len(self.running), "waiting": len(self.waiting),
                 "swapped": len(self.swapped), "copies": self.total_copies,
                 "preempt_recompute": self.total_preempt["recompute"],

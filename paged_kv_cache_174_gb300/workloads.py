@@ -231,16 +231,17 @@ def tiny_decode(poison: bool = True) -> PagedBatch:
                       scale=1.0 / 8.0, poison=poison)
 
 
-def decode_batch(poison: bool = True, num_seqs: int = 64, seed: Optional[int] = None
-                 ) -> PagedBatch:
+def decode_batch(poison: bool = True, num_seqs: int = 64, seed: Optional[int] = None,
+                 block_size: int = 16) -> PagedBatch:
+    """block_size 32 keeps the pool's token slots (half as many blocks)."""
     w = WORKLOADS["decode_batch"]
     seed = w.seed if seed is None else seed
     rng = np.random.default_rng(seed + 7)
     lens = rng.integers(128, 4096, size=num_seqs, endpoint=True)
     return make_batch(w.key, lens, [1] * num_seqs, num_q_heads=w.num_q_heads,
                       num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
-                      block_size=w.block_size, num_blocks=w.num_blocks, seed=seed,
-                      poison=poison)
+                      block_size=block_size, num_blocks=w.num_blocks * w.block_size // block_size,
+                      seed=seed, poison=poison)
 
 
 def long_decode(poison: bool = True, seq_len: int = 32768, num_seqs: int = 8) -> PagedBatch:
@@ -253,8 +254,9 @@ def long_decode(poison: bool = True, seq_len: int = 32768, num_seqs: int = 8) ->
 
 
 def mixed_step(poison: bool = True, num_decode: int = 128, chunk: int = 512,
-               cached: int = 3584) -> PagedBatch:
-    """Decodes first, then the prefill chunk (the order the step driver uses)."""
+               cached: int = 3584, block_size: int = 16) -> PagedBatch:
+    """Decodes first, then the prefill chunk (the order the step driver uses);
+    block_size 32 keeps the pool's token slots (half as many blocks)."""
     w = WORKLOADS["mixed_step"]
     rng = np.random.default_rng(w.seed + 7)
     lens = list(rng.integers(256, 2048, size=num_decode, endpoint=True))
@@ -262,8 +264,8 @@ def mixed_step(poison: bool = True, num_decode: int = 128, chunk: int = 512,
     q_lens = [1] * num_decode + [chunk]
     return make_batch(w.key, seq_lens, q_lens, num_q_heads=w.num_q_heads,
                       num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
-                      block_size=w.block_size, num_blocks=w.num_blocks, seed=w.seed,
-                      poison=poison)
+                      block_size=block_size, num_blocks=w.num_blocks * w.block_size // block_size,
+                      seed=w.seed, poison=poison)
 
 
 def by_name(name: str, **kw) -> PagedBatch:

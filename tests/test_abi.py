@@ -60,7 +60,9 @@ def test_host_side_argument_checks(lib):
                                             a["qsl"], a["S"], a["T"], a["mq"], a["ms"],
                                             ctypes.c_float(a["scale"]), a["out"], a["ws"],
                                             a["wsb"], a["st"]))
-    assert attn(bs=32) == "PA_ERR_UNSUPPORTED"
+    assert attn(bs=64) == "PA_ERR_UNSUPPORTED"
+    assert attn(bs=32) == "PA_ERR_INVALID_ARG"  # supported: stops at the null pointers
+    assert attn(bs=32, nb=1 << 26) == "PA_ERR_UNSUPPORTED"  # 2^31 token slots
     assert attn(d=96) == "PA_ERR_UNSUPPORTED"
     assert attn(nq=6, nkv=4) == "PA_ERR_INVALID_ARG"
     assert attn(nq=48, nkv=2) == "PA_ERR_UNSUPPORTED"  # group 24

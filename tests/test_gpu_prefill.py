@@ -128,3 +128,24 @@ def test_prefill_key_split_plan(lens, q_lens, nq, nkv, d, pieces):
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("plan thresholds depend on the SM count")
     assert ops.prefill_splits(sum(q_lens), nq, nkv, d, max(q_lens), max(lens)) == pieces
+
+
+def test_one_workspace_for_a_large_step_serves_a_short_one():
+    """pa_workspace_size bounds every call with smaller sizes: a buffer sized
+    for a 2048-token step serves a 64-token chunk whose keys split into
+    pieces (fewer tokens, more pieces); a buffer with only the decode scratch
+    runs the same call without pieces.  Both agree with the oracle."""
+    b = _batch([4096], [64], seed=13)
+    _, _, ref = run_oracle_step(b)
+    big = ops.alloc_workspace(8, 2048, 32, 8, 128, 512, 4096, "cuda")
+    small = ops.alloc_workspace(1, 64, 32, 8, 128, 1, 4096, "cuda")  # decode scratch only
+    assert ops.prefill_splits(64, 32, 8, 128, 64, 4096) > 1
+    for ws in (big, small):
+        d = W.to_device(b, "cuda")
+        ops.reshape_and_cache(d.k_new, d.v_new, d.k_cache, d.v_cache, d.slot_mapping)
+        out = torch.full_like(d.q, float("nan"))
+        ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens,
+                            d.query_start_loc, b.scale, max_q_len=64, max_seq_len=4096, out=out,
+                            workspace=ws)
+        ops.check_device_errors()
+        assert_attn_close(to_f64(out), ref, f"workspace of {ws.numel()} bytes")

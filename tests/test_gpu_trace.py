@@ -110,11 +110,12 @@ def test_trace_full_configuration_sampled_rows():
     assert tr.total_copies > 0
 
 
-def test_trace_small_heads_all_rows():
+@pytest.mark.parametrize("block_size", [16, 32])
+def test_trace_small_heads_all_rows(block_size):
     cfg = TraceConfig(steps=40, arrival_rate=4.0, prompt_median=150.0, prompt_min=8,
                       prompt_max=700, output_mean=20.0, prefix=60, chunk=64, budget=256,
-                      max_num_seqs=32, num_blocks=1200, num_q_heads=8, num_kv_heads=2,
-                      head_dim=64, seed=21)
+                      max_num_seqs=32, num_blocks=1200 * 16 // block_size, num_q_heads=8,
+                      num_kv_heads=2, head_dim=64, seed=21, block_size=block_size)
     tr, worst = _replay(cfg, steps=40, full_rows=True)
     assert tr.total_copies > 0 and len(tr.finished) > 0
 
