@@ -337,6 +337,57 @@ def _run_trace(dev, stream, ops, warmup):
     ms = np.array([t for _, t in res])
     toks = sum(pl.num_tokens for pl, _ in res)
     launches = sum(3 + (pl.max_q_len >= 2) + (len(pl.copy_pairs) > 0) for pl, _ in res)
+    del kc, vc
+
+    # the same steps, each one launch of the step captured as a CUDA graph at
+    # fixed maxima (metadata copied from pinned host memory inside the graph)
+    def run_graph(g, plan_list, record):
+        times = []
+        for pl in plan_list:
+            if pl.num_tokens == 0:
+                continue
+            T = pl.num_tokens
+            g.q[:T] = torch.randn(T, cfg.num_q_heads, cfg.head_dim, generator=gen,
+                                  device=dev).bfloat16()
+            g.k_new[:T] = torch.randn(T, cfg.num_kv_heads, cfg.head_dim, generator=gen,
+                                      device=dev).bfloat16()
+            g.v_new[:T] = torch.randn(T, cfg.num_kv_heads, cfg.head_dim, generator=gen,
+                                      device=dev).bfloat16()
+            g.stage(pl.slot_mapping, pl.block_tables, pl.seq_lens, pl.query_start_loc,
+                    pl.copy_pairs)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.launch(stream=stream)
+            e1.record(stream)
+            if record:
+                times.append((pl, e0, e1))
+        torch.cuda.synchronize()
+        ops.check_device_errors()
+        return [(pl, a.elapsed_time(b)) for pl, a, b in times]
+
+    def make_graph(kc, vc):
+        return ops.StepGraph(kc, vc, num_q_heads=cfg.num_q_heads, max_tokens=cfg.budget,
+                             max_seqs=cfg.max_num_seqs,
+                             max_blocks=max(pl.block_tables.shape[1] for pl in plans),
+                             max_pairs=max(len(pl.copy_pairs) for pl in plans),
+                             max_q_len=cfg.chunk,
+                             max_seq_len=max(pl.max_seq_len for pl in plans), scale=scale)
+
+    kc, vc = fresh_cache()
+    g = make_graph(kc, vc)
+    run_graph(g, plans[:warmup], False)
+    g.close()
+    kc, vc = fresh_cache()
+    g = make_graph(kc, vc)
+    gres = run_graph(g, plans, True)
+    g.close()
+    gms = np.array([t for _, t in gres])
+    graph = {"tokens_per_s": round(toks / (gms.sum() * 1e-3), 1),
+             "gpu_ms_total": round(float(gms.sum()), 3),
+             "step_ms_p50": round(float(np.percentile(gms, 50)), 5),
+             "step_ms_p99": round(float(np.percentile(gms, 99)), 5),
+             "graph_launches": len(gres),
+             "maxima": {"tokens": cfg.budget, "seqs": cfg.max_num_seqs, "q_len": cfg.chunk}}
     return {"workload": "continuous-batching trace", "steps": len(res),
             "description": "200 steps, Poisson 8 arrivals/step, lognormal prompts (median 600, "
                            "sigma 1, clamp 64-8192), geometric outputs (mean 200), 500-token "
@@ -349,7 +400,7 @@ def _run_trace(dev, stream, ops, warmup):
             "cow_copies": int(tr.total_copies), "finished_requests": len(tr.finished),
             "mean_block_utilisation": round(tr.summary()["mean_block_utilisation"], 4),
             "mean_waste_fraction": round(tr.summary()["mean_waste_fraction"], 4),
-            "gpu_launches": int(launches)}
+            "gpu_launches": int(launches), "step_graph": graph}
 
 
 def _block32(args, dev, stream, ops, peaks):

@@ -156,8 +156,9 @@ int pa_paged_attention(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *
  * table, Copy-on-Write sharing of prompt blocks; "连续批处理：推理吞吐的范式革命",
  * section 4.2, prefix sharing).  Destinations must be distinct and no
  * destination may be a source of the same call (pairs are then independent
- * and run in parallel).  An id outside [0, num_blocks) skips the pair and
- * flags PA_ERR_DEVICE_BOUNDS.
+ * and run in parallel).  A pair whose source is -1 is padding and is skipped
+ * (a fixed-size pair list, as a captured step graph uses); any other id
+ * outside [0, num_blocks) skips the pair and flags PA_ERR_DEVICE_BOUNDS.
  *
  *   src_dst_pairs [num_pairs, 2] int32 device array, read
  */
@@ -234,6 +235,75 @@ int pa_paged_attention_noalloc(const pa_bf16 *q, const pa_bf16 *k_cache,
                                int32_t num_seqs, int32_t num_tokens, int32_t max_q_len,
                                int32_t max_seq_len, float scale, pa_bf16 *out,
                                cudaStream_t stream);
+
+/*
+ * One serving step captured as a CUDA graph: block copies (pa_copy_blocks),
+ * slot scatter (pa_reshape_and_cache) and attention (pa_paged_attention) of
+ * the iteration-level schedule ("PagedAttention 显存分页与连续批处理
+ * (Continuous Batching)实战", continuous batching and Chunked Prefill
+ * sections: every step runs the same sequence of operations over whichever
+ * requests the scheduler picked), launched with one call instead of three to
+ * five kernel launches.  The pages have no counterpart for the graph itself.
+ *
+ * The graph is built once over fixed device buffers sized for the largest
+ * step (the pa_step_buffers maxima); before each launch the caller writes the
+ * step's inputs into those buffers, padded to the maxima:
+ *   - tokens t >= the step's count: slot_mapping[t] = -1 (not written);
+ *   - sequences s >= the step's count: query_start_loc[s + 1] =
+ *     query_start_loc[s] (no rows) and seq_lens[s] = 0;
+ *   - copy pairs i >= the step's count: copy_pairs[2i] = -1 (skipped).
+ * A step's sizes must stay within the maxima (max_q_len and max_seq_len
+ * included: a request beyond them flags PA_ERR_DEVICE_BOUNDS at run time).
+ * Rows of out that belong to no request are left as they were.
+ *
+ * If host_meta is not NULL, every launch first copies meta_bytes from
+ * host_meta (pinned host memory) to dev_meta, so that the per-step integer
+ * inputs (slot_mapping, block_tables, ...) can live in one region of dev_meta
+ * and reach the GPU inside the graph.  The copy reads host_meta when the
+ * launch executes on the GPU, not when it is issued: do not rewrite it until
+ * then (for example, alternate two graphs over two host buffers).
+ *
+ * Buffers stay owned by the caller and must outlive the graph.  Launches of
+ * one graph, and of graphs sharing buffers, must not overlap on the GPU.
+ */
+typedef struct pa_step_buffers {
+  pa_bf16 *k_cache, *v_cache;   /* [num_blocks, block_size, num_kv_heads, head_dim] */
+  int32_t num_blocks, block_size, num_q_heads, num_kv_heads, head_dim;
+  int32_t max_tokens;           /* rows of q, k_new, v_new, out, slot_mapping */
+  int32_t max_seqs;             /* rows of block_tables and seq_lens (+1: query_start_loc) */
+  int32_t max_blocks;           /* columns of block_tables */
+  int32_t max_pairs;            /* rows of copy_pairs; 0: the graph has no copy step */
+  int32_t max_q_len, max_seq_len;
+  float scale;
+  const pa_bf16 *q;             /* [max_tokens, num_q_heads, head_dim] */
+  const pa_bf16 *k_new, *v_new; /* [max_tokens, num_kv_heads, head_dim] */
+  pa_bf16 *out;                 /* [max_tokens, num_q_heads, head_dim] */
+  const int32_t *slot_mapping;  /* [max_tokens] */
+  const int32_t *block_tables;  /* [max_seqs, max_blocks] */
+  const int32_t *seq_lens;      /* [max_seqs] */
+  const int32_t *query_start_loc; /* [max_seqs + 1] */
+  const int32_t *copy_pairs;    /* [max_pairs, 2] or NULL when max_pairs == 0 */
+  void *workspace;              /* >= pa_workspace_size(max_seqs, max_tokens, ...) bytes */
+  size_t workspace_bytes;
+  const void *host_meta;        /* optional pinned host source of a per-launch copy */
+  void *dev_meta;
+  size_t meta_bytes;
+} pa_step_buffers;
+
+typedef struct pa_step_graph pa_step_graph;
+
+/*
+ * Validates the buffers (the same checks as the three calls), captures the
+ * step on the current device and instantiates it.  On success *graph owns
+ * the graph; destroy it with pa_step_graph_destroy.  Nothing runs on the GPU.
+ */
+int pa_step_graph_create(const pa_step_buffers *buffers, pa_step_graph **graph);
+
+/* Launches the captured step on `stream` (asynchronous). */
+int pa_step_graph_launch(pa_step_graph *graph, cudaStream_t stream);
+
+/* Frees the graph (NULL is a no-op).  Launches in flight may finish first. */
+int pa_step_graph_destroy(pa_step_graph *graph);
 
 #ifdef __cplusplus
 }

@@ -76,6 +76,22 @@ int check_cache_geometry(int32_t num_blocks, int32_t block_size, int32_t num_kv_
 
 }  // namespace
 
+namespace pa {
+
+int api_fail(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return status;
+}
+
+int api_warm_device() { return device_state(nullptr, nullptr); }
+
+}  // namespace pa
+
 extern "C" {
 
 int pa_version(void) { return 100; }

@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(kCopyThreads)
                        unsigned* err) {
   const int64_t src = pairs[2 * (int64_t)blockIdx.x];
   const int64_t dst = pairs[2 * (int64_t)blockIdx.x + 1];
+  if (src == -1) return;  // padding of a fixed-size pair list
   if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
     if (threadIdx.x == 0) flag_error(err, DEVERR_BOUNDS);
     return;

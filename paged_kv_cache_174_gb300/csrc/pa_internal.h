@@ -95,4 +95,9 @@ cudaError_t launch_swap(uint16_t* k_cache, uint16_t* v_cache, int32_t num_blocks
                         uint16_t* host_k, uint16_t* host_v, bool out, unsigned* err,
                         cudaStream_t stream);
 
+// Error reporting of the C ABI (sets the message pa_get_last_error returns)
+// and the per-device state lookup, for the parts of the ABI outside pa_api.cu.
+int api_fail(int status, const char* fmt, ...);
+int api_warm_device();
+
 }  // namespace pa

@@ -35,6 +35,22 @@ class PagedAttnError(RuntimeError):
 _lib = None
 
 
+class StepBuffers(ctypes.Structure):
+    """struct pa_step_buffers of include/pagedattn.h."""
+    _vp, _i32 = ctypes.c_void_p, ctypes.c_int32
+    _fields_ = [("k_cache", _vp), ("v_cache", _vp),
+                ("num_blocks", _i32), ("block_size", _i32), ("num_q_heads", _i32),
+                ("num_kv_heads", _i32), ("head_dim", _i32),
+                ("max_tokens", _i32), ("max_seqs", _i32), ("max_blocks", _i32),
+                ("max_pairs", _i32), ("max_q_len", _i32), ("max_seq_len", _i32),
+                ("scale", ctypes.c_float),
+                ("q", _vp), ("k_new", _vp), ("v_new", _vp), ("out", _vp),
+                ("slot_mapping", _vp), ("block_tables", _vp), ("seq_lens", _vp),
+                ("query_start_loc", _vp), ("copy_pairs", _vp),
+                ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
+                ("host_meta", _vp), ("dev_meta", _vp), ("meta_bytes", ctypes.c_size_t)]
+
+
 def _load() -> ctypes.CDLL:
     global _lib
     if _lib is not None:
@@ -66,6 +82,12 @@ def _load() -> ctypes.CDLL:
     L.pa_copy_blocks.restype = ctypes.c_int
     L.pa_check_device_errors.argtypes = [vp]
     L.pa_check_device_errors.restype = ctypes.c_int
+    L.pa_step_graph_create.argtypes = [ctypes.POINTER(StepBuffers), ctypes.POINTER(vp)]
+    L.pa_step_graph_create.restype = ctypes.c_int
+    L.pa_step_graph_launch.argtypes = [vp, vp]
+    L.pa_step_graph_launch.restype = ctypes.c_int
+    L.pa_step_graph_destroy.argtypes = [vp]
+    L.pa_step_graph_destroy.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -256,3 +278,123 @@ def swap_in(k_cache: torch.Tensor, v_cache: torch.Tensor, block_ids: torch.Tenso
 def check_device_errors(stream=None) -> None:
     """Synchronise the stream and raise if a kernel flagged an error."""
     _check(_load().pa_check_device_errors(_stream(stream)))
+
+
+class StepGraph:
+    """One serving step (block copies, slot scatter, attention) captured as a
+    CUDA graph by the library (pa_step_graph_create) over fixed buffers sized
+    for the largest step.
+
+    Per step: write the step's q / k_new / v_new rows into ``self.q``,
+    ``self.k_new``, ``self.v_new`` (first num_tokens rows, on the launching
+    stream), then call :meth:`launch` with the step's integer inputs as host
+    arrays (or :meth:`stage` them first and call :meth:`launch` with none);
+    they are padded to the maxima in a pinned buffer and reach the GPU
+    through the graph's own copy node.  The output is ``self.out[:num_tokens]``.
+    Two graphs alternate over two pinned buffers, so the host fills one while
+    the GPU may still copy from the other.  ``stream`` is a torch.cuda.Stream
+    or None (the current stream).
+    """
+
+    def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, *, num_q_heads: int,
+                 max_tokens: int, max_seqs: int, max_blocks: int, max_pairs: int,
+                 max_q_len: int, max_seq_len: int, scale: float):
+        import numpy as np
+        L = _load()
+        _need(k_cache, "k_cache", torch.bfloat16, 4)
+        _need(v_cache, "v_cache", torch.bfloat16, 4)
+        if v_cache.shape != k_cache.shape:
+            raise ValueError("k_cache and v_cache shapes differ")
+        nb, bs, nkv, d = k_cache.shape
+        dev = k_cache.device
+        T, S, MB, P = int(max_tokens), int(max_seqs), int(max_blocks), int(max_pairs)
+        self.max_tokens, self.max_seqs, self.max_blocks, self.max_pairs = T, S, MB, P
+        self.q = torch.zeros(T, num_q_heads, d, dtype=torch.bfloat16, device=dev)
+        self.k_new = torch.zeros(T, nkv, d, dtype=torch.bfloat16, device=dev)
+        self.v_new = torch.zeros(T, nkv, d, dtype=torch.bfloat16, device=dev)
+        self.out = torch.zeros(T, num_q_heads, d, dtype=torch.bfloat16, device=dev)
+        # int32 metadata region: slots [T] | tables [S*MB] | seq_lens [S] | qsl [S+1] | pairs [2P]
+        self._off = np.cumsum([0, T, S * MB, S, S + 1, 2 * P])
+        n = int(self._off[-1])
+        self._dev_meta = torch.zeros(n, dtype=torch.int32, device=dev)
+        self._host = [torch.zeros(n, dtype=torch.int32).pin_memory() for _ in range(2)]
+        self._events = [None, None]
+        self.workspace = alloc_workspace(S, T, num_q_heads, nkv, d, max_q_len, max_seq_len, dev)
+        base = self._dev_meta.data_ptr()
+        o = [base + 4 * int(x) for x in self._off]
+        self._graphs = []
+        for h in self._host:
+            b = StepBuffers(k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, num_q_heads, nkv, d,
+                            T, S, MB, P, int(max_q_len), int(max_seq_len), float(scale),
+                            self.q.data_ptr(), self.k_new.data_ptr(), self.v_new.data_ptr(),
+                            self.out.data_ptr(), o[0], o[1], o[2], o[3], o[4] if P else None,
+                            self.workspace.data_ptr(), self.workspace.numel(), h.data_ptr(),
+                            base, 4 * n)
+            g = ctypes.c_void_p()
+            _check(L.pa_step_graph_create(ctypes.byref(b), ctypes.byref(g)))
+            self._graphs.append(g)
+        self._next = 0
+        self._staged = False
+        self._keep = (k_cache, v_cache)  # the graphs hold their pointers
+
+    def launch(self, slot_mapping=None, block_tables=None, seq_lens=None, query_start_loc=None,
+               copy_pairs=None, stream=None) -> None:
+        if slot_mapping is not None:
+            self.stage(slot_mapping, block_tables, seq_lens, query_start_loc, copy_pairs)
+        if not self._staged:
+            raise ValueError("no step staged")
+        i = self._next
+        _check(_load().pa_step_graph_launch(self._graphs[i], _stream(stream)))
+        ev = torch.cuda.Event()
+        ev.record(torch.cuda.current_stream(self.q.device) if stream is None else stream)
+        self._events[i] = ev
+        self._next = 1 - i
+        self._staged = False
+
+    def stage(self, slot_mapping, block_tables, seq_lens, query_start_loc,
+              copy_pairs=None) -> None:
+        """Pad the step's integer inputs into the pinned buffer of the next launch."""
+        import numpy as np
+        T, S, MB, P = self.max_tokens, self.max_seqs, self.max_blocks, self.max_pairs
+        sm = np.asarray(slot_mapping, np.int32).reshape(-1)
+        bt = np.asarray(block_tables, np.int32)
+        sl = np.asarray(seq_lens, np.int32).reshape(-1)
+        qsl = np.asarray(query_start_loc, np.int32).reshape(-1)
+        cp = np.zeros((0, 2), np.int32) if copy_pairs is None else \
+            np.asarray(copy_pairs, np.int32).reshape(-1, 2)
+        ns = sl.shape[0]
+        if (sm.shape[0] > T or ns > S or bt.shape[0] != ns or bt.shape[1] > MB
+                or qsl.shape[0] != ns + 1 or cp.shape[0] > P):
+            raise ValueError(f"step beyond the graph's maxima (tokens {sm.shape[0]}/{T}, "
+                             f"seqs {ns}/{S}, table columns {bt.shape[1]}/{MB}, "
+                             f"pairs {cp.shape[0]}/{P}) or inconsistent shapes")
+        i = self._next
+        if self._events[i] is not None:
+            self._events[i].synchronize()  # that launch has read this pinned buffer
+        h = self._host[i].numpy()
+        o = self._off
+        h[o[0]:o[1]] = -1
+        h[o[0]:o[0] + sm.shape[0]] = sm
+        tab = h[o[1]:o[2]].reshape(S, MB)
+        tab[:] = -1
+        tab[:ns, :bt.shape[1]] = bt
+        h[o[2]:o[3]] = 0
+        h[o[2]:o[2] + ns] = sl
+        h[o[3]:o[4]] = qsl[-1] if ns else 0
+        h[o[3]:o[3] + ns + 1] = qsl
+        if P:
+            pr = h[o[4]:o[5]].reshape(P, 2)
+            pr[:] = -1
+            pr[:cp.shape[0]] = cp
+        self._staged = True
+
+    def close(self) -> None:
+        for g in getattr(self, "_graphs", []):
+            _load().pa_step_graph_destroy(g)
+        self._graphs = []
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -88,3 +88,20 @@ def test_torch_side_checks_without_gpu():
         ops.reshape_and_cache(torch.zeros(1, 2, 64), torch.zeros(1, 2, 64),
                               torch.zeros(4, 16, 2, 64), torch.zeros(4, 16, 2, 64),
                               torch.zeros(1, dtype=torch.int32))
+
+
+def test_step_graph_argument_checks_without_gpu():
+    """pa_step_graph_create rejects bad maxima before touching CUDA."""
+    from paged_kv_cache_174_gb300.ops import StepBuffers
+    L = ops.lib()
+    b = StepBuffers()
+    g = ctypes.c_void_p()
+    assert _status(L.pa_step_graph_create(ctypes.byref(b), ctypes.byref(g))) \
+        == "PA_ERR_INVALID_ARG"
+    assert _status(L.pa_step_graph_create(None, ctypes.byref(g))) == "PA_ERR_INVALID_ARG"
+    b.max_tokens, b.max_seqs, b.max_blocks, b.max_q_len, b.max_seq_len = 8, 2, 4, 8, 64
+    b.max_pairs = 3  # copy_pairs left NULL
+    assert _status(L.pa_step_graph_create(ctypes.byref(b), ctypes.byref(g))) \
+        == "PA_ERR_INVALID_ARG"
+    assert b"copy_pairs" in L.pa_get_last_error()
+    assert L.pa_step_graph_destroy(None) == 0
