@@ -46,6 +46,16 @@ def lib() -> ctypes.CDLL:
                                                   vp, i32, vp, vp, i32, dbl, vp, i32,
                                                   vp, i32]
         L.oracle_paged_attention_rows.restype = ctypes.c_int
+        L.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_to_double.restype = dbl
+        L.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+        L.oracle_e4m3_from_float.restype = ctypes.c_uint8
+        L.oracle_reshape_and_cache_fp8.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, i32, i32,
+                                                   i32, vp]
+        L.oracle_reshape_and_cache_fp8.restype = ctypes.c_int
+        L.oracle_paged_attention_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                                 vp, i32, vp, vp, i32, dbl, vp, i32]
+        L.oracle_paged_attention_fp8.restype = ctypes.c_int
         _LIB = L
     return _LIB
 
@@ -170,4 +180,75 @@ def paged_attention_rows(q, k_cache, v_cache, block_tables, seq_lens, query_star
                                            int(smp.shape[0]), _ptr(out), int(threads))
     if st:
         raise OracleError(f"oracle_paged_attention_rows status {st}")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# The 8-bit (FP8 E4M3) cache variant, defined in oracle.c's header comment.
+# ---------------------------------------------------------------------------
+
+def e4m3_to_double(codes) -> np.ndarray:
+    """Values of E4M3 codes (uint8 array), exact, as fp64."""
+    c = np.asarray(codes, np.uint8)
+    f = lib().oracle_e4m3_to_double
+    return np.array([f(int(x)) for x in c.reshape(-1)], np.float64).reshape(c.shape)
+
+
+def e4m3_from_float(values) -> np.ndarray:
+    """fp32 values -> E4M3 codes (nearest, ties to even, saturating at 448)."""
+    v = np.asarray(values, np.float32)
+    f = lib().oracle_e4m3_from_float
+    return np.array([f(float(x)) for x in v.reshape(-1)], np.uint8).reshape(v.shape)
+
+
+def fp8_cache(num_blocks: int, block_size: int, num_kv_heads: int, head_dim: int,
+              fill_code: int = 0x7F):
+    """Empty 8-bit cache: (k codes, v codes, k scales, v scales); codes filled
+    with fill_code (NaN by default), scales with NaN."""
+    shape = (num_blocks, block_size, num_kv_heads, head_dim)
+    kc = np.full(shape, fill_code, np.uint8)
+    vc = np.full(shape, fill_code, np.uint8)
+    ks = np.full(shape[:3], np.nan, np.float32)
+    vs = np.full(shape[:3], np.nan, np.float32)
+    return kc, vc, ks, vs
+
+
+def reshape_and_cache_fp8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping) -> None:
+    """In place: quantise each new (token, kv head) row into the 8-bit cache."""
+    for a, dt in ((k_cache, np.uint8), (v_cache, np.uint8), (k_scale, np.float32),
+                  (v_scale, np.float32)):
+        assert a.dtype == dt and a.flags.c_contiguous
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    sm = _c(slot_mapping, np.int32)
+    nb, bs, nkv, d = k_cache.shape
+    st = lib().oracle_reshape_and_cache_fp8(_ptr(k), _ptr(v), int(sm.shape[0]), _ptr(k_cache),
+                                            _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), nb,
+                                            bs, nkv, d, _ptr(sm))
+    if st:
+        raise OracleError(f"oracle_reshape_and_cache_fp8 status {st}")
+
+
+def paged_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens,
+                        query_start_loc, scale: float, threads: int = 0) -> np.ndarray:
+    """oracle paged attention with every cached value = code * row scale."""
+    q = _c(q, np.uint16)
+    kc = _c(k_cache, np.uint8)
+    vc = _c(v_cache, np.uint8)
+    ks = _c(k_scale, np.float32)
+    vs = _c(v_scale, np.float32)
+    bt = _c(block_tables, np.int32)
+    sl = _c(seq_lens, np.int32)
+    qsl = _c(query_start_loc, np.int32)
+    T, nq, d = q.shape
+    nb, bs, nkv, d2 = kc.shape
+    assert d == d2 and ks.shape == (nb, bs, nkv) and vs.shape == ks.shape
+    S = int(sl.shape[0])
+    maxb = int(bt.shape[1]) if bt.ndim == 2 else 0
+    out = np.full((T, nq, d), np.nan, dtype=np.float64)
+    st = lib().oracle_paged_attention_fp8(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), nb,
+                                          bs, nq, nkv, d, _ptr(bt), maxb, _ptr(sl), _ptr(qsl),
+                                          S, float(scale), _ptr(out), int(threads))
+    if st:
+        raise OracleError(f"oracle_paged_attention_fp8 status {st}")
     return out

@@ -42,6 +42,18 @@
  *    section 2.1: swap is block-grained): swap-out packs the listed blocks,
  *    in list order, into host arrays [n, block_size, num_kv_heads, head_dim];
  *    swap-in writes the host arrays' blocks back at the listed block ids.
+ *
+ * The 8-bit cache variant is not on the pages.  It stores each cached key or
+ * value row (one token, one kv head: head_dim values) as FP8 E4M3 codes plus
+ * one fp32 scale, so that a cache of the same layout holds half the bytes.
+ * Its definition, written out below: E4M3 is the 8-bit format with 1 sign
+ * bit, 4 exponent bits of bias 7 and 3 mantissa bits, no infinities, the
+ * all-ones exponent and mantissa pattern as NaN, largest finite magnitude 448
+ * and subnormals m * 2^-9; a row x quantises to scale = max_c |x_c| / 448
+ * (1 for an all-zero row) and codes round_e4m3(x_c / scale), rounding to
+ * nearest with ties to even and saturating at +-448; the divisions are fp32,
+ * which fixes every code; attention then uses code * scale in place of the
+ * bfloat16 value.
  */
 #include <math.h>
 #include <stdint.h>
@@ -64,6 +76,51 @@ static double bf16_to_double(uint16_t bits) {
   float f;
   memcpy(&f, &u, sizeof f);
   return (double)f;
+}
+
+/* E4M3 code -> value (exact in double). */
+double oracle_e4m3_to_double(uint8_t code) {
+  const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+  double mag;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    mag = ldexp((double)m, -9); /* subnormal: m/8 * 2^(1-7) */
+  else
+    mag = ldexp(1.0 + m / 8.0, e - 7);
+  return sign ? -mag : mag;
+}
+
+/* fp32 value -> E4M3 code, rounding to nearest (ties to even), saturating at
+ * the largest finite magnitude; NaN -> 0x7f.  The quantum (spacing of codes)
+ * is 2^-9 below 2^-6 and 2^(e-3) in the binade [2^e, 2^(e+1)), so the value
+ * rounds to an integer multiple of its binade's quantum; a value rounded up to
+ * the next power of two is still a multiple of the new binade's quantum. */
+uint8_t oracle_e4m3_from_float(float y) {
+  if (isnan(y)) return 0x7f;
+  const int sign = signbit(y) ? 1 : 0;
+  double a = fabs((double)y);
+  double q;
+  if (a < ldexp(1.0, -6)) {
+    q = ldexp(1.0, -9);
+  } else {
+    int e;
+    frexp(a, &e); /* a = f * 2^e, f in [0.5, 1): a in [2^(e-1), 2^e) */
+    q = ldexp(1.0, e - 1 - 3);
+  }
+  double v = nearbyint(a / q) * q; /* a / q is exact; nearbyint: ties to even */
+  if (v > 448.0) v = 448.0;
+  uint8_t bits;
+  if (v < ldexp(1.0, -6)) {
+    bits = (uint8_t)(v / ldexp(1.0, -9)); /* 0..8; 8 means 2^-6, the first normal */
+    if (bits == 8) bits = (uint8_t)(1 << 3);
+  } else {
+    int e;
+    double f = frexp(v, &e); /* v = f * 2^e, f in [0.5, 1) */
+    int ebias = (e - 1) + 7;
+    int m = (int)((f * 2.0 - 1.0) * 8.0);
+    bits = (uint8_t)((ebias << 3) | m);
+  }
+  return (uint8_t)(bits | (sign << 7));
 }
 
 int oracle_num_threads(void) {
@@ -105,6 +162,47 @@ int oracle_reshape_and_cache(const uint16_t *k, const uint16_t *v,
     for (int64_t c = 0; c < row; ++c) {
       k_cache[s * row + c] = k[(int64_t)t * row + c];
       v_cache[s * row + c] = v[(int64_t)t * row + c];
+    }
+  }
+  return ORACLE_OK;
+}
+
+/* The 8-bit cache's scatter: like oracle_reshape_and_cache, but each
+ * (token, kv head) row of head_dim values is quantised (see the header):
+ * scale = max |x| / 448 in fp32 (1 if the row is all zero), code_c =
+ * round_e4m3(x_c / scale) with the division in fp32.  Codes go to
+ * k_cache / v_cache [num_blocks, block_size, num_kv_heads, head_dim] (bytes),
+ * scales to k_scale / v_scale [num_blocks, block_size, num_kv_heads]. */
+static void quantise_row(const uint16_t *x, int32_t n, uint8_t *codes, float *scale) {
+  float amax = 0.0f;
+  for (int32_t c = 0; c < n; ++c) {
+    float a = fabsf((float)bf16_to_double(x[c]));
+    if (a > amax) amax = a;
+  }
+  float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+  for (int32_t c = 0; c < n; ++c)
+    codes[c] = oracle_e4m3_from_float((float)bf16_to_double(x[c]) / sc);
+  *scale = sc;
+}
+
+int oracle_reshape_and_cache_fp8(const uint16_t *k, const uint16_t *v, int32_t num_tokens,
+                                 uint8_t *k_cache, uint8_t *v_cache, float *k_scale,
+                                 float *v_scale, int32_t num_blocks, int32_t block_size,
+                                 int32_t num_kv_heads, int32_t head_dim,
+                                 const int32_t *slot_mapping) {
+  if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 ||
+      num_kv_heads <= 0 || head_dim <= 0)
+    return ORACLE_ERR_ARG;
+  const int64_t num_slots = (int64_t)num_blocks * block_size;
+  for (int32_t t = 0; t < num_tokens; ++t) {
+    int64_t s = slot_mapping[t];
+    if (s < 0) continue;
+    if (s >= num_slots) return ORACLE_ERR_INDEX;
+    for (int32_t g = 0; g < num_kv_heads; ++g) {
+      int64_t src = ((int64_t)t * num_kv_heads + g) * head_dim;
+      int64_t dst = (s * num_kv_heads + g) * head_dim;
+      quantise_row(k + src, head_dim, k_cache + dst, k_scale + s * num_kv_heads + g);
+      quantise_row(v + src, head_dim, v_cache + dst, v_scale + s * num_kv_heads + g);
     }
   }
   return ORACLE_OK;
@@ -188,7 +286,23 @@ typedef struct {
   const int32_t *query_start_loc; /* [num_seqs + 1]                            */
   int32_t num_seqs;
   double scale;
+  /* 8-bit cache (k_cache / v_cache unused when k8 is set) */
+  const uint8_t *k8, *v8;         /* codes, same layout as k_cache             */
+  const float *k_scale, *v_scale; /* [num_blocks, block_size, num_kv_heads]   */
 } oracle_geom;
+
+/* Value c of the cached row (slot, kv head g) of the key (is_v = 0) or value
+ * cache. */
+static double cached(const oracle_geom *G, int is_v, int64_t slot, int32_t g, int32_t c) {
+  const int64_t row = slot * G->num_kv_heads + g;
+  if (G->k8) {
+    const uint8_t *codes = is_v ? G->v8 : G->k8;
+    const float *sc = is_v ? G->v_scale : G->k_scale;
+    return oracle_e4m3_to_double(codes[row * G->head_dim + c]) * (double)sc[row];
+  }
+  const uint16_t *cache = is_v ? G->v_cache : G->k_cache;
+  return bf16_to_double(cache[row * G->head_dim + c]);
+}
 
 /* One output row: sequence s, query row i of that sequence, q head h.
  * scratch holds at least seq_len doubles.  Writes head_dim doubles to out.
@@ -221,10 +335,9 @@ static int attention_row(const oracle_geom *G, int32_t s, int32_t i, int32_t h,
     int32_t phys = table[j / G->block_size];
     if (phys < 0 || phys >= G->num_blocks) return ORACLE_ERR_INDEX;
     int64_t slot = (int64_t)phys * G->block_size + j % G->block_size;
-    const uint16_t *krow = G->k_cache + (slot * G->num_kv_heads + g) * d;
     double acc = 0.0;
     for (int32_t c = 0; c < d; ++c)
-      acc += bf16_to_double(qrow[c]) * bf16_to_double(krow[c]);
+      acc += bf16_to_double(qrow[c]) * cached(G, 0, slot, g, c);
     scratch[j] = G->scale * acc;
   }
   /* softmax */
@@ -241,8 +354,7 @@ static int attention_row(const oracle_geom *G, int32_t s, int32_t i, int32_t h,
   for (int32_t j = 0; j <= p; ++j) {
     int32_t phys = table[j / G->block_size];
     int64_t slot = (int64_t)phys * G->block_size + j % G->block_size;
-    const uint16_t *vrow = G->v_cache + (slot * G->num_kv_heads + g) * d;
-    for (int32_t c = 0; c < d; ++c) out[c] += scratch[j] * bf16_to_double(vrow[c]);
+    for (int32_t c = 0; c < d; ++c) out[c] += scratch[j] * cached(G, 1, slot, g, c);
   }
   for (int32_t c = 0; c < d; ++c) out[c] /= denom;
   return ORACLE_OK;
@@ -260,18 +372,9 @@ static int check_geom(const oracle_geom *G) {
 /* Full paged attention: writes out[t, h, :] (fp64) for every query token t of
  * every sequence.  Rows of out that belong to no sequence are left untouched.
  * num_threads <= 0 means "all available". */
-int oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache,
-                           const uint16_t *v_cache, int32_t num_blocks,
-                           int32_t block_size, int32_t num_q_heads,
-                           int32_t num_kv_heads, int32_t head_dim,
-                           const int32_t *block_tables, int32_t max_blocks,
-                           const int32_t *seq_lens,
-                           const int32_t *query_start_loc, int32_t num_seqs,
-                           double scale, double *out, int32_t num_threads) {
-  oracle_geom G = {q,          k_cache,       v_cache,         num_blocks,
-                   block_size, num_q_heads,   num_kv_heads,    head_dim,
-                   block_tables, max_blocks,  seq_lens,        query_start_loc,
-                   num_seqs,   scale};
+static int paged_attention(oracle_geom G, double *out, int32_t num_threads) {
+  const int32_t num_q_heads = G.num_q_heads, head_dim = G.head_dim, num_seqs = G.num_seqs;
+  const int32_t *query_start_loc = G.query_start_loc, *seq_lens = G.seq_lens;
   int st = check_geom(&G);
   if (st) return st;
   /* enumerate (sequence, row) pairs */
@@ -337,6 +440,39 @@ int oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache,
   return status;
 }
 
+int oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache,
+                           const uint16_t *v_cache, int32_t num_blocks,
+                           int32_t block_size, int32_t num_q_heads,
+                           int32_t num_kv_heads, int32_t head_dim,
+                           const int32_t *block_tables, int32_t max_blocks,
+                           const int32_t *seq_lens,
+                           const int32_t *query_start_loc, int32_t num_seqs,
+                           double scale, double *out, int32_t num_threads) {
+  oracle_geom G = {q,          k_cache,       v_cache,         num_blocks,
+                   block_size, num_q_heads,   num_kv_heads,    head_dim,
+                   block_tables, max_blocks,  seq_lens,        query_start_loc,
+                   num_seqs,   scale, NULL, NULL, NULL, NULL};
+  return paged_attention(G, out, num_threads);
+}
+
+/* Paged attention over the 8-bit cache: every cached value is code * scale
+ * of its row (see the header); the rest is oracle_paged_attention. */
+int oracle_paged_attention_fp8(const uint16_t *q, const uint8_t *k_cache,
+                               const uint8_t *v_cache, const float *k_scale,
+                               const float *v_scale, int32_t num_blocks,
+                               int32_t block_size, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim,
+                               const int32_t *block_tables, int32_t max_blocks,
+                               const int32_t *seq_lens, const int32_t *query_start_loc,
+                               int32_t num_seqs, double scale, double *out,
+                               int32_t num_threads) {
+  oracle_geom G = {q,          NULL,          NULL,            num_blocks,
+                   block_size, num_q_heads,   num_kv_heads,    head_dim,
+                   block_tables, max_blocks,  seq_lens,        query_start_loc,
+                   num_seqs,   scale, k_cache, v_cache, k_scale, v_scale};
+  return paged_attention(G, out, num_threads);
+}
+
 /* Sampled paged attention: computes only the listed (sequence, row, head)
  * triples, so that very large calls can be checked one output row at a time.
  * out is [num_samples, head_dim]. */
@@ -353,7 +489,7 @@ int oracle_paged_attention_rows(const uint16_t *q, const uint16_t *k_cache,
   oracle_geom G = {q,          k_cache,       v_cache,         num_blocks,
                    block_size, num_q_heads,   num_kv_heads,    head_dim,
                    block_tables, max_blocks,  seq_lens,        query_start_loc,
-                   num_seqs,   scale};
+                   num_seqs,   scale, NULL, NULL, NULL, NULL};
   int st = check_geom(&G);
   if (st) return st;
   int32_t max_len = 0;

@@ -356,3 +356,103 @@ def test_pin_swap_round_trip_and_library_gather():
         oracle.swap_out(kc, vc, np.array([nb], np.int32))
     with pytest.raises(oracle.OracleError):
         oracle.swap_in(k2, v2, np.array([-1], np.int32), hk[:1], hv[:1])
+
+
+# ---------------------------------------------------------------------------
+# The 8-bit (FP8 E4M3) cache variant
+# ---------------------------------------------------------------------------
+
+def test_pin_e4m3_codec_against_torch():
+    """The oracle's E4M3 decode equals torch.float8_e4m3fn on all 256 codes;
+    its encode equals torch's conversion on every finite value, every midpoint
+    between neighbours (ties to even) and random values; beyond 448 it
+    saturates."""
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.e4m3_to_double(codes)
+    assert np.array_equal(got, ref, equal_nan=True)
+    fin = np.unique(np.abs(got[np.isfinite(got)]))
+    mids = (fin[1:] + fin[:-1]) / 2
+    rng = np.random.default_rng(3)
+    vals = np.concatenate([fin, mids, -fin, -mids, rng.uniform(-448, 448, 4000),
+                           rng.normal(0, 1e-2, 4000)]).astype(np.float32)
+    t = torch.from_numpy(vals).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_from_float(vals), t)
+    assert oracle.e4m3_from_float(np.array([460, 1000, 3e38, -1000], np.float32)).tolist() == \
+        [0x7E, 0x7E, 0x7E, 0xFE]
+    assert oracle.e4m3_from_float(np.array([np.nan], np.float32)).tolist() == [0x7F]
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
+
+
+def _torch_quantise(x_bf16_bits):
+    """Independent quantiser: per row (last axis) amax / 448 in fp32, x / scale
+    in fp32, torch's float8_e4m3fn conversion."""
+    x = torch.from_numpy(W.f32_from_bf16(x_bf16_bits))
+    amax = x.abs().amax(dim=-1, keepdim=True)
+    sc = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    codes = (x / sc).to(torch.float8_e4m3fn)
+    return codes.view(torch.uint8).numpy(), sc[..., 0].numpy()
+
+
+@pytest.mark.parametrize("lens,q_lens,nq,nkv,d,bs", CASES[:3])
+def test_pin_fp8_cache_attention_equals_dense_sdpa_on_dequantised(lens, q_lens, nq, nkv, d, bs):
+    """Scatter into the 8-bit cache gives, through the block tables, exactly
+    the codes and scales of an independent torch quantiser of the dense rows;
+    attention over the 8-bit cache equals torch's fp64 SDPA on the dequantised
+    dense K/V."""
+    rng = np.random.default_rng(11 + sum(lens))
+    nb = sum(-(-L // bs) for L in lens) + 3
+    (Qs, Ks, Vs), P = _paged_from_dense(rng, lens, q_lens, nq, nkv, d, bs, nb)
+    kc8, vc8, ks, vs = oracle.fp8_cache(nb, bs, nkv, d)
+    for s, L in enumerate(lens):
+        slots = np.array([oracle.slot_of(P["block_tables"][s], p, bs) for p in range(L)],
+                         np.int32)
+        oracle.reshape_and_cache_fp8(Ks[s], Vs[s], kc8, vc8, ks, vs, slots)
+    Kd, Vd = [], []
+    for s, L in enumerate(lens):
+        kq, kscale = _torch_quantise(Ks[s])
+        vq, vscale = _torch_quantise(Vs[s])
+        t = P["block_tables"][s]
+        pos = np.arange(L)
+        blk, row = t[pos // bs], pos % bs
+        assert np.array_equal(kc8[blk, row], kq) and np.array_equal(vc8[blk, row], vq)
+        assert np.array_equal(ks[blk, row], kscale) and np.array_equal(vs[blk, row], vscale)
+        deq = lambda c, sc: torch.from_numpy(c.copy()).view(torch.float8_e4m3fn).to(
+            torch.float64).numpy() * sc[..., None].astype(np.float64)
+        Kd.append(deq(kq, kscale))
+        Vd.append(deq(vq, vscale))
+    got = oracle.paged_attention_fp8(P["q"], kc8, vc8, ks, vs, P["block_tables"], P["seq_lens"],
+                                     P["query_start_loc"], P["scale"])
+    outs = []
+    for s, L in enumerate(lens):
+        q = torch.from_numpy(W.f32_from_bf16(Qs[s]).astype(np.float64)).permute(1, 0, 2)
+        k = torch.from_numpy(Kd[s]).permute(1, 0, 2)
+        v = torch.from_numpy(Vd[s]).permute(1, 0, 2)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            q[None], k[None], v[None], is_causal=True, scale=P["scale"], enable_gqa=True)[0]
+        outs.append(o.permute(1, 0, 2)[L - q_lens[s]:].numpy())
+    np.testing.assert_allclose(got, np.concatenate(outs, axis=0), rtol=1e-10, atol=1e-12)
+
+
+def test_pin_fp8_quantisation_error_bound_and_edges():
+    """Each dequantised value is within half a code spacing (times the row
+    scale) of the input; the row's largest magnitude maps to +-448 exactly; an
+    all-zero row has scale 1 and zero codes."""
+    rng = np.random.default_rng(5)
+    k = W.randn_bf16(rng, (40, 2, 64))
+    k[3, 1] = 0  # an all-zero row
+    kc8, vc8, ks, vs = oracle.fp8_cache(4, 16, 2, 64)
+    oracle.reshape_and_cache_fp8(k, k, kc8, vc8, ks, vs, np.arange(40, dtype=np.int32))
+    x = W.f32_from_bf16(k).astype(np.float64)
+    codes = kc8.reshape(-1, 2, 64)[:40]
+    sc = ks.reshape(-1, 2)[:40].astype(np.float64)
+    deq = oracle.e4m3_to_double(codes) * sc[..., None]
+    y = np.abs(x) / np.where(sc > 0, sc, 1)[..., None]
+    e = np.floor(np.log2(np.maximum(y, 2.0 ** -6)))
+    half = 2.0 ** (e - 3) / 2 * sc[..., None]
+    assert (np.abs(deq - x) <= half * (1 + 1e-6) + 1e-30).all()
+    assert sc[3, 1] == 1.0 and (codes[3, 1] == 0).all()
+    am = np.abs(x).argmax(axis=-1)
+    top = np.take_along_axis(codes, am[..., None], axis=-1)[..., 0]
+    nz = np.abs(x).max(axis=-1) > 0
+    assert set((top[nz] & 0x7F).tolist()) == {0x7E}
