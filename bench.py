@@ -403,6 +403,71 @@ def _run_trace(dev, stream, ops, warmup):
             "gpu_launches": int(launches), "step_graph": graph}
 
 
+def _fp8(args, dev, stream, ops, peaks, bf16_attn_ms):
+    """The decode batch over the 8-bit cache (E4M3 codes + one fp32 scale per
+    cached row): the context is quantised once on the device, then each step
+    quantises the new tokens and runs decode attention, timed like the main
+    line."""
+    import torch
+    from paged_kv_cache_174_gb300 import workloads as W
+
+    b = W.decode_batch(poison=False)
+    nb, bs, nkv, d = b.k_cache.shape
+    k8, v8, ks, vs = ops.empty_fp8_cache(nb, bs, nkv, d, dev)
+    slots = W.context_slots(b)
+    rows = b.k_cache.reshape(-1, nkv, d)
+    ops.reshape_and_cache_fp8(W.bf16_tensor(rows[slots], dev),
+                              W.bf16_tensor(b.v_cache.reshape(-1, nkv, d)[slots], dev),
+                              k8, v8, ks, vs, W.int32_tensor(slots, dev))
+    q = W.bf16_tensor(b.q, dev)
+    kn, vn = W.bf16_tensor(b.k_new, dev), W.bf16_tensor(b.v_new, dev)
+    meta = {k: W.int32_tensor(getattr(b, k), dev)
+            for k in ("slot_mapping", "block_tables", "seq_lens", "query_start_loc")}
+    ws = ops.alloc_workspace(b.num_seqs, b.num_tokens, b.num_q_heads, nkv, d, 1,
+                             b.max_seq_len, dev)
+    out = torch.empty_like(q)
+
+    def step(ev=None):
+        ops.reshape_and_cache_fp8(kn, vn, k8, v8, ks, vs, meta["slot_mapping"])
+        if ev is not None:
+            ev[0].record(stream)
+        ops.paged_attention_fp8(q, k8, v8, ks, vs, meta["block_tables"], meta["seq_lens"],
+                                meta["query_start_loc"], b.scale, max_q_len=1,
+                                max_seq_len=b.max_seq_len, out=out, workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    ops.check_device_errors()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ops.check_device_errors()
+    ms = t0.elapsed_time(t1) / args.steps
+    attn_ms = statistics.mean(a.elapsed_time(c) for a, c in evs)
+    alg = W.algorithmic_bytes_fp8(b)
+    gbs = alg["attention"] / (attn_ms * 1e-3) / 1e9
+    return {"workload": "decode_batch, 8-bit cache (E4M3 codes + fp32 scale per row)",
+            "ms_per_step": round(ms, 5), "attention_ms": round(attn_ms, 5),
+            "tokens_per_s": round(b.num_tokens / (ms * 1e-3), 1),
+            "kv_tokens_per_s": round(int(b.seq_lens.sum()) / (attn_ms * 1e-3), 1),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                         "algorithmic_bytes_per_launch": alg["attention"],
+                         "traffic": _profiled_traffic(
+                             "decode_kernel_fp8_decode_batch.md",
+                             ["pa_decode_kernel.cuh", "pa_decode_fp8.cu", "pa_common.cuh"],
+                             "decode_batch", "decode_batch")},
+            "attention_speedup_vs_bf16": round(bf16_attn_ms / attn_ms, 3)}
+
+
 def _block32(args, dev, stream, ops, peaks):
     """32-token blocks against 16: the decode batch and the mixed step with the
     same token slots in half as many blocks, timed like the main line, and
@@ -545,8 +610,8 @@ def run_ours(args):
                      "unit": "GB/s", "frac": round(attn_gbs / peaks["hbm_gbs"], 4),
                      "peak_source": peaks["source"] + " (hbm_gbs)",
                      "traffic": _profiled_traffic("decode_kernel_decode_batch.md",
-                                                  ["pa_decode.cu", "pa_common.cuh"], b.name,
-                                                  "decode_batch"),
+                                                  ["pa_decode_kernel.cuh", "pa_decode.cu",
+                                                   "pa_common.cuh"], b.name, "decode_batch"),
                      "algorithmic_bytes_per_launch": alg["attention"],
                      "avg_launch_ms": round(attn_ms, 5)},
         "e2e": {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
@@ -584,6 +649,8 @@ def run_ours(args):
         line["trace"] = _run_trace(dev, stream, ops, args.warmup)
     if not args.no_block32:
         line["block_size_32"] = _block32(args, dev, stream, ops, peaks)
+    if not args.no_fp8:
+        line["fp8_cache"] = _fp8(args, dev, stream, ops, peaks, attn_ms)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(b, args.cpu_seconds)
     if world > 1:
@@ -685,6 +752,8 @@ def main():
                     help="skip the mixed chunked-prefill step measurement")
     ap.add_argument("--no-trace", action="store_true",
                     help="skip the continuous-batching trace measurement")
+    ap.add_argument("--no-fp8", action="store_true",
+                    help="skip the 8-bit cache decode measurement")
     ap.add_argument("--no-block32", action="store_true",
                     help="skip the 32-token block comparison")
     args = ap.parse_args()

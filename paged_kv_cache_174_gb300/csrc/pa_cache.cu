@@ -15,6 +15,9 @@
 //   (swap is block-grained and asynchronous on its own streams).  A kernel
 //   packs the listed blocks into a staging buffer (or unpacks them), so the
 //   host transfer is two large copies rather than one per block.
+// 8-bit cache scatter: each (token, kv head) row is quantised to E4M3 codes
+//   with one fp32 scale (row max / 448); the block copy of that cache moves
+//   the codes and the scales with the same copy kernel.
 #include <cstdint>
 
 #include "pa_common.cuh"
@@ -50,6 +53,61 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
     const uint4 b = __ldg(vs + i);
     kd[i] = a;
     vd[i] = b;
+  }
+}
+
+// One warp per new token, quantising its K and V rows into the 8-bit cache:
+// LPH = head_dim / 8 lanes per kv head, each with 8 elements; the row max
+// comes from a shuffle reduction over those lanes, then scale = max / 448
+// (1 for an all-zero row) and code = e4m3(x / scale), both divisions IEEE
+// round-to-nearest, as the definition fixes.
+template <int LPH>
+__global__ void __launch_bounds__(kScatterWarps * 32)
+    reshape_and_cache_fp8_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                                 int32_t num_tokens, uint2* __restrict__ k_cache,
+                                 uint2* __restrict__ v_cache, float* __restrict__ k_scale,
+                                 float* __restrict__ v_scale, int64_t num_slots,
+                                 int32_t num_kv_heads, const int32_t* __restrict__ slot_mapping,
+                                 unsigned* err) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * kScatterWarps + warp;
+  if (t >= num_tokens) return;
+  const int64_t slot = slot_mapping[t];
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (lane == 0) flag_error(err, DEVERR_BOUNDS);
+    return;
+  }
+  constexpr int HPP = 32 / LPH;  // kv heads per pass of the warp
+  const int sub = lane % LPH;
+  const int row_vec = num_kv_heads * LPH;  // 8-element vectors per token row
+  for (int h0 = 0; h0 < num_kv_heads; h0 += HPP) {
+    const int h = h0 + lane / LPH;
+    const bool on = h < num_kv_heads;
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const uint4* src = which ? v : k;
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);
+      if (on) w = __ldg(src + t * row_vec + h * LPH + sub);
+      const float2 x0 = bf16x2_to_float2(w.x), x1 = bf16x2_to_float2(w.y);
+      const float2 x2 = bf16x2_to_float2(w.z), x3 = bf16x2_to_float2(w.w);
+      float amax = fmaxf(fmaxf(fmaxf(fabsf(x0.x), fabsf(x0.y)), fmaxf(fabsf(x1.x), fabsf(x1.y))),
+                         fmaxf(fmaxf(fabsf(x2.x), fabsf(x2.y)), fmaxf(fabsf(x3.x), fabsf(x3.y))));
+#pragma unroll
+      for (int m = LPH / 2; m >= 1; m >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+      const float sc = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+      uint2 codes;
+      codes.x = (uint32_t)e4m3x2_from_floats(__fdiv_rn(x0.x, sc), __fdiv_rn(x0.y, sc)) |
+                ((uint32_t)e4m3x2_from_floats(__fdiv_rn(x1.x, sc), __fdiv_rn(x1.y, sc)) << 16);
+      codes.y = (uint32_t)e4m3x2_from_floats(__fdiv_rn(x2.x, sc), __fdiv_rn(x2.y, sc)) |
+                ((uint32_t)e4m3x2_from_floats(__fdiv_rn(x3.x, sc), __fdiv_rn(x3.y, sc)) << 16);
+      if (on) {
+        uint2* dst = which ? v_cache : k_cache;
+        dst[slot * row_vec + h * LPH + sub] = codes;
+        if (sub == 0) (which ? v_scale : k_scale)[slot * num_kv_heads + h] = sc;
+      }
+    }
   }
 }
 
@@ -149,6 +207,26 @@ cudaError_t launch_reshape_and_cache(const uint16_t* k, const uint16_t* v, int32
       reinterpret_cast<uint4*>(k_cache), reinterpret_cast<uint4*>(v_cache), num_slots,
       row_elems / 8, slot_mapping, err);
   return cudaGetLastError();
+}
+
+cudaError_t launch_reshape_and_cache_fp8(const uint16_t* k, const uint16_t* v,
+                                         int32_t num_tokens, uint8_t* k_cache, uint8_t* v_cache,
+                                         float* k_scale, float* v_scale, int64_t num_slots,
+                                         int32_t num_kv_heads, int32_t head_dim,
+                                         const int32_t* slot_mapping, unsigned* err,
+                                         cudaStream_t stream) {
+  if (num_tokens == 0) return cudaSuccess;
+  const int grid = (num_tokens + kScatterWarps - 1) / kScatterWarps;
+  auto args = [&](auto kern) {
+    kern<<<grid, kScatterWarps * 32, 0, stream>>>(
+        reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v), num_tokens,
+        reinterpret_cast<uint2*>(k_cache), reinterpret_cast<uint2*>(v_cache), k_scale, v_scale,
+        num_slots, num_kv_heads, slot_mapping, err);
+    return cudaGetLastError();
+  };
+  if (head_dim == 128) return args(reshape_and_cache_fp8_kernel<16>);
+  if (head_dim == 64) return args(reshape_and_cache_fp8_kernel<8>);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, int32_t num_blocks,

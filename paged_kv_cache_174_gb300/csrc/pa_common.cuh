@@ -32,6 +32,27 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
+// half pair (low half = element 2i) -> floats (exact).
+__device__ __forceinline__ float2 half2_bits_to_float2(uint32_t w) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.f32.f16 %0, l;\n\t"
+      "cvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(w));
+  return make_float2(lo, hi);
+}
+
+// Two floats -> two E4M3 codes (lo in the low byte): nearest, ties to even,
+// saturating at +-448 (cvt.rn.satfinite puts its first source in the upper
+// byte).
+__device__ __forceinline__ uint16_t e4m3x2_from_floats(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // float -> bfloat16 bits, round to nearest even (NaN stays NaN).
 __device__ __forceinline__ uint16_t float_to_bf16_rn(float f) {
   uint16_t r;

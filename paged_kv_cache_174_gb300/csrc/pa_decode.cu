@@ -1,744 +1,8 @@
-// pa_decode.cu -- split-KV decode attention over the paged KV cache, and the
-// log-sum-exp merge of the splits.
-//
-// What it computes ("连续批处理：推理吞吐的范式革命", section 4.1): for every
-// request with exactly one query token, walk its Block Table, score each
-// cached key against q (scaled dot product), softmax over the keys, and sum
-// the values with those weights; the page's "many small per-block matmuls
-// then merge the softmax results" is the split/merge structure used here.
-// The page's kernel is one thread block per (token, head) with a scalar loop;
-// this kernel is organised around GB300's memory system instead:
-//
-//  * Work is the flat list of (request, page) pairs of all decode requests.
-//    One persistent CTA per SM takes an equal contiguous slice of it, so the
-//    load is balanced to within one page whatever the length mix.  A slice
-//    may start or end inside a request; such pieces leave a partial result
-//    (unnormalised o, running max m, sum l) that the merge kernel combines.
-//  * A page of the cache ([16 tokens][num_kv_heads][head_dim] bf16) is one
-//    contiguous block of memory, so K and V pages are fetched whole with one
-//    bulk asynchronous copy each into a ring of shared-memory stages, issued
-//    by a producer warp and tracked by mbarriers: several pages per SM are in
-//    flight at once, which is what keeps HBM busy.
-//  * Each consumer warp owns one kv head (and a slice of the page's tokens)
-//    and all q heads of its GQA group, so every K/V byte is read from HBM
-//    once.  Lanes hold a 16-byte slice of head_dim; q.k is reduced with
-//    warp shuffles that also spread the group's heads across lanes.
-//  * Online softmax per page in base 2 (q is pre-scaled by scale * log2 e),
-//    fp32 accumulation with packed fp32x2 FMAs.
-#include <cstdint>
-#include <cfloat>
-
-#include "pa_common.cuh"
-#include "pa_internal.h"
+// pa_decode.cu -- the bf16-cache instantiations of the split-KV decode
+// kernel (pa_decode_kernel.cuh), its workspace layout and the dispatch.
+#include "pa_decode_kernel.cuh"
 
 namespace pa {
-namespace {
-
-constexpr int kBlock = 16;  // tokens per physical block
-constexpr float kNegInf = -INFINITY;
-
-struct DecodeParams {
-  const uint16_t* q;
-  const uint16_t* k_cache;
-  const uint16_t* v_cache;
-  const int32_t* block_tables;
-  const int32_t* seq_lens;
-  const int32_t* qsl;
-  uint16_t* out;
-  float* part_o;
-  float* part_ml;
-  int4* seq_rec;
-  unsigned* err;
-  int32_t num_blocks, max_blocks, num_seqs, num_tokens, n_q, n_kv, max_seq_len;
-  int32_t block_shift;  // log2(block_size / 16)
-  float scale_log2;
-  int32_t nstages;
-  int32_t ctas;
-  uint32_t stage_bytes;  // K page + V page
-  uint32_t page_bytes;   // one K (or V) page of 16 tokens: 16 * n_kv * head_dim * 2
-  uint32_t row_bytes;    // one token row of one cache: n_kv * head_dim * 2
-};
-
-// Pages this kernel processes for request s (0 if it is not a decode request
-// or is invalid; invalid ones flag the error word once, from CTA 0).
-__device__ __forceinline__ int decode_pages(const DecodeParams& p, int s, bool report) {
-  const int a = __ldg(p.qsl + s), b = __ldg(p.qsl + s + 1);
-  if (b - a != 1) return 0;
-  const int L = __ldg(p.seq_lens + s);
-  if (L < 1 || L > p.max_seq_len || L > (p.max_blocks << p.block_shift) * kBlock || a < 0 ||
-      a >= p.num_tokens) {
-    if (report) flag_error(p.err, DEVERR_BOUNDS);
-    return 0;
-  }
-  return (L + kBlock - 1) / kBlock;
-}
-
-__device__ __forceinline__ int64_t slice_begin(int64_t c, int64_t F, int64_t C) {
-  return c * F / C;
-}
-
-// Shared-memory state after the stage ring (dynamic shared memory).
-template <int G>
-struct PBuf {          // hand-off from the QK warp to the PV warp of one kv head
-  float p[kBlock][G];  // exp2(score - m) of the page's tokens
-  float alpha[G];      // rescale of the running output for this page
-  float m[G];          // running max after this page (segment end only)
-  float l[G];          // running sum after this page (segment end only)
-};
-
-template <int G, int NKV>
-struct DecodeSmem {
-  uint64_t full[8];           // stage holds its page (bulk-copy transaction count)
-  uint64_t p_full[NKV][2];    // QK warp -> PV warp: page's p is ready
-  uint64_t p_empty[NKV][2];   // PV warp -> QK warp: buffer may be rewritten
-  int released[8];            // warps done with the page in the stage
-  int last_issued[8];         // last page whose copies went into the stage (-1: none)
-  PBuf<G> pb[NKV][2];
-  int plan[2];
-  int abort_flag;
-};
-
-// Walks the flat page list of the decode requests: (request s, page j).
-struct PageCursor {
-  int s, j, np;
-  __device__ __forceinline__ void next(const DecodeParams& p) {
-    if (++j == np) {
-      j = 0;
-      do {
-        ++s;
-      } while (s < p.num_seqs && (np = decode_pages(p, s, false)) == 0);
-    }
-  }
-};
-
-// Issue the bulk copies of page (c.s, c.j) into a stage.
-__device__ __forceinline__ void fetch_page(const DecodeParams& p, const PageCursor& c,
-                                           uint32_t stage_smem, uint32_t full_bar) {
-  const int L = __ldg(p.seq_lens + c.s);
-  const int ntok = min(kBlock, L - c.j * kBlock);
-  const int phys =
-      __ldg(p.block_tables + (int64_t)c.s * p.max_blocks + (c.j >> p.block_shift));
-  if (phys < 0 || phys >= p.num_blocks) {
-    flag_error(p.err, DEVERR_BOUNDS);
-    mbar_arrive_expect_tx(full_bar, 0);  // completes the phase with no data
-    return;
-  }
-  const uint32_t bytes = (uint32_t)ntok * p.row_bytes;
-  mbar_arrive_expect_tx(full_bar, 2 * bytes);
-  // 16-token page index in the pool: a block of 32 tokens is two pages
-  const size_t page = ((size_t)phys << p.block_shift) + (c.j & ((1 << p.block_shift) - 1));
-  const size_t off = page * p.page_bytes;
-  bulk_g2s(stage_smem, reinterpret_cast<const unsigned char*>(p.k_cache) + off, bytes, full_bar);
-  bulk_g2s(stage_smem + p.page_bytes, reinterpret_cast<const unsigned char*>(p.v_cache) + off,
-           bytes, full_bar);
-}
-
-template <int N>
-__device__ __forceinline__ void lds_floats(uint32_t addr, float (&v)[N]) {
-  if constexpr (N % 4 == 0) {
-#pragma unroll
-    for (int i = 0; i < N; i += 4) {
-      const float4 x = lds128f(addr + 4 * i);
-      v[i] = x.x, v[i + 1] = x.y, v[i + 2] = x.z, v[i + 3] = x.w;
-    }
-  } else if constexpr (N == 2) {
-    float2 x;
-    asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(x.x), "=f"(x.y) : "r"(addr));
-    v[0] = x.x, v[1] = x.y;
-  } else {
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v[0]) : "r"(addr));
-  }
-}
-
-// Sum over the LPT lanes of one token, handing out the G values: after the
-// call, lane holds the total of value index (lane % LPT) / (LPT / G).
-template <int G, int LPT>
-__device__ __forceinline__ float reduce_scatter(float (&part)[G], int lane) {
-  int cnt = G;
-#pragma unroll
-  for (int m = LPT / 2; m >= 1; m >>= 1) {
-    if (cnt > 1) {
-      const int half = cnt / 2;
-      const bool upper = (lane & m) != 0;
-#pragma unroll
-      for (int x = 0; x < G / 2; ++x) {
-        if (x < half) {
-          const float send = upper ? part[x] : part[x + half];
-          const float keep = upper ? part[x + half] : part[x];
-          part[x] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-        }
-      }
-      cnt = half;
-    } else {
-      part[0] += __shfl_xor_sync(0xffffffffu, part[0], m);
-    }
-  }
-  return part[0];
-}
-
-// Scores of one page for one QK warp.  kb points at this lane's 16-byte piece
-// of its first token's key row in the stage; FULL pages need no per-token
-// predicate.  sc[it] is the base-2 score of token it * TPI + tok_lane for the
-// head this lane holds after the reduce-scatter (-inf past the page's end).
-template <int D, int G, int E_QK, int LPT, uint32_t ROW, bool FULL>
-__device__ __forceinline__ void qk_scores(const unsigned char* kb, int ntok, int tok_lane,
-                                          const float2 (&qf)[G][E_QK / 2],
-                                          float (&sc)[kBlock / (32 / LPT)], int lane) {
-  constexpr int TPI = 32 / LPT;
-  constexpr int NIT = kBlock / TPI;
-#pragma unroll
-  for (int it = 0; it < NIT; ++it) {
-    const bool valid = FULL || (it * TPI + tok_lane < ntok);
-    float2 a2[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) a2[h] = make_float2(0.f, 0.f);
-    if (valid) {
-#pragma unroll
-      for (int piece = 0; piece < E_QK / 8; ++piece) {
-        const uint4 kw = *reinterpret_cast<const uint4*>(kb + it * TPI * ROW + piece * D);
-        const uint32_t ks[4] = {kw.x, kw.y, kw.z, kw.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 k2 = bf16x2_to_float2(ks[e]);
-#pragma unroll
-          for (int h = 0; h < G; ++h) a2[h] = __ffma2_rn(qf[h][piece * 4 + e], k2, a2[h]);
-        }
-      }
-    }
-    float part[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) part[h] = a2[h].x + a2[h].y;
-    const float s = reduce_scatter<G, LPT>(part, lane);
-    sc[it] = valid ? s : kNegInf;
-  }
-}
-
-// p * V of one page for one PV warp: vb points at this lane's 16-byte piece of
-// its first token's value row, pp at p[tok_lane][0] of the page's hand-off.
-template <int D, int G, int LPT, uint32_t ROW, bool FULL>
-__device__ __forceinline__ void pv_accumulate(const unsigned char* vb, const float* pp, int ntok,
-                                              int tok_lane, float2 (&acc)[G][4]) {
-  constexpr int TPI = 32 / LPT;
-  constexpr int NIT = kBlock / TPI;
-#pragma unroll
-  for (int it = 0; it < NIT; ++it) {
-    if (FULL || it * TPI + tok_lane < ntok) {
-      const uint4 vw = *reinterpret_cast<const uint4*>(vb + it * TPI * ROW);
-      const uint32_t vs[4] = {vw.x, vw.y, vw.z, vw.w};
-      float pr[G];
-      if constexpr (G % 4 == 0) {
-#pragma unroll
-        for (int h = 0; h < G; h += 4) {
-          const float4 x = *reinterpret_cast<const float4*>(pp + it * TPI * G + h);
-          pr[h] = x.x, pr[h + 1] = x.y, pr[h + 2] = x.z, pr[h + 3] = x.w;
-        }
-      } else {
-#pragma unroll
-        for (int h = 0; h < G; ++h) pr[h] = pp[it * TPI * G + h];
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 v2 = bf16x2_to_float2(vs[e]);
-#pragma unroll
-        for (int h = 0; h < G; ++h) acc[h][e] = __ffma2_rn(v2, make_float2(pr[h], pr[h]), acc[h][e]);
-      }
-    }
-  }
-}
-
-// D: head_dim; G: q heads per kv head; NKV: kv heads (= warps of each role).
-// Warps 0..NKV-1 compute scores and the softmax (QK warps), warps
-// NKV..2*NKV-1 accumulate p * V (PV warps); warp g and warp NKV + g serve kv
-// head g and hand over p through a double-buffered slot in shared memory.
-template <int D, int G, int NKV>
-__global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodeParams p) {
-  constexpr int NW = 2 * NKV;
-  // QK lanes: E_QK head_dim elements each (two 16-byte pieces when 16)
-  constexpr int E_QK = (G <= 4 && D == 128) ? 16 : 8;
-  constexpr int LPT_QK = D / E_QK;
-  constexpr int TPI_QK = 32 / LPT_QK;
-  constexpr int NIT_QK = kBlock / TPI_QK;
-  constexpr int REP_QK = LPT_QK / G;
-  // PV lanes: 8 elements (16 bytes) each
-  constexpr int LPT_PV = D / 8;
-  constexpr int TPI_PV = 32 / LPT_PV;
-  constexpr uint32_t ROW = NKV * D * 2;  // bytes of one token row in a page
-  static_assert(LPT_QK >= G && LPT_QK % G == 0, "group too large for the lane split");
-
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  using Smem = DecodeSmem<G, NKV>;
-  unsigned char* stages = smem_raw;
-  Smem& S = *reinterpret_cast<Smem*>(smem_raw + (size_t)p.nstages * p.stage_bytes);
-  __shared__ long long red[NW];
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int C = p.ctas;
-  const int c = blockIdx.x;
-  const int NST = p.nstages;
-  // the merge kernel waits for this whole grid anyway; let it be scheduled
-  asm volatile("griddepcontrol.launch_dependents;");
-
-  // ---------------------------------------------------------------- plan
-  // pass 1: total decode pages F (all threads)
-  long long mine = 0;
-  for (int s = threadIdx.x; s < p.num_seqs; s += blockDim.x)
-    mine += decode_pages(p, s, c == 0);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
-  if (lane == 0) red[warp] = mine;
-  __syncthreads();
-  long long F = 0;
-#pragma unroll
-  for (int w = 0; w < NW; ++w) F += red[w];
-  const int64_t f0 = slice_begin(c, F, C), f1 = slice_begin(c + 1, F, C);
-  const int n_pages = (int)(f1 - f0);
-  if (n_pages <= 0) return;  // uniform: the whole CTA leaves
-
-  // pass 2: locate the request holding flat page f0 (warp 0), start the ring
-  if (warp == 0) {
-    long long run = 0;
-    int found_s = -1, found_j = 0;
-    for (int base = 0; base < p.num_seqs && found_s < 0; base += 32) {
-      const int s = base + lane;
-      const int np = s < p.num_seqs ? decode_pages(p, s, false) : 0;
-      long long incl = np;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const long long y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const long long excl = run + incl - np;
-      const bool hit = np > 0 && f0 >= excl && f0 < excl + np;
-      const unsigned ball = __ballot_sync(0xffffffffu, hit);
-      if (ball) {
-        const int src = __ffs(ball) - 1;
-        found_s = base + src;
-        found_j = (int)(f0 - __shfl_sync(0xffffffffu, excl, src));
-      }
-      run += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) {
-      S.plan[0] = found_s;
-      S.plan[1] = found_j;
-      S.abort_flag = 0;
-      for (int i = 0; i < NST; ++i) {
-        mbar_init(smem_addr(&S.full[i]), 1);
-        S.released[i] = 0;
-        S.last_issued[i] = -1;
-      }
-      for (int g = 0; g < NKV; ++g)
-        for (int b = 0; b < 2; ++b) {
-          mbar_init(smem_addr(&S.p_full[g][b]), 1);
-          mbar_init(smem_addr(&S.p_empty[g][b]), 1);
-        }
-      fence_mbar_init();
-      if (found_s >= 0) {
-        PageCursor fc{found_s, found_j, decode_pages(p, found_s, false)};
-        for (int i = 0; i < NST && i < n_pages; ++i) {
-          fetch_page(p, fc, smem_addr(stages + (size_t)i * p.stage_bytes),
-                     smem_addr(&S.full[i]));
-          S.last_issued[i] = i;
-          fc.next(p);
-        }
-      }
-    }
-  }
-  __syncthreads();
-  const int s_begin = S.plan[0];
-  const int j_begin = S.plan[1];
-  if (s_begin < 0) return;  // cannot happen when n_pages > 0
-  volatile int* abort_flag = &S.abort_flag;
-
-  const bool is_qk = warp < NKV;
-  const int g = is_qk ? warp : warp - NKV;  // kv head served by this warp
-  PageCursor cur{s_begin, j_begin, decode_pages(p, s_begin, false)};
-  PageCursor fc = cur;  // page to fetch when this warp is the last to release a stage
-  for (int i = 0; i < NST; ++i) fc.next(p);
-
-  int L = __ldg(p.seq_lens + cur.s);
-  int seg_j0 = j_begin;
-
-  if (is_qk) {
-    // ================================================================ QK warp
-    const int tok_lane = lane / LPT_QK;
-    const int dl = lane % LPT_QK;
-    const int my_h = dl / REP_QK;
-    const int rep = dl % REP_QK;
-    float2 qf[G][E_QK / 2];
-    float m_run = kNegInf, l_lane = 0.f;
-    auto load_q = [&](int seq) {
-      const int tok = __ldg(p.qsl + seq);
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const uint16_t* qrow = p.q + ((int64_t)tok * p.n_q + g * G + h) * D;
-#pragma unroll
-        for (int piece = 0; piece < E_QK / 8; ++piece) {
-          const uint4 w = __ldg(reinterpret_cast<const uint4*>(qrow + piece * (D / 2) + dl * 8));
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = bf16x2_to_float2(ws[e]);
-            qf[h][piece * 4 + e] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
-          }
-        }
-      }
-      m_run = kNegInf;
-      l_lane = 0.f;
-    };
-    load_q(cur.s);
-    // this lane's piece of its first token's key row, relative to a stage
-    const uint32_t k_off = (uint32_t)(g * D * 2 + dl * 16) + (uint32_t)tok_lane * ROW;
-    int st = 0, st_phase = 0;
-    const unsigned char* stage = stages;
-    for (int i = 0; i < n_pages; ++i) {
-      const int b = i & 1;
-      if (i >= 2) mbar_wait(smem_addr(&S.p_empty[g][b]), ((i >> 1) - 1) & 1, p.err, abort_flag);
-      mbar_wait(smem_addr(&S.full[st]), st_phase, p.err, abort_flag);
-      const int ntok = min(kBlock, L - cur.j * kBlock);
-      float sc[NIT_QK];
-      if (ntok == kBlock)
-        qk_scores<D, G, E_QK, LPT_QK, ROW, true>(stage + k_off, ntok, tok_lane, qf, sc, lane);
-      else
-        qk_scores<D, G, E_QK, LPT_QK, ROW, false>(stage + k_off, ntok, tok_lane, qf, sc, lane);
-      // online softmax (base 2) for head my_h over the page's 16 tokens
-      float mx = sc[0];
-#pragma unroll
-      for (int it = 1; it < NIT_QK; ++it) mx = fmaxf(mx, sc[it]);
-#pragma unroll
-      for (int m = LPT_QK; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-      const float m_new = fmaxf(m_run, mx);
-      const float m_use = (m_new == kNegInf) ? 0.f : m_new;
-      const float alpha = fast_exp2(m_run - m_use);
-      PBuf<G>& pb = S.pb[g][b];
-      float* pw = &pb.p[tok_lane][my_h];
-      float lsum = 0.f;
-#pragma unroll
-      for (int it = 0; it < NIT_QK; ++it) {
-        const float pr = fast_exp2(sc[it] - m_use);
-        lsum += pr;
-        if (rep == 0) pw[it * TPI_QK * G] = pr;
-      }
-      l_lane = l_lane * alpha + lsum;
-      m_run = m_new;
-      if (tok_lane == 0 && rep == 0) pb.alpha[my_h] = alpha;
-      const bool seq_done = (cur.j + 1 == cur.np);
-      const bool seg_end = seq_done || (i + 1 == n_pages);
-      if (seg_end) {
-        float lt = l_lane;
-#pragma unroll
-        for (int m = LPT_QK; m < 32; m <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, m);
-        if (tok_lane == 0 && rep == 0) {
-          pb.m[my_h] = m_run;
-          pb.l[my_h] = lt;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_addr(&S.p_full[g][b]));
-        // release the stage; the last warp out refills it NST pages ahead
-        if (atomicAdd(&S.released[st], 1) == NW - 1) {
-          S.released[st] = 0;
-          if (i + NST < n_pages && !*abort_flag) {
-            fetch_page(p, fc, smem_addr(stage), smem_addr(&S.full[st]));
-            S.last_issued[st] = i + NST;
-          }
-        }
-        fc.next(p);
-      }
-      stage += p.stage_bytes;
-      if (++st == NST) st = 0, st_phase ^= 1, stage = stages;
-      const int prev_s = cur.s;
-      cur.next(p);
-      if (seg_end && cur.s != prev_s && i + 1 < n_pages) {
-        L = __ldg(p.seq_lens + cur.s);
-        load_q(cur.s);
-      }
-    }
-  } else {
-    // ================================================================ PV warp
-    const int tok_lane = lane / LPT_PV;
-    const int dl = lane % LPT_PV;
-    float2 acc[G][4];
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[h][e] = make_float2(0.f, 0.f);
-    // this lane's piece of its first token's value row, relative to a stage
-    const uint32_t v_off = p.page_bytes + (uint32_t)(g * D * 2 + dl * 16) + (uint32_t)tok_lane * ROW;
-    int st = 0, st_phase = 0;
-    const unsigned char* stage = stages;
-    for (int i = 0; i < n_pages; ++i) {
-      const int b = i & 1;
-      mbar_wait(smem_addr(&S.full[st]), st_phase, p.err, abort_flag);
-      mbar_wait(smem_addr(&S.p_full[g][b]), (i >> 1) & 1, p.err, abort_flag);
-      const int ntok = min(kBlock, L - cur.j * kBlock);
-      const PBuf<G>& pb = S.pb[g][b];
-      const uint32_t pb_addr = smem_addr(&pb);
-      float al[G];
-      lds_floats<G>(pb_addr + offsetof(PBuf<G>, alpha), al);
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float2 a2 = make_float2(al[h], al[h]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[h][e] = __fmul2_rn(acc[h][e], a2);
-      }
-      const float* pp = &pb.p[tok_lane][0];
-      if (ntok == kBlock)
-        pv_accumulate<D, G, LPT_PV, ROW, true>(stage + v_off, pp, ntok, tok_lane, acc);
-      else
-        pv_accumulate<D, G, LPT_PV, ROW, false>(stage + v_off, pp, ntok, tok_lane, acc);
-      const bool seq_done = (cur.j + 1 == cur.np);
-      const bool seg_end = seq_done || (i + 1 == n_pages);
-      float m_fin[G], l_fin[G];
-      if (seg_end) {
-        lds_floats<G>(pb_addr + offsetof(PBuf<G>, m), m_fin);
-        lds_floats<G>(pb_addr + offsetof(PBuf<G>, l), l_fin);
-      }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_addr(&S.p_empty[g][b]));
-        if (atomicAdd(&S.released[st], 1) == NW - 1) {
-          S.released[st] = 0;
-          if (i + NST < n_pages && !*abort_flag) {
-            fetch_page(p, fc, smem_addr(stage), smem_addr(&S.full[st]));
-            S.last_issued[st] = i + NST;
-          }
-        }
-        fc.next(p);
-      }
-      stage += p.stage_bytes;
-      if (++st == NST) st = 0, st_phase ^= 1, stage = stages;
-      if (seg_end) {
-        // sum over the token lanes of the warp
-#pragma unroll
-        for (int m = LPT_PV; m < 32; m <<= 1)
-#pragma unroll
-          for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, m);
-              acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, m);
-            }
-        if (tok_lane == 0) {
-          const int tok = __ldg(p.qsl + cur.s);
-          const bool whole = (seg_j0 == 0) && seq_done;
-          const int slot = 2 * c + (cur.s == s_begin ? 0 : 1);
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const int qh = g * G + h;
-            if (whole) {
-              const float inv = 1.f / l_fin[h];
-              uint4 w;
-              w.x = pack_bf16x2(acc[h][0].x * inv, acc[h][0].y * inv);
-              w.y = pack_bf16x2(acc[h][1].x * inv, acc[h][1].y * inv);
-              w.z = pack_bf16x2(acc[h][2].x * inv, acc[h][2].y * inv);
-              w.w = pack_bf16x2(acc[h][3].x * inv, acc[h][3].y * inv);
-              *reinterpret_cast<uint4*>(p.out + ((int64_t)tok * p.n_q + qh) * D + dl * 8) = w;
-            } else {
-              float4* dst = reinterpret_cast<float4*>(
-                  p.part_o + ((int64_t)slot * p.n_q + qh) * D + dl * 8);
-              dst[0] = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
-              dst[1] = make_float4(acc[h][2].x, acc[h][2].y, acc[h][3].x, acc[h][3].y);
-              if (dl == 0) {
-                p.part_ml[((int64_t)slot * p.n_q + qh) * 2 + 0] = m_fin[h];
-                p.part_ml[((int64_t)slot * p.n_q + qh) * 2 + 1] = l_fin[h];
-              }
-            }
-          }
-          if (g == 0 && lane == 0 && seg_j0 == 0) {
-            // this CTA owns the request's first page: record where its pieces are
-            int c_last = c;
-            if (!seq_done) {
-              const int64_t f_last = f0 + i + (cur.np - 1 - cur.j);
-              const int64_t cl = ((f_last + 1) * C + F - 1) / F - 1;
-              c_last = (int)(cl < C - 1 ? cl : C - 1);
-            }
-            p.seq_rec[cur.s] = make_int4(c, c_last, slot, (int)F);
-          }
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[h][e] = make_float2(0.f, 0.f);
-      }
-      const int prev_s = cur.s;
-      cur.next(p);
-      if (seg_end && cur.s != prev_s && i + 1 < n_pages) {
-        L = __ldg(p.seq_lens + cur.s);
-        seg_j0 = 0;
-      }
-    }
-  }
-
-  // never hand back shared memory with a copy still landing in it
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int st = 0; st < NST; ++st) {
-      const int i = S.last_issued[st];
-      if (i < 0) continue;
-      const uint32_t full = smem_addr(&S.full[st]);
-      const unsigned long long t0 = global_ns();
-      while (!mbar_try_wait(full, (i / NST) & 1)) {
-        if (global_ns() - t0 > kWaitLimitNs) {
-          flag_error(p.err, DEVERR_TIMEOUT);
-          break;
-        }
-      }
-    }
-  }
-}
-
-// Combine the pieces of every decode request that spans several CTAs.  One
-// warp per (request, q head); lanes own 4 consecutive elements of head_dim.
-// Launched as a programmatic dependent of the decode kernel: it may start
-// while the decode grid drains and waits for it before reading partials.
-constexpr int kMergeWarps = 8;
-
-template <int D>
-__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const DecodeParams p) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int s = blockIdx.x;
-  const int h = blockIdx.y * kMergeWarps + warp;
-  if (h >= p.n_q) return;
-  if (decode_pages(p, s, false) == 0) return;  // not a (valid) decode request
-  const int4 rec = p.seq_rec[s];
-  const int C = p.ctas;
-  const int c_first = rec.x, c_last = rec.y, first_slot = rec.z;
-  const int64_t F = rec.w;
-  if (c_first == c_last) return;  // written directly by the decode kernel
-  if (c_first < 0 || c_last >= C || c_first > c_last || first_slot < 0 || first_slot >= 2 * C ||
-      F <= 0) {
-    if (lane == 0) flag_error(p.err, DEVERR_BOUNDS);
-    return;
-  }
-  // online merge over the pieces, eight at a time so that their loads are in
-  // flight together (a long request can span tens of CTAs)
-  const bool active = lane * 4 < D;
-  float M = kNegInf, Lsum = 0.f;
-  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int cc0 = c_first; cc0 <= c_last; cc0 += 8) {
-    float2 ml[8];
-    float4 o[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int cc = cc0 + k;
-      const bool v = cc <= c_last && slice_begin(cc, F, C) != slice_begin(cc + 1, F, C);
-      const int slot = (cc == c_first) ? first_slot : 2 * cc;
-      ml[k] = make_float2(kNegInf, 0.f);
-      o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (v) {
-        ml[k] = __ldg(reinterpret_cast<const float2*>(p.part_ml) + (int64_t)slot * p.n_q + h);
-        if (active)
-          o[k] = __ldg(reinterpret_cast<const float4*>(
-              p.part_o + ((int64_t)slot * p.n_q + h) * D + lane * 4));
-      }
-    }
-    float bm = M;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) bm = fmaxf(bm, ml[k].x);
-    const float mu = (bm == kNegInf) ? 0.f : bm;
-    const float f = fast_exp2(M - mu);
-    Lsum *= f;
-    O.x *= f, O.y *= f, O.z *= f, O.w *= f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const float w = fast_exp2(ml[k].x - mu);
-      Lsum += ml[k].y * w;
-      O.x += o[k].x * w, O.y += o[k].y * w, O.z += o[k].z * w, O.w += o[k].w * w;
-    }
-    M = bm;
-  }
-  if (active) {
-    const float inv = 1.f / Lsum;
-    uint2 w;
-    w.x = pack_bf16x2(O.x * inv, O.y * inv);
-    w.y = pack_bf16x2(O.z * inv, O.w * inv);
-    const int a = __ldg(p.qsl + s);
-    *reinterpret_cast<uint2*>(p.out + ((int64_t)a * p.n_q + h) * D + lane * 4) = w;
-  }
-}
-
-constexpr size_t kSmemBudget = 220 * 1024;
-
-template <int D, int G, int NKV>
-cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ctas,
-                            cudaStream_t stream) {
-  DecodeParams p;
-  p.q = a.q;
-  p.k_cache = a.k_cache;
-  p.v_cache = a.v_cache;
-  p.block_tables = a.block_tables;
-  p.seq_lens = a.seq_lens;
-  p.qsl = a.query_start_loc;
-  p.out = a.out;
-  p.part_o = ws.part_o;
-  p.part_ml = ws.part_ml;
-  p.seq_rec = ws.seq_rec;
-  p.err = a.err;
-  p.num_blocks = a.num_blocks;
-  p.max_blocks = a.max_blocks;
-  p.num_seqs = a.num_seqs;
-  p.num_tokens = a.num_tokens;
-  p.n_q = a.num_q_heads;
-  p.n_kv = a.num_kv_heads;
-  p.max_seq_len = a.max_seq_len;
-  p.block_shift = a.block_shift;
-  p.scale_log2 = a.scale * 1.4426950408889634f;
-  p.ctas = ctas;
-  p.row_bytes = (uint32_t)NKV * D * 2;
-  p.page_bytes = kBlock * p.row_bytes;
-  p.stage_bytes = 2 * p.page_bytes;
-  const size_t fixed = sizeof(DecodeSmem<G, NKV>);
-  int nst = (int)((kSmemBudget - fixed) / p.stage_bytes);
-  nst = nst > 8 ? 8 : nst;
-  if (nst < 2) return cudaErrorInvalidConfiguration;
-  p.nstages = nst;
-  const size_t smem = (size_t)nst * p.stage_bytes + fixed;
-  auto kern = decode_kernel<D, G, NKV>;
-  static int configured_device = -1;  // one attribute set per process and device
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(kSmemBudget + 4096));
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
-  cudaError_t e;
-  if (a.after_prefill) {
-    // overlaps the prefill grid (no data dependence: different output rows,
-    // and the cache writes of the step finished before the prefill started)
-    cudaLaunchConfig_t pcfg = {};
-    pcfg.gridDim = dim3(ctas);
-    pcfg.blockDim = dim3(2 * NKV * 32);
-    pcfg.dynamicSmemBytes = smem;
-    pcfg.stream = stream;
-    cudaLaunchAttribute pattr[1];
-    pattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    pattr[0].val.programmaticStreamSerializationAllowed = 1;
-    pcfg.attrs = pattr;
-    pcfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&pcfg, kern, p);
-  } else {
-    kern<<<ctas, 2 * NKV * 32, smem, stream>>>(p);
-    e = cudaGetLastError();
-  }
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.num_seqs, (a.num_q_heads + kMergeWarps - 1) / kMergeWarps, 1);
-  cfg.blockDim = dim3(kMergeWarps * 32, 1, 1);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, p);
-}
-
-}  // namespace
 
 int decode_ctas(int sm_count) { return sm_count; }
 
@@ -769,33 +33,10 @@ bool decode_supported(int head_dim, int group, int num_kv_heads) {
   return num_kv_heads == 1 || num_kv_heads == 2 || num_kv_heads == 4 || num_kv_heads == 8;
 }
 
-template <int D, int G>
-static cudaError_t launch_decode_dg(const AttnArgs& a, const DecodeWorkspace& ws, int ctas,
-                                    cudaStream_t stream) {
-  switch (a.num_kv_heads) {
-    case 1: return launch_decode_t<D, G, 1>(a, ws, ctas, stream);
-    case 2: return launch_decode_t<D, G, 2>(a, ws, ctas, stream);
-    case 4: return launch_decode_t<D, G, 4>(a, ws, ctas, stream);
-    case 8: return launch_decode_t<D, G, 8>(a, ws, ctas, stream);
-  }
-  return cudaErrorInvalidValue;
-}
-
 cudaError_t launch_decode(const AttnArgs& a, const DecodeWorkspace& ws, int ctas,
                           cudaStream_t stream) {
-  const int group = a.num_q_heads / a.num_kv_heads;
-  if (a.head_dim == 128) {
-    if (group == 1) return launch_decode_dg<128, 1>(a, ws, ctas, stream);
-    if (group == 2) return launch_decode_dg<128, 2>(a, ws, ctas, stream);
-    if (group == 4) return launch_decode_dg<128, 4>(a, ws, ctas, stream);
-    if (group == 8) return launch_decode_dg<128, 8>(a, ws, ctas, stream);
-  } else if (a.head_dim == 64) {
-    if (group == 1) return launch_decode_dg<64, 1>(a, ws, ctas, stream);
-    if (group == 2) return launch_decode_dg<64, 2>(a, ws, ctas, stream);
-    if (group == 4) return launch_decode_dg<64, 4>(a, ws, ctas, stream);
-    if (group == 8) return launch_decode_dg<64, 8>(a, ws, ctas, stream);
-  }
-  return cudaErrorInvalidValue;
+  if (a.fp8) return launch_decode_fp8(a, ws, ctas, stream);
+  return launch_decode_any<false>(a, ws, ctas, stream);
 }
 
 }  // namespace pa

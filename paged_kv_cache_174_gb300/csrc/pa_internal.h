@@ -17,8 +17,11 @@ enum : unsigned {
 // Geometry and pointers of one paged-attention call, already validated.
 struct AttnArgs {
   const uint16_t* q;
-  const uint16_t* k_cache;
-  const uint16_t* v_cache;
+  const void* k_cache;     // bf16 values, or E4M3 codes when fp8
+  const void* v_cache;
+  const float* k_scale;    // fp8: one scale per (slot, kv head); else null
+  const float* v_scale;
+  bool fp8;
   int32_t num_blocks;
   int32_t num_q_heads;
   int32_t num_kv_heads;
@@ -61,6 +64,8 @@ int decode_ctas(int sm_count);
 bool decode_supported(int head_dim, int group, int num_kv_heads);
 cudaError_t launch_decode(const AttnArgs& a, const DecodeWorkspace& ws, int ctas,
                           cudaStream_t stream);
+cudaError_t launch_decode_fp8(const AttnArgs& a, const DecodeWorkspace& ws, int ctas,
+                              cudaStream_t stream);
 
 bool prefill_supported(int head_dim, int group, int num_kv_heads);
 // How the prefill kernel splits the keys of each query-tile pair, and the
@@ -83,6 +88,12 @@ cudaError_t launch_reshape_and_cache(const uint16_t* k, const uint16_t* v, int32
                                      int32_t row_elems, const int32_t* slot_mapping,
                                      unsigned* err, cudaStream_t stream);
 
+cudaError_t launch_reshape_and_cache_fp8(const uint16_t* k, const uint16_t* v,
+                                         int32_t num_tokens, uint8_t* k_cache, uint8_t* v_cache,
+                                         float* k_scale, float* v_scale, int64_t num_slots,
+                                         int32_t num_kv_heads, int32_t head_dim,
+                                         const int32_t* slot_mapping, unsigned* err,
+                                         cudaStream_t stream);
 cudaError_t launch_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, int32_t num_blocks,
                                int64_t block_elems, const int32_t* pairs, int32_t num_pairs,
                                unsigned* err, cudaStream_t stream);

@@ -82,6 +82,14 @@ def _load() -> ctypes.CDLL:
     L.pa_copy_blocks.restype = ctypes.c_int
     L.pa_check_device_errors.argtypes = [vp]
     L.pa_check_device_errors.restype = ctypes.c_int
+    L.pa_reshape_and_cache_fp8.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp,
+                                           vp]
+    L.pa_reshape_and_cache_fp8.restype = ctypes.c_int
+    L.pa_paged_attention_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, i32,
+                                         vp, vp, i32, i32, i32, i32, f32, vp, vp, sz, vp]
+    L.pa_paged_attention_fp8.restype = ctypes.c_int
+    L.pa_copy_blocks_fp8.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, i32, vp]
+    L.pa_copy_blocks_fp8.restype = ctypes.c_int
     L.pa_step_graph_create.argtypes = [ctypes.POINTER(StepBuffers), ctypes.POINTER(vp)]
     L.pa_step_graph_create.restype = ctypes.c_int
     L.pa_step_graph_launch.argtypes = [vp, vp]
@@ -273,6 +281,88 @@ def swap_in(k_cache: torch.Tensor, v_cache: torch.Tensor, block_ids: torch.Tenso
             stream=None) -> torch.Tensor:
     """host_k / host_v -> blocks block_ids (distinct) of both caches."""
     return _swap(False, k_cache, v_cache, block_ids, host_k, host_v, staging, stream)
+
+
+# ---------------------------------------------------------------------------
+# 8-bit (FP8 E4M3) cache: uint8 codes [num_blocks, block_size, n_kv, d] and
+# fp32 scales [num_blocks, block_size, n_kv], one per cached row.
+# ---------------------------------------------------------------------------
+
+def empty_fp8_cache(num_blocks: int, block_size: int, num_kv_heads: int, head_dim: int,
+                    device=None):
+    """(k codes, v codes, k scales, v scales), zero-filled, on the device."""
+    dev = device or "cuda"
+    codes = (num_blocks, block_size, num_kv_heads, head_dim)
+    return (torch.zeros(codes, dtype=torch.uint8, device=dev),
+            torch.zeros(codes, dtype=torch.uint8, device=dev),
+            torch.zeros(codes[:3], dtype=torch.float32, device=dev),
+            torch.zeros(codes[:3], dtype=torch.float32, device=dev))
+
+
+def _need_fp8(k_cache, v_cache, k_scale, v_scale):
+    _need(k_cache, "k_cache", torch.uint8, 4)
+    _need(v_cache, "v_cache", torch.uint8, 4)
+    _need(k_scale, "k_scale", torch.float32, 3)
+    _need(v_scale, "v_scale", torch.float32, 3)
+    if v_cache.shape != k_cache.shape or k_scale.shape != k_cache.shape[:3] or \
+            v_scale.shape != k_scale.shape:
+        raise ValueError("codes must be [nb, bs, n_kv, d] and scales [nb, bs, n_kv], alike")
+
+
+def reshape_and_cache_fp8(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
+                          v_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+                          slot_mapping: torch.Tensor, stream=None) -> None:
+    """Quantise each new (token, kv head) row of k / v into its slot."""
+    L = _load()
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need_fp8(k_cache, v_cache, k_scale, v_scale)
+    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    nb, bs, nkv, d = k_cache.shape
+    _check(L.pa_reshape_and_cache_fp8(k.data_ptr(), v.data_ptr(), k.shape[0], k_cache.data_ptr(),
+                                      v_cache.data_ptr(), k_scale.data_ptr(), v_scale.data_ptr(),
+                                      nb, bs, nkv, d, slot_mapping.data_ptr(), _stream(stream)))
+
+
+def paged_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                        k_scale: torch.Tensor, v_scale: torch.Tensor, block_tables: torch.Tensor,
+                        seq_lens: torch.Tensor, query_start_loc: torch.Tensor, scale: float, *,
+                        max_q_len: int, max_seq_len: int, out: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """paged_attention over the 8-bit cache (decode rows only)."""
+    L = _load()
+    _need(q, "q", torch.bfloat16, 3)
+    _need_fp8(k_cache, v_cache, k_scale, v_scale)
+    for name, t in (("block_tables", block_tables), ("seq_lens", seq_lens),
+                    ("query_start_loc", query_start_loc)):
+        _need(t, name, torch.int32)
+    T, nq, d = q.shape
+    nb, bs, nkv, _ = k_cache.shape
+    S = seq_lens.shape[0]
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = alloc_workspace(S, T, nq, nkv, d, max_q_len, max_seq_len, q.device)
+    _check(L.pa_paged_attention_fp8(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                    k_scale.data_ptr(), v_scale.data_ptr(), nb, bs, nq, nkv, d,
+                                    block_tables.data_ptr(), block_tables.shape[1],
+                                    seq_lens.data_ptr(), query_start_loc.data_ptr(), S, T,
+                                    int(max_q_len), int(max_seq_len), float(scale),
+                                    out.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                    _stream(stream)))
+    return out
+
+
+def copy_blocks_fp8(k_cache, v_cache, k_scale, v_scale, src_dst_pairs: torch.Tensor,
+                    stream=None) -> None:
+    """Copy-on-write on the 8-bit cache: codes and scales of block dst <- src."""
+    L = _load()
+    _need_fp8(k_cache, v_cache, k_scale, v_scale)
+    _need(src_dst_pairs, "src_dst_pairs", torch.int32, 2)
+    nb, bs, nkv, d = k_cache.shape
+    _check(L.pa_copy_blocks_fp8(k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(),
+                                v_scale.data_ptr(), nb, bs, nkv, d, src_dst_pairs.data_ptr(),
+                                src_dst_pairs.shape[0], _stream(stream)))
 
 
 def check_device_errors(stream=None) -> None:

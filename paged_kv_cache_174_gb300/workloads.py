@@ -293,6 +293,35 @@ def algorithmic_bytes(b: PagedBatch) -> Dict[str, int]:
             "total": attn_kv + q_out + tables + meta + scatter + 4 * b.num_tokens}
 
 
+def algorithmic_bytes_fp8(b: PagedBatch) -> Dict[str, int]:
+    """algorithmic_bytes for the 8-bit cache: a cached row is head_dim one-byte
+    codes plus one 4-byte scale per kv head; the scatter reads bf16 rows and
+    writes codes and scales."""
+    kv_row = b.num_kv_heads * (b.head_dim + 4)
+    ql = b.q_lens
+    attn_kv = int(b.seq_lens.astype(np.int64).sum()) * 2 * kv_row
+    q_out = 2 * int(ql.sum()) * b.num_q_heads * b.head_dim * 2
+    tables = int(sum(_blocks_needed(int(L), b.block_size) for L in b.seq_lens)) * 4
+    meta = 4 * (2 * b.num_seqs + 1)
+    n_new = int((b.slot_mapping >= 0).sum())
+    scatter = n_new * 2 * (b.num_kv_heads * b.head_dim * 2 + kv_row)
+    return {"attention": attn_kv + q_out + tables + meta, "attention_kv": attn_kv,
+            "scatter": scatter + 4 * b.num_tokens,
+            "total": attn_kv + q_out + tables + meta + scatter + 4 * b.num_tokens}
+
+
+def context_slots(b: PagedBatch) -> np.ndarray:
+    """Slots of every cached position before this step's tokens, request by
+    request (the rows an 8-bit copy of the batch's cache must hold)."""
+    out = []
+    for s in range(b.num_seqs):
+        ctx = int(b.seq_lens[s]) - int(b.q_lens[s])
+        pos = np.arange(ctx, dtype=np.int64)
+        out.append(b.block_tables[s, pos // b.block_size].astype(np.int64) * b.block_size
+                   + pos % b.block_size)
+    return np.concatenate(out).astype(np.int32) if out else np.zeros(0, np.int32)
+
+
 def causal_flops(b: PagedBatch, min_q_len: int = 2) -> int:
     """QK^T and PV multiply-adds (2 flops each) over the causal (query, key)
     pairs of the requests with q_len >= min_q_len."""

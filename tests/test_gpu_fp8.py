@@ -1,0 +1,144 @@
+"""The 8-bit (FP8 E4M3) KV cache on the GPU against the oracle: the
+quantising scatter bit for bit (codes and scales), decode attention over the
+8-bit cache against the oracle's attention over code * scale, the block copy
+of codes and scales, and the calls it rejects."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_174_gb300 import ops
+from paged_kv_cache_174_gb300 import workloads as W
+
+from gpu_util import assert_attn_close, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _context_slots(b):
+    """Slots of every cached (context) position of every request, and the
+    bf16 rows that live there."""
+    slots = []
+    for s in range(b.num_seqs):
+        ctx = int(b.seq_lens[s]) - int(b.query_start_loc[s + 1] - b.query_start_loc[s])
+        for p in range(ctx):
+            slots.append(oracle.slot_of(b.block_tables[s], p, b.block_size))
+    slots = np.array(slots, np.int32)
+    nkv, d = b.k_cache.shape[2:]
+    rows_k = b.k_cache.reshape(-1, nkv, d)[slots]
+    rows_v = b.v_cache.reshape(-1, nkv, d)[slots]
+    return slots, rows_k, rows_v
+
+
+def fp8_step(b):
+    """Quantise the batch's context and its new tokens into an 8-bit cache on
+    both sides (GPU scatter and oracle scatter, compared bit for bit), then
+    run decode attention on both.  Returns (gpu out, oracle out)."""
+    nb, bs, nkv, d = b.k_cache.shape
+    slots, rk, rv = _context_slots(b)
+    dk8, dv8, dks, dvs = ops.empty_fp8_cache(nb, bs, nkv, d)
+    ok8, ov8, oks, ovs = oracle.fp8_cache(nb, bs, nkv, d, fill_code=0)
+    oks[:] = 0
+    ovs[:] = 0
+    for ks_, vs_, sl in ((rk, rv, slots), (b.k_new, b.v_new, b.slot_mapping)):
+        if len(sl) == 0:
+            continue
+        ops.reshape_and_cache_fp8(W.bf16_tensor(ks_, "cuda"), W.bf16_tensor(vs_, "cuda"), dk8,
+                                  dv8, dks, dvs, W.int32_tensor(sl, "cuda"))
+        oracle.reshape_and_cache_fp8(ks_, vs_, ok8, ov8, oks, ovs, sl)
+    ops.check_device_errors()
+    assert np.array_equal(dk8.cpu().numpy(), ok8) and np.array_equal(dv8.cpu().numpy(), ov8), \
+        "codes differ from the oracle"
+    assert np.array_equal(dks.cpu().numpy().view(np.uint32), oks.view(np.uint32)) and \
+        np.array_equal(dvs.cpu().numpy().view(np.uint32), ovs.view(np.uint32)), \
+        "scales differ from the oracle"
+    out = torch.full((b.num_tokens, b.num_q_heads, d), float("nan"), dtype=torch.bfloat16,
+                     device="cuda")
+    ops.paged_attention_fp8(W.bf16_tensor(b.q, "cuda"), dk8, dv8, dks, dvs,
+                            W.int32_tensor(b.block_tables, "cuda"),
+                            W.int32_tensor(b.seq_lens, "cuda"),
+                            W.int32_tensor(b.query_start_loc, "cuda"), b.scale, max_q_len=1,
+                            max_seq_len=b.max_seq_len, out=out)
+    ops.check_device_errors()
+    ref = oracle.paged_attention_fp8(b.q, ok8, ov8, oks, ovs, b.block_tables, b.seq_lens,
+                                     b.query_start_loc, b.scale)
+    return to_f64(out), ref
+
+
+def _decode(lens, nq=32, nkv=8, d=128, seed=0, bs=16):
+    nb = sum(-(-L // bs) for L in lens) + 5
+    return W.make_batch("fp8", lens, [1] * len(lens), num_q_heads=nq, num_kv_heads=nkv,
+                        head_dim=d, block_size=bs, num_blocks=nb, seed=seed)
+
+
+@pytest.mark.parametrize("lens,nq,nkv,d,bs", [
+    ([1, 2, 15, 16, 17, 31, 33], 32, 8, 128, 16),  # ragged page tails
+    ([5000, 3, 900], 16, 8, 128, 16),              # group 2, split across CTAs
+    ([4096, 4095, 1], 64, 8, 128, 16),             # group 8
+    ([257, 1000], 8, 2, 64, 16),                   # 2 kv heads, d 64
+    ([130, 7, 64], 4, 1, 128, 16),                 # multi-query
+    ([300, 47], 32, 8, 128, 32),                   # 32-token blocks
+    ([20] * 300, 32, 8, 128, 16),                  # many short requests
+])
+def test_fp8_decode_edge_shapes(lens, nq, nkv, d, bs):
+    got, ref = fp8_step(_decode(lens, nq, nkv, d, seed=len(lens), bs=bs))
+    assert_attn_close(got, ref, f"fp8 lens={lens[:4]} nq={nq} nkv={nkv} d={d} bs={bs}")
+
+
+def test_fp8_decode_batch_workload():
+    """The 64-request decode batch (lens U[128, 4096], 32/8 heads, d 128)."""
+    got, ref = fp8_step(W.decode_batch())
+    assert_attn_close(got, ref, "fp8 decode batch")
+
+
+def test_fp8_quantises_zero_and_large_rows():
+    """All-zero rows (scale 1, zero codes) and rows of large bf16 magnitudes
+    quantise bit for bit like the oracle."""
+    rng = np.random.default_rng(4)
+    k = W.randn_bf16(rng, (24, 8, 128))
+    v = W.randn_bf16(rng, (24, 8, 128))
+    k[3] = 0
+    v[5, 2] = 0
+    big = (W.f32_from_bf16(k[7]) * np.float32(3e37)).astype(np.float32)
+    k[7] = W.bf16_from_f32(big)
+    slots = rng.permutation(64)[:24].astype(np.int32)
+    dk8, dv8, dks, dvs = ops.empty_fp8_cache(4, 16, 8, 128)
+    ok8, ov8, oks, ovs = oracle.fp8_cache(4, 16, 8, 128, fill_code=0)
+    oks[:] = 0
+    ovs[:] = 0
+    ops.reshape_and_cache_fp8(W.bf16_tensor(k, "cuda"), W.bf16_tensor(v, "cuda"), dk8, dv8, dks,
+                              dvs, W.int32_tensor(slots, "cuda"))
+    ops.check_device_errors()
+    oracle.reshape_and_cache_fp8(k, v, ok8, ov8, oks, ovs, slots)
+    assert np.array_equal(dk8.cpu().numpy(), ok8) and np.array_equal(dv8.cpu().numpy(), ov8)
+    assert np.array_equal(dks.cpu().numpy().view(np.uint32), oks.view(np.uint32))
+    assert np.array_equal(dvs.cpu().numpy().view(np.uint32), ovs.view(np.uint32))
+
+
+def test_fp8_copy_blocks_moves_codes_and_scales():
+    rng = np.random.default_rng(8)
+    dk8 = torch.from_numpy(rng.integers(0, 256, (10, 16, 8, 128), dtype=np.uint8)).cuda()
+    dv8 = torch.from_numpy(rng.integers(0, 256, (10, 16, 8, 128), dtype=np.uint8)).cuda()
+    dks = torch.from_numpy(rng.standard_normal((10, 16, 8)).astype(np.float32)).cuda()
+    dvs = torch.from_numpy(rng.standard_normal((10, 16, 8)).astype(np.float32)).cuda()
+    before = [t.cpu().numpy().copy() for t in (dk8, dv8, dks, dvs)]
+    pairs = np.array([[1, 4], [-1, -1], [6, 2]], np.int32)
+    ops.copy_blocks_fp8(dk8, dv8, dks, dvs, W.int32_tensor(pairs, "cuda"))
+    ops.check_device_errors()
+    for dev_t, host in zip((dk8, dv8, dks, dvs), before):
+        host[4] = host[1]
+        host[2] = host[6]
+        assert np.array_equal(dev_t.cpu().numpy(), host)
+
+
+def test_fp8_rejects_prefill_rows():
+    b = W.make_batch("fp8", [40], [4], num_q_heads=8, num_kv_heads=2, head_dim=64,
+                     block_size=16, num_blocks=4, seed=1)
+    dk8, dv8, dks, dvs = ops.empty_fp8_cache(4, 16, 2, 64)
+    with pytest.raises(ops.PagedAttnError) as ei:
+        ops.paged_attention_fp8(W.bf16_tensor(b.q, "cuda"), dk8, dv8, dks, dvs,
+                                W.int32_tensor(b.block_tables, "cuda"),
+                                W.int32_tensor(b.seq_lens, "cuda"),
+                                W.int32_tensor(b.query_start_loc, "cuda"), b.scale, max_q_len=4,
+                                max_seq_len=40)
+    assert ei.value.code == 2
