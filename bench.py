@@ -248,9 +248,11 @@ def _time_prefill(b, d, steps, warmup, stream, ops):
                              sub.head_dim, sub.max_q_len, sub.max_seq_len, d.q.device)
 
     def call():
+        # prefill rows only: min_q_len >= 2 lets the call skip the decode launch
         ops.paged_attention(t["q"], d.k_cache, d.v_cache, t["block_tables"], t["seq_lens"],
                             t["query_start_loc"], sub.scale, max_q_len=sub.max_q_len,
-                            max_seq_len=sub.max_seq_len, out=out, workspace=ws)
+                            max_seq_len=sub.max_seq_len, out=out, workspace=ws,
+                            min_q_len=int(sub.q_lens.min()))
 
     for _ in range(warmup):
         call()

@@ -150,6 +150,24 @@ int pa_paged_attention(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *
                        void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * pa_paged_attention with a host-side lower bound on the requests' query
+ * rows as well: min_q_len <= q_len for every request with at least one row
+ * (0 or 1: no bound).  With min_q_len >= 2 the call has no decode rows, so
+ * only the prefill kernel runs (no empty decode launch after it); a request
+ * with exactly one row then flags PA_ERR_DEVICE_BOUNDS and its row is not
+ * written.  min_q_len > max_q_len is PA_ERR_INVALID_ARG.  Everything else is
+ * pa_paged_attention.
+ */
+int pa_paged_attention_qrange(const pa_bf16 *q, const pa_bf16 *k_cache, const pa_bf16 *v_cache,
+                              int32_t num_blocks, int32_t block_size, int32_t num_q_heads,
+                              int32_t num_kv_heads, int32_t head_dim, const int32_t *block_tables,
+                              int32_t max_blocks, const int32_t *seq_lens,
+                              const int32_t *query_start_loc, int32_t num_seqs,
+                              int32_t num_tokens, int32_t min_q_len, int32_t max_q_len,
+                              int32_t max_seq_len, float scale, pa_bf16 *out, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Copy-on-write block copy: for each pair i, physical block
  * src_dst_pairs[2i+1] of both caches becomes a bit copy of block
  * src_dst_pairs[2i] ("PagedAttention 显存分页与连续批处理实战", comparison
@@ -260,6 +278,18 @@ int pa_copy_blocks_fp8(uint8_t *k_cache, uint8_t *v_cache, float *k_scale, float
  * PA_ERR_DEVICE_BOUNDS, PA_ERR_TIMEOUT or PA_ERR_CUDA.
  */
 int pa_check_device_errors(cudaStream_t stream);
+
+/*
+ * Failure-detection self-test.  Every wait inside the library's kernels (on
+ * a copy landing, on a tensor-core product, on another warp's hand-off) is
+ * bounded: past its limit (2 s) the kernel sets PA_ERR_TIMEOUT's bit in the
+ * device error word, stops waiting and returns, so the context stays usable.
+ * This call runs that same wait, with limit_ns (at most 1 s), on a barrier
+ * that nothing completes; pa_check_device_errors afterwards returns
+ * PA_ERR_TIMEOUT.  It faults nothing and hangs nothing.  limit_ns of 0 or
+ * above 1 s is PA_ERR_INVALID_ARG.
+ */
+int pa_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
 
 /*
  * Allocation-free form of pa_paged_attention.  The pages have no counterpart

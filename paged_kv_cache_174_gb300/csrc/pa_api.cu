@@ -304,8 +304,8 @@ int paged_attention_impl(const pa_bf16* q, KvCache kv,
                          int32_t num_kv_heads, int32_t head_dim, const int32_t* block_tables,
                          int32_t max_blocks, const int32_t* seq_lens,
                          const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens,
-                         int32_t max_q_len, int32_t max_seq_len, float scale, pa_bf16* out,
-                         void* workspace, size_t workspace_bytes, size_t split_cap,
+                         int32_t min_q_len, int32_t max_q_len, int32_t max_seq_len, float scale,
+                         pa_bf16* out, void* workspace, size_t workspace_bytes, size_t split_cap,
                          cudaStream_t stream);
 
 }  // namespace
@@ -321,9 +321,24 @@ int pa_paged_attention(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* 
                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   return paged_attention_impl(q, KvCache{k_cache, v_cache, nullptr, nullptr, false}, num_blocks,
                               block_size, num_q_heads, num_kv_heads, head_dim, block_tables,
-                              max_blocks, seq_lens, query_start_loc, num_seqs, num_tokens,
+                              max_blocks, seq_lens, query_start_loc, num_seqs, num_tokens, 0,
                               max_q_len, max_seq_len, scale, out, workspace, workspace_bytes,
                               ~size_t(0), stream);
+}
+
+int pa_paged_attention_qrange(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
+                              int32_t num_blocks, int32_t block_size, int32_t num_q_heads,
+                              int32_t num_kv_heads, int32_t head_dim, const int32_t* block_tables,
+                              int32_t max_blocks, const int32_t* seq_lens,
+                              const int32_t* query_start_loc, int32_t num_seqs,
+                              int32_t num_tokens, int32_t min_q_len, int32_t max_q_len,
+                              int32_t max_seq_len, float scale, pa_bf16* out, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+  return paged_attention_impl(q, KvCache{k_cache, v_cache, nullptr, nullptr, false}, num_blocks,
+                              block_size, num_q_heads, num_kv_heads, head_dim, block_tables,
+                              max_blocks, seq_lens, query_start_loc, num_seqs, num_tokens,
+                              min_q_len, max_q_len, max_seq_len, scale, out, workspace,
+                              workspace_bytes, ~size_t(0), stream);
 }
 
 int pa_paged_attention_fp8(const pa_bf16* q, const uint8_t* k_cache, const uint8_t* v_cache,
@@ -336,7 +351,7 @@ int pa_paged_attention_fp8(const pa_bf16* q, const uint8_t* k_cache, const uint8
                            size_t workspace_bytes, cudaStream_t stream) {
   return paged_attention_impl(q, KvCache{k_cache, v_cache, k_scale, v_scale, true}, num_blocks,
                               block_size, num_q_heads, num_kv_heads, head_dim, block_tables,
-                              max_blocks, seq_lens, query_start_loc, num_seqs, num_tokens,
+                              max_blocks, seq_lens, query_start_loc, num_seqs, num_tokens, 0,
                               max_q_len, max_seq_len, scale, out, workspace, workspace_bytes,
                               ~size_t(0), stream);
 }
@@ -350,8 +365,8 @@ int paged_attention_impl(const pa_bf16* q, KvCache kv,
                          int32_t num_kv_heads, int32_t head_dim, const int32_t* block_tables,
                          int32_t max_blocks, const int32_t* seq_lens,
                          const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens,
-                         int32_t max_q_len, int32_t max_seq_len, float scale, pa_bf16* out,
-                         void* workspace, size_t workspace_bytes, size_t split_cap,
+                         int32_t min_q_len, int32_t max_q_len, int32_t max_seq_len, float scale,
+                         pa_bf16* out, void* workspace, size_t workspace_bytes, size_t split_cap,
                          cudaStream_t stream) {
   int st = check_cache_geometry(num_blocks, block_size, num_kv_heads, head_dim);
   if (st) return st;
@@ -362,6 +377,8 @@ int paged_attention_impl(const pa_bf16* q, KvCache kv,
     return fail(PA_ERR_INVALID_ARG, "negative size argument");
   if (max_q_len > max_seq_len)
     return fail(PA_ERR_INVALID_ARG, "max_q_len %d > max_seq_len %d", max_q_len, max_seq_len);
+  if (min_q_len > max_q_len)
+    return fail(PA_ERR_INVALID_ARG, "min_q_len %d > max_q_len %d", min_q_len, max_q_len);
   if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "scale is NaN");
   if (block_size != 16 && block_size != 32)
     return fail(PA_ERR_UNSUPPORTED, "block_size %d (16 and 32 are implemented)", block_size);
@@ -430,6 +447,7 @@ int paged_attention_impl(const pa_bf16* q, KvCache kv,
   a.out = out;
   a.err = err;
   a.after_prefill = false;
+  a.no_decode = min_q_len >= 2;
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   if (max_q_len >= 2) {
@@ -438,6 +456,7 @@ int paged_attention_impl(const pa_bf16* q, KvCache kv,
     // with key pieces the merge kernel comes last and must not be overtaken
     a.after_prefill = plan.nsplit == 1;
   }
+  if (a.no_decode) return PA_OK;  // no request has a single query row
   pa::DecodeWorkspace dws = pa::decode_workspace(ws, ctas, num_seqs, num_q_heads, head_dim);
   cudaError_t e = pa::launch_decode(a, dws, ctas, stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
@@ -447,6 +466,18 @@ int paged_attention_impl(const pa_bf16* q, KvCache kv,
 }  // namespace
 
 extern "C" {
+
+int pa_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream) {
+  if (limit_ns == 0 || limit_ns > 1000000000ull)
+    return fail(PA_ERR_INVALID_ARG, "limit_ns %llu outside (0, 1 s]",
+                (unsigned long long)limit_ns);
+  unsigned* err = nullptr;
+  int st = device_state(&err, nullptr);
+  if (st) return st;
+  cudaError_t e = pa::launch_wait_timeout_selftest(limit_ns, err, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "wait timeout self-test launch");
+  return PA_OK;
+}
 
 int pa_check_device_errors(cudaStream_t stream) {
   unsigned* err = nullptr;
@@ -541,7 +572,7 @@ int pa_paged_attention_noalloc(const pa_bf16* q, const pa_bf16* k_cache,
   if (st) return st;
   return paged_attention_impl(q, KvCache{k_cache, v_cache, nullptr, nullptr, false}, num_blocks,
                               block_size, num_q_heads, num_kv_heads, head_dim, block_tables,
-                              max_blocks, seq_lens, query_start_loc, num_seqs, num_tokens,
+                              max_blocks, seq_lens, query_start_loc, num_seqs, num_tokens, 0,
                               max_q_len, max_seq_len, scale, out, scratch, kNoAllocScratchBytes,
                               kNoAllocScratchBytes - need, stream);
 }

@@ -111,6 +111,22 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
   }
 }
 
+// Failure-detection self-test: the bounded wait every kernel uses, on a
+// barrier that nothing ever completes, with a short limit.  The wait gives
+// up, sets the timeout bit of the error word and the kernel returns, so the
+// context stays usable.
+__global__ void wait_timeout_selftest_kernel(unsigned long long limit_ns, unsigned* err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait(smem_addr(&bar), 0, err, &abort_flag, limit_ns);  // nothing arrives
+}
+
 constexpr int kCopyThreads = 256;
 
 // One CTA per (src, dst) pair: copy the K block and the V block.
@@ -227,6 +243,12 @@ cudaError_t launch_reshape_and_cache_fp8(const uint16_t* k, const uint16_t* v,
   if (head_dim == 128) return args(reshape_and_cache_fp8_kernel<16>);
   if (head_dim == 64) return args(reshape_and_cache_fp8_kernel<8>);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_wait_timeout_selftest(unsigned long long limit_ns, unsigned* err,
+                                         cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 64, 0, stream>>>(limit_ns, err);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, int32_t num_blocks,

@@ -141,17 +141,19 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Gives up after
-// kWaitLimitNs, or at once when *abort becomes non-zero; on giving up it sets
-// the error word (once) and *abort, and returns false.
+// limit_ns (kWaitLimitNs unless a test asks for less), or at once when *abort
+// becomes non-zero; on giving up it sets the error word (once) and *abort,
+// and returns false.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err,
-                                          volatile int* abort) {
+                                          volatile int* abort,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if (global_ns() - t0 > limit_ns) {
         *abort = 1;
         flag_error(err, DEVERR_TIMEOUT);
         return false;

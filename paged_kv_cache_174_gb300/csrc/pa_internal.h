@@ -45,6 +45,10 @@ struct AttnArgs {
   // (which triggers its dependents at once and writes only prefill rows):
   // the decode kernel may then start on SMs it leaves free.
   bool after_prefill;
+  // The caller promised that no request has exactly one query row: the
+  // decode kernel is not launched, and the prefill kernel flags a request
+  // with one row as a bounds error instead of leaving its row unwritten.
+  bool no_decode;
 };
 
 // Workspace carve-up shared by the launchers (sizes in bytes, 256-aligned).
@@ -105,6 +109,9 @@ cudaError_t launch_swap(uint16_t* k_cache, uint16_t* v_cache, int32_t num_blocks
                         int64_t block_elems, const int32_t* ids, int32_t n, uint16_t* staging,
                         uint16_t* host_k, uint16_t* host_v, bool out, unsigned* err,
                         cudaStream_t stream);
+
+cudaError_t launch_wait_timeout_selftest(unsigned long long limit_ns, unsigned* err,
+                                         cudaStream_t stream);
 
 // Error reporting of the C ABI (sets the message pa_get_last_error returns)
 // and the per-device state lookup, for the parts of the ABI outside pa_api.cu.

@@ -74,6 +74,7 @@ struct PrefillParams {
   unsigned* err;
   int32_t num_blocks, max_blocks, num_seqs, num_tokens, n_q, n_kv, max_seq_len, nsplit;
   int32_t block_shift;  // log2(block_size / 16)
+  int32_t no_decode;    // a request with one query row is an error (no decode kernel runs)
   float scale_log2;
 };
 
@@ -83,7 +84,10 @@ __device__ __forceinline__ bool prefill_request(const PrefillParams& p, int s, i
   a = __ldg(p.qsl + s);
   const int b = __ldg(p.qsl + s + 1);
   ql = b - a;
-  if (ql < 2) return false;
+  if (ql < 2) {
+    if (ql == 1 && p.no_decode && report) flag_error(p.err, DEVERR_BOUNDS);
+    return false;
+  }
   L = __ldg(p.seq_lens + s);
   if (L < ql || L > p.max_seq_len || L > (p.max_blocks << p.block_shift) * kBlock || a < 0 ||
       b > p.num_tokens) {
@@ -841,6 +845,7 @@ cudaError_t launch_prefill_t(const AttnArgs& a, const PrefillPlan& plan, void* w
   p.n_kv = a.num_kv_heads;
   p.max_seq_len = a.max_seq_len;
   p.block_shift = a.block_shift;
+  p.no_decode = a.no_decode ? 1 : 0;
   p.nsplit = plan.nsplit;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   if (plan.nsplit > 1) {

@@ -74,12 +74,17 @@ def _load() -> ctypes.CDLL:
     L.pa_paged_attention.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, vp, vp, i32,
                                      i32, i32, i32, f32, vp, vp, sz, vp]
     L.pa_paged_attention.restype = ctypes.c_int
+    L.pa_paged_attention_qrange.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, vp, vp,
+                                            i32, i32, i32, i32, i32, f32, vp, vp, sz, vp]
+    L.pa_paged_attention_qrange.restype = ctypes.c_int
     L.pa_copy_blocks.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, vp]
     L.pa_swap_staging_bytes.argtypes = [i32, i32, i32, i32]
     L.pa_swap_staging_bytes.restype = sz
     L.pa_swap_out.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, vp, vp, vp, vp]
     L.pa_swap_in.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, vp, vp, vp, vp]
     L.pa_copy_blocks.restype = ctypes.c_int
+    L.pa_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+    L.pa_selftest_wait_timeout.restype = ctypes.c_int
     L.pa_check_device_errors.argtypes = [vp]
     L.pa_check_device_errors.restype = ctypes.c_int
     L.pa_reshape_and_cache_fp8.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp,
@@ -193,11 +198,14 @@ def paged_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
                     block_tables: torch.Tensor, seq_lens: torch.Tensor,
                     query_start_loc: torch.Tensor, scale: float, *, max_q_len: int,
                     max_seq_len: int, out: Optional[torch.Tensor] = None,
-                    workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                    workspace: Optional[torch.Tensor] = None, stream=None,
+                    min_q_len: int = 0) -> torch.Tensor:
     """Causal GQA varlen attention over the paged cache (see pa_paged_attention).
 
     ``max_q_len`` / ``max_seq_len`` are host-side bounds that size the launch
-    without reading device memory.  Returns ``out``.
+    without reading device memory; ``min_q_len`` >= 2 promises that no
+    request has a single query row (pa_paged_attention_qrange: no decode
+    launch).  Returns ``out``.
     """
     L = _load()
     _need(q, "q", torch.bfloat16, 3)
@@ -222,6 +230,14 @@ def paged_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
         workspace = alloc_workspace(S, T, nq, nkv, d, max_q_len, max_seq_len, q.device)
     if workspace.dtype != torch.uint8 or not workspace.is_cuda or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous CUDA uint8 tensor")
+    if min_q_len >= 2:
+        _check(L.pa_paged_attention_qrange(
+            q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, nq, nkv, d,
+            block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),
+            query_start_loc.data_ptr(), S, T, int(min_q_len), int(max_q_len), int(max_seq_len),
+            float(scale), out.data_ptr(), workspace.data_ptr(), workspace.numel(),
+            _stream(stream)))
+        return out
     _check(L.pa_paged_attention(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), nb, bs,
                                 nq, nkv, d, block_tables.data_ptr(), block_tables.shape[1],
                                 seq_lens.data_ptr(), query_start_loc.data_ptr(), S, T,
@@ -363,6 +379,12 @@ def copy_blocks_fp8(k_cache, v_cache, k_scale, v_scale, src_dst_pairs: torch.Ten
     _check(L.pa_copy_blocks_fp8(k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(),
                                 v_scale.data_ptr(), nb, bs, nkv, d, src_dst_pairs.data_ptr(),
                                 src_dst_pairs.shape[0], _stream(stream)))
+
+
+def selftest_wait_timeout(limit_ns: int = 5_000_000, stream=None) -> None:
+    """Run the kernels' bounded wait on a barrier nothing completes (see
+    pa_selftest_wait_timeout); check_device_errors then raises PA_ERR_TIMEOUT."""
+    _check(_load().pa_selftest_wait_timeout(int(limit_ns), _stream(stream)))
 
 
 def check_device_errors(stream=None) -> None:

@@ -68,6 +68,12 @@ def test_host_side_argument_checks(lib):
     assert attn(nq=48, nkv=2) == "PA_ERR_UNSUPPORTED"  # group 24
     assert attn(mq=5, ms=4) == "PA_ERR_INVALID_ARG"
     assert attn(scale=float("nan")) == "PA_ERR_INVALID_ARG"
+    a = {**args, "mq": 2}
+    assert _status(L.pa_paged_attention_qrange(
+        a["q"], a["k"], a["v"], a["nb"], a["bs"], a["nq"], a["nkv"], a["d"], a["bt"], a["maxb"],
+        a["sl"], a["qsl"], a["S"], a["T"], 3, a["mq"], a["ms"], ctypes.c_float(0.125), a["out"],
+        a["ws"], a["wsb"], a["st"])) == "PA_ERR_INVALID_ARG"  # min_q_len > max_q_len
+    assert b"min_q_len" in L.pa_get_last_error()
     assert attn(S=0) == "PA_OK"   # nothing to do
     assert attn() == "PA_ERR_INVALID_ARG"  # null pointers
     assert vp  # keep the import used
@@ -105,3 +111,5 @@ def test_step_graph_argument_checks_without_gpu():
         == "PA_ERR_INVALID_ARG"
     assert b"copy_pairs" in L.pa_get_last_error()
     assert L.pa_step_graph_destroy(None) == 0
+    assert _status(L.pa_selftest_wait_timeout(0, None)) == "PA_ERR_INVALID_ARG"
+    assert _status(L.pa_selftest_wait_timeout(2_000_000_000, None)) == "PA_ERR_INVALID_ARG"

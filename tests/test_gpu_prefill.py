@@ -149,3 +149,27 @@ def test_one_workspace_for_a_large_step_serves_a_short_one():
                             workspace=ws)
         ops.check_device_errors()
         assert_attn_close(to_f64(out), ref, f"workspace of {ws.numel()} bytes")
+
+
+def test_min_q_len_bound_skips_the_decode_launch_with_identical_bits():
+    """pa_paged_attention_qrange with min_q_len >= 2 (no decode rows) gives
+    the same bits as the plain call; a request with one row under that
+    promise is flagged."""
+    b = _batch([700, 300, 90], [64, 300, 2], seed=14)
+    _, out1 = run_gpu_step(b)
+    d = W.to_device(b, "cuda")
+    ops.reshape_and_cache(d.k_new, d.v_new, d.k_cache, d.v_cache, d.slot_mapping)
+    out2 = torch.full_like(d.q, float("nan"))
+    ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens,
+                        d.query_start_loc, b.scale, max_q_len=b.max_q_len,
+                        max_seq_len=b.max_seq_len, out=out2, min_q_len=2)
+    ops.check_device_errors()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    bad = _batch([50, 40], [4, 1], seed=15)
+    d = W.to_device(bad, "cuda")
+    with pytest.raises(ops.PagedAttnError) as ei:
+        ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens,
+                            d.query_start_loc, bad.scale, max_q_len=4, max_seq_len=50,
+                            min_q_len=2)
+        ops.check_device_errors()
+    assert ei.value.code == 4
