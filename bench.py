@@ -470,6 +470,29 @@ def _fp8(args, dev, stream, ops, peaks, bf16_attn_ms):
             "attention_speedup_vs_bf16": round(bf16_attn_ms / attn_ms, 3)}
 
 
+def _other_decodes(args, dev, stream, ops, peaks):
+    """The tiny decode (latency only) and the long-context decode (8 x 32768
+    tokens, HBM-bound), timed like the main line."""
+    import torch
+    from paged_kv_cache_174_gb300 import workloads as W
+    res = {}
+    for name in ("tiny_decode", "long_decode"):
+        b = W.by_name(name, poison=False)
+        d = W.to_device(b, dev)
+        ws = ops.alloc_workspace(b.num_seqs, b.num_tokens, b.num_q_heads, b.num_kv_heads,
+                                 b.head_dim, b.max_q_len, b.max_seq_len, dev)
+        out = torch.empty_like(d.q)
+        ms, attn_ms = _time_steps(b, d, ws, out, args.steps, args.warmup, stream, ops)
+        alg = W.algorithmic_bytes(b)
+        gbs = alg["attention"] / (attn_ms * 1e-3) / 1e9
+        res[name] = {"description": W.WORKLOADS[name].description,
+                     "ms_per_step": round(ms, 5), "attention_ms": round(attn_ms, 5),
+                     "attention_GB_per_s": round(gbs, 1),
+                     "attention_frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+        del d, ws, out
+    return res
+
+
 def _block32(args, dev, stream, ops, peaks):
     """32-token blocks against 16: the decode batch and the mixed step with the
     same token slots in half as many blocks, timed like the main line, and
@@ -651,6 +674,8 @@ def run_ours(args):
         line["trace"] = _run_trace(dev, stream, ops, args.warmup)
     if not args.no_block32:
         line["block_size_32"] = _block32(args, dev, stream, ops, peaks)
+    if not args.no_other_decodes:
+        line["other_decodes"] = _other_decodes(args, dev, stream, ops, peaks)
     if not args.no_fp8:
         line["fp8_cache"] = _fp8(args, dev, stream, ops, peaks, attn_ms)
     if rank == 0 and not args.no_cpu_baseline:
@@ -661,7 +686,7 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
 
 
-def _oracle_sample_step(b, n_seqs, rng):
+def _oracle_sample_step(b, n_seqs, rng, threads=0):
     """One oracle pass over a sample of n_seqs requests of batch b (scatter of
     their new tokens + attention); returns (seconds, algorithmic bytes)."""
     import oracle
@@ -681,7 +706,7 @@ def _oracle_sample_step(b, n_seqs, rng):
     t = time.perf_counter()
     oracle.reshape_and_cache(sub.k_new, sub.v_new, b.k_cache, b.v_cache, sub.slot_mapping)
     oracle.paged_attention(sub.q, b.k_cache, b.v_cache, sub.block_tables, sub.seq_lens,
-                           sub.query_start_loc, sub.scale)
+                           sub.query_start_loc, sub.scale, threads=threads)
     dt = time.perf_counter() - t
     return dt, W.algorithmic_bytes(sub)["total"], len(idx)
 
@@ -698,10 +723,19 @@ def cpu_baseline(b, seconds: float):
         total_t += dt
         total_b += nb
         passes += 1
+    # the same on one thread, for a bounded ~2 s
+    t1, b1, p1 = 0.0, 0, 0
+    while t1 < min(2.0, seconds) and p1 < 100:
+        dt, nb, _ = _oracle_sample_step(b, n_seqs, rng, threads=1)
+        t1 += dt
+        b1 += nb
+        p1 += 1
     return {"value": round(total_b / total_t / 1e9, 4), "unit": "GB/s",
             "cores": oracle.num_threads(), "kind": "oracle",
+            "single_thread_value": round(b1 / t1 / 1e9, 4),
             "sample": f"{passes} passes, each over {n_seqs} random requests of the batch "
-                      f"(scatter + attention), {total_t:.1f} s total"}
+                      f"(scatter + attention), {total_t:.1f} s total; one thread: {p1} "
+                      f"passes, {t1:.1f} s"}
 
 
 def run_reference(args):
@@ -754,6 +788,8 @@ def main():
                     help="skip the mixed chunked-prefill step measurement")
     ap.add_argument("--no-trace", action="store_true",
                     help="skip the continuous-batching trace measurement")
+    ap.add_argument("--no-other-decodes", action="store_true",
+                    help="skip the tiny and long-context decode measurements")
     ap.add_argument("--no-fp8", action="store_true",
                     help="skip the 8-bit cache decode measurement")
     ap.add_argument("--no-block32", action="store_true",

@@ -657,19 +657,29 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
   }
 }
 
-// Combine the pieces of every decode request that spans several CTAs.  One
-// warp per (request, q head); lanes own 4 consecutive elements of head_dim.
-// Launched as a programmatic dependent of the decode kernel: it may start
-// while the decode grid drains and waits for it before reading partials.
-constexpr int kMergeWarps = 8;
+// Combine the pieces of every decode request that spans several CTAs, eight
+// pieces' loads in flight at a time.  Two shapes, chosen on the host from the
+// number of requests per CTA of the decode grid:
+//  * SPLIT = false (many requests, a few pieces each): a warp per (request,
+//    q head), kMergeWarps heads per CTA;
+//  * SPLIT = true (few long requests, up to a piece per decode CTA each): a
+//    CTA per (request, q head) whose warps take every kMergeWarps-th piece,
+//    then warp 0 combines the warps' partial results.
+// Lanes own 4 consecutive elements of head_dim.  Launched as a programmatic
+// dependent of the decode kernel: it may start while the decode grid drains
+// and waits for it before reading partials.
+constexpr int kMergeWarps = 4;
 
-template <int D>
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const DecodeParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ float w_m[kMergeWarps], w_l[kMergeWarps];
+  __shared__ float4 w_o[kMergeWarps][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s = blockIdx.x;
-  const int h = blockIdx.y * kMergeWarps + warp;
-  if (h >= p.n_q) return;
+  const int h = SPLIT ? (int)blockIdx.y : (int)blockIdx.y * kMergeWarps + warp;
+  if (!SPLIT && h >= p.n_q) return;
+  // with SPLIT every early return below is the same for the whole CTA
   if (decode_pages(p, s, false) == 0) return;  // not a (valid) decode request
   const int4 rec = p.seq_rec[s];
   const int C = p.ctas;
@@ -678,21 +688,23 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
   if (c_first == c_last) return;  // written directly by the decode kernel
   if (c_first < 0 || c_last >= C || c_first > c_last || first_slot < 0 || first_slot >= 2 * C ||
       F <= 0) {
-    if (lane == 0) flag_error(p.err, DEVERR_BOUNDS);
+    if (threadIdx.x == 0) flag_error(p.err, DEVERR_BOUNDS);
     return;
   }
-  // online merge over the pieces, eight at a time so that their loads are in
-  // flight together (a long request can span tens of CTAs)
+  // with at least as many pages as CTAs no slice is empty (skip the divisions)
+  const bool may_be_empty = F < C;
   const bool active = lane * 4 < D;
   float M = kNegInf, Lsum = 0.f;
   float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int cc0 = c_first; cc0 <= c_last; cc0 += 8) {
+  constexpr int STEP = SPLIT ? kMergeWarps : 1;  // piece stride of this warp
+  for (int cc0 = c_first + (SPLIT ? warp : 0); cc0 <= c_last; cc0 += 8 * STEP) {
     float2 ml[8];
     float4 o[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const int cc = cc0 + k;
-      const bool v = cc <= c_last && slice_begin(cc, F, C) != slice_begin(cc + 1, F, C);
+      const int cc = cc0 + k * STEP;
+      const bool v = cc <= c_last &&
+                     (!may_be_empty || slice_begin(cc, F, C) != slice_begin(cc + 1, F, C));
       const int slot = (cc == c_first) ? first_slot : 2 * cc;
       ml[k] = make_float2(kNegInf, 0.f);
       o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -718,13 +730,41 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
     }
     M = bm;
   }
+  if constexpr (!SPLIT) {
+    if (active) {
+      const float inv = 1.f / Lsum;
+      uint2 wv;
+      wv.x = pack_bf16x2(O.x * inv, O.y * inv);
+      wv.y = pack_bf16x2(O.z * inv, O.w * inv);
+      const int a = __ldg(p.qsl + s);
+      *reinterpret_cast<uint2*>(p.out + ((int64_t)a * p.n_q + h) * D + lane * 4) = wv;
+    }
+    return;
+  }
+  if (lane == 0) w_m[warp] = M, w_l[warp] = Lsum;
+  w_o[warp][lane] = O;
+  __syncthreads();
+  if (warp != 0) return;
+  float bm = kNegInf;
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) bm = fmaxf(bm, w_m[w]);
+  const float mu = (bm == kNegInf) ? 0.f : bm;
+  float Lt = 0.f;
+  float4 Ot = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) {
+    const float f = fast_exp2(w_m[w] - mu);
+    const float4 ow = w_o[w][lane];
+    Lt += w_l[w] * f;
+    Ot.x += ow.x * f, Ot.y += ow.y * f, Ot.z += ow.z * f, Ot.w += ow.w * f;
+  }
   if (active) {
-    const float inv = 1.f / Lsum;
-    uint2 w;
-    w.x = pack_bf16x2(O.x * inv, O.y * inv);
-    w.y = pack_bf16x2(O.z * inv, O.w * inv);
+    const float inv = 1.f / Lt;
+    uint2 wv;
+    wv.x = pack_bf16x2(Ot.x * inv, Ot.y * inv);
+    wv.y = pack_bf16x2(Ot.z * inv, Ot.w * inv);
     const int a = __ldg(p.qsl + s);
-    *reinterpret_cast<uint2*>(p.out + ((int64_t)a * p.n_q + h) * D + lane * 4) = w;
+    *reinterpret_cast<uint2*>(p.out + ((int64_t)a * p.n_q + h) * D + lane * 4) = wv;
   }
 }
 
@@ -798,7 +838,11 @@ cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ct
   }
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.num_seqs, (a.num_q_heads + kMergeWarps - 1) / kMergeWarps, 1);
+  // a request spans about ctas / num_seqs + 1 CTAs: with eight or more, split
+  // each request's pieces over a CTA's warps
+  const bool split = ctas >= 8 * a.num_seqs;
+  cfg.gridDim = split ? dim3(a.num_seqs, a.num_q_heads, 1)
+                      : dim3(a.num_seqs, (a.num_q_heads + kMergeWarps - 1) / kMergeWarps, 1);
   cfg.blockDim = dim3(kMergeWarps * 32, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -807,7 +851,8 @@ cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ct
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, p);
+  return split ? cudaLaunchKernelEx(&cfg, decode_merge_kernel<D, true>, p)
+               : cudaLaunchKernelEx(&cfg, decode_merge_kernel<D, false>, p);
 }
 
 template <int D, int G, bool F8>

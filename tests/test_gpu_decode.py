@@ -165,3 +165,23 @@ def test_repeated_calls_are_deterministic():
     torch.cuda.synchronize()
     for o in outs:
         assert torch.equal(o.view(torch.int16), out.view(torch.int16))
+
+
+@pytest.mark.parametrize("lens", [[4096], [32768], [40000, 16], [300, 200, 100]])
+def test_one_long_request_over_every_cta(lens):
+    """A request longer than the grid's pages per CTA is cut into a piece per
+    CTA (up to all of them) and merged; few pages leave CTAs without any."""
+    b = _decode(lens, seed=len(lens) + lens[0] % 7, nb=sum(-(-L // 16) for L in lens) + 3)
+    _, out = run_gpu_step(b)
+    if sum(lens) > 20000:
+        rng = np.random.default_rng(1)
+        samples = np.array([(s, 0, int(h)) for s in range(len(lens))
+                            for h in rng.choice(32, size=6, replace=False)], np.int32)
+        kc, vc, _ = run_oracle_step(b, attention=False)
+        ref = oracle.paged_attention_rows(b.q, kc, vc, b.block_tables, b.seq_lens,
+                                          b.query_start_loc, b.scale, samples)
+        got = to_f64(out)[b.query_start_loc[samples[:, 0]], samples[:, 2]]
+        assert_attn_close(got, ref, f"lens={lens} sampled heads")
+    else:
+        _, _, ref = run_oracle_step(b)
+        assert_attn_close(to_f64(out), ref, f"lens={lens}")
