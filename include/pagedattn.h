@@ -339,11 +339,14 @@ int pa_paged_attention_noalloc(const pa_bf16 *q, const pa_bf16 *k_cache,
  * Rows of out that belong to no request are left as they were.
  *
  * If host_meta is not NULL, every launch first copies meta_bytes from
- * host_meta (pinned host memory) to dev_meta, so that the per-step integer
- * inputs (slot_mapping, block_tables, ...) can live in one region of dev_meta
- * and reach the GPU inside the graph.  The copy reads host_meta when the
- * launch executes on the GPU, not when it is issued: do not rewrite it until
- * then (for example, alternate two graphs over two host buffers).
+ * host_meta (pinned host memory) to dev_meta, so that the step's inputs (the
+ * integer arrays, and q / k_new / v_new too if the caller places them there)
+ * can live in one region of dev_meta and reach the GPU in one copy inside the
+ * graph.  If host_out is not NULL, every launch ends by copying the first
+ * out_copy_bytes of out to host_out (pinned host memory).  The copies read
+ * and write host memory when the launch executes on the GPU, not when it is
+ * issued: do not touch those buffers until then (for example, alternate two
+ * graphs over two sets of host buffers).
  *
  * Buffers stay owned by the caller and must outlive the graph.  Launches of
  * one graph, and of graphs sharing buffers, must not overlap on the GPU.
@@ -370,6 +373,8 @@ typedef struct pa_step_buffers {
   const void *host_meta;        /* optional pinned host source of a per-launch copy */
   void *dev_meta;
   size_t meta_bytes;
+  void *host_out;               /* optional pinned host destination of out */
+  size_t out_copy_bytes;        /* <= max_tokens * num_q_heads * head_dim * 2 */
 } pa_step_buffers;
 
 typedef struct pa_step_graph pa_step_graph;

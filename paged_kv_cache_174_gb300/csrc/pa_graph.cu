@@ -45,11 +45,17 @@ int record_step(const pa_step_buffers& b, cudaStream_t s) {
   st = pa_reshape_and_cache(b.k_new, b.v_new, b.max_tokens, b.k_cache, b.v_cache, b.num_blocks,
                             b.block_size, b.num_kv_heads, b.head_dim, b.slot_mapping, s);
   if (st) return st;
-  return pa_paged_attention(b.q, b.k_cache, b.v_cache, b.num_blocks, b.block_size,
-                            b.num_q_heads, b.num_kv_heads, b.head_dim, b.block_tables,
-                            b.max_blocks, b.seq_lens, b.query_start_loc, b.max_seqs,
-                            b.max_tokens, b.max_q_len, b.max_seq_len, b.scale, b.out,
-                            b.workspace, b.workspace_bytes, s);
+  st = pa_paged_attention(b.q, b.k_cache, b.v_cache, b.num_blocks, b.block_size, b.num_q_heads,
+                          b.num_kv_heads, b.head_dim, b.block_tables, b.max_blocks, b.seq_lens,
+                          b.query_start_loc, b.max_seqs, b.max_tokens, b.max_q_len,
+                          b.max_seq_len, b.scale, b.out, b.workspace, b.workspace_bytes, s);
+  if (st) return st;
+  if (b.host_out) {
+    cudaError_t e = cudaMemcpyAsync(b.host_out, b.out, b.out_copy_bytes, cudaMemcpyDeviceToHost,
+                                    s);
+    if (e != cudaSuccess) return graph_fail(e, "step output copy");
+  }
+  return PA_OK;
 }
 
 }  // namespace
@@ -71,6 +77,11 @@ int pa_step_graph_create(const pa_step_buffers* b, pa_step_graph** out) {
                         b->max_pairs);
   if (b->host_meta && (!b->dev_meta || b->meta_bytes == 0))
     return pa::api_fail(PA_ERR_INVALID_ARG, "host_meta needs dev_meta and meta_bytes");
+  if (b->host_out && (b->out_copy_bytes == 0 ||
+                      b->out_copy_bytes > (size_t)b->max_tokens * b->num_q_heads * b->head_dim *
+                                              sizeof(pa_bf16)))
+    return pa::api_fail(PA_ERR_INVALID_ARG, "out_copy_bytes %zu outside (0, out's size]",
+                        b->out_copy_bytes);
   // Look up the per-device state outside the capture.
   int st = pa::api_warm_device();
   if (st) return st;

@@ -48,7 +48,8 @@ class StepBuffers(ctypes.Structure):
                 ("slot_mapping", _vp), ("block_tables", _vp), ("seq_lens", _vp),
                 ("query_start_loc", _vp), ("copy_pairs", _vp),
                 ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
-                ("host_meta", _vp), ("dev_meta", _vp), ("meta_bytes", ctypes.c_size_t)]
+                ("host_meta", _vp), ("dev_meta", _vp), ("meta_bytes", ctypes.c_size_t),
+                ("host_out", _vp), ("out_copy_bytes", ctypes.c_size_t)]
 
 
 def _load() -> ctypes.CDLL:
@@ -397,20 +398,30 @@ class StepGraph:
     CUDA graph by the library (pa_step_graph_create) over fixed buffers sized
     for the largest step.
 
-    Per step: write the step's q / k_new / v_new rows into ``self.q``,
-    ``self.k_new``, ``self.v_new`` (first num_tokens rows, on the launching
-    stream), then call :meth:`launch` with the step's integer inputs as host
-    arrays (or :meth:`stage` them first and call :meth:`launch` with none);
-    they are padded to the maxima in a pinned buffer and reach the GPU
-    through the graph's own copy node.  The output is ``self.out[:num_tokens]``.
-    Two graphs alternate over two pinned buffers, so the host fills one while
-    the GPU may still copy from the other.  ``stream`` is a torch.cuda.Stream
-    or None (the current stream).
+    Per step: write the step's q / k_new / v_new rows (first num_tokens rows),
+    then call :meth:`launch` with the step's integer inputs as host arrays (or
+    :meth:`stage` them first and call :meth:`launch` with none); they are
+    padded to the maxima in a pinned buffer.  ``stream`` is a
+    torch.cuda.Stream or None (the current stream).
+
+    * ``host_io=False``: q / k_new / v_new / out are device tensors
+      (``self.q`` ...); the graph's own first node copies the integer inputs
+      from the pinned buffer.  Two graphs alternate over two pinned buffers,
+      so the host fills one while the GPU may still read the other.
+    * ``host_io=True``: a step's whole input (integer arrays and q / k_new /
+      v_new) sits in one pinned region (fill the views :meth:`inputs_host`
+      returns) and its output comes back into pinned memory
+      (:meth:`output_host`, after :meth:`wait_output`).  Two graphs
+      alternate over two device copies of the region; each launch copies its
+      region in on one side stream and its output out on another, so the copy
+      of step i+1's inputs and of step i's output overlap step i's kernels.
+      :meth:`fork` / :meth:`join` order the side streams after / before a
+      point of the launching stream (to time a run of launches).
     """
 
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, *, num_q_heads: int,
                  max_tokens: int, max_seqs: int, max_blocks: int, max_pairs: int,
-                 max_q_len: int, max_seq_len: int, scale: float):
+                 max_q_len: int, max_seq_len: int, scale: float, host_io: bool = False):
         import numpy as np
         L = _load()
         _need(k_cache, "k_cache", torch.bfloat16, 4)
@@ -419,35 +430,77 @@ class StepGraph:
             raise ValueError("k_cache and v_cache shapes differ")
         nb, bs, nkv, d = k_cache.shape
         dev = k_cache.device
+        self.device = dev
         T, S, MB, P = int(max_tokens), int(max_seqs), int(max_blocks), int(max_pairs)
         self.max_tokens, self.max_seqs, self.max_blocks, self.max_pairs = T, S, MB, P
-        self.q = torch.zeros(T, num_q_heads, d, dtype=torch.bfloat16, device=dev)
-        self.k_new = torch.zeros(T, nkv, d, dtype=torch.bfloat16, device=dev)
-        self.v_new = torch.zeros(T, nkv, d, dtype=torch.bfloat16, device=dev)
-        self.out = torch.zeros(T, num_q_heads, d, dtype=torch.bfloat16, device=dev)
-        # int32 metadata region: slots [T] | tables [S*MB] | seq_lens [S] | qsl [S+1] | pairs [2P]
+        # int32 metadata: slots [T] | tables [S*MB] | seq_lens [S] | qsl [S+1] | pairs [2P]
         self._off = np.cumsum([0, T, S * MB, S, S + 1, 2 * P])
         n = int(self._off[-1])
-        self._dev_meta = torch.zeros(n, dtype=torch.int32, device=dev)
-        self._host = [torch.zeros(n, dtype=torch.int32).pin_memory() for _ in range(2)]
-        self._events = [None, None]
+        meta_bytes = -(-4 * n // 256) * 256
+        q_bytes, kv_bytes = T * num_q_heads * d * 2, T * nkv * d * 2
+        total = meta_bytes + (q_bytes + 2 * kv_bytes if host_io else 0)
+        self.host_io = host_io
+
+        def bf16_views(region):
+            q0, k0, v0 = meta_bytes, meta_bytes + q_bytes, meta_bytes + q_bytes + kv_bytes
+            return (region[q0:k0].view(torch.bfloat16).view(T, num_q_heads, d),
+                    region[k0:v0].view(torch.bfloat16).view(T, nkv, d),
+                    region[v0:v0 + kv_bytes].view(torch.bfloat16).view(T, nkv, d))
+
+        self._host_region = [torch.zeros(total, dtype=torch.uint8).pin_memory() for _ in range(2)]
+        self._host = [h[:4 * n].view(torch.int32) for h in self._host_region]
         self.workspace = alloc_workspace(S, T, num_q_heads, nkv, d, max_q_len, max_seq_len, dev)
-        base = self._dev_meta.data_ptr()
-        o = [base + 4 * int(x) for x in self._off]
+        if host_io:
+            self._dev_region = [torch.zeros(total, dtype=torch.uint8, device=dev)
+                                for _ in range(2)]
+            self._dev_in = [bf16_views(r) for r in self._dev_region]
+            self._host_inputs = [bf16_views(h) for h in self._host_region]
+            self._out = [torch.zeros(T, num_q_heads, d, dtype=torch.bfloat16, device=dev)
+                         for _ in range(2)]
+            self._out_host = [torch.zeros(T, num_q_heads, d, dtype=torch.bfloat16).pin_memory()
+                              for _ in range(2)]
+            self._h2d = torch.cuda.Stream(dev)
+            self._d2h = torch.cuda.Stream(dev)
+            self._in_ready = [None, None]
+            self._comp_done = [None, None]
+            self._out_ready = [None, None]
+        else:
+            self._dev_region = [torch.zeros(total, dtype=torch.uint8, device=dev)] * 2
+            self.q = torch.zeros(T, num_q_heads, d, dtype=torch.bfloat16, device=dev)
+            self.k_new = torch.zeros(T, nkv, d, dtype=torch.bfloat16, device=dev)
+            self.v_new = torch.zeros(T, nkv, d, dtype=torch.bfloat16, device=dev)
+            self.out = torch.zeros(T, num_q_heads, d, dtype=torch.bfloat16, device=dev)
+            self._dev_in = [(self.q, self.k_new, self.v_new)] * 2
+            self._out = [self.out] * 2
+            self._events = [None, None]
         self._graphs = []
-        for h in self._host:
+        for i in range(2):
+            base = self._dev_region[i].data_ptr()
+            o = [base + 4 * int(x) for x in self._off]
+            q, k, v = self._dev_in[i]
             b = StepBuffers(k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, num_q_heads, nkv, d,
                             T, S, MB, P, int(max_q_len), int(max_seq_len), float(scale),
-                            self.q.data_ptr(), self.k_new.data_ptr(), self.v_new.data_ptr(),
-                            self.out.data_ptr(), o[0], o[1], o[2], o[3], o[4] if P else None,
-                            self.workspace.data_ptr(), self.workspace.numel(), h.data_ptr(),
-                            base, 4 * n)
+                            q.data_ptr(), k.data_ptr(), v.data_ptr(), self._out[i].data_ptr(),
+                            o[0], o[1], o[2], o[3], o[4] if P else None,
+                            self.workspace.data_ptr(), self.workspace.numel(),
+                            None if host_io else self._host_region[i].data_ptr(),
+                            base, 4 * n, None, 0)
             g = ctypes.c_void_p()
             _check(L.pa_step_graph_create(ctypes.byref(b), ctypes.byref(g)))
             self._graphs.append(g)
+        self.input_bytes = total if host_io else 4 * n   # copied in by every launch
+        self.output_bytes = q_bytes if host_io else 0    # copied out by every launch
+        self._last = None
         self._next = 0
         self._staged = False
+        self._filled = [False, False]    # buffer i holds a staged step
         self._keep = (k_cache, v_cache)  # the graphs hold their pointers
+
+    def _free_host_buffer(self, i: int) -> None:
+        """Block until buffer i's pinned input region may be rewritten."""
+        ev = self._in_ready[i] if self.host_io else self._events[i]
+        if ev is not None:
+            ev.synchronize()
 
     def launch(self, slot_mapping=None, block_tables=None, seq_lens=None, query_start_loc=None,
                copy_pairs=None, stream=None) -> None:
@@ -456,12 +509,77 @@ class StepGraph:
         if not self._staged:
             raise ValueError("no step staged")
         i = self._next
-        _check(_load().pa_step_graph_launch(self._graphs[i], _stream(stream)))
-        ev = torch.cuda.Event()
-        ev.record(torch.cuda.current_stream(self.q.device) if stream is None else stream)
-        self._events[i] = ev
+        main = torch.cuda.current_stream(self.device) if stream is None else stream
+        if self.host_io:
+            if self._comp_done[i] is not None:
+                self._h2d.wait_event(self._comp_done[i])  # its last graph is done with it
+            with torch.cuda.stream(self._h2d):
+                self._dev_region[i].copy_(self._host_region[i], non_blocking=True)
+                self._in_ready[i] = torch.cuda.Event()
+                self._in_ready[i].record(self._h2d)
+            main.wait_event(self._in_ready[i])
+        _check(_load().pa_step_graph_launch(self._graphs[i], main.cuda_stream))
+        done = torch.cuda.Event()
+        done.record(main)
+        if self.host_io:
+            self._comp_done[i] = done
+            self._d2h.wait_event(done)
+            with torch.cuda.stream(self._d2h):
+                self._out_host[i].copy_(self._out[i], non_blocking=True)
+                self._out_ready[i] = torch.cuda.Event()
+                self._out_ready[i].record(self._d2h)
+        else:
+            self._events[i] = done
+        self._last = i
         self._next = 1 - i
         self._staged = False
+
+    def relaunch(self, stream=None) -> None:
+        """Launch the next buffer's inputs as they stand (the step it last
+        held, with whatever the caller rewrote in place since)."""
+        if not self._filled[self._next]:
+            raise ValueError("the next buffer has never been staged")
+        self._free_host_buffer(self._next)
+        self._staged = True
+        self.launch(stream=stream)
+
+    def inputs_host(self):
+        """(q, k_new, v_new) pinned views for the next launch (host_io)."""
+        if not self.host_io:
+            raise ValueError("the graph was built without host_io")
+        self._free_host_buffer(self._next)
+        return self._host_inputs[self._next]
+
+    def wait_output(self) -> None:
+        """Block until the last launch's output is in pinned memory (host_io)."""
+        if self.host_io and self._last is not None and self._out_ready[self._last] is not None:
+            self._out_ready[self._last].synchronize()
+
+    def output_host(self) -> torch.Tensor:
+        """Pinned copy of out from the last launch (host_io; call wait_output
+        first)."""
+        if not self.host_io or self._last is None:
+            raise ValueError("no host_io launch yet")
+        return self._out_host[self._last]
+
+    def output(self) -> torch.Tensor:
+        """Device out of the last launch."""
+        return self._out[self._last if self._last is not None else 0]
+
+    def fork(self, stream=None) -> None:
+        """Order the side copy streams after everything issued so far on stream."""
+        if self.host_io:
+            main = torch.cuda.current_stream(self.device) if stream is None else stream
+            ev = torch.cuda.Event()
+            ev.record(main)
+            self._h2d.wait_event(ev)
+            self._d2h.wait_event(ev)
+
+    def join(self, stream=None) -> None:
+        """Make stream wait for the last launch's output copy."""
+        if self.host_io and self._last is not None:
+            main = torch.cuda.current_stream(self.device) if stream is None else stream
+            main.wait_event(self._out_ready[self._last])
 
     def stage(self, slot_mapping, block_tables, seq_lens, query_start_loc,
               copy_pairs=None) -> None:
@@ -481,8 +599,7 @@ class StepGraph:
                              f"seqs {ns}/{S}, table columns {bt.shape[1]}/{MB}, "
                              f"pairs {cp.shape[0]}/{P}) or inconsistent shapes")
         i = self._next
-        if self._events[i] is not None:
-            self._events[i].synchronize()  # that launch has read this pinned buffer
+        self._free_host_buffer(i)
         h = self._host[i].numpy()
         o = self._off
         h[o[0]:o[1]] = -1
@@ -499,6 +616,7 @@ class StepGraph:
             pr[:] = -1
             pr[:cp.shape[0]] = cp
         self._staged = True
+        self._filled[i] = True
 
     def close(self) -> None:
         for g in getattr(self, "_graphs", []):
