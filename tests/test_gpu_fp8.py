@@ -115,12 +115,13 @@ def test_fp8_quantises_zero_and_large_rows():
     assert np.array_equal(dvs.cpu().numpy().view(np.uint32), ovs.view(np.uint32))
 
 
-def test_fp8_copy_blocks_moves_codes_and_scales():
+@pytest.mark.parametrize("bs", [16, 32])
+def test_fp8_copy_blocks_moves_codes_and_scales(bs):
     rng = np.random.default_rng(8)
-    dk8 = torch.from_numpy(rng.integers(0, 256, (10, 16, 8, 128), dtype=np.uint8)).cuda()
-    dv8 = torch.from_numpy(rng.integers(0, 256, (10, 16, 8, 128), dtype=np.uint8)).cuda()
-    dks = torch.from_numpy(rng.standard_normal((10, 16, 8)).astype(np.float32)).cuda()
-    dvs = torch.from_numpy(rng.standard_normal((10, 16, 8)).astype(np.float32)).cuda()
+    dk8 = torch.from_numpy(rng.integers(0, 256, (10, bs, 8, 128), dtype=np.uint8)).cuda()
+    dv8 = torch.from_numpy(rng.integers(0, 256, (10, bs, 8, 128), dtype=np.uint8)).cuda()
+    dks = torch.from_numpy(rng.standard_normal((10, bs, 8)).astype(np.float32)).cuda()
+    dvs = torch.from_numpy(rng.standard_normal((10, bs, 8)).astype(np.float32)).cuda()
     before = [t.cpu().numpy().copy() for t in (dk8, dv8, dks, dvs)]
     pairs = np.array([[1, 4], [-1, -1], [6, 2]], np.int32)
     ops.copy_blocks_fp8(dk8, dv8, dks, dvs, W.int32_tensor(pairs, "cuda"))

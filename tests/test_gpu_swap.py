@@ -25,13 +25,14 @@ def _host(n, bs, nkv, d):
             torch.empty(n, bs, nkv, d, dtype=torch.bfloat16).pin_memory())
 
 
-@pytest.mark.parametrize("nkv,d,nb,n", [(2, 64, 16, 1), (8, 128, 600, 37), (8, 128, 4096, 512)])
-def test_swap_out_then_in_bit_exact(nkv, d, nb, n):
+@pytest.mark.parametrize("nkv,d,nb,n,bs", [(2, 64, 16, 1, 16), (8, 128, 600, 37, 16),
+                                           (8, 128, 4096, 512, 16), (8, 128, 300, 45, 32)])
+def test_swap_out_then_in_bit_exact(nkv, d, nb, n, bs):
     rng = np.random.default_rng(nb + n)
-    kc, vc = _random_cache(rng, nb, nkv, d)
+    kc, vc = _random_cache(rng, nb, nkv, d, bs)
     ids = rng.choice(nb, size=n, replace=False).astype(np.int32)
     dk, dv = W.bf16_tensor(kc, "cuda"), W.bf16_tensor(vc, "cuda")
-    hk, hv = _host(n, 16, nkv, d)
+    hk, hv = _host(n, bs, nkv, d)
     staging = ops.swap_out(dk, dv, W.int32_tensor(ids, "cuda"), hk, hv)
     ops.check_device_errors()
     ok, ov = oracle.swap_out(kc, vc, ids)
