@@ -503,45 +503,52 @@ class StepGraph:
             ev.synchronize()
 
     def launch(self, slot_mapping=None, block_tables=None, seq_lens=None, query_start_loc=None,
-               copy_pairs=None, stream=None) -> None:
+               copy_pairs=None, stream=None, copy_in: bool = True,
+               copy_out: bool = True) -> None:
+        """Launch the staged step.  With host_io, copy_in=False reuses the
+        device copy of the buffer's inputs from its last launch (inputs
+        already resident) and copy_out=False leaves out on the device."""
         if slot_mapping is not None:
             self.stage(slot_mapping, block_tables, seq_lens, query_start_loc, copy_pairs)
         if not self._staged:
             raise ValueError("no step staged")
         i = self._next
         main = torch.cuda.current_stream(self.device) if stream is None else stream
-        if self.host_io:
+        if self.host_io and copy_in:
             if self._comp_done[i] is not None:
                 self._h2d.wait_event(self._comp_done[i])  # its last graph is done with it
             with torch.cuda.stream(self._h2d):
                 self._dev_region[i].copy_(self._host_region[i], non_blocking=True)
                 self._in_ready[i] = torch.cuda.Event()
                 self._in_ready[i].record(self._h2d)
+        if self.host_io and self._in_ready[i] is not None:
             main.wait_event(self._in_ready[i])
         _check(_load().pa_step_graph_launch(self._graphs[i], main.cuda_stream))
         done = torch.cuda.Event()
         done.record(main)
         if self.host_io:
             self._comp_done[i] = done
-            self._d2h.wait_event(done)
-            with torch.cuda.stream(self._d2h):
-                self._out_host[i].copy_(self._out[i], non_blocking=True)
-                self._out_ready[i] = torch.cuda.Event()
-                self._out_ready[i].record(self._d2h)
+            if copy_out:
+                self._d2h.wait_event(done)
+                with torch.cuda.stream(self._d2h):
+                    self._out_host[i].copy_(self._out[i], non_blocking=True)
+                    self._out_ready[i] = torch.cuda.Event()
+                    self._out_ready[i].record(self._d2h)
         else:
             self._events[i] = done
         self._last = i
         self._next = 1 - i
         self._staged = False
 
-    def relaunch(self, stream=None) -> None:
+    def relaunch(self, stream=None, copy_in: bool = True, copy_out: bool = True) -> None:
         """Launch the next buffer's inputs as they stand (the step it last
         held, with whatever the caller rewrote in place since)."""
         if not self._filled[self._next]:
             raise ValueError("the next buffer has never been staged")
-        self._free_host_buffer(self._next)
+        if copy_in:
+            self._free_host_buffer(self._next)
         self._staged = True
-        self.launch(stream=stream)
+        self.launch(stream=stream, copy_in=copy_in, copy_out=copy_out)
 
     def inputs_host(self):
         """(q, k_new, v_new) pinned views for the next launch (host_io)."""
