@@ -708,11 +708,16 @@ def run_ours(args):
                                   mb.head_dim, mb.max_q_len, mb.max_seq_len, dev)
         mout = torch.empty_like(md.q)
         mms, mattn = _time_steps(mb, md, mws, mout, args.steps, args.warmup, stream, ops)
+        mgms, mgout = _time_graph_steps(mb, md, args.steps, args.warmup, stream, ops)
+        if not torch.equal(mgout[:mb.num_tokens].view(torch.int16), mout.view(torch.int16)):
+            raise RuntimeError("the mixed step's graph output differs from separate launches'")
         pre = _time_prefill(mb, md, args.steps, args.warmup, stream, ops)
         line["mixed_batch"] = {
             "workload": mb.name, "description": W.WORKLOADS[mb.name].description,
             "tokens_per_s": round(mb.num_tokens * world / (mms * 1e-3), 1),
             "ms_per_step": round(mms, 5), "attention_ms": round(mattn, 5),
+            "graph_tokens_per_s": round(mb.num_tokens * world / (mgms * 1e-3), 1),
+            "graph_ms_per_step": round(mgms, 5),
             "gpu_launches": _launch_count(mb) * args.steps}
         if pre:
             line["roofline_prefill"] = {
