@@ -697,7 +697,10 @@ def run_ours(args):
                         "inputs from pinned host memory (side stream), scatter + attention, "
                         "one copy of out back to pinned memory (side stream); the copies "
                         "of one step overlap the kernels of its neighbours"},
-        "gpu_launches": _launch_count(b) * args.steps,
+        # the timed value path: a graph launch per step, whose decode-only
+        # steps run scatter + attention as one kernel (+ the merge)
+        "gpu_launches": (_launch_count(b) - (1 if b.max_q_len <= 1 and b.num_tokens else 0))
+        * args.steps,
         "clocks": clk,
     }
     # ---- the mixed chunked-prefill step (second half of the metric)

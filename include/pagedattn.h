@@ -168,6 +168,28 @@ int pa_paged_attention_qrange(const pa_bf16 *q, const pa_bf16 *k_cache, const pa
                               size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * One decode step in one kernel: pa_reshape_and_cache followed by
+ * pa_paged_attention, for a step whose requests all have q_len <= 1 (every
+ * row a decode row; max_q_len is 1).  The decode kernel takes each request's
+ * new key and value rows (token t = query_start_loc[s]) from k_new / v_new
+ * straight into its copy of the request's last page, and stores them to
+ * slot_mapping[t] from there, so no separate scatter runs and the new rows
+ * are read from HBM once.  Precondition: slot_mapping[t] is the slot of the
+ * request's position seq_lens[s] - 1 (its block table entry), or negative (the
+ * row is not written and the cache's row is read, as with a separate
+ * scatter); any other slot flags PA_ERR_DEVICE_BOUNDS.  Tokens outside every
+ * request are not written.  bf16 cache only; arguments, workspace and errors
+ * otherwise as pa_reshape_and_cache and pa_paged_attention.
+ */
+int pa_decode_step(const pa_bf16 *q, const pa_bf16 *k_new, const pa_bf16 *v_new,
+                   pa_bf16 *k_cache, pa_bf16 *v_cache, int32_t num_blocks, int32_t block_size,
+                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                   const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens,
+                   const int32_t *query_start_loc, int32_t num_seqs, int32_t num_tokens,
+                   int32_t max_seq_len, const int32_t *slot_mapping, float scale, pa_bf16 *out,
+                   void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Copy-on-write block copy: for each pair i, physical block
  * src_dst_pairs[2i+1] of both caches becomes a bit copy of block
  * src_dst_pairs[2i] ("PagedAttention 显存分页与连续批处理实战", comparison
@@ -336,6 +358,8 @@ int pa_paged_attention_noalloc(const pa_bf16 *q, const pa_bf16 *k_cache,
  *   - copy pairs i >= the step's count: copy_pairs[2i] = -1 (skipped).
  * A step's sizes must stay within the maxima (max_q_len and max_seq_len
  * included: a request beyond them flags PA_ERR_DEVICE_BOUNDS at run time).
+ * With max_q_len 1 the graph runs scatter + attention as pa_decode_step (one
+ * kernel; its slot precondition applies).
  * Rows of out that belong to no request are left as they were.
  *
  * If host_meta is not NULL, every launch first copies meta_bytes from

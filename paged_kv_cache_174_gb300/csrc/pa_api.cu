@@ -306,7 +306,9 @@ int paged_attention_impl(const pa_bf16* q, KvCache kv,
                          const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens,
                          int32_t min_q_len, int32_t max_q_len, int32_t max_seq_len, float scale,
                          pa_bf16* out, void* workspace, size_t workspace_bytes, size_t split_cap,
-                         cudaStream_t stream);
+                         cudaStream_t stream, const pa_bf16* fuse_k_new = nullptr,
+                         const pa_bf16* fuse_v_new = nullptr,
+                         const int32_t* fuse_slot_mapping = nullptr);
 
 }  // namespace
 
@@ -341,6 +343,22 @@ int pa_paged_attention_qrange(const pa_bf16* q, const pa_bf16* k_cache, const pa
                               workspace_bytes, ~size_t(0), stream);
 }
 
+int pa_decode_step(const pa_bf16* q, const pa_bf16* k_new, const pa_bf16* v_new,
+                   pa_bf16* k_cache, pa_bf16* v_cache, int32_t num_blocks, int32_t block_size,
+                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                   const int32_t* block_tables, int32_t max_blocks, const int32_t* seq_lens,
+                   const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens,
+                   int32_t max_seq_len, const int32_t* slot_mapping, float scale, pa_bf16* out,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!slot_mapping && num_tokens > 0)
+    return fail(PA_ERR_INVALID_ARG, "null pointer argument (slot_mapping)");
+  return paged_attention_impl(q, KvCache{k_cache, v_cache, nullptr, nullptr, false}, num_blocks,
+                              block_size, num_q_heads, num_kv_heads, head_dim, block_tables,
+                              max_blocks, seq_lens, query_start_loc, num_seqs, num_tokens, 0, 1,
+                              max_seq_len, scale, out, workspace, workspace_bytes, ~size_t(0),
+                              stream, k_new, v_new, slot_mapping);
+}
+
 int pa_paged_attention_fp8(const pa_bf16* q, const uint8_t* k_cache, const uint8_t* v_cache,
                            const float* k_scale, const float* v_scale, int32_t num_blocks,
                            int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads,
@@ -367,7 +385,10 @@ int paged_attention_impl(const pa_bf16* q, KvCache kv,
                          const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens,
                          int32_t min_q_len, int32_t max_q_len, int32_t max_seq_len, float scale,
                          pa_bf16* out, void* workspace, size_t workspace_bytes, size_t split_cap,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, const pa_bf16* fuse_k_new,
+                         const pa_bf16* fuse_v_new,
+                         const int32_t* fuse_slot_mapping) {
+  const bool fuse = fuse_slot_mapping != nullptr;  // pa_decode_step
   int st = check_cache_geometry(num_blocks, block_size, num_kv_heads, head_dim);
   if (st) return st;
   if (num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
@@ -394,6 +415,9 @@ int paged_attention_impl(const pa_bf16* q, KvCache kv,
     return fail(PA_ERR_INVALID_ARG, "null pointer argument");
   if (kv.fp8 && (!aligned(kv.k_scale, 16) || !aligned(kv.v_scale, 16)))
     return fail(PA_ERR_INVALID_ARG, "scale arrays must be 16-byte aligned");
+  if (fuse && (!fuse_k_new || !fuse_v_new || !aligned(fuse_k_new, 16) ||
+               !aligned(fuse_v_new, 16) || !aligned(fuse_slot_mapping, 4)))
+    return fail(PA_ERR_INVALID_ARG, "k_new / v_new must be 16-byte aligned, slot_mapping 4-byte");
   if (!aligned(q, 16) || !aligned(kv.k, 16) || !aligned(kv.v, 16) || !aligned(out, 16) ||
       !aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(query_start_loc, 4))
     return fail(PA_ERR_INVALID_ARG, "bf16 arrays must be 16-byte aligned, int32 arrays 4-byte");
@@ -402,6 +426,9 @@ int paged_attention_impl(const pa_bf16* q, KvCache kv,
                 max_blocks, max_seq_len);
   if (max_q_len >= 2 && kv.fp8)
     return fail(PA_ERR_UNSUPPORTED, "rows with q_len >= 2 over the 8-bit cache (decode only)");
+  if (fuse && max_q_len > 1)
+    return fail(PA_ERR_INVALID_ARG, "pa_decode_step takes decode rows only (max_q_len %d)",
+                max_q_len);
   if (max_q_len >= 2 && !pa::prefill_supported(head_dim, group, num_kv_heads))
     return fail(PA_ERR_UNSUPPORTED, "prefill rows (q_len >= 2) for head_dim=%d group=%d",
                 head_dim, group);
@@ -430,6 +457,9 @@ int paged_attention_impl(const pa_bf16* q, KvCache kv,
   a.k_scale = kv.k_scale;
   a.v_scale = kv.v_scale;
   a.fp8 = kv.fp8;
+  a.fuse_k_new = fuse_k_new;
+  a.fuse_v_new = fuse_v_new;
+  a.fuse_slot_mapping = fuse_slot_mapping;
   a.num_blocks = num_blocks;
   a.num_q_heads = num_q_heads;
   a.num_kv_heads = num_kv_heads;

@@ -183,6 +183,25 @@ __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, un
 // --------------------------------------------------------- bulk async copy
 // Global -> shared, completion counted on an mbarrier (transaction bytes).
 // Both addresses 16-byte aligned, bytes a multiple of 16.
+// Bulk asynchronous store shared -> global (16-byte aligned, size a multiple
+// of 16), tracked by this thread's bulk groups.
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(src_smem), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// All of this thread's bulk stores have read their shared-memory source.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// All of this thread's bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uint32_t bytes,
                                          uint32_t bar) {
   asm volatile(

@@ -50,6 +50,13 @@ struct DecodeParams {
   const void* v_cache;
   const float* k_scale;    // F8: [num_blocks * block_size, n_kv] row scales
   const float* v_scale;
+  // Fused scatter (bf16 cache, decode-only steps): the new token of a decode
+  // request comes from k_new / v_new into its page in shared memory and is
+  // stored from there to its slot slot_mapping[t], which must be the slot of
+  // position seq_len - 1; null when the scatter ran separately.
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  const int32_t* slot_mapping;
   const int32_t* block_tables;
   const int32_t* seq_lens;
   const int32_t* qsl;
@@ -103,6 +110,7 @@ struct DecodeSmem {
   uint64_t p_empty[NKV][2];   // PV warp -> QK warp: buffer may be rewritten
   int released[8];            // warps done with the page in the stage
   int last_issued[8];         // last page whose copies went into the stage (-1: none)
+  int fused_slot[8];          // slot the stage's last row goes to (fused scatter), else -1
   PBuf<G> pb[NKV][2];
   int plan[2];
   int abort_flag;
@@ -121,13 +129,16 @@ struct PageCursor {
   }
 };
 
-// Issue the bulk copies of page (c.s, c.j) into a stage.
+// Issue the bulk copies of page (c.s, c.j) into a stage.  *fused_slot gets the
+// slot the stage's last row must be stored to (fused scatter), or -1.
 __device__ __forceinline__ void fetch_page(const DecodeParams& p, const PageCursor& c,
-                                           uint32_t stage_smem, uint32_t full_bar) {
+                                           uint32_t stage_smem, uint32_t full_bar,
+                                           int* fused_slot) {
   const int L = __ldg(p.seq_lens + c.s);
   const int ntok = min(kBlock, L - c.j * kBlock);
   const int phys =
       __ldg(p.block_tables + (int64_t)c.s * p.max_blocks + (c.j >> p.block_shift));
+  *fused_slot = -1;
   if (phys < 0 || phys >= p.num_blocks) {
     flag_error(p.err, DEVERR_BOUNDS);
     mbar_arrive_expect_tx(full_bar, 0);  // completes the phase with no data
@@ -138,6 +149,31 @@ __device__ __forceinline__ void fetch_page(const DecodeParams& p, const PageCurs
   // 16-token page index in the pool: a block of 32 tokens is two pages
   const size_t page = ((size_t)phys << p.block_shift) + (c.j & ((1 << p.block_shift) - 1));
   const size_t off = page * p.page_bytes;
+  if (p.slot_mapping && c.j == c.np - 1) {
+    // the request's new token (position L - 1, last row of this page) comes
+    // from k_new / v_new instead of the cache, which does not hold it yet
+    const int a = __ldg(p.qsl + c.s);
+    const int64_t slot = __ldg(p.slot_mapping + a);
+    const int64_t want = (int64_t)page * kBlock + (ntok - 1);
+    if (slot == want) {
+      const uint32_t head = (uint32_t)(ntok - 1) * p.row_bytes;  // rows before the new one
+      if (head) {
+        bulk_g2s(stage_smem, reinterpret_cast<const unsigned char*>(p.k_cache) + off, head,
+                 full_bar);
+        bulk_g2s(stage_smem + p.page_bytes,
+                 reinterpret_cast<const unsigned char*>(p.v_cache) + off, head, full_bar);
+      }
+      bulk_g2s(stage_smem + head, p.k_new + (int64_t)a * (p.row_bytes / 2), p.row_bytes,
+               full_bar);
+      bulk_g2s(stage_smem + p.page_bytes + head, p.v_new + (int64_t)a * (p.row_bytes / 2),
+               p.row_bytes, full_bar);
+      *fused_slot = (int)slot;
+      return;
+    }
+    // a negative slot is a token not to be written: the cache's row is read,
+    // as with a separate scatter; any other slot breaks the precondition
+    if (slot >= 0) flag_error(p.err, DEVERR_BOUNDS);
+  }
   bulk_g2s(stage_smem, reinterpret_cast<const unsigned char*>(p.k_cache) + off, bytes, full_bar);
   bulk_g2s(stage_smem + p.page_bytes, reinterpret_cast<const unsigned char*>(p.v_cache) + off,
            bytes, full_bar);
@@ -383,6 +419,7 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
         mbar_init(smem_addr(&S.full[i]), 1);
         S.released[i] = 0;
         S.last_issued[i] = -1;
+        S.fused_slot[i] = -1;
       }
       for (int g = 0; g < NKV; ++g)
         for (int b = 0; b < 2; ++b) {
@@ -394,7 +431,7 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
         PageCursor fc{found_s, found_j, decode_pages(p, found_s, false)};
         for (int i = 0; i < NST && i < n_pages; ++i) {
           fetch_page(p, fc, smem_addr(stages + (size_t)i * p.stage_bytes),
-                     smem_addr(&S.full[i]));
+                     smem_addr(&S.full[i]), &S.fused_slot[i]);
           S.last_issued[i] = i;
           fc.next(p);
         }
@@ -424,6 +461,7 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
     const int rep = dl % REP_QK;
     float2 qf[G][E_QK / 2];
     float m_run = kNegInf, l_lane = 0.f;
+    bool stored = false;  // this lane issued fused-scatter stores
     auto load_q = [&](int seq) {
       const int tok = __ldg(p.qsl + seq);
 #pragma unroll
@@ -455,6 +493,15 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
       if (i >= 2) mbar_wait(smem_addr(&S.p_empty[g][b]), ((i >> 1) - 1) & 1, p.err, abort_flag);
       mbar_wait(smem_addr(&S.full[st]), st_phase, p.err, abort_flag);
       const int ntok = min(kBlock, L - cur.j * kBlock);
+      const int fslot = S.fused_slot[st];
+      if (fslot >= 0 && lane == 0) {
+        // fused scatter: this kv head's slice of the new key row to its slot
+        bulk_s2g(reinterpret_cast<unsigned char*>(const_cast<void*>(p.k_cache)) +
+                     (size_t)fslot * ROW + g * D * ES,
+                 smem_addr(stage + (ntok - 1) * ROW + g * D * ES), D * ES);
+        bulk_commit();
+        stored = true;
+      }
       float sc[NIT_QK];
       const float* ksc = reinterpret_cast<const float*>(stage + ks_off);
       if (ntok == kBlock)
@@ -497,12 +544,13 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
       }
       __syncwarp();
       if (lane == 0) {
+        if (fslot >= 0) bulk_wait_read();  // the store has read the stage
         mbar_arrive(smem_addr(&S.p_full[g][b]));
         // release the stage; the last warp out refills it NST pages ahead
         if (atomicAdd(&S.released[st], 1) == NW - 1) {
           S.released[st] = 0;
           if (i + NST < n_pages && !*abort_flag) {
-            fetch_page(p, fc, smem_addr(stage), smem_addr(&S.full[st]));
+            fetch_page(p, fc, smem_addr(stage), smem_addr(&S.full[st]), &S.fused_slot[st]);
             S.last_issued[st] = i + NST;
           }
         }
@@ -517,11 +565,13 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
         load_q(cur.s);
       }
     }
+    if (stored) bulk_wait_all();  // the stores are complete before the CTA exits
   } else {
     // ================================================================ PV warp
     const int tok_lane = lane / LPT_PV;
     const int dl = lane % LPT_PV;
     float2 acc[G][4];
+    bool stored = false;  // this lane issued fused-scatter stores
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
@@ -536,8 +586,17 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
     for (int i = 0; i < n_pages; ++i) {
       const int b = i & 1;
       mbar_wait(smem_addr(&S.full[st]), st_phase, p.err, abort_flag);
-      mbar_wait(smem_addr(&S.p_full[g][b]), (i >> 1) & 1, p.err, abort_flag);
       const int ntok = min(kBlock, L - cur.j * kBlock);
+      const int fslot = S.fused_slot[st];
+      if (fslot >= 0 && lane == 0) {
+        // fused scatter: this kv head's slice of the new value row to its slot
+        bulk_s2g(reinterpret_cast<unsigned char*>(const_cast<void*>(p.v_cache)) +
+                     (size_t)fslot * ROW + g * D * ES,
+                 smem_addr(stage + p.page_bytes + (ntok - 1) * ROW + g * D * ES), D * ES);
+        bulk_commit();
+        stored = true;
+      }
+      mbar_wait(smem_addr(&S.p_full[g][b]), (i >> 1) & 1, p.err, abort_flag);
       const PBuf<G>& pb = S.pb[g][b];
       const uint32_t pb_addr = smem_addr(&pb);
       float al[G];
@@ -565,11 +624,12 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
       }
       __syncwarp();
       if (lane == 0) {
+        if (fslot >= 0) bulk_wait_read();  // the store has read the stage
         mbar_arrive(smem_addr(&S.p_empty[g][b]));
         if (atomicAdd(&S.released[st], 1) == NW - 1) {
           S.released[st] = 0;
           if (i + NST < n_pages && !*abort_flag) {
-            fetch_page(p, fc, smem_addr(stage), smem_addr(&S.full[st]));
+            fetch_page(p, fc, smem_addr(stage), smem_addr(&S.full[st]), &S.fused_slot[st]);
             S.last_issued[st] = i + NST;
           }
         }
@@ -637,6 +697,7 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
         seg_j0 = 0;
       }
     }
+    if (stored) bulk_wait_all();  // the stores are complete before the CTA exits
   }
 
   // never hand back shared memory with a copy still landing in it
@@ -779,6 +840,9 @@ cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ct
   p.v_cache = a.v_cache;
   p.k_scale = a.k_scale;
   p.v_scale = a.v_scale;
+  p.k_new = a.fuse_k_new;
+  p.v_new = a.fuse_v_new;
+  p.slot_mapping = a.fuse_slot_mapping;
   p.block_tables = a.block_tables;
   p.seq_lens = a.seq_lens;
   p.qsl = a.query_start_loc;

@@ -8,7 +8,8 @@
 // graph: one launch replaces the three to five kernel launches of the step
 // and the per-step metadata can ride in with one host-to-device copy node.
 // The captured calls are the library's own public entry points, so the graph
-// checks and computes exactly what those calls do.
+// checks and computes exactly what those calls do; a graph whose steps have
+// decode rows only (max_q_len 1) runs scatter + attention as pa_decode_step.
 #include <cuda_runtime.h>
 
 #include <new>
@@ -42,14 +43,25 @@ int record_step(const pa_step_buffers& b, cudaStream_t s) {
                         b.head_dim, b.copy_pairs, b.max_pairs, s);
     if (st) return st;
   }
-  st = pa_reshape_and_cache(b.k_new, b.v_new, b.max_tokens, b.k_cache, b.v_cache, b.num_blocks,
-                            b.block_size, b.num_kv_heads, b.head_dim, b.slot_mapping, s);
-  if (st) return st;
-  st = pa_paged_attention(b.q, b.k_cache, b.v_cache, b.num_blocks, b.block_size, b.num_q_heads,
-                          b.num_kv_heads, b.head_dim, b.block_tables, b.max_blocks, b.seq_lens,
-                          b.query_start_loc, b.max_seqs, b.max_tokens, b.max_q_len,
-                          b.max_seq_len, b.scale, b.out, b.workspace, b.workspace_bytes, s);
-  if (st) return st;
+  if (b.max_q_len <= 1) {
+    // decode rows only: scatter and attention in one kernel
+    st = pa_decode_step(b.q, b.k_new, b.v_new, b.k_cache, b.v_cache, b.num_blocks, b.block_size,
+                        b.num_q_heads, b.num_kv_heads, b.head_dim, b.block_tables, b.max_blocks,
+                        b.seq_lens, b.query_start_loc, b.max_seqs, b.max_tokens, b.max_seq_len,
+                        b.slot_mapping, b.scale, b.out, b.workspace, b.workspace_bytes, s);
+    if (st) return st;
+  } else {
+    st = pa_reshape_and_cache(b.k_new, b.v_new, b.max_tokens, b.k_cache, b.v_cache,
+                              b.num_blocks, b.block_size, b.num_kv_heads, b.head_dim,
+                              b.slot_mapping, s);
+    if (st) return st;
+    st = pa_paged_attention(b.q, b.k_cache, b.v_cache, b.num_blocks, b.block_size,
+                            b.num_q_heads, b.num_kv_heads, b.head_dim, b.block_tables,
+                            b.max_blocks, b.seq_lens, b.query_start_loc, b.max_seqs,
+                            b.max_tokens, b.max_q_len, b.max_seq_len, b.scale, b.out,
+                            b.workspace, b.workspace_bytes, s);
+    if (st) return st;
+  }
   if (b.host_out) {
     cudaError_t e = cudaMemcpyAsync(b.host_out, b.out, b.out_copy_bytes, cudaMemcpyDeviceToHost,
                                     s);

@@ -22,6 +22,12 @@ struct AttnArgs {
   const float* k_scale;    // fp8: one scale per (slot, kv head); else null
   const float* v_scale;
   bool fp8;
+  // Fused scatter (decode-only steps over the bf16 cache): the decode kernel
+  // takes each decode request's new row from these and stores it to its
+  // slot; all null when the scatter ran as its own kernel.
+  const uint16_t* fuse_k_new;
+  const uint16_t* fuse_v_new;
+  const int32_t* fuse_slot_mapping;
   int32_t num_blocks;
   int32_t num_q_heads;
   int32_t num_kv_heads;

@@ -78,6 +78,9 @@ def _load() -> ctypes.CDLL:
     L.pa_paged_attention_qrange.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, vp, vp,
                                             i32, i32, i32, i32, i32, f32, vp, vp, sz, vp]
     L.pa_paged_attention_qrange.restype = ctypes.c_int
+    L.pa_decode_step.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, vp, vp,
+                                 i32, i32, i32, vp, f32, vp, vp, sz, vp]
+    L.pa_decode_step.restype = ctypes.c_int
     L.pa_copy_blocks.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, vp]
     L.pa_swap_staging_bytes.argtypes = [i32, i32, i32, i32]
     L.pa_swap_staging_bytes.restype = sz
@@ -244,6 +247,37 @@ def paged_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
                                 seq_lens.data_ptr(), query_start_loc.data_ptr(), S, T,
                                 int(max_q_len), int(max_seq_len), float(scale), out.data_ptr(),
                                 workspace.data_ptr(), workspace.numel(), _stream(stream)))
+    return out
+
+
+def decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                seq_lens: torch.Tensor, query_start_loc: torch.Tensor,
+                slot_mapping: torch.Tensor, scale: float, *, max_seq_len: int,
+                out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+    """reshape_and_cache + paged_attention of a decode-only step in one kernel
+    (pa_decode_step).  Returns ``out``."""
+    L = _load()
+    for name, t, dim in (("q", q, 3), ("k_new", k_new, 3), ("v_new", v_new, 3),
+                         ("k_cache", k_cache, 4), ("v_cache", v_cache, 4)):
+        _need(t, name, torch.bfloat16, dim)
+    for name, t in (("block_tables", block_tables), ("seq_lens", seq_lens),
+                    ("query_start_loc", query_start_loc), ("slot_mapping", slot_mapping)):
+        _need(t, name, torch.int32)
+    T, nq, d = q.shape
+    nb, bs, nkv, _ = k_cache.shape
+    S = seq_lens.shape[0]
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = alloc_workspace(S, T, nq, nkv, d, 1, max_seq_len, q.device)
+    _check(L.pa_decode_step(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                            k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, nq, nkv, d,
+                            block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),
+                            query_start_loc.data_ptr(), S, T, int(max_seq_len),
+                            slot_mapping.data_ptr(), float(scale), out.data_ptr(),
+                            workspace.data_ptr(), workspace.numel(), _stream(stream)))
     return out
 
 

@@ -185,3 +185,57 @@ def test_one_long_request_over_every_cta(lens):
     else:
         _, _, ref = run_oracle_step(b)
         assert_attn_close(to_f64(out), ref, f"lens={lens}")
+
+
+@pytest.mark.parametrize("lens,nq,nkv,d,bs", [
+    ([1, 2, 15, 16, 17, 33, 300], 32, 8, 128, 16),   # first row of a page, page edges
+    (None, 32, 8, 128, 16),                          # the decode batch
+    ([257, 1000, 40], 8, 2, 64, 16),
+    ([31, 32, 33, 500], 32, 8, 128, 32),              # 32-token blocks
+])
+def test_fused_decode_step_equals_scatter_then_attention(lens, nq, nkv, d, bs):
+    """pa_decode_step (the new rows taken into the page in shared memory and
+    stored from there) gives the same output bits and the same cache bits as
+    pa_reshape_and_cache followed by pa_paged_attention."""
+    if lens is None:
+        b = W.decode_batch(seed=21)
+    else:
+        nb = sum(-(-L // bs) for L in lens) + 5
+        b = W.make_batch("fused", lens, [1] * len(lens), num_q_heads=nq, num_kv_heads=nkv,
+                         head_dim=d, block_size=bs, num_blocks=nb, seed=len(lens))
+    d1, out1 = run_gpu_step(b)
+    d2 = W.to_device(b)
+    out2 = torch.full_like(d2.q, float("nan"))
+    ops.decode_step(d2.q, d2.k_new, d2.v_new, d2.k_cache, d2.v_cache, d2.block_tables,
+                    d2.seq_lens, d2.query_start_loc, d2.slot_mapping, b.scale,
+                    max_seq_len=b.max_seq_len, out=out2)
+    ops.check_device_errors()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(d1.k_cache.view(torch.int16), d2.k_cache.view(torch.int16))
+    assert torch.equal(d1.v_cache.view(torch.int16), d2.v_cache.view(torch.int16))
+
+
+def test_fused_decode_step_slot_rules():
+    """A negative slot leaves the row unwritten and reads the cache's row (as
+    a separate scatter that skips it would); a slot that is not the last
+    position's slot is flagged."""
+    b = _decode([40, 70], nq=8, nkv=2, d=64, seed=3)
+    b.slot_mapping = b.slot_mapping.copy()
+    b.slot_mapping[1] = -1
+    d1, out1 = run_gpu_step(b)
+    d2 = W.to_device(b)
+    out2 = ops.decode_step(d2.q, d2.k_new, d2.v_new, d2.k_cache, d2.v_cache, d2.block_tables,
+                           d2.seq_lens, d2.query_start_loc, d2.slot_mapping, b.scale,
+                           max_seq_len=b.max_seq_len)
+    ops.check_device_errors()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(d1.k_cache.view(torch.int16), d2.k_cache.view(torch.int16))
+    bad = b.slot_mapping.copy()
+    bad[0] = bad[0] - 1 if bad[0] > 0 else bad[0] + 1
+    d3 = W.to_device(b)
+    ops.decode_step(d3.q, d3.k_new, d3.v_new, d3.k_cache, d3.v_cache, d3.block_tables,
+                    d3.seq_lens, d3.query_start_loc, W.int32_tensor(bad, "cuda"), b.scale,
+                    max_seq_len=b.max_seq_len)
+    with pytest.raises(ops.PagedAttnError) as ei:
+        ops.check_device_errors()
+    assert ei.value.code == 4
