@@ -112,4 +112,8 @@ def test_step_graph_argument_checks_without_gpu():
     assert b"copy_pairs" in L.pa_get_last_error()
     assert L.pa_step_graph_destroy(None) == 0
     assert _status(L.pa_selftest_wait_timeout(0, None)) == "PA_ERR_INVALID_ARG"
+    # the fused decode step needs its slot_mapping
+    assert _status(L.pa_decode_step(None, None, None, None, None, 32, 16, 4, 2, 64, None, 3,
+                                    None, None, 4, 4, 48, None, ctypes.c_float(0.125), None,
+                                    None, 0, None)) == "PA_ERR_INVALID_ARG"
     assert _status(L.pa_selftest_wait_timeout(2_000_000_000, None)) == "PA_ERR_INVALID_ARG"

@@ -213,6 +213,9 @@ def test_fused_decode_step_equals_scatter_then_attention(lens, nq, nkv, d, bs):
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
     assert torch.equal(d1.k_cache.view(torch.int16), d2.k_cache.view(torch.int16))
     assert torch.equal(d1.v_cache.view(torch.int16), d2.v_cache.view(torch.int16))
+    kc, vc, ref = run_oracle_step(b)
+    assert np.array_equal(W.bits_of(d2.k_cache), kc) and np.array_equal(W.bits_of(d2.v_cache), vc)
+    assert_attn_close(to_f64(out2), ref, "fused decode step")
 
 
 def test_fused_decode_step_slot_rules():
