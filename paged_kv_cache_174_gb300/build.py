@@ -22,8 +22,8 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libpagedattn.so"
 LIB = os.path.join(OUT_DIR, LIB_NAME)
 
-SOURCES = ["pa_api.cu", "pa_cache.cu", "pa_decode.cu", "pa_decode_fp8.cu", "pa_prefill.cu",
-           "pa_graph.cu"]
+SOURCES = ["pa_api.cu", "pa_cache.cu", "pa_decode.cu", "pa_decode_fp8.cu", "pa_decode_fused.cu",
+           "pa_prefill.cu", "pa_graph.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -36,7 +36,8 @@ bool decode_supported(int head_dim, int group, int num_kv_heads) {
 cudaError_t launch_decode(const AttnArgs& a, const DecodeWorkspace& ws, int ctas,
                           cudaStream_t stream) {
   if (a.fp8) return launch_decode_fp8(a, ws, ctas, stream);
-  return launch_decode_any<false>(a, ws, ctas, stream);
+  if (a.fuse_slot_mapping) return launch_decode_fused(a, ws, ctas, stream);
+  return launch_decode_any<false, false>(a, ws, ctas, stream);
 }
 
 }  // namespace pa

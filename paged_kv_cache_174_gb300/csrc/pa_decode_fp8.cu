@@ -8,7 +8,7 @@ namespace pa {
 
 cudaError_t launch_decode_fp8(const AttnArgs& a, const DecodeWorkspace& ws, int ctas,
                               cudaStream_t stream) {
-  return launch_decode_any<true>(a, ws, ctas, stream);
+  return launch_decode_any<true, false>(a, ws, ctas, stream);
 }
 
 }  // namespace pa

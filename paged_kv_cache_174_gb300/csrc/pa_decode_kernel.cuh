@@ -131,6 +131,7 @@ struct PageCursor {
 
 // Issue the bulk copies of page (c.s, c.j) into a stage.  *fused_slot gets the
 // slot the stage's last row must be stored to (fused scatter), or -1.
+template <bool FUSE>
 __device__ __forceinline__ void fetch_page(const DecodeParams& p, const PageCursor& c,
                                            uint32_t stage_smem, uint32_t full_bar,
                                            int* fused_slot) {
@@ -149,7 +150,7 @@ __device__ __forceinline__ void fetch_page(const DecodeParams& p, const PageCurs
   // 16-token page index in the pool: a block of 32 tokens is two pages
   const size_t page = ((size_t)phys << p.block_shift) + (c.j & ((1 << p.block_shift) - 1));
   const size_t off = page * p.page_bytes;
-  if (p.slot_mapping && c.j == c.np - 1) {
+  if (FUSE && c.j == c.np - 1) {
     // the request's new token (position L - 1, last row of this page) comes
     // from k_new / v_new instead of the cache, which does not hold it yet
     const int a = __ldg(p.qsl + c.s);
@@ -343,7 +344,8 @@ __device__ __forceinline__ void pv_accumulate(const unsigned char* vb, const flo
 // Warps 0..NKV-1 compute scores and the softmax (QK warps), warps
 // NKV..2*NKV-1 accumulate p * V (PV warps); warp g and warp NKV + g serve kv
 // head g and hand over p through a double-buffered slot in shared memory.
-template <int D, int G, int NKV, bool F8>
+// F8: 8-bit cache; FUSE: decode-only step with the scatter done here (bf16).
+template <int D, int G, int NKV, bool F8, bool FUSE>
 __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodeParams p) {
   constexpr int NW = 2 * NKV;
   // QK lanes: E_QK head_dim elements each (two 16-byte pieces when 16)
@@ -430,7 +432,7 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
       if (found_s >= 0) {
         PageCursor fc{found_s, found_j, decode_pages(p, found_s, false)};
         for (int i = 0; i < NST && i < n_pages; ++i) {
-          fetch_page(p, fc, smem_addr(stages + (size_t)i * p.stage_bytes),
+          fetch_page<FUSE>(p, fc, smem_addr(stages + (size_t)i * p.stage_bytes),
                      smem_addr(&S.full[i]), &S.fused_slot[i]);
           S.last_issued[i] = i;
           fc.next(p);
@@ -493,8 +495,8 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
       if (i >= 2) mbar_wait(smem_addr(&S.p_empty[g][b]), ((i >> 1) - 1) & 1, p.err, abort_flag);
       mbar_wait(smem_addr(&S.full[st]), st_phase, p.err, abort_flag);
       const int ntok = min(kBlock, L - cur.j * kBlock);
-      const int fslot = S.fused_slot[st];
-      if (fslot >= 0 && lane == 0) {
+      const int fslot = FUSE ? S.fused_slot[st] : -1;
+      if (FUSE && fslot >= 0 && lane == 0) {
         // fused scatter: this kv head's slice of the new key row to its slot
         bulk_s2g(reinterpret_cast<unsigned char*>(const_cast<void*>(p.k_cache)) +
                      (size_t)fslot * ROW + g * D * ES,
@@ -544,13 +546,14 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
       }
       __syncwarp();
       if (lane == 0) {
-        if (fslot >= 0) bulk_wait_read();  // the store has read the stage
+        if (FUSE && fslot >= 0) bulk_wait_read();  // the store has read the stage
         mbar_arrive(smem_addr(&S.p_full[g][b]));
         // release the stage; the last warp out refills it NST pages ahead
         if (atomicAdd(&S.released[st], 1) == NW - 1) {
           S.released[st] = 0;
           if (i + NST < n_pages && !*abort_flag) {
-            fetch_page(p, fc, smem_addr(stage), smem_addr(&S.full[st]), &S.fused_slot[st]);
+            fetch_page<FUSE>(p, fc, smem_addr(stage), smem_addr(&S.full[st]),
+                             &S.fused_slot[st]);
             S.last_issued[st] = i + NST;
           }
         }
@@ -565,7 +568,7 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
         load_q(cur.s);
       }
     }
-    if (stored) bulk_wait_all();  // the stores are complete before the CTA exits
+    if (FUSE && stored) bulk_wait_all();  // the stores are complete before the CTA exits
   } else {
     // ================================================================ PV warp
     const int tok_lane = lane / LPT_PV;
@@ -587,8 +590,8 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
       const int b = i & 1;
       mbar_wait(smem_addr(&S.full[st]), st_phase, p.err, abort_flag);
       const int ntok = min(kBlock, L - cur.j * kBlock);
-      const int fslot = S.fused_slot[st];
-      if (fslot >= 0 && lane == 0) {
+      const int fslot = FUSE ? S.fused_slot[st] : -1;
+      if (FUSE && fslot >= 0 && lane == 0) {
         // fused scatter: this kv head's slice of the new value row to its slot
         bulk_s2g(reinterpret_cast<unsigned char*>(const_cast<void*>(p.v_cache)) +
                      (size_t)fslot * ROW + g * D * ES,
@@ -624,12 +627,13 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
       }
       __syncwarp();
       if (lane == 0) {
-        if (fslot >= 0) bulk_wait_read();  // the store has read the stage
+        if (FUSE && fslot >= 0) bulk_wait_read();  // the store has read the stage
         mbar_arrive(smem_addr(&S.p_empty[g][b]));
         if (atomicAdd(&S.released[st], 1) == NW - 1) {
           S.released[st] = 0;
           if (i + NST < n_pages && !*abort_flag) {
-            fetch_page(p, fc, smem_addr(stage), smem_addr(&S.full[st]), &S.fused_slot[st]);
+            fetch_page<FUSE>(p, fc, smem_addr(stage), smem_addr(&S.full[st]),
+                             &S.fused_slot[st]);
             S.last_issued[st] = i + NST;
           }
         }
@@ -697,7 +701,7 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
         seg_j0 = 0;
       }
     }
-    if (stored) bulk_wait_all();  // the stores are complete before the CTA exits
+    if (FUSE && stored) bulk_wait_all();  // the stores are complete before the CTA exits
   }
 
   // never hand back shared memory with a copy still landing in it
@@ -831,7 +835,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
 
 constexpr size_t kSmemBudget = 220 * 1024;
 
-template <int D, int G, int NKV, bool F8>
+template <int D, int G, int NKV, bool F8, bool FUSE>
 cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ctas,
                             cudaStream_t stream) {
   DecodeParams p;
@@ -871,7 +875,7 @@ cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ct
   if (nst < 2) return cudaErrorInvalidConfiguration;
   p.nstages = nst;
   const size_t smem = (size_t)nst * p.stage_bytes + fixed;
-  auto kern = decode_kernel<D, G, NKV, F8>;
+  auto kern = decode_kernel<D, G, NKV, F8, FUSE>;
   static int configured_device = -1;  // one attribute set per process and device
   int dev = 0;
   cudaGetDevice(&dev);
@@ -919,32 +923,32 @@ cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ct
                : cudaLaunchKernelEx(&cfg, decode_merge_kernel<D, false>, p);
 }
 
-template <int D, int G, bool F8>
+template <int D, int G, bool F8, bool FUSE>
 cudaError_t launch_decode_dg(const AttnArgs& a, const DecodeWorkspace& ws, int ctas,
                              cudaStream_t stream) {
   switch (a.num_kv_heads) {
-    case 1: return launch_decode_t<D, G, 1, F8>(a, ws, ctas, stream);
-    case 2: return launch_decode_t<D, G, 2, F8>(a, ws, ctas, stream);
-    case 4: return launch_decode_t<D, G, 4, F8>(a, ws, ctas, stream);
-    case 8: return launch_decode_t<D, G, 8, F8>(a, ws, ctas, stream);
+    case 1: return launch_decode_t<D, G, 1, F8, FUSE>(a, ws, ctas, stream);
+    case 2: return launch_decode_t<D, G, 2, F8, FUSE>(a, ws, ctas, stream);
+    case 4: return launch_decode_t<D, G, 4, F8, FUSE>(a, ws, ctas, stream);
+    case 8: return launch_decode_t<D, G, 8, F8, FUSE>(a, ws, ctas, stream);
   }
   return cudaErrorInvalidValue;
 }
 
-template <bool F8>
+template <bool F8, bool FUSE>
 cudaError_t launch_decode_any(const AttnArgs& a, const DecodeWorkspace& ws, int ctas,
                               cudaStream_t stream) {
   const int group = a.num_q_heads / a.num_kv_heads;
   if (a.head_dim == 128) {
-    if (group == 1) return launch_decode_dg<128, 1, F8>(a, ws, ctas, stream);
-    if (group == 2) return launch_decode_dg<128, 2, F8>(a, ws, ctas, stream);
-    if (group == 4) return launch_decode_dg<128, 4, F8>(a, ws, ctas, stream);
-    if (group == 8) return launch_decode_dg<128, 8, F8>(a, ws, ctas, stream);
+    if (group == 1) return launch_decode_dg<128, 1, F8, FUSE>(a, ws, ctas, stream);
+    if (group == 2) return launch_decode_dg<128, 2, F8, FUSE>(a, ws, ctas, stream);
+    if (group == 4) return launch_decode_dg<128, 4, F8, FUSE>(a, ws, ctas, stream);
+    if (group == 8) return launch_decode_dg<128, 8, F8, FUSE>(a, ws, ctas, stream);
   } else if (a.head_dim == 64) {
-    if (group == 1) return launch_decode_dg<64, 1, F8>(a, ws, ctas, stream);
-    if (group == 2) return launch_decode_dg<64, 2, F8>(a, ws, ctas, stream);
-    if (group == 4) return launch_decode_dg<64, 4, F8>(a, ws, ctas, stream);
-    if (group == 8) return launch_decode_dg<64, 8, F8>(a, ws, ctas, stream);
+    if (group == 1) return launch_decode_dg<64, 1, F8, FUSE>(a, ws, ctas, stream);
+    if (group == 2) return launch_decode_dg<64, 2, F8, FUSE>(a, ws, ctas, stream);
+    if (group == 4) return launch_decode_dg<64, 4, F8, FUSE>(a, ws, ctas, stream);
+    if (group == 8) return launch_decode_dg<64, 8, F8, FUSE>(a, ws, ctas, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -76,6 +76,8 @@ cudaError_t launch_decode(const AttnArgs& a, const DecodeWorkspace& ws, int ctas
                           cudaStream_t stream);
 cudaError_t launch_decode_fp8(const AttnArgs& a, const DecodeWorkspace& ws, int ctas,
                               cudaStream_t stream);
+cudaError_t launch_decode_fused(const AttnArgs& a, const DecodeWorkspace& ws, int ctas,
+                                cudaStream_t stream);
 
 bool prefill_supported(int head_dim, int group, int num_kv_heads);
 // How the prefill kernel splits the keys of each query-tile pair, and the
