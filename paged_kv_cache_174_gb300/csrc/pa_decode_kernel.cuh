@@ -295,6 +295,81 @@ __device__ __forceinline__ void qk_scores(const unsigned char* kb, const float* 
   }
 }
 
+// 8-bit cache: q . k of one page on the tensor cores (mma.sync m16n8k16,
+// f16 operands, f32 accumulation).  The MMA rows are the G q heads of the kv
+// group (rows G..15 zero), the columns the page's 16 tokens (two n-tiles of
+// 8), the reduction head_dim.  The reduction order is free, so lane (g, t) =
+// (lane / 4, lane % 4) takes head_dim elements [t * D/4, (t + 1) * D/4) for
+// every k-step: k-step s holds elements t * D/4 + 4s .. + 3, which is one
+// 32-bit word of codes per token -- two f16x2 B registers -- and the same
+// elements of q in its A registers.  E4M3 values are exact in f16.
+__device__ __forceinline__ uint32_t f16x2_from_floats(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t two_codes) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+      : "=r"(r)
+      : "r"(two_codes));
+  return r;
+}
+__device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32_t a2,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_f16_16816_full(float (&c)[4], uint32_t a0, uint32_t a1,
+                                                   uint32_t a2, uint32_t a3, uint32_t b0,
+                                                   uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Scores of one page for one QK warp on the tensor cores: sc[2T + j] is the
+// base-2 score of head lane / 4 for token 8T + 2 (lane % 4) + j (-inf past
+// the page's end).  kb: the page's codes of this kv head (token 0); ksc: the
+// page's key scales of this kv head (token 0; stride n_kv).
+template <int D, int NKV, uint32_t ROW>
+__device__ __forceinline__ void qk_scores_mma(const unsigned char* kb, const float* ksc,
+                                              int ntok, const uint32_t (&qa)[D / 16][2],
+                                              float (&sc)[4], int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  float c[2][4];
+#pragma unroll
+  for (int T = 0; T < 2; ++T) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) c[T][e] = 0.f;
+    // this lane's D/4 codes of token 8T + g
+    const unsigned char* src = kb + (8 * T + g) * ROW + t * (D / 4);
+    uint32_t w[D / 16];
+#pragma unroll
+    for (int v = 0; v < D / 64; ++v) {
+      const uint4 x = *reinterpret_cast<const uint4*>(src + 16 * v);
+      w[4 * v] = x.x, w[4 * v + 1] = x.y, w[4 * v + 2] = x.z, w[4 * v + 3] = x.w;
+    }
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks)
+      mma_f16_16816(c[T], qa[ks][0], qa[ks][1], f16x2_from_e4m3x2(w[ks] & 0xffffu),
+                    f16x2_from_e4m3x2(w[ks] >> 16));
+  }
+#pragma unroll
+  for (int T = 0; T < 2; ++T)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int tok = 8 * T + 2 * t + j;
+      sc[2 * T + j] = tok < ntok ? c[T][j] * ksc[tok * NKV] : kNegInf;
+    }
+}
+
 // p * V of one page for one PV warp: vb points at this lane's 16-byte piece of
 // its first token's value row, pp at p[tok_lane][0] of the page's hand-off.
 //   F8: vb points into the page's codes; vsc at the value scale of this kv
@@ -356,7 +431,6 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
   constexpr int REP_QK = LPT_QK / G;
   // PV lanes: 8 elements (16 bytes) each
   constexpr int LPT_PV = D / 8;
-  constexpr int TPI_PV = 32 / LPT_PV;
   constexpr uint32_t ES = F8 ? 1 : 2;      // bytes per cached element
   constexpr uint32_t ROW = NKV * D * ES;  // bytes of one token row in a page
   static_assert(LPT_QK >= G && LPT_QK % G == 0, "group too large for the lane split");
@@ -461,22 +535,41 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
     const int dl = lane % LPT_QK;
     const int my_h = dl / REP_QK;
     const int rep = dl % REP_QK;
-    float2 qf[G][E_QK / 2];
+    float2 qf[G][E_QK / 2];  // bf16 cache: this lane's slice of q, fp32
+    uint32_t qa[D / 16][2];  // 8-bit cache: MMA A registers of head lane / 4 (see qk_scores_mma)
     float m_run = kNegInf, l_lane = 0.f;
     bool stored = false;  // this lane issued fused-scatter stores
     auto load_q = [&](int seq) {
       const int tok = __ldg(p.qsl + seq);
+      if constexpr (F8) {
+        const int hq = lane >> 2, t = lane & 3;
+        const uint16_t* qrow = p.q + ((int64_t)tok * p.n_q + g * G + (hq < G ? hq : 0)) * D;
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const uint16_t* qrow = p.q + ((int64_t)tok * p.n_q + g * G + h) * D;
-#pragma unroll
-        for (int piece = 0; piece < E_QK / 8; ++piece) {
-          const uint4 w = __ldg(reinterpret_cast<const uint4*>(qrow + piece * (D / 2) + dl * 8));
+        for (int v = 0; v < D / 32; ++v) {  // D/4 elements, 8 per load
+          uint4 w = make_uint4(0u, 0u, 0u, 0u);
+          if (hq < G) w = __ldg(reinterpret_cast<const uint4*>(qrow + t * (D / 4) + 8 * v));
           const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = bf16x2_to_float2(ws[e]);
-            qf[h][piece * 4 + e] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
+          for (int e = 0; e < 4; e += 2) {  // 4 elements = one k-step
+            const float2 f0 = bf16x2_to_float2(ws[e]), f1 = bf16x2_to_float2(ws[e + 1]);
+            qa[2 * v + e / 2][0] = f16x2_from_floats(f0.x * p.scale_log2, f0.y * p.scale_log2);
+            qa[2 * v + e / 2][1] = f16x2_from_floats(f1.x * p.scale_log2, f1.y * p.scale_log2);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const uint16_t* qrow = p.q + ((int64_t)tok * p.n_q + g * G + h) * D;
+#pragma unroll
+          for (int piece = 0; piece < E_QK / 8; ++piece) {
+            const uint4 w =
+                __ldg(reinterpret_cast<const uint4*>(qrow + piece * (D / 2) + dl * 8));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = bf16x2_to_float2(ws[e]);
+              qf[h][piece * 4 + e] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
+            }
           }
         }
       }
@@ -504,44 +597,81 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
         bulk_commit();
         stored = true;
       }
-      float sc[NIT_QK];
-      const float* ksc = reinterpret_cast<const float*>(stage + ks_off);
-      if (ntok == kBlock)
-        qk_scores<D, G, E_QK, LPT_QK, ROW, true, F8, NKV>(stage + k_off, ksc, ntok, tok_lane, qf,
-                                                          sc, lane);
-      else
-        qk_scores<D, G, E_QK, LPT_QK, ROW, false, F8, NKV>(stage + k_off, ksc, ntok, tok_lane,
-                                                           qf, sc, lane);
-      // online softmax (base 2) for head my_h over the page's 16 tokens
-      float mx = sc[0];
-#pragma unroll
-      for (int it = 1; it < NIT_QK; ++it) mx = fmaxf(mx, sc[it]);
-#pragma unroll
-      for (int m = LPT_QK; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-      const float m_new = fmaxf(m_run, mx);
-      const float m_use = (m_new == kNegInf) ? 0.f : m_new;
-      const float alpha = fast_exp2(m_run - m_use);
-      PBuf<G>& pb = S.pb[g][b];
-      float* pw = &pb.p[tok_lane][my_h];
-      float lsum = 0.f;
-#pragma unroll
-      for (int it = 0; it < NIT_QK; ++it) {
-        const float pr = fast_exp2(sc[it] - m_use);
-        lsum += pr;
-        if (rep == 0) pw[it * TPI_QK * G] = pr;
-      }
-      l_lane = l_lane * alpha + lsum;
-      m_run = m_new;
-      if (tok_lane == 0 && rep == 0) pb.alpha[my_h] = alpha;
       const bool seq_done = (cur.j + 1 == cur.np);
       const bool seg_end = seq_done || (i + 1 == n_pages);
-      if (seg_end) {
-        float lt = l_lane;
+      PBuf<G>& pb = S.pb[g][b];
+      if constexpr (F8) {
+        // scores on the tensor cores; lane holds head lane / 4, 4 tokens
+        const int hq = lane >> 2, t = lane & 3;
+        float sc4[4];
+        qk_scores_mma<D, NKV, ROW>(stage + g * D, reinterpret_cast<const float*>(
+                                                      stage + 2 * p.page_bytes + g * 4),
+                                   ntok, qa, sc4, lane);
+        // online softmax (base 2) for head hq over the page's 16 tokens: the
+        // head's 16 scores sit in lanes 4 hq .. 4 hq + 3
+        float mx = fmaxf(fmaxf(sc4[0], sc4[1]), fmaxf(sc4[2], sc4[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run, mx);
+        const float m_use = (m_new == kNegInf) ? 0.f : m_new;
+        const float alpha = fast_exp2(m_run - m_use);
+        float lsum = 0.f;
 #pragma unroll
-        for (int m = LPT_QK; m < 32; m <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, m);
-        if (tok_lane == 0 && rep == 0) {
-          pb.m[my_h] = m_run;
-          pb.l[my_h] = lt;
+        for (int jj = 0; jj < 4; ++jj) {
+          const float pr = fast_exp2(sc4[jj] - m_use);
+          lsum += pr;
+          if (hq < G) pb.p[8 * (jj >> 1) + 2 * t + (jj & 1)][hq] = pr;
+        }
+        l_lane = l_lane * alpha + lsum;
+        m_run = m_new;
+        if (t == 0 && hq < G) pb.alpha[hq] = alpha;
+        if (seg_end) {
+          float lt = l_lane;
+          lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+          lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+          if (t == 0 && hq < G) {
+            pb.m[hq] = m_run;
+            pb.l[hq] = lt;
+          }
+        }
+      } else {
+        float sc[NIT_QK];
+        const float* ksc = reinterpret_cast<const float*>(stage + ks_off);
+        if (ntok == kBlock)
+          qk_scores<D, G, E_QK, LPT_QK, ROW, true, F8, NKV>(stage + k_off, ksc, ntok, tok_lane,
+                                                            qf, sc, lane);
+        else
+          qk_scores<D, G, E_QK, LPT_QK, ROW, false, F8, NKV>(stage + k_off, ksc, ntok,
+                                                             tok_lane, qf, sc, lane);
+        // online softmax (base 2) for head my_h over the page's 16 tokens
+        float mx = sc[0];
+#pragma unroll
+        for (int it = 1; it < NIT_QK; ++it) mx = fmaxf(mx, sc[it]);
+#pragma unroll
+        for (int m = LPT_QK; m < 32; m <<= 1)
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+        const float m_new = fmaxf(m_run, mx);
+        const float m_use = (m_new == kNegInf) ? 0.f : m_new;
+        const float alpha = fast_exp2(m_run - m_use);
+        float* pw = &pb.p[tok_lane][my_h];
+        float lsum = 0.f;
+#pragma unroll
+        for (int it = 0; it < NIT_QK; ++it) {
+          const float pr = fast_exp2(sc[it] - m_use);
+          lsum += pr;
+          if (rep == 0) pw[it * TPI_QK * G] = pr;
+        }
+        l_lane = l_lane * alpha + lsum;
+        m_run = m_new;
+        if (tok_lane == 0 && rep == 0) pb.alpha[my_h] = alpha;
+        if (seg_end) {
+          float lt = l_lane;
+#pragma unroll
+          for (int m = LPT_QK; m < 32; m <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, m);
+          if (tok_lane == 0 && rep == 0) {
+            pb.m[my_h] = m_run;
+            pb.l[my_h] = lt;
+          }
         }
       }
       __syncwarp();
@@ -569,6 +699,153 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
       }
     }
     if (FUSE && stored) bulk_wait_all();  // the stores are complete before the CTA exits
+  } else {
+  if constexpr (F8) {
+    // ============================================ PV warp, 8-bit cache (tensor cores)
+    // O^T [D x heads] += V^T [D x 16 tokens] * P^T [16 tokens x heads] with
+    // mma.sync m16n8k16: the MMA rows are head_dim (16 per tile), the columns
+    // the G heads (columns G..7 zero), the reduction the page's 16 tokens.
+    // Rows are assigned so that a lane reads 4 consecutive codes per token
+    // for a pair of tiles: in tile pair q, lane (r, t) = (lane / 4, lane % 4)
+    // holds rows d = 32q + 4r + {0, 1} (first tile) and + {2, 3} (second);
+    // its accumulators o[2q + u][c] are out element d = 32q + 4r + 2u + (c >> 1)
+    // of head 2t + (c & 1).
+    const int r = lane >> 2, t = lane & 3;
+    float o[D / 16][4];
+#pragma unroll
+    for (int m = 0; m < D / 16; ++m)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) o[m][c] = 0.f;
+    int st = 0, st_phase = 0;
+    const unsigned char* stage = stages;
+    for (int i = 0; i < n_pages; ++i) {
+      const int b = i & 1;
+      mbar_wait(smem_addr(&S.full[st]), st_phase, p.err, abort_flag);
+      const int ntok = min(kBlock, L - cur.j * kBlock);
+      mbar_wait(smem_addr(&S.p_full[g][b]), (i >> 1) & 1, p.err, abort_flag);
+      const PBuf<G>& pb = S.pb[g][b];
+      // rescale the running output of heads 2t, 2t + 1
+      const float a0 = 2 * t < G ? pb.alpha[2 * t] : 1.f;
+      const float a1 = 2 * t + 1 < G ? pb.alpha[2 * t + 1] : 1.f;
+#pragma unroll
+      for (int m = 0; m < D / 16; ++m) {
+        o[m][0] *= a0, o[m][1] *= a1, o[m][2] *= a0, o[m][3] *= a1;
+      }
+      // B = P^T scaled by each token's value scale and by 2^9, which keeps
+      // p * scale (scale = row max / 448) in the normal range of f16 for row
+      // maxima from about 1e-3 to 5e4; lane holds tokens 2t, 2t + 1 (b0) and
+      // 2t + 8, 2t + 9 (b1) of head r
+      const float* vsc = reinterpret_cast<const float*>(stage + 2 * p.page_bytes +
+                                                        p.scale_bytes + g * 4);
+      float pv[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int tok = 2 * t + (k & 1) + 8 * (k >> 1);
+        pv[k] = (r < G && tok < ntok) ? pb.p[tok][r < G ? r : 0] * (vsc[tok * NKV] * 512.f)
+                                      : 0.f;
+      }
+      const uint32_t b0 = f16x2_from_floats(pv[0], pv[1]);
+      const uint32_t b1 = f16x2_from_floats(pv[2], pv[3]);
+      // A = V^T: codes of tokens 2t, 2t + 1, 2t + 8, 2t + 9 at d = 32q + 4r .. + 3
+      const unsigned char* vb = stage + p.page_bytes + g * D + 4 * r;
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t x[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int tok = 2 * t + (k & 1) + 8 * (k >> 1);
+          // rows past the page's end hold stale codes; their P is 0, but a
+          // stale NaN code would still poison the product: read token 0
+          x[k] = *reinterpret_cast<const uint32_t*>(vb + (tok < ntok ? tok : 0) * ROW + 32 * q);
+        }
+        // first tile: d + {0, 1}; second: d + {2, 3}; tokens (k0, k1) in the
+        // low/high byte of each code pair
+        uint32_t lo01, hi01, lo23, hi23;
+        asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(lo01) : "r"(x[0]), "r"(x[1]));
+        asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(hi01) : "r"(x[0]), "r"(x[1]));
+        asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(lo23) : "r"(x[2]), "r"(x[3]));
+        asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(hi23) : "r"(x[2]), "r"(x[3]));
+        // tile 2q: rows (d, d + 1) -> A regs {row r: d}, {row r + 8: d + 1}
+        mma_f16_16816_full(o[2 * q], f16x2_from_e4m3x2(lo01 & 0xffffu),
+                           f16x2_from_e4m3x2(lo01 >> 16), f16x2_from_e4m3x2(lo23 & 0xffffu),
+                           f16x2_from_e4m3x2(lo23 >> 16), b0, b1);
+        mma_f16_16816_full(o[2 * q + 1], f16x2_from_e4m3x2(hi01 & 0xffffu),
+                           f16x2_from_e4m3x2(hi01 >> 16), f16x2_from_e4m3x2(hi23 & 0xffffu),
+                           f16x2_from_e4m3x2(hi23 >> 16), b0, b1);
+      }
+      const bool seq_done = (cur.j + 1 == cur.np);
+      const bool seg_end = seq_done || (i + 1 == n_pages);
+      float m_fin[2] = {0.f, 0.f}, l_fin[2] = {1.f, 1.f};
+      if (seg_end) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          if (2 * t + c < G) m_fin[c] = pb.m[2 * t + c], l_fin[c] = pb.l[2 * t + c];
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_addr(&S.p_empty[g][b]));
+        if (atomicAdd(&S.released[st], 1) == NW - 1) {
+          S.released[st] = 0;
+          if (i + NST < n_pages && !*abort_flag) {
+            fetch_page<FUSE>(p, fc, smem_addr(stage), smem_addr(&S.full[st]),
+                             &S.fused_slot[st]);
+            S.last_issued[st] = i + NST;
+          }
+        }
+        fc.next(p);
+      }
+      stage += p.stage_bytes;
+      if (++st == NST) st = 0, st_phase ^= 1, stage = stages;
+      if (seg_end) {
+        const int tok = __ldg(p.qsl + cur.s);
+        const bool whole = (seg_j0 == 0) && seq_done;
+        const int slot = 2 * c + (cur.s == s_begin ? 0 : 1);
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int h = 2 * t + cc;
+          if (h >= G) continue;
+          const int qh = g * G + h;
+          const float inv = 1.f / l_fin[cc];
+#pragma unroll
+          for (int m = 0; m < D / 16; ++m) {
+            const int d = 32 * (m >> 1) + 4 * r + 2 * (m & 1);
+            // elements d, d + 1, the 2^9 of B taken out (exact)
+            const float v0 = o[m][cc] * (1.f / 512.f), v1 = o[m][2 + cc] * (1.f / 512.f);
+            if (whole) {
+              *reinterpret_cast<uint32_t*>(p.out + ((int64_t)tok * p.n_q + qh) * D + d) =
+                  pack_bf16x2(v0 * inv, v1 * inv);
+            } else {
+              *reinterpret_cast<float2*>(p.part_o + ((int64_t)slot * p.n_q + qh) * D + d) =
+                  make_float2(v0, v1);
+            }
+          }
+          if (!whole && r == 0) {
+            p.part_ml[((int64_t)slot * p.n_q + qh) * 2 + 0] = m_fin[cc];
+            p.part_ml[((int64_t)slot * p.n_q + qh) * 2 + 1] = l_fin[cc];
+          }
+        }
+        if (g == 0 && lane == 0 && seg_j0 == 0) {
+          // this CTA owns the request's first page: record where its pieces are
+          int c_last = c;
+          if (!seq_done) {
+            const int64_t f_last = f0 + i + (cur.np - 1 - cur.j);
+            const int64_t cl = ((f_last + 1) * C + F - 1) / F - 1;
+            c_last = (int)(cl < C - 1 ? cl : C - 1);
+          }
+          p.seq_rec[cur.s] = make_int4(c, c_last, slot, (int)F);
+        }
+#pragma unroll
+        for (int m = 0; m < D / 16; ++m)
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) o[m][cc] = 0.f;
+      }
+      const int prev_s = cur.s;
+      cur.next(p);
+      if (seg_end && cur.s != prev_s && i + 1 < n_pages) {
+        L = __ldg(p.seq_lens + cur.s);
+        seg_j0 = 0;
+      }
+    }
   } else {
     // ================================================================ PV warp
     const int tok_lane = lane / LPT_PV;
@@ -703,7 +980,7 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
     }
     if (FUSE && stored) bulk_wait_all();  // the stores are complete before the CTA exits
   }
-
+  }
   // never hand back shared memory with a copy still landing in it
   __syncthreads();
   if (threadIdx.x == 0) {
