@@ -31,6 +31,7 @@
 //  * Online softmax per page in base 2 (q is pre-scaled by scale * log2 e),
 //    fp32 accumulation with packed fp32x2 FMAs.
 #pragma once
+#include <type_traits>
 
 #include <cstdint>
 #include <cfloat>
@@ -115,6 +116,20 @@ struct DecodeSmem {
   int plan[2];
   int abort_flag;
 };
+
+// 8-bit cache: running state of the odd-page warp of one kv head at the end
+// of a segment, read by the even-page warp (after the stage ring and DecodeSmem).
+template <int G, int D>
+struct Comb {
+  float o[G][D];  // unnormalised output of the odd pages
+  float m[2][G];  // running max per page parity
+  float l[2][G];  // running sum per page parity
+};
+
+template <int G, int NKV>
+__host__ __device__ constexpr size_t comb_offset() {
+  return (sizeof(DecodeSmem<G, NKV>) + 15) / 16 * 16;
+}
 
 // Walks the flat page list of the decode requests: (request s, page j).
 struct PageCursor {
@@ -308,12 +323,13 @@ __device__ __forceinline__ uint32_t f16x2_from_floats(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-__device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t two_codes) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
-      : "=r"(r)
-      : "r"(two_codes));
-  return r;
+// Four E4M3 codes -> two f16 pairs: lo gets codes 0, 1 (bytes 0, 1 of w),
+// hi codes 2, 3.
+__device__ __forceinline__ void f16x2x2_from_e4m3x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 __device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32_t a2,
                                               uint32_t b0, uint32_t b1) {
@@ -324,6 +340,16 @@ __device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32
       : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ uint32_t chunk_word(const uint4& x, int q) {
+  return q == 0 ? x.x : q == 1 ? x.y : q == 2 ? x.z : x.w;
+}
+__device__ __forceinline__ uint32_t chunk_word(const uint2& x, int q) {
+  return q == 0 ? x.x : x.y;
+}
+// Barrier over the `threads` threads (whole warps) that name barrier `id`.
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 __device__ __forceinline__ void mma_f16_16816_full(float (&c)[4], uint32_t a0, uint32_t a1,
                                                    uint32_t a2, uint32_t a3, uint32_t b0,
                                                    uint32_t b1) {
@@ -334,10 +360,14 @@ __device__ __forceinline__ void mma_f16_16816_full(float (&c)[4], uint32_t a0, u
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Scores of one page for one QK warp on the tensor cores: sc[2T + j] is the
+// Scores of one page on the tensor cores (8-bit cache): sc[2T + j] is the
 // base-2 score of head lane / 4 for token 8T + 2 (lane % 4) + j (-inf past
 // the page's end).  kb: the page's codes of this kv head (token 0); ksc: the
-// page's key scales of this kv head (token 0; stride n_kv).
+// page's key scales of this kv head (token 0; stride n_kv).  The product is
+// S^T = K Q^T per 8-token tile with m16n8k16: rows the heads (q in A, rows
+// G.. zero), columns the tokens, the reduction head_dim; lane (r, t) takes
+// its k-steps from head_dim chunk [t D/4, (t + 1) D/4) so that one 32-bit
+// word of codes is one k-step.
 template <int D, int NKV, uint32_t ROW>
 __device__ __forceinline__ void qk_scores_mma(const unsigned char* kb, const float* ksc,
                                               int ntok, const uint32_t (&qa)[D / 16][2],
@@ -358,8 +388,11 @@ __device__ __forceinline__ void qk_scores_mma(const unsigned char* kb, const flo
     }
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks)
-      mma_f16_16816(c[T], qa[ks][0], qa[ks][1], f16x2_from_e4m3x2(w[ks] & 0xffffu),
-                    f16x2_from_e4m3x2(w[ks] >> 16));
+    {
+      uint32_t b0, b1;
+      f16x2x2_from_e4m3x4(w[ks], b0, b1);
+      mma_f16_16816(c[T], qa[ks][0], qa[ks][1], b0, b1);
+    }
   }
 #pragma unroll
   for (int T = 0; T < 2; ++T)
@@ -439,6 +472,8 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
   using Smem = DecodeSmem<G, NKV>;
   unsigned char* stages = smem_raw;
   Smem& S = *reinterpret_cast<Smem*>(smem_raw + (size_t)p.nstages * p.stage_bytes);
+  Comb<G, D>* comb = reinterpret_cast<Comb<G, D>*>(
+      smem_raw + (size_t)p.nstages * p.stage_bytes + comb_offset<G, NKV>());
   __shared__ long long red[NW];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -529,6 +564,240 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
   int L = __ldg(p.seq_lens + cur.s);
   int seg_j0 = j_begin;
 
+  if constexpr (F8) {
+    // ======================================================= 8-bit cache
+    // One warp computes a page's scores, its softmax and p * V for all G heads
+    // of its kv head, keeping p in registers: the score fragment of the q * k
+    // product (head r = lane / 4, tokens 2t, 2t + 1, 2t + 8, 2t + 9 with
+    // t = lane % 4) is exactly the B fragment of the p * V product.  Warp g
+    // and warp NKV + g serve kv head g and take the even and the odd pages;
+    // at the end of each segment (a request's pages in this CTA) the odd-page
+    // warp hands its running state to the even-page warp through shared
+    // memory, which merges and writes.
+    //
+    // p * V is O^T [D x heads] += V^T [D x 16 tokens] * P^T [16 tokens x heads]
+    // (mma.sync m16n8k16, f16 in, f32 accumulate): MMA rows are head_dim,
+    // columns heads (G..7 unused), the reduction the page's tokens.  Rows
+    // are assigned so that lane r reads one contiguous run of D/8 codes per
+    // token: in tile pair q the first tile holds d = r D/8 + 4q + {0, 1} in
+    // rows (r, r + 8), the second d + {2, 3}; accumulator o[2q + u][c] is
+    // element r D/8 + 4q + 2u + (c >> 1) of head 2t + (c & 1).
+    const int rho = is_qk ? 0 : 1;  // page parity served
+    const int r = lane >> 2, t = lane & 3;
+    constexpr int DW = D / 32;      // 4-byte words of codes per lane and token
+    using Chunk = typename std::conditional<DW == 4, uint4, uint2>::type;
+    uint32_t qa[D / 16][2];         // A registers of q for head r (see qk_scores_mma)
+    float o[D / 16][4];
+    float m_run = kNegInf, l_lane = 0.f;
+    auto load_q = [&](int seq) {
+      const int tok = __ldg(p.qsl + seq);
+      const uint16_t* qrow = p.q + ((int64_t)tok * p.n_q + g * G + (r < G ? r : 0)) * D;
+#pragma unroll
+      for (int v = 0; v < D / 32; ++v) {  // D/4 elements, 8 per load
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (r < G) w = __ldg(reinterpret_cast<const uint4*>(qrow + t * (D / 4) + 8 * v));
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {  // 4 elements = one k-step
+          const float2 f0 = bf16x2_to_float2(ws[e]), f1 = bf16x2_to_float2(ws[e + 1]);
+          qa[2 * v + e / 2][0] = f16x2_from_floats(f0.x * p.scale_log2, f0.y * p.scale_log2);
+          qa[2 * v + e / 2][1] = f16x2_from_floats(f1.x * p.scale_log2, f1.y * p.scale_log2);
+        }
+      }
+    };
+    load_q(cur.s);
+#pragma unroll
+    for (int m = 0; m < D / 16; ++m)
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) o[m][cc] = 0.f;
+    Comb<G, D>& cb = comb[g];
+    int st = 0, st_phase = 0;
+    const unsigned char* stage = stages;
+    for (int i = 0; i < n_pages; ++i) {
+      const bool seq_done = (cur.j + 1 == cur.np);
+      const bool seg_end = seq_done || (i + 1 == n_pages);
+      if ((i & 1) == rho) {
+        mbar_wait(smem_addr(&S.full[st]), st_phase, p.err, abort_flag);
+        const int ntok = min(kBlock, L - cur.j * kBlock);
+        // Scores from the key codes; value codes of tokens 2t, 2t + 1, 2t + 8,
+        // 2t + 9 at lane r's D/8 head_dim offsets, and their scales, for p * V
+        // (rows past the page's end hold stale codes whose p is 0, but a stale
+        // NaN code would still poison the sum: read token 0 instead).  The
+        // stage is released after p * V: releasing it earlier, with the codes
+        // held in registers, measured slower (the loads' latency is then
+        // exposed instead of overlapping the arithmetic).
+        float sc4[4];
+        qk_scores_mma<D, NKV, ROW>(stage + g * D,
+                                   reinterpret_cast<const float*>(stage + 2 * p.page_bytes + g * 4),
+                                   ntok, qa, sc4, lane);
+        // online softmax (base 2) of head r: its 16 scores sit in lanes 4r .. 4r + 3
+        float mx = fmaxf(fmaxf(sc4[0], sc4[1]), fmaxf(sc4[2], sc4[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run, mx);
+        const float m_use = (m_new == kNegInf) ? 0.f : m_new;
+        const float alpha = fast_exp2(m_run - m_use);
+        Chunk x[4];
+        float vs[4];
+        {
+          const unsigned char* vb = stage + p.page_bytes + g * D + r * (D / 8);
+          const float* vsc =
+              reinterpret_cast<const float*>(stage + 2 * p.page_bytes + p.scale_bytes + g * 4);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int tok = 2 * t + (k & 1) + 8 * (k >> 1);
+            x[k] = *reinterpret_cast<const Chunk*>(vb + (tok < ntok ? tok : 0) * ROW);
+            vs[k] = vsc[tok * NKV];
+          }
+        }
+        float pv[4];
+        float lsum = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int tok = 2 * t + (k & 1) + 8 * (k >> 1);
+          const float pr = fast_exp2(sc4[k] - m_use);  // 0 past the page's end
+          lsum += pr;
+          // B = P^T times the token's value scale and 2^9, which keeps the
+          // product in f16's normal range for row maxima from about 1e-3 to
+          // 5e4 (the 2^9 comes out exactly when the result is written)
+          pv[k] = tok < ntok ? pr * (vs[k] * 512.f) : 0.f;
+        }
+        l_lane = l_lane * alpha + lsum;
+        m_run = m_new;
+        // the accumulator columns are heads 2t, 2t + 1: their rescale factors
+        // live in lanes 8t and 8t + 4
+        // (skipped when no head's running max moved, the common case)
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
+          const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
+#pragma unroll
+          for (int m = 0; m < D / 16; ++m) {
+            o[m][0] *= a0, o[m][1] *= a1, o[m][2] *= a0, o[m][3] *= a1;
+          }
+        }
+        const uint32_t b0 = f16x2_from_floats(pv[0], pv[1]);
+        const uint32_t b1 = f16x2_from_floats(pv[2], pv[3]);
+        // A = V^T from the value codes in x
+#pragma unroll
+        for (int q = 0; q < DW; ++q) {
+          const uint32_t w0 = chunk_word(x[0], q), w1 = chunk_word(x[1], q);
+          const uint32_t w2 = chunk_word(x[2], q), w3 = chunk_word(x[3], q);
+          // (token 2t, token 2t + 1) code pairs of d + 0 | d + 1, and d + 2 | d + 3
+          uint32_t lo01, hi01, lo23, hi23;
+          asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(lo01) : "r"(w0), "r"(w1));
+          asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(hi01) : "r"(w0), "r"(w1));
+          asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(lo23) : "r"(w2), "r"(w3));
+          asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(hi23) : "r"(w2), "r"(w3));
+          uint32_t a[2][4];
+          f16x2x2_from_e4m3x4(lo01, a[0][0], a[0][1]);
+          f16x2x2_from_e4m3x4(lo23, a[0][2], a[0][3]);
+          f16x2x2_from_e4m3x4(hi01, a[1][0], a[1][1]);
+          f16x2x2_from_e4m3x4(hi23, a[1][2], a[1][3]);
+          mma_f16_16816_full(o[2 * q], a[0][0], a[0][1], a[0][2], a[0][3], b0, b1);
+          mma_f16_16816_full(o[2 * q + 1], a[1][0], a[1][1], a[1][2], a[1][3], b0, b1);
+        }
+        __syncwarp();
+        if (lane == 0) {
+          // release the stage; the last of the NKV warps of this parity refills it
+          if (atomicAdd(&S.released[st], 1) == NKV - 1) {
+            S.released[st] = 0;
+            if (i + NST < n_pages && !*abort_flag) {
+              fetch_page<FUSE>(p, fc, smem_addr(stage), smem_addr(&S.full[st]),
+                               &S.fused_slot[st]);
+              S.last_issued[st] = i + NST;
+            }
+          }
+        }
+      }
+      if (lane == 0) fc.next(p);
+      stage += p.stage_bytes;
+      if (++st == NST) st = 0, st_phase ^= 1, stage = stages;
+      if (seg_end) {
+        // running sum of head r over its four lanes
+        float lt = l_lane;
+        lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+        lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+        if (t == 0 && r < G) {
+          cb.m[rho][r] = m_run;
+          cb.l[rho][r] = lt;
+        }
+        if (rho == 1) {
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int h = 2 * t + cc;
+            if (h >= G) continue;
+#pragma unroll
+            for (int m = 0; m < D / 16; ++m) {
+              const int d = r * (D / 8) + 4 * (m >> 1) + 2 * (m & 1);
+              *reinterpret_cast<float2*>(&cb.o[h][d]) = make_float2(o[m][cc], o[m][2 + cc]);
+            }
+          }
+        }
+        named_barrier_sync(1 + g, 64);  // the pair's state is in shared memory
+        if (rho == 0) {
+          const int tok = __ldg(p.qsl + cur.s);
+          const bool whole = (seg_j0 == 0) && seq_done;
+          const int slot = 2 * c + (cur.s == s_begin ? 0 : 1);
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int h = 2 * t + cc;
+            if (h >= G) continue;
+            const int qh = g * G + h;
+            // merge the even-page (this warp) and odd-page states of head h;
+            // a warp with no page in the segment has m = -inf, l = 0, o = 0
+            const float m0 = cb.m[0][h], m1 = cb.m[1][h];
+            const float mm = fmaxf(m0, m1);
+            const float s0 = fast_exp2(m0 - mm), s1 = fast_exp2(m1 - mm);
+            const float l_all = cb.l[0][h] * s0 + cb.l[1][h] * s1;
+            const float inv = 1.f / l_all;
+#pragma unroll
+            for (int m = 0; m < D / 16; ++m) {
+              const int d = r * (D / 8) + 4 * (m >> 1) + 2 * (m & 1);
+              const float2 w = *reinterpret_cast<const float2*>(&cb.o[h][d]);
+              // elements d, d + 1, the 2^9 of B taken out (exact)
+              const float v0 = (o[m][cc] * s0 + w.x * s1) * (1.f / 512.f);
+              const float v1 = (o[m][2 + cc] * s0 + w.y * s1) * (1.f / 512.f);
+              if (whole) {
+                *reinterpret_cast<uint32_t*>(p.out + ((int64_t)tok * p.n_q + qh) * D + d) =
+                    pack_bf16x2(v0 * inv, v1 * inv);
+              } else {
+                *reinterpret_cast<float2*>(p.part_o + ((int64_t)slot * p.n_q + qh) * D + d) =
+                    make_float2(v0, v1);
+              }
+            }
+            if (!whole && r == 0) {
+              p.part_ml[((int64_t)slot * p.n_q + qh) * 2 + 0] = mm;
+              p.part_ml[((int64_t)slot * p.n_q + qh) * 2 + 1] = l_all;
+            }
+          }
+          if (g == 0 && lane == 0 && seg_j0 == 0) {
+            // this CTA owns the request's first page: record where its pieces are
+            int c_last = c;
+            if (!seq_done) {
+              const int64_t f_last = f0 + i + (cur.np - 1 - cur.j);
+              const int64_t cl = ((f_last + 1) * C + F - 1) / F - 1;
+              c_last = (int)(cl < C - 1 ? cl : C - 1);
+            }
+            p.seq_rec[cur.s] = make_int4(c, c_last, slot, (int)F);
+          }
+        }
+        named_barrier_sync(1 + g, 64);  // the state buffer may be rewritten
+#pragma unroll
+        for (int m = 0; m < D / 16; ++m)
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) o[m][cc] = 0.f;
+        m_run = kNegInf;
+        l_lane = 0.f;
+      }
+      const int prev_s = cur.s;
+      cur.next(p);
+      if (seg_end && cur.s != prev_s && i + 1 < n_pages) {
+        L = __ldg(p.seq_lens + cur.s);
+        seg_j0 = 0;
+        load_q(cur.s);
+      }
+    }
+  } else {
   if (is_qk) {
     // ================================================================ QK warp
     const int tok_lane = lane / LPT_QK;
@@ -536,40 +805,22 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
     const int my_h = dl / REP_QK;
     const int rep = dl % REP_QK;
     float2 qf[G][E_QK / 2];  // bf16 cache: this lane's slice of q, fp32
-    uint32_t qa[D / 16][2];  // 8-bit cache: MMA A registers of head lane / 4 (see qk_scores_mma)
     float m_run = kNegInf, l_lane = 0.f;
     bool stored = false;  // this lane issued fused-scatter stores
     auto load_q = [&](int seq) {
       const int tok = __ldg(p.qsl + seq);
-      if constexpr (F8) {
-        const int hq = lane >> 2, t = lane & 3;
-        const uint16_t* qrow = p.q + ((int64_t)tok * p.n_q + g * G + (hq < G ? hq : 0)) * D;
 #pragma unroll
-        for (int v = 0; v < D / 32; ++v) {  // D/4 elements, 8 per load
-          uint4 w = make_uint4(0u, 0u, 0u, 0u);
-          if (hq < G) w = __ldg(reinterpret_cast<const uint4*>(qrow + t * (D / 4) + 8 * v));
+      for (int h = 0; h < G; ++h) {
+        const uint16_t* qrow = p.q + ((int64_t)tok * p.n_q + g * G + h) * D;
+#pragma unroll
+        for (int piece = 0; piece < E_QK / 8; ++piece) {
+          const uint4 w =
+              __ldg(reinterpret_cast<const uint4*>(qrow + piece * (D / 2) + dl * 8));
           const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-          for (int e = 0; e < 4; e += 2) {  // 4 elements = one k-step
-            const float2 f0 = bf16x2_to_float2(ws[e]), f1 = bf16x2_to_float2(ws[e + 1]);
-            qa[2 * v + e / 2][0] = f16x2_from_floats(f0.x * p.scale_log2, f0.y * p.scale_log2);
-            qa[2 * v + e / 2][1] = f16x2_from_floats(f1.x * p.scale_log2, f1.y * p.scale_log2);
-          }
-        }
-      } else {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const uint16_t* qrow = p.q + ((int64_t)tok * p.n_q + g * G + h) * D;
-#pragma unroll
-          for (int piece = 0; piece < E_QK / 8; ++piece) {
-            const uint4 w =
-                __ldg(reinterpret_cast<const uint4*>(qrow + piece * (D / 2) + dl * 8));
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = bf16x2_to_float2(ws[e]);
-              qf[h][piece * 4 + e] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
-            }
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = bf16x2_to_float2(ws[e]);
+            qf[h][piece * 4 + e] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
           }
         }
       }
@@ -600,78 +851,42 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
       const bool seq_done = (cur.j + 1 == cur.np);
       const bool seg_end = seq_done || (i + 1 == n_pages);
       PBuf<G>& pb = S.pb[g][b];
-      if constexpr (F8) {
-        // scores on the tensor cores; lane holds head lane / 4, 4 tokens
-        const int hq = lane >> 2, t = lane & 3;
-        float sc4[4];
-        qk_scores_mma<D, NKV, ROW>(stage + g * D, reinterpret_cast<const float*>(
-                                                      stage + 2 * p.page_bytes + g * 4),
-                                   ntok, qa, sc4, lane);
-        // online softmax (base 2) for head hq over the page's 16 tokens: the
-        // head's 16 scores sit in lanes 4 hq .. 4 hq + 3
-        float mx = fmaxf(fmaxf(sc4[0], sc4[1]), fmaxf(sc4[2], sc4[3]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run, mx);
-        const float m_use = (m_new == kNegInf) ? 0.f : m_new;
-        const float alpha = fast_exp2(m_run - m_use);
-        float lsum = 0.f;
+      float sc[NIT_QK];
+      const float* ksc = reinterpret_cast<const float*>(stage + ks_off);
+      if (ntok == kBlock)
+        qk_scores<D, G, E_QK, LPT_QK, ROW, true, F8, NKV>(stage + k_off, ksc, ntok, tok_lane,
+                                                          qf, sc, lane);
+      else
+        qk_scores<D, G, E_QK, LPT_QK, ROW, false, F8, NKV>(stage + k_off, ksc, ntok,
+                                                           tok_lane, qf, sc, lane);
+      // online softmax (base 2) for head my_h over the page's 16 tokens
+      float mx = sc[0];
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const float pr = fast_exp2(sc4[jj] - m_use);
-          lsum += pr;
-          if (hq < G) pb.p[8 * (jj >> 1) + 2 * t + (jj & 1)][hq] = pr;
-        }
-        l_lane = l_lane * alpha + lsum;
-        m_run = m_new;
-        if (t == 0 && hq < G) pb.alpha[hq] = alpha;
-        if (seg_end) {
-          float lt = l_lane;
-          lt += __shfl_xor_sync(0xffffffffu, lt, 1);
-          lt += __shfl_xor_sync(0xffffffffu, lt, 2);
-          if (t == 0 && hq < G) {
-            pb.m[hq] = m_run;
-            pb.l[hq] = lt;
-          }
-        }
-      } else {
-        float sc[NIT_QK];
-        const float* ksc = reinterpret_cast<const float*>(stage + ks_off);
-        if (ntok == kBlock)
-          qk_scores<D, G, E_QK, LPT_QK, ROW, true, F8, NKV>(stage + k_off, ksc, ntok, tok_lane,
-                                                            qf, sc, lane);
-        else
-          qk_scores<D, G, E_QK, LPT_QK, ROW, false, F8, NKV>(stage + k_off, ksc, ntok,
-                                                             tok_lane, qf, sc, lane);
-        // online softmax (base 2) for head my_h over the page's 16 tokens
-        float mx = sc[0];
+      for (int it = 1; it < NIT_QK; ++it) mx = fmaxf(mx, sc[it]);
 #pragma unroll
-        for (int it = 1; it < NIT_QK; ++it) mx = fmaxf(mx, sc[it]);
+      for (int m = LPT_QK; m < 32; m <<= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+      const float m_new = fmaxf(m_run, mx);
+      const float m_use = (m_new == kNegInf) ? 0.f : m_new;
+      const float alpha = fast_exp2(m_run - m_use);
+      float* pw = &pb.p[tok_lane][my_h];
+      float lsum = 0.f;
 #pragma unroll
-        for (int m = LPT_QK; m < 32; m <<= 1)
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-        const float m_new = fmaxf(m_run, mx);
-        const float m_use = (m_new == kNegInf) ? 0.f : m_new;
-        const float alpha = fast_exp2(m_run - m_use);
-        float* pw = &pb.p[tok_lane][my_h];
-        float lsum = 0.f;
+      for (int it = 0; it < NIT_QK; ++it) {
+        const float pr = fast_exp2(sc[it] - m_use);
+        lsum += pr;
+        if (rep == 0) pw[it * TPI_QK * G] = pr;
+      }
+      l_lane = l_lane * alpha + lsum;
+      m_run = m_new;
+      if (tok_lane == 0 && rep == 0) pb.alpha[my_h] = alpha;
+      if (seg_end) {
+        float lt = l_lane;
 #pragma unroll
-        for (int it = 0; it < NIT_QK; ++it) {
-          const float pr = fast_exp2(sc[it] - m_use);
-          lsum += pr;
-          if (rep == 0) pw[it * TPI_QK * G] = pr;
-        }
-        l_lane = l_lane * alpha + lsum;
-        m_run = m_new;
-        if (tok_lane == 0 && rep == 0) pb.alpha[my_h] = alpha;
-        if (seg_end) {
-          float lt = l_lane;
-#pragma unroll
-          for (int m = LPT_QK; m < 32; m <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, m);
-          if (tok_lane == 0 && rep == 0) {
-            pb.m[my_h] = m_run;
-            pb.l[my_h] = lt;
-          }
+        for (int m = LPT_QK; m < 32; m <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, m);
+        if (tok_lane == 0 && rep == 0) {
+          pb.m[my_h] = m_run;
+          pb.l[my_h] = lt;
         }
       }
       __syncwarp();
@@ -699,153 +914,6 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
       }
     }
     if (FUSE && stored) bulk_wait_all();  // the stores are complete before the CTA exits
-  } else {
-  if constexpr (F8) {
-    // ============================================ PV warp, 8-bit cache (tensor cores)
-    // O^T [D x heads] += V^T [D x 16 tokens] * P^T [16 tokens x heads] with
-    // mma.sync m16n8k16: the MMA rows are head_dim (16 per tile), the columns
-    // the G heads (columns G..7 zero), the reduction the page's 16 tokens.
-    // Rows are assigned so that a lane reads 4 consecutive codes per token
-    // for a pair of tiles: in tile pair q, lane (r, t) = (lane / 4, lane % 4)
-    // holds rows d = 32q + 4r + {0, 1} (first tile) and + {2, 3} (second);
-    // its accumulators o[2q + u][c] are out element d = 32q + 4r + 2u + (c >> 1)
-    // of head 2t + (c & 1).
-    const int r = lane >> 2, t = lane & 3;
-    float o[D / 16][4];
-#pragma unroll
-    for (int m = 0; m < D / 16; ++m)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) o[m][c] = 0.f;
-    int st = 0, st_phase = 0;
-    const unsigned char* stage = stages;
-    for (int i = 0; i < n_pages; ++i) {
-      const int b = i & 1;
-      mbar_wait(smem_addr(&S.full[st]), st_phase, p.err, abort_flag);
-      const int ntok = min(kBlock, L - cur.j * kBlock);
-      mbar_wait(smem_addr(&S.p_full[g][b]), (i >> 1) & 1, p.err, abort_flag);
-      const PBuf<G>& pb = S.pb[g][b];
-      // rescale the running output of heads 2t, 2t + 1
-      const float a0 = 2 * t < G ? pb.alpha[2 * t] : 1.f;
-      const float a1 = 2 * t + 1 < G ? pb.alpha[2 * t + 1] : 1.f;
-#pragma unroll
-      for (int m = 0; m < D / 16; ++m) {
-        o[m][0] *= a0, o[m][1] *= a1, o[m][2] *= a0, o[m][3] *= a1;
-      }
-      // B = P^T scaled by each token's value scale and by 2^9, which keeps
-      // p * scale (scale = row max / 448) in the normal range of f16 for row
-      // maxima from about 1e-3 to 5e4; lane holds tokens 2t, 2t + 1 (b0) and
-      // 2t + 8, 2t + 9 (b1) of head r
-      const float* vsc = reinterpret_cast<const float*>(stage + 2 * p.page_bytes +
-                                                        p.scale_bytes + g * 4);
-      float pv[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int tok = 2 * t + (k & 1) + 8 * (k >> 1);
-        pv[k] = (r < G && tok < ntok) ? pb.p[tok][r < G ? r : 0] * (vsc[tok * NKV] * 512.f)
-                                      : 0.f;
-      }
-      const uint32_t b0 = f16x2_from_floats(pv[0], pv[1]);
-      const uint32_t b1 = f16x2_from_floats(pv[2], pv[3]);
-      // A = V^T: codes of tokens 2t, 2t + 1, 2t + 8, 2t + 9 at d = 32q + 4r .. + 3
-      const unsigned char* vb = stage + p.page_bytes + g * D + 4 * r;
-#pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
-        uint32_t x[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int tok = 2 * t + (k & 1) + 8 * (k >> 1);
-          // rows past the page's end hold stale codes; their P is 0, but a
-          // stale NaN code would still poison the product: read token 0
-          x[k] = *reinterpret_cast<const uint32_t*>(vb + (tok < ntok ? tok : 0) * ROW + 32 * q);
-        }
-        // first tile: d + {0, 1}; second: d + {2, 3}; tokens (k0, k1) in the
-        // low/high byte of each code pair
-        uint32_t lo01, hi01, lo23, hi23;
-        asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(lo01) : "r"(x[0]), "r"(x[1]));
-        asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(hi01) : "r"(x[0]), "r"(x[1]));
-        asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(lo23) : "r"(x[2]), "r"(x[3]));
-        asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(hi23) : "r"(x[2]), "r"(x[3]));
-        // tile 2q: rows (d, d + 1) -> A regs {row r: d}, {row r + 8: d + 1}
-        mma_f16_16816_full(o[2 * q], f16x2_from_e4m3x2(lo01 & 0xffffu),
-                           f16x2_from_e4m3x2(lo01 >> 16), f16x2_from_e4m3x2(lo23 & 0xffffu),
-                           f16x2_from_e4m3x2(lo23 >> 16), b0, b1);
-        mma_f16_16816_full(o[2 * q + 1], f16x2_from_e4m3x2(hi01 & 0xffffu),
-                           f16x2_from_e4m3x2(hi01 >> 16), f16x2_from_e4m3x2(hi23 & 0xffffu),
-                           f16x2_from_e4m3x2(hi23 >> 16), b0, b1);
-      }
-      const bool seq_done = (cur.j + 1 == cur.np);
-      const bool seg_end = seq_done || (i + 1 == n_pages);
-      float m_fin[2] = {0.f, 0.f}, l_fin[2] = {1.f, 1.f};
-      if (seg_end) {
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-          if (2 * t + c < G) m_fin[c] = pb.m[2 * t + c], l_fin[c] = pb.l[2 * t + c];
-      }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_addr(&S.p_empty[g][b]));
-        if (atomicAdd(&S.released[st], 1) == NW - 1) {
-          S.released[st] = 0;
-          if (i + NST < n_pages && !*abort_flag) {
-            fetch_page<FUSE>(p, fc, smem_addr(stage), smem_addr(&S.full[st]),
-                             &S.fused_slot[st]);
-            S.last_issued[st] = i + NST;
-          }
-        }
-        fc.next(p);
-      }
-      stage += p.stage_bytes;
-      if (++st == NST) st = 0, st_phase ^= 1, stage = stages;
-      if (seg_end) {
-        const int tok = __ldg(p.qsl + cur.s);
-        const bool whole = (seg_j0 == 0) && seq_done;
-        const int slot = 2 * c + (cur.s == s_begin ? 0 : 1);
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int h = 2 * t + cc;
-          if (h >= G) continue;
-          const int qh = g * G + h;
-          const float inv = 1.f / l_fin[cc];
-#pragma unroll
-          for (int m = 0; m < D / 16; ++m) {
-            const int d = 32 * (m >> 1) + 4 * r + 2 * (m & 1);
-            // elements d, d + 1, the 2^9 of B taken out (exact)
-            const float v0 = o[m][cc] * (1.f / 512.f), v1 = o[m][2 + cc] * (1.f / 512.f);
-            if (whole) {
-              *reinterpret_cast<uint32_t*>(p.out + ((int64_t)tok * p.n_q + qh) * D + d) =
-                  pack_bf16x2(v0 * inv, v1 * inv);
-            } else {
-              *reinterpret_cast<float2*>(p.part_o + ((int64_t)slot * p.n_q + qh) * D + d) =
-                  make_float2(v0, v1);
-            }
-          }
-          if (!whole && r == 0) {
-            p.part_ml[((int64_t)slot * p.n_q + qh) * 2 + 0] = m_fin[cc];
-            p.part_ml[((int64_t)slot * p.n_q + qh) * 2 + 1] = l_fin[cc];
-          }
-        }
-        if (g == 0 && lane == 0 && seg_j0 == 0) {
-          // this CTA owns the request's first page: record where its pieces are
-          int c_last = c;
-          if (!seq_done) {
-            const int64_t f_last = f0 + i + (cur.np - 1 - cur.j);
-            const int64_t cl = ((f_last + 1) * C + F - 1) / F - 1;
-            c_last = (int)(cl < C - 1 ? cl : C - 1);
-          }
-          p.seq_rec[cur.s] = make_int4(c, c_last, slot, (int)F);
-        }
-#pragma unroll
-        for (int m = 0; m < D / 16; ++m)
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) o[m][cc] = 0.f;
-      }
-      const int prev_s = cur.s;
-      cur.next(p);
-      if (seg_end && cur.s != prev_s && i + 1 < n_pages) {
-        L = __ldg(p.seq_lens + cur.s);
-        seg_j0 = 0;
-      }
-    }
   } else {
     // ================================================================ PV warp
     const int tok_lane = lane / LPT_PV;
@@ -1111,6 +1179,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
 }
 
 constexpr size_t kSmemBudget = 220 * 1024;
+constexpr size_t kSmemBudgetF8 = 226 * 1024;  // below the 227 KB opt-in limit per block
 
 template <int D, int G, int NKV, bool F8, bool FUSE>
 cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ctas,
@@ -1146,8 +1215,12 @@ cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ct
   p.page_bytes = kBlock * p.row_bytes;
   p.scale_bytes = F8 ? (uint32_t)(kBlock * NKV * sizeof(float)) : 0u;
   p.stage_bytes = 2 * p.page_bytes + 2 * p.scale_bytes;
-  const size_t fixed = sizeof(DecodeSmem<G, NKV>);
-  int nst = (int)((kSmemBudget - fixed) / p.stage_bytes);
+  // the 8-bit kernel also holds the per-kv-head merge buffers, and takes
+  // the shared memory up to the opt-in limit to keep six stages
+  const size_t fixed =
+      F8 ? comb_offset<G, NKV>() + NKV * sizeof(Comb<G, D>) : sizeof(DecodeSmem<G, NKV>);
+  const size_t budget = F8 ? kSmemBudgetF8 : kSmemBudget;
+  int nst = (int)((budget - fixed) / p.stage_bytes);
   nst = nst > 8 ? 8 : nst;
   if (nst < 2) return cudaErrorInvalidConfiguration;
   p.nstages = nst;
@@ -1158,7 +1231,7 @@ cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ct
   cudaGetDevice(&dev);
   if (configured_device != dev) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(kSmemBudget + 4096));
+                                         (int)(F8 ? kSmemBudgetF8 : kSmemBudget + 4096));
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }

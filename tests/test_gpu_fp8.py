@@ -91,6 +91,19 @@ def test_fp8_decode_batch_workload():
     assert_attn_close(got, ref, "fp8 decode batch")
 
 
+@pytest.mark.parametrize("mag", [1e-2, 3e3])
+def test_fp8_decode_small_and_large_values(mag):
+    """Values far from unit size: the decode kernel multiplies p by each
+    token's value scale in f16 (times a power of two), which must neither
+    lose small products nor overflow.  Compared after dividing by mag."""
+    b = _decode([700, 130, 2000, 1], seed=21)
+    for name in ("v_cache", "v_new"):
+        a = W.f32_from_bf16(getattr(b, name)) * np.float32(mag)
+        setattr(b, name, W.bf16_from_f32(a.astype(np.float32)))
+    got, ref = fp8_step(b)
+    assert_attn_close(got / mag, ref / mag, f"fp8 values x {mag}")
+
+
 def test_fp8_quantises_zero_and_large_rows():
     """All-zero rows (scale 1, zero codes) and rows of large bf16 magnitudes
     quantise bit for bit like the oracle."""
