@@ -360,6 +360,50 @@ __device__ __forceinline__ void mma_f16_16816_full(float (&c)[4], uint32_t a0, u
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Scores of one page on the tensor cores (bf16 cache), as qk_scores_mma
+// below but with the cached bf16 values as B directly (two 32-bit words per
+// k-step) and q unscaled in A; the fp32 score takes scale * log2(e).
+template <int D, uint32_t ROW>
+__device__ __forceinline__ void qk_scores_mma_bf16(const unsigned char* kb, int ntok,
+                                                   const uint32_t (&qa)[D / 16][2],
+                                                   float scale_log2, float (&sc)[4], int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  float c[2][4];
+#pragma unroll
+  for (int T = 0; T < 2; ++T) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) c[T][e] = 0.f;
+    // this lane's D/4 values of token 8T + g (2 bytes each)
+    const unsigned char* src = kb + (8 * T + g) * ROW + t * (D / 2);
+    uint32_t w[D / 8];
+#pragma unroll
+    for (int v = 0; v < D / 32; ++v) {
+      const uint4 x = *reinterpret_cast<const uint4*>(src + 16 * v);
+      w[4 * v] = x.x, w[4 * v + 1] = x.y, w[4 * v + 2] = x.z, w[4 * v + 3] = x.w;
+    }
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks)
+      mma_bf16_16816(c[T], qa[ks][0], 0u, qa[ks][1], 0u, w[2 * ks], w[2 * ks + 1]);
+  }
+#pragma unroll
+  for (int T = 0; T < 2; ++T)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int tok = 8 * T + 2 * t + j;
+      sc[2 * T + j] = tok < ntok ? c[T][j] * scale_log2 : kNegInf;
+    }
+}
+
 // Scores of one page on the tensor cores (8-bit cache): sc[2T + j] is the
 // base-2 score of head lane / 4 for token 8T + 2 (lane % 4) + j (-inf past
 // the page's end).  kb: the page's codes of this kv head (token 0); ksc: the
@@ -448,14 +492,30 @@ __device__ __forceinline__ void pv_accumulate(const unsigned char* vb, const flo
   }
 }
 
-// D: head_dim; G: q heads per kv head; NKV: kv heads (= warps of each role).
-// Warps 0..NKV-1 compute scores and the softmax (QK warps), warps
-// NKV..2*NKV-1 accumulate p * V (PV warps); warp g and warp NKV + g serve kv
-// head g and hand over p through a double-buffered slot in shared memory.
-// F8: 8-bit cache; FUSE: decode-only step with the scatter done here (bf16).
-template <int D, int G, int NKV, bool F8, bool FUSE>
-__global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodeParams p) {
-  constexpr int NW = 2 * NKV;
+// Threads of a decode CTA: MW (tensor-core warps) with a bf16 cache runs one
+// warp per kv head, every other form two.
+template <int NKV, bool F8, bool MW>
+__host__ __device__ constexpr int decode_threads() {
+  return (MW && !F8 ? 1 : 2) * NKV * 32;
+}
+
+// D: head_dim; G: q heads per kv head; NKV: kv heads.  F8: 8-bit cache;
+// FUSE: decode-only step with the scatter done here (bf16); MW: the page's
+// arithmetic on the tensor cores by one warp (always with F8).
+//  * MW: a warp computes q . k, the softmax and p * V of a page for all G
+//    heads of its kv head, p staying in registers.  With a bf16 cache warp g
+//    serves kv head g and takes every page; with the 8-bit cache warps g and
+//    NKV + g take the even and the odd pages.
+//  * otherwise: warps 0..NKV-1 compute scores and the softmax (QK warps),
+//    warps NKV..2*NKV-1 accumulate p * V (PV warps) on the FMA pipe; warp g
+//    and warp NKV + g serve kv head g and hand over p through a
+//    double-buffered slot in shared memory.
+template <int D, int G, int NKV, bool F8, bool FUSE, bool MW>
+__global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
+    decode_kernel(const DecodeParams p) {
+  constexpr bool MMA = F8 || MW;
+  constexpr int R = F8 ? 2 : 1;  // tensor-core warps per kv head
+  constexpr int NW = decode_threads<NKV, F8, MW>() / 32;
   // QK lanes: E_QK head_dim elements each (two 16-byte pieces when 16)
   constexpr int E_QK = (G <= 4 && D == 128) ? 16 : 8;
   constexpr int LPT_QK = D / E_QK;
@@ -564,31 +624,32 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
   int L = __ldg(p.seq_lens + cur.s);
   int seg_j0 = j_begin;
 
-  if constexpr (F8) {
-    // ======================================================= 8-bit cache
-    // One warp computes a page's scores, its softmax and p * V for all G heads
-    // of its kv head, keeping p in registers: the score fragment of the q * k
-    // product (head r = lane / 4, tokens 2t, 2t + 1, 2t + 8, 2t + 9 with
-    // t = lane % 4) is exactly the B fragment of the p * V product.  Warp g
-    // and warp NKV + g serve kv head g and take the even and the odd pages;
-    // at the end of each segment (a request's pages in this CTA) the odd-page
-    // warp hands its running state to the even-page warp through shared
-    // memory, which merges and writes.
+  if constexpr (MMA) {
+    // ================================================== tensor-core warps
+    // The score fragment of the q * k product (head r = lane / 4, tokens 2t,
+    // 2t + 1, 2t + 8, 2t + 9 with t = lane % 4) is exactly the B fragment of
+    // the p * V product, so p stays in registers.  With the 8-bit cache the
+    // odd-page warp of a kv head hands its running state to the even-page
+    // warp through shared memory at the end of each segment (a request's
+    // pages in this CTA), which merges and writes.
     //
     // p * V is O^T [D x heads] += V^T [D x 16 tokens] * P^T [16 tokens x heads]
-    // (mma.sync m16n8k16, f16 in, f32 accumulate): MMA rows are head_dim,
-    // columns heads (G..7 unused), the reduction the page's tokens.  Rows
-    // are assigned so that lane r reads one contiguous run of D/8 codes per
-    // token: in tile pair q the first tile holds d = r D/8 + 4q + {0, 1} in
-    // rows (r, r + 8), the second d + {2, 3}; accumulator o[2q + u][c] is
-    // element r D/8 + 4q + 2u + (c >> 1) of head 2t + (c & 1).
-    const int rho = is_qk ? 0 : 1;  // page parity served
+    // (mma.sync m16n8k16, f32 accumulate; f16 for codes, bf16 for a bf16
+    // cache): MMA rows are head_dim, columns heads (G..7 unused), the
+    // reduction the page's tokens.  Rows are assigned so that lane r reads one
+    // contiguous run of D/8 elements per token: in tile pair q the first tile
+    // holds d = r D/8 + 4q + {0, 1} in rows (r, r + 8), the second d + {2, 3};
+    // accumulator o[2q + u][c] is element r D/8 + 4q + 2u + (c >> 1) of head
+    // 2t + (c & 1).
+    const int rho = (R == 1 || is_qk) ? 0 : 1;  // page parity served (8-bit cache)
     const int r = lane >> 2, t = lane & 3;
-    constexpr int DW = D / 32;      // 4-byte words of codes per lane and token
-    using Chunk = typename std::conditional<DW == 4, uint4, uint2>::type;
-    uint32_t qa[D / 16][2];         // A registers of q for head r (see qk_scores_mma)
+    constexpr uint32_t ESZ = F8 ? 1 : 2;
+    constexpr int VW = D / 8 * ESZ / 4;  // 4-byte words per lane and token of p * V
+    constexpr float OUT_SCALE = F8 ? 1.f / 512.f : 1.f;
+    uint32_t qa[D / 16][2];  // A registers of q for head r (see qk_scores_mma)
     float o[D / 16][4];
     float m_run = kNegInf, l_lane = 0.f;
+    bool stored = false;  // this lane issued fused-scatter stores
     auto load_q = [&](int seq) {
       const int tok = __ldg(p.qsl + seq);
       const uint16_t* qrow = p.q + ((int64_t)tok * p.n_q + g * G + (r < G ? r : 0)) * D;
@@ -599,9 +660,14 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int e = 0; e < 4; e += 2) {  // 4 elements = one k-step
-          const float2 f0 = bf16x2_to_float2(ws[e]), f1 = bf16x2_to_float2(ws[e + 1]);
-          qa[2 * v + e / 2][0] = f16x2_from_floats(f0.x * p.scale_log2, f0.y * p.scale_log2);
-          qa[2 * v + e / 2][1] = f16x2_from_floats(f1.x * p.scale_log2, f1.y * p.scale_log2);
+          if constexpr (F8) {
+            const float2 f0 = bf16x2_to_float2(ws[e]), f1 = bf16x2_to_float2(ws[e + 1]);
+            qa[2 * v + e / 2][0] = f16x2_from_floats(f0.x * p.scale_log2, f0.y * p.scale_log2);
+            qa[2 * v + e / 2][1] = f16x2_from_floats(f1.x * p.scale_log2, f1.y * p.scale_log2);
+          } else {
+            qa[2 * v + e / 2][0] = ws[e];
+            qa[2 * v + e / 2][1] = ws[e + 1];
+          }
         }
       }
     };
@@ -610,15 +676,27 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
     for (int m = 0; m < D / 16; ++m)
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) o[m][cc] = 0.f;
-    Comb<G, D>& cb = comb[g];
+    Comb<G, D>& cb = comb[g];  // 8-bit cache only
     int st = 0, st_phase = 0;
     const unsigned char* stage = stages;
     for (int i = 0; i < n_pages; ++i) {
       const bool seq_done = (cur.j + 1 == cur.np);
       const bool seg_end = seq_done || (i + 1 == n_pages);
-      if ((i & 1) == rho) {
+      if (R == 1 || (i & 1) == rho) {
         mbar_wait(smem_addr(&S.full[st]), st_phase, p.err, abort_flag);
         const int ntok = min(kBlock, L - cur.j * kBlock);
+        const int fslot = FUSE ? S.fused_slot[st] : -1;
+        if (FUSE && fslot >= 0 && lane == 0) {
+          // fused scatter: this kv head's slices of the new key and value rows
+          bulk_s2g(reinterpret_cast<unsigned char*>(const_cast<void*>(p.k_cache)) +
+                       (size_t)fslot * ROW + g * D * ES,
+                   smem_addr(stage + (ntok - 1) * ROW + g * D * ES), D * ES);
+          bulk_s2g(reinterpret_cast<unsigned char*>(const_cast<void*>(p.v_cache)) +
+                       (size_t)fslot * ROW + g * D * ES,
+                   smem_addr(stage + p.page_bytes + (ntok - 1) * ROW + g * D * ES), D * ES);
+          bulk_commit();
+          stored = true;
+        }
         // Scores from the key codes; value codes of tokens 2t, 2t + 1, 2t + 8,
         // 2t + 9 at lane r's D/8 head_dim offsets, and their scales, for p * V
         // (rows past the page's end hold stale codes whose p is 0, but a stale
@@ -627,9 +705,12 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
         // held in registers, measured slower (the loads' latency is then
         // exposed instead of overlapping the arithmetic).
         float sc4[4];
-        qk_scores_mma<D, NKV, ROW>(stage + g * D,
-                                   reinterpret_cast<const float*>(stage + 2 * p.page_bytes + g * 4),
-                                   ntok, qa, sc4, lane);
+        if constexpr (F8)
+          qk_scores_mma<D, NKV, ROW>(
+              stage + g * D, reinterpret_cast<const float*>(stage + 2 * p.page_bytes + g * 4),
+              ntok, qa, sc4, lane);
+        else
+          qk_scores_mma_bf16<D, ROW>(stage + g * D * ES, ntok, qa, p.scale_log2, sc4, lane);
         // online softmax (base 2) of head r: its 16 scores sit in lanes 4r .. 4r + 3
         float mx = fmaxf(fmaxf(sc4[0], sc4[1]), fmaxf(sc4[2], sc4[3]));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -637,17 +718,28 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
         const float m_new = fmaxf(m_run, mx);
         const float m_use = (m_new == kNegInf) ? 0.f : m_new;
         const float alpha = fast_exp2(m_run - m_use);
-        Chunk x[4];
+        uint32_t x[4][VW];
         float vs[4];
         {
-          const unsigned char* vb = stage + p.page_bytes + g * D + r * (D / 8);
+          const unsigned char* vb = stage + p.page_bytes + (g * D + r * (D / 8)) * ES;
           const float* vsc =
               reinterpret_cast<const float*>(stage + 2 * p.page_bytes + p.scale_bytes + g * 4);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int tok = 2 * t + (k & 1) + 8 * (k >> 1);
-            x[k] = *reinterpret_cast<const Chunk*>(vb + (tok < ntok ? tok : 0) * ROW);
-            vs[k] = vsc[tok * NKV];
+            const unsigned char* src = vb + (tok < ntok ? tok : 0) * ROW;
+            if constexpr (VW % 4 == 0) {
+#pragma unroll
+              for (int v = 0; v < VW / 4; ++v) {
+                const uint4 w = *reinterpret_cast<const uint4*>(src + 16 * v);
+                x[k][4 * v] = w.x, x[k][4 * v + 1] = w.y, x[k][4 * v + 2] = w.z,
+                x[k][4 * v + 3] = w.w;
+              }
+            } else {
+              const uint2 w = *reinterpret_cast<const uint2*>(src);
+              x[k][0] = w.x, x[k][1] = w.y;
+            }
+            vs[k] = F8 ? vsc[tok * NKV] : 1.f;
           }
         }
         float pv[4];
@@ -657,10 +749,10 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
           const int tok = 2 * t + (k & 1) + 8 * (k >> 1);
           const float pr = fast_exp2(sc4[k] - m_use);  // 0 past the page's end
           lsum += pr;
-          // B = P^T times the token's value scale and 2^9, which keeps the
-          // product in f16's normal range for row maxima from about 1e-3 to
-          // 5e4 (the 2^9 comes out exactly when the result is written)
-          pv[k] = tok < ntok ? pr * (vs[k] * 512.f) : 0.f;
+          // B = P^T; for codes times the token's value scale and 2^9, which
+          // keeps the product in f16's normal range for row maxima from about
+          // 1e-3 to 5e4 (the 2^9 comes out exactly when the result is written)
+          pv[k] = tok < ntok ? (F8 ? pr * (vs[k] * 512.f) : pr) : 0.f;
         }
         l_lane = l_lane * alpha + lsum;
         m_run = m_new;
@@ -675,13 +767,33 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
             o[m][0] *= a0, o[m][1] *= a1, o[m][2] *= a0, o[m][3] *= a1;
           }
         }
+        if constexpr (!F8) {
+          // A = V^T from the bf16 values in x: words 2q, 2q + 1 of a token
+          // are its elements d, d + 1 and d + 2, d + 3 of tile pair q
+          const uint32_t b0 = pack_bf16x2(pv[0], pv[1]);
+          const uint32_t b1 = pack_bf16x2(pv[2], pv[3]);
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const uint32_t wa = x[0][2 * q + u], wb = x[1][2 * q + u];
+              const uint32_t wc = x[2][2 * q + u], wd = x[3][2 * q + u];
+              uint32_t a0, a1, a2, a3;
+              asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(a0) : "r"(wa), "r"(wb));
+              asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(a1) : "r"(wa), "r"(wb));
+              asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(a2) : "r"(wc), "r"(wd));
+              asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(a3) : "r"(wc), "r"(wd));
+              mma_bf16_16816(o[2 * q + u], a0, a1, a2, a3, b0, b1);
+            }
+          }
+        } else {
         const uint32_t b0 = f16x2_from_floats(pv[0], pv[1]);
         const uint32_t b1 = f16x2_from_floats(pv[2], pv[3]);
         // A = V^T from the value codes in x
 #pragma unroll
-        for (int q = 0; q < DW; ++q) {
-          const uint32_t w0 = chunk_word(x[0], q), w1 = chunk_word(x[1], q);
-          const uint32_t w2 = chunk_word(x[2], q), w3 = chunk_word(x[3], q);
+        for (int q = 0; q < D / 32; ++q) {
+          const uint32_t w0 = x[0][q], w1 = x[1][q];
+          const uint32_t w2 = x[2][q], w3 = x[3][q];
           // (token 2t, token 2t + 1) code pairs of d + 0 | d + 1, and d + 2 | d + 3
           uint32_t lo01, hi01, lo23, hi23;
           asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(lo01) : "r"(w0), "r"(w1));
@@ -696,8 +808,10 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
           mma_f16_16816_full(o[2 * q], a[0][0], a[0][1], a[0][2], a[0][3], b0, b1);
           mma_f16_16816_full(o[2 * q + 1], a[1][0], a[1][1], a[1][2], a[1][3], b0, b1);
         }
+        }
         __syncwarp();
         if (lane == 0) {
+          if (FUSE && fslot >= 0) bulk_wait_read();  // the stores have read the stage
           // release the stage; the last of the NKV warps of this parity refills it
           if (atomicAdd(&S.released[st], 1) == NKV - 1) {
             S.released[st] = 0;
@@ -717,11 +831,19 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
         float lt = l_lane;
         lt += __shfl_xor_sync(0xffffffffu, lt, 1);
         lt += __shfl_xor_sync(0xffffffffu, lt, 2);
-        if (t == 0 && r < G) {
+        // running max and sum of the accumulator columns' heads 2t, 2t + 1
+        // (lanes 8t and 8t + 4 hold them)
+        float mh[2], lh[2];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          mh[cc] = __shfl_sync(0xffffffffu, m_run, 8 * t + 4 * cc);
+          lh[cc] = __shfl_sync(0xffffffffu, lt, 8 * t + 4 * cc);
+        }
+        if (R == 2 && t == 0 && r < G) {
           cb.m[rho][r] = m_run;
           cb.l[rho][r] = lt;
         }
-        if (rho == 1) {
+        if (R == 2 && rho == 1) {
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             const int h = 2 * t + cc;
@@ -733,7 +855,7 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
             }
           }
         }
-        named_barrier_sync(1 + g, 64);  // the pair's state is in shared memory
+        if (R == 2) named_barrier_sync(1 + g, 64);  // the pair's state is in shared memory
         if (rho == 0) {
           const int tok = __ldg(p.qsl + cur.s);
           const bool whole = (seg_j0 == 0) && seq_done;
@@ -743,20 +865,25 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
             const int h = 2 * t + cc;
             if (h >= G) continue;
             const int qh = g * G + h;
-            // merge the even-page (this warp) and odd-page states of head h;
-            // a warp with no page in the segment has m = -inf, l = 0, o = 0
-            const float m0 = cb.m[0][h], m1 = cb.m[1][h];
-            const float mm = fmaxf(m0, m1);
-            const float s0 = fast_exp2(m0 - mm), s1 = fast_exp2(m1 - mm);
-            const float l_all = cb.l[0][h] * s0 + cb.l[1][h] * s1;
+            // 8-bit cache: merge the even-page (this warp) and odd-page states
+            // of head h; a warp with no page in the segment has m = -inf,
+            // l = 0, o = 0
+            float mm = mh[cc], s0 = 1.f, s1 = 0.f, l_all = lh[cc];
+            if constexpr (R == 2) {
+              const float m0 = cb.m[0][h], m1 = cb.m[1][h];
+              mm = fmaxf(m0, m1);
+              s0 = fast_exp2(m0 - mm), s1 = fast_exp2(m1 - mm);
+              l_all = cb.l[0][h] * s0 + cb.l[1][h] * s1;
+            }
             const float inv = 1.f / l_all;
 #pragma unroll
             for (int m = 0; m < D / 16; ++m) {
               const int d = r * (D / 8) + 4 * (m >> 1) + 2 * (m & 1);
-              const float2 w = *reinterpret_cast<const float2*>(&cb.o[h][d]);
-              // elements d, d + 1, the 2^9 of B taken out (exact)
-              const float v0 = (o[m][cc] * s0 + w.x * s1) * (1.f / 512.f);
-              const float v1 = (o[m][2 + cc] * s0 + w.y * s1) * (1.f / 512.f);
+              float2 w = make_float2(0.f, 0.f);
+              if constexpr (R == 2) w = *reinterpret_cast<const float2*>(&cb.o[h][d]);
+              // elements d, d + 1 (for codes the 2^9 of B taken out, exact)
+              const float v0 = (o[m][cc] * s0 + w.x * s1) * OUT_SCALE;
+              const float v1 = (o[m][2 + cc] * s0 + w.y * s1) * OUT_SCALE;
               if (whole) {
                 *reinterpret_cast<uint32_t*>(p.out + ((int64_t)tok * p.n_q + qh) * D + d) =
                     pack_bf16x2(v0 * inv, v1 * inv);
@@ -781,7 +908,7 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
             p.seq_rec[cur.s] = make_int4(c, c_last, slot, (int)F);
           }
         }
-        named_barrier_sync(1 + g, 64);  // the state buffer may be rewritten
+        if (R == 2) named_barrier_sync(1 + g, 64);  // the state buffer may be rewritten
 #pragma unroll
         for (int m = 0; m < D / 16; ++m)
 #pragma unroll
@@ -797,6 +924,7 @@ __global__ void __launch_bounds__(2 * NKV * 32, 1) decode_kernel(const DecodePar
         load_q(cur.s);
       }
     }
+    if (FUSE && stored) bulk_wait_all();  // the stores are complete before the CTA exits
   } else {
   if (is_qk) {
     // ================================================================ QK warp
@@ -1181,7 +1309,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
 constexpr size_t kSmemBudget = 220 * 1024;
 constexpr size_t kSmemBudgetF8 = 226 * 1024;  // below the 227 KB opt-in limit per block
 
-template <int D, int G, int NKV, bool F8, bool FUSE>
+template <int D, int G, int NKV, bool F8, bool FUSE, bool MW>
 cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ctas,
                             cudaStream_t stream) {
   DecodeParams p;
@@ -1225,7 +1353,8 @@ cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ct
   if (nst < 2) return cudaErrorInvalidConfiguration;
   p.nstages = nst;
   const size_t smem = (size_t)nst * p.stage_bytes + fixed;
-  auto kern = decode_kernel<D, G, NKV, F8, FUSE>;
+  auto kern = decode_kernel<D, G, NKV, F8, FUSE, MW>;
+  constexpr int threads = decode_threads<NKV, F8, MW>();
   static int configured_device = -1;  // one attribute set per process and device
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1241,7 +1370,7 @@ cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ct
     // and the cache writes of the step finished before the prefill started)
     cudaLaunchConfig_t pcfg = {};
     pcfg.gridDim = dim3(ctas);
-    pcfg.blockDim = dim3(2 * NKV * 32);
+    pcfg.blockDim = dim3(threads);
     pcfg.dynamicSmemBytes = smem;
     pcfg.stream = stream;
     cudaLaunchAttribute pattr[1];
@@ -1251,7 +1380,7 @@ cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ct
     pcfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&pcfg, kern, p);
   } else {
-    kern<<<ctas, 2 * NKV * 32, smem, stream>>>(p);
+    kern<<<ctas, threads, smem, stream>>>(p);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return e;
@@ -1273,14 +1402,22 @@ cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ct
                : cudaLaunchKernelEx(&cfg, decode_merge_kernel<D, false>, p);
 }
 
+// Tensor-core warps for the 8-bit cache always; for a bf16 cache when the
+// group is 8 (the FMA form's accumulators do not fit its registers there).
+template <bool F8, int G>
+constexpr bool decode_uses_mma() {
+  return F8 || G == 8;
+}
+
 template <int D, int G, bool F8, bool FUSE>
 cudaError_t launch_decode_dg(const AttnArgs& a, const DecodeWorkspace& ws, int ctas,
                              cudaStream_t stream) {
+  constexpr bool MW = decode_uses_mma<F8, G>();
   switch (a.num_kv_heads) {
-    case 1: return launch_decode_t<D, G, 1, F8, FUSE>(a, ws, ctas, stream);
-    case 2: return launch_decode_t<D, G, 2, F8, FUSE>(a, ws, ctas, stream);
-    case 4: return launch_decode_t<D, G, 4, F8, FUSE>(a, ws, ctas, stream);
-    case 8: return launch_decode_t<D, G, 8, F8, FUSE>(a, ws, ctas, stream);
+    case 1: return launch_decode_t<D, G, 1, F8, FUSE, MW>(a, ws, ctas, stream);
+    case 2: return launch_decode_t<D, G, 2, F8, FUSE, MW>(a, ws, ctas, stream);
+    case 4: return launch_decode_t<D, G, 4, F8, FUSE, MW>(a, ws, ctas, stream);
+    case 8: return launch_decode_t<D, G, 8, F8, FUSE, MW>(a, ws, ctas, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -37,7 +37,9 @@ def _decode(lens, nq=32, nkv=8, d=128, seed=0, nb=None, q_lens=None, poison=True
     ([1, 2, 15, 16, 17, 31, 33], 32, 8, 128),  # ragged page tails
     (list(range(1, 700, 7)), 8, 8, 128),       # 100 requests, group 1
     ([5000, 3, 900], 16, 8, 128),              # group 2
-    ([4096, 4095, 1], 64, 8, 128),             # group 8
+    ([4096, 4095, 1], 64, 8, 128),             # group 8 (tensor-core warps)
+    ([300, 77, 1], 32, 4, 64),                 # group 8, d 64
+    ([130, 7, 64], 8, 1, 128),                 # group 8, one kv head
     ([257, 1000], 8, 2, 64),                   # 2 kv heads, d 64
     ([130, 7, 64], 4, 1, 128),                 # multi-query
     ([64, 3000], 16, 4, 64),
@@ -192,6 +194,8 @@ def test_one_long_request_over_every_cta(lens):
     (None, 32, 8, 128, 16),                          # the decode batch
     ([257, 1000, 40], 8, 2, 64, 16),
     ([31, 32, 33, 500], 32, 8, 128, 32),              # 32-token blocks
+    ([1, 2, 15, 16, 17, 33, 300], 64, 8, 128, 16),   # group 8 (tensor-core warps)
+    ([257, 1000, 40], 16, 2, 64, 32),                # group 8, d 64, 32-token blocks
 ])
 def test_fused_decode_step_equals_scatter_then_attention(lens, nq, nkv, d, bs):
     """pa_decode_step (the new rows taken into the page in shared memory and
