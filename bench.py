@@ -507,13 +507,17 @@ def _fp8(args, dev, stream, ops, peaks, bf16_attn_ms):
 
 
 def _other_decodes(args, dev, stream, ops, peaks):
-    """The tiny decode (latency only) and the long-context decode (8 x 32768
-    tokens, HBM-bound), timed like the main line."""
+    """The tiny decode (latency only), the long-context decode (8 x 32768
+    tokens, HBM-bound) and the decode batch at group 8 (64 q / 8 kv heads,
+    the same cache), timed like the main line."""
     import torch
     from paged_kv_cache_174_gb300 import workloads as W
     res = {}
-    for name in ("tiny_decode", "long_decode"):
-        b = W.by_name(name, poison=False)
+    for name in ("tiny_decode", "long_decode", "group8_decode"):
+        if name == "group8_decode":
+            b = W.decode_batch(poison=False, num_q_heads=64)
+        else:
+            b = W.by_name(name, poison=False)
         d = W.to_device(b, dev)
         ws = ops.alloc_workspace(b.num_seqs, b.num_tokens, b.num_q_heads, b.num_kv_heads,
                                  b.head_dim, b.max_q_len, b.max_seq_len, dev)
@@ -521,7 +525,9 @@ def _other_decodes(args, dev, stream, ops, peaks):
         ms, attn_ms = _time_steps(b, d, ws, out, args.steps, args.warmup, stream, ops)
         alg = W.algorithmic_bytes(b)
         gbs = alg["attention"] / (attn_ms * 1e-3) / 1e9
-        res[name] = {"description": W.WORKLOADS[name].description,
+        desc = (W.WORKLOADS[name].description if name in W.WORKLOADS else
+                "decode batch of 64 requests (lens U[128, 4096]) at 64 q / 8 kv heads, d 128")
+        res[name] = {"description": desc,
                      "ms_per_step": round(ms, 5), "attention_ms": round(attn_ms, 5),
                      "attention_GB_per_s": round(gbs, 1),
                      "attention_frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}

@@ -232,13 +232,15 @@ def tiny_decode(poison: bool = True) -> PagedBatch:
 
 
 def decode_batch(poison: bool = True, num_seqs: int = 64, seed: Optional[int] = None,
-                 block_size: int = 16) -> PagedBatch:
-    """block_size 32 keeps the pool's token slots (half as many blocks)."""
+                 block_size: int = 16, num_q_heads: Optional[int] = None) -> PagedBatch:
+    """block_size 32 keeps the pool's token slots (half as many blocks);
+    num_q_heads changes the GQA group over the same cache (64: group 8)."""
     w = WORKLOADS["decode_batch"]
     seed = w.seed if seed is None else seed
     rng = np.random.default_rng(seed + 7)
     lens = rng.integers(128, 4096, size=num_seqs, endpoint=True)
-    return make_batch(w.key, lens, [1] * num_seqs, num_q_heads=w.num_q_heads,
+    nq = w.num_q_heads if num_q_heads is None else num_q_heads
+    return make_batch(w.key, lens, [1] * num_seqs, num_q_heads=nq,
                       num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
                       block_size=block_size, num_blocks=w.num_blocks * w.block_size // block_size,
                       seed=seed, poison=poison)
