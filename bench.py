@@ -523,12 +523,17 @@ def _other_decodes(args, dev, stream, ops, peaks):
                                  b.head_dim, b.max_q_len, b.max_seq_len, dev)
         out = torch.empty_like(d.q)
         ms, attn_ms = _time_steps(b, d, ws, out, args.steps, args.warmup, stream, ops)
+        # the same step as one graph launch (decode-only: the decode kernel
+        # does the scatter), which shows the device latency of a small step
+        # without the host's per-call overhead
+        graph_ms, _ = _time_graph_steps(b, d, args.steps, args.warmup, stream, ops)
         alg = W.algorithmic_bytes(b)
         gbs = alg["attention"] / (attn_ms * 1e-3) / 1e9
         desc = (W.WORKLOADS[name].description if name in W.WORKLOADS else
                 "decode batch of 64 requests (lens U[128, 4096]) at 64 q / 8 kv heads, d 128")
         res[name] = {"description": desc,
                      "ms_per_step": round(ms, 5), "attention_ms": round(attn_ms, 5),
+                     "graph_ms_per_step": round(graph_ms, 5),
                      "attention_GB_per_s": round(gbs, 1),
                      "attention_frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
         del d, ws, out

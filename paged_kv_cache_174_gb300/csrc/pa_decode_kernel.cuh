@@ -747,7 +747,10 @@ __global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int tok = 2 * t + (k & 1) + 8 * (k >> 1);
-          const float pr = fast_exp2(sc4[k] - m_use);  // 0 past the page's end
+          float pr = fast_exp2(sc4[k] - m_use);  // 0 past the page's end
+          // bf16 cache: p enters p * V in bf16, so the sum takes the same
+          // rounded value (numerator and denominator stay consistent)
+          if constexpr (!F8) pr = __uint_as_float(pack_bf16x2(pr, 0.f) << 16);
           lsum += pr;
           // B = P^T; for codes times the token's value scale and 2^9, which
           // keeps the product in f16's normal range for row maxima from about

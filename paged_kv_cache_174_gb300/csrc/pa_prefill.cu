@@ -190,6 +190,15 @@ struct PrefillShared {
   int warp_n[kThreads / 32], warp_tiles[kThreads / 32];
 };
 
+// acc += the two bf16 values of w (low half into x, high half into y),
+// exactly as fp32 additions of the widened values.
+__device__ __forceinline__ void add_bf16x2_to(float2& acc, uint32_t w) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y)
+      : "r"(w));
+}
+
 // Byte offset of 16-byte chunk c (0..7) of row r inside a [rows][64 x bf16]
 // block stored with the 128-byte swizzle (8-row, 1024-byte atoms).
 __device__ __forceinline__ uint32_t sw128_chunk(int r, int c) {
@@ -596,7 +605,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // p = 2^(emul * s - m_ref), packed in bf16 pairs in place (sr[j] holds
         // keys 2j, 2j+1 of this half), stored over the first 32 columns of the
-        // half; a row with no visible key so far gets p = 0
+        // half; a row with no visible key so far gets p = 0.  The row sum adds
+        // the bf16 values the P V product uses, so that the output is an exact
+        // convex combination of V rows with those weights (summing the fp32
+        // values instead leaves numerator and denominator 2^-9 apart, which
+        // rows with few keys of large values showed as errors past 1e-2)
         const float mu = (m_ref == kNegInf) ? 0.f : m_ref;
         const float2 e2 = make_float2(emul, emul);
         const float2 nm2 = make_float2(-mu, -mu);
@@ -607,13 +620,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 32; ++j) {
           const float2 x = __ffma2_rn(
               make_float2(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])), e2, nm2);
-          const float2 pj = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-          l4[j & 3] = __fadd2_rn(l4[j & 3], pj);
-          sr[j] = pack_bf16x2(pj.x, pj.y);
+          sr[j] = pack_bf16x2(fast_exp2(x.x), fast_exp2(x.y));
+          add_bf16x2_to(l4[j & 3], sr[j]);
         }
         tc::tmem_st32(s_cols, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
         l += ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) +
              ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
+
         // rescale this half of the running output when the reference max moved
         // (rare); the P V product of the last tile must have landed first
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
