@@ -202,23 +202,6 @@ __device__ __forceinline__ void fetch_page(const DecodeParams& p, const PageCurs
   }
 }
 
-// Eight E4M3 codes (little-endian in w) -> eight floats, as four pairs.
-__device__ __forceinline__ void e4m3x8_to_float2x4(uint2 w, float2 (&f)[4]) {
-  const uint32_t ws[2] = {w.x, w.y};
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    uint32_t h0, h1;
-    asm("{\n\t.reg .b16 lo, hi;\n\t"
-        "mov.b32 {lo, hi}, %2;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
-        : "=r"(h0), "=r"(h1)
-        : "r"(ws[i]));
-    f[2 * i] = half2_bits_to_float2(h0);
-    f[2 * i + 1] = half2_bits_to_float2(h1);
-  }
-}
-
 template <int N>
 __device__ __forceinline__ void lds_floats(uint32_t addr, float (&v)[N]) {
   if constexpr (N % 4 == 0) {
@@ -266,10 +249,9 @@ __device__ __forceinline__ float reduce_scatter(float (&part)[G], int lane) {
 // of its first token's key row in the stage; FULL pages need no per-token
 // predicate.  sc[it] is the base-2 score of token it * TPI + tok_lane for the
 // head this lane holds after the reduce-scatter (-inf past the page's end).
-//   F8: kb points into the page's codes; ksc at the key scale of this kv head
-//   for the lane's first token (stride n_kv floats per token).
-template <int D, int G, int E_QK, int LPT, uint32_t ROW, bool FULL, bool F8, int NKV>
-__device__ __forceinline__ void qk_scores(const unsigned char* kb, const float* ksc, int ntok,
+// (bf16 cache; the 8-bit cache runs on the tensor cores, qk_scores_mma.)
+template <int D, int G, int E_QK, int LPT, uint32_t ROW, bool FULL>
+__device__ __forceinline__ void qk_scores(const unsigned char* kb, int ntok,
                                           int tok_lane, const float2 (&qf)[G][E_QK / 2],
                                           float (&sc)[kBlock / (32 / LPT)], int lane) {
   constexpr int TPI = 32 / LPT;
@@ -284,14 +266,9 @@ __device__ __forceinline__ void qk_scores(const unsigned char* kb, const float* 
 #pragma unroll
       for (int piece = 0; piece < E_QK / 8; ++piece) {
         float2 k2[4];
-        if constexpr (F8) {
-          e4m3x8_to_float2x4(
-              *reinterpret_cast<const uint2*>(kb + it * TPI * ROW + piece * (D / 2)), k2);
-        } else {
-          const uint4 kw = *reinterpret_cast<const uint4*>(kb + it * TPI * ROW + piece * D);
-          k2[0] = bf16x2_to_float2(kw.x), k2[1] = bf16x2_to_float2(kw.y);
-          k2[2] = bf16x2_to_float2(kw.z), k2[3] = bf16x2_to_float2(kw.w);
-        }
+        const uint4 kw = *reinterpret_cast<const uint4*>(kb + it * TPI * ROW + piece * D);
+        k2[0] = bf16x2_to_float2(kw.x), k2[1] = bf16x2_to_float2(kw.y);
+        k2[2] = bf16x2_to_float2(kw.z), k2[3] = bf16x2_to_float2(kw.w);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
 #pragma unroll
@@ -302,10 +279,7 @@ __device__ __forceinline__ void qk_scores(const unsigned char* kb, const float* 
     float part[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) part[h] = a2[h].x + a2[h].y;
-    float s = reduce_scatter<G, LPT>(part, lane);
-    if constexpr (F8) {
-      if (valid) s *= ksc[it * TPI * NKV];  // ksc already points at this lane's token
-    }
+    const float s = reduce_scatter<G, LPT>(part, lane);
     sc[it] = valid ? s : kNegInf;
   }
 }
@@ -448,12 +422,11 @@ __device__ __forceinline__ void qk_scores_mma(const unsigned char* kb, const flo
 }
 
 // p * V of one page for one PV warp: vb points at this lane's 16-byte piece of
-// its first token's value row, pp at p[tok_lane][0] of the page's hand-off.
-//   F8: vb points into the page's codes; vsc at the value scale of this kv
-//   head for the lane's first token (stride n_kv floats per token).
-template <int D, int G, int LPT, uint32_t ROW, bool FULL, bool F8, int NKV>
-__device__ __forceinline__ void pv_accumulate(const unsigned char* vb, const float* vsc,
-                                              const float* pp, int ntok, int tok_lane,
+// its first token's value row, pp at p[tok_lane][0] of the page's hand-off
+// (bf16 cache).
+template <int D, int G, int LPT, uint32_t ROW, bool FULL>
+__device__ __forceinline__ void pv_accumulate(const unsigned char* vb, const float* pp, int ntok,
+                                              int tok_lane,
                                               float2 (&acc)[G][4]) {
   constexpr int TPI = 32 / LPT;
   constexpr int NIT = kBlock / TPI;
@@ -461,16 +434,9 @@ __device__ __forceinline__ void pv_accumulate(const unsigned char* vb, const flo
   for (int it = 0; it < NIT; ++it) {
     if (FULL || it * TPI + tok_lane < ntok) {
       float2 v2[4];
-      if constexpr (F8) {
-        e4m3x8_to_float2x4(*reinterpret_cast<const uint2*>(vb + it * TPI * ROW), v2);
-        const float s = vsc[it * TPI * NKV];  // vsc already points at this lane's token
-#pragma unroll
-        for (int e = 0; e < 4; ++e) v2[e] = __fmul2_rn(v2[e], make_float2(s, s));
-      } else {
-        const uint4 vw = *reinterpret_cast<const uint4*>(vb + it * TPI * ROW);
-        v2[0] = bf16x2_to_float2(vw.x), v2[1] = bf16x2_to_float2(vw.y);
-        v2[2] = bf16x2_to_float2(vw.z), v2[3] = bf16x2_to_float2(vw.w);
-      }
+      const uint4 vw = *reinterpret_cast<const uint4*>(vb + it * TPI * ROW);
+      v2[0] = bf16x2_to_float2(vw.x), v2[1] = bf16x2_to_float2(vw.y);
+      v2[2] = bf16x2_to_float2(vw.z), v2[3] = bf16x2_to_float2(vw.w);
       float pr[G];
       if constexpr (G % 4 == 0) {
 #pragma unroll
@@ -961,8 +927,6 @@ __global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
     load_q(cur.s);
     // this lane's piece of its first token's key row, relative to a stage
     const uint32_t k_off = (uint32_t)(g * D * ES + dl * 8 * ES) + (uint32_t)tok_lane * ROW;
-    // this kv head's scale of the lane's first token, relative to a stage (F8)
-    const uint32_t ks_off = 2 * p.page_bytes + (uint32_t)(tok_lane * NKV + g) * 4;
     int st = 0, st_phase = 0;
     const unsigned char* stage = stages;
     for (int i = 0; i < n_pages; ++i) {
@@ -983,13 +947,10 @@ __global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
       const bool seg_end = seq_done || (i + 1 == n_pages);
       PBuf<G>& pb = S.pb[g][b];
       float sc[NIT_QK];
-      const float* ksc = reinterpret_cast<const float*>(stage + ks_off);
       if (ntok == kBlock)
-        qk_scores<D, G, E_QK, LPT_QK, ROW, true, F8, NKV>(stage + k_off, ksc, ntok, tok_lane,
-                                                          qf, sc, lane);
+        qk_scores<D, G, E_QK, LPT_QK, ROW, true>(stage + k_off, ntok, tok_lane, qf, sc, lane);
       else
-        qk_scores<D, G, E_QK, LPT_QK, ROW, false, F8, NKV>(stage + k_off, ksc, ntok,
-                                                           tok_lane, qf, sc, lane);
+        qk_scores<D, G, E_QK, LPT_QK, ROW, false>(stage + k_off, ntok, tok_lane, qf, sc, lane);
       // online softmax (base 2) for head my_h over the page's 16 tokens
       float mx = sc[0];
 #pragma unroll
@@ -1058,8 +1019,6 @@ __global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
     // this lane's piece of its first token's value row, relative to a stage
     const uint32_t v_off =
         p.page_bytes + (uint32_t)(g * D * ES + dl * 8 * ES) + (uint32_t)tok_lane * ROW;
-    const uint32_t vs_off =
-        2 * p.page_bytes + p.scale_bytes + (uint32_t)(tok_lane * NKV + g) * 4;
     int st = 0, st_phase = 0;
     const unsigned char* stage = stages;
     for (int i = 0; i < n_pages; ++i) {
@@ -1087,13 +1046,10 @@ __global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
         for (int e = 0; e < 4; ++e) acc[h][e] = __fmul2_rn(acc[h][e], a2);
       }
       const float* pp = &pb.p[tok_lane][0];
-      const float* vsc = reinterpret_cast<const float*>(stage + vs_off);
       if (ntok == kBlock)
-        pv_accumulate<D, G, LPT_PV, ROW, true, F8, NKV>(stage + v_off, vsc, pp, ntok, tok_lane,
-                                                        acc);
+        pv_accumulate<D, G, LPT_PV, ROW, true>(stage + v_off, pp, ntok, tok_lane, acc);
       else
-        pv_accumulate<D, G, LPT_PV, ROW, false, F8, NKV>(stage + v_off, vsc, pp, ntok, tok_lane,
-                                                         acc);
+        pv_accumulate<D, G, LPT_PV, ROW, false>(stage + v_off, pp, ntok, tok_lane, acc);
       const bool seq_done = (cur.j + 1 == cur.np);
       const bool seg_end = seq_done || (i + 1 == n_pages);
       float m_fin[G], l_fin[G];
@@ -1213,15 +1169,18 @@ constexpr int kMergeWarps = 4;
 
 template <int D, bool SPLIT>
 __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const DecodeParams p) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float w_m[kMergeWarps], w_l[kMergeWarps];
   __shared__ float4 w_o[kMergeWarps][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s = blockIdx.x;
   const int h = SPLIT ? (int)blockIdx.y : (int)blockIdx.y * kMergeWarps + warp;
   if (!SPLIT && h >= p.n_q) return;
-  // with SPLIT every early return below is the same for the whole CTA
+  // the request's shape and output row come from the call's inputs, which
+  // are complete before the decode grid starts: read them before waiting for
+  // it (with SPLIT every early return below is the same for the whole CTA)
   if (decode_pages(p, s, false) == 0) return;  // not a (valid) decode request
+  const int a_row = __ldg(p.qsl + s);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int4 rec = p.seq_rec[s];
   const int C = p.ctas;
   const int c_first = rec.x, c_last = rec.y, first_slot = rec.z;
@@ -1277,8 +1236,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
       uint2 wv;
       wv.x = pack_bf16x2(O.x * inv, O.y * inv);
       wv.y = pack_bf16x2(O.z * inv, O.w * inv);
-      const int a = __ldg(p.qsl + s);
-      *reinterpret_cast<uint2*>(p.out + ((int64_t)a * p.n_q + h) * D + lane * 4) = wv;
+      *reinterpret_cast<uint2*>(p.out + ((int64_t)a_row * p.n_q + h) * D + lane * 4) = wv;
     }
     return;
   }
@@ -1304,8 +1262,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
     uint2 wv;
     wv.x = pack_bf16x2(Ot.x * inv, Ot.y * inv);
     wv.y = pack_bf16x2(Ot.z * inv, Ot.w * inv);
-    const int a = __ldg(p.qsl + s);
-    *reinterpret_cast<uint2*>(p.out + ((int64_t)a * p.n_q + h) * D + lane * 4) = wv;
+    *reinterpret_cast<uint2*>(p.out + ((int64_t)a_row * p.n_q + h) * D + lane * 4) = wv;
   }
 }
 
