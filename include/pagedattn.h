@@ -137,7 +137,11 @@ int pa_prefill_splits(int32_t num_tokens, int32_t num_q_heads, int32_t num_kv_he
  *                 it must not be used by another call running concurrently
  * Accumulation is fp32; out is rounded to nearest even.  Rows with q_len == 1
  * run on the split-KV decode kernel, rows of requests with q_len >= 2 on the
- * tensor-core prefill kernel.  A request with q_len > seq_len, seq_len >
+ * tensor-core prefill kernel.  Where p . V runs on the tensor cores (prefill
+ * rows, and decode rows when num_q_heads / num_kv_heads is 8) the softmax
+ * weights enter it rounded to bf16, and the normalising sum adds the same
+ * rounded weights, so every output row is an exact convex combination of V
+ * rows with those weights.  A request with q_len > seq_len, seq_len >
  * max_blocks * block_size or a block id outside [0, num_blocks) flags
  * PA_ERR_DEVICE_BOUNDS.
  */
@@ -255,8 +259,10 @@ int pa_swap_in(pa_bf16 *k_cache, pa_bf16 *v_cache, int32_t num_blocks, int32_t b
  * A row x (head_dim bf16 values) is stored as scale = max |x| / 448 (1 when
  * the row is all zero) and codes e4m3(x_c / scale), rounding to nearest with
  * ties to even and saturating; both divisions are fp32, round to nearest.
- * Attention uses code * scale in place of each cached value.  head_dim is 64
- * or 128.  Only decode rows (q_len 1) are implemented for this cache:
+ * Attention uses code * scale in place of each cached value; the decode
+ * kernel runs q . k and p . V on the tensor cores with q * scale * log2(e)
+ * and p * value scale * 2^9 rounded to f16 (codes convert to f16 exactly;
+ * the 2^9 is removed exactly).  head_dim is 64 or 128.  Only decode rows (q_len 1) are implemented for this cache:
  * pa_paged_attention_fp8 with max_q_len >= 2 returns PA_ERR_UNSUPPORTED.
  *
  * pa_reshape_and_cache_fp8: pa_reshape_and_cache, quantising each new row
