@@ -524,6 +524,10 @@ __global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
   const int64_t f0 = slice_begin(c, F, C), f1 = slice_begin(c + 1, F, C);
   const int n_pages = (int)(f1 - f0);
   if (n_pages <= 0) return;  // uniform: the whole CTA leaves
+  if (MMA && R == 2 && (NST & 1)) {  // see the stage count in the launcher
+    if (threadIdx.x == 0) flag_error(p.err, DEVERR_BOUNDS);
+    return;  // uniform
+  }
 
   // pass 2: locate the request holding flat page f0 (warp 0), start the ring
   if (warp == 0) {
@@ -1310,6 +1314,13 @@ cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ct
   const size_t budget = F8 ? kSmemBudgetF8 : kSmemBudget;
   int nst = (int)((budget - fixed) / p.stage_bytes);
   nst = nst > 8 ? 8 : nst;
+  // The 8-bit kernel's two warps per kv head take alternate pages and wait
+  // only on their own pages' stages.  With an odd stage count a stage would
+  // hold pages of both parities in turn, so a warp could wait on a barrier
+  // two phases ahead, where the phase-parity wait cannot tell the phase it
+  // wants from the one before it; an even count keeps each stage to one
+  // parity (the kernel refuses an odd count).
+  if (F8) nst &= ~1;
   if (nst < 2) return cudaErrorInvalidConfiguration;
   p.nstages = nst;
   const size_t smem = (size_t)nst * p.stage_bytes + fixed;
