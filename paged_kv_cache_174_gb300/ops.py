@@ -148,6 +148,48 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, dim: Optional[int] = N
         raise ValueError(f"{name} must have {dim} dimensions, got {t.dim()}")
 
 
+def _attention_shapes(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc,
+                      out=None):
+    """Shape agreement of an attention call's tensors (the library only sees
+    pointers, so a mismatch here would be an out-of-bounds access there).
+    Returns (T, n_q, d, num_blocks, block_size, n_kv, S)."""
+    if q.dim() != 3 or k_cache.dim() != 4:
+        raise ValueError("q must be [T, n_q, d] and k_cache [num_blocks, block_size, n_kv, d]")
+    T, nq, d = q.shape
+    nb, bs, nkv, d2 = k_cache.shape
+    if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("q / k_cache / v_cache head_dim or shapes disagree")
+    if nkv <= 0 or nq % nkv != 0:
+        raise ValueError(f"num_q_heads {nq} must be a multiple of num_kv_heads {nkv}")
+    if seq_lens.dim() != 1 or query_start_loc.dim() != 1 or block_tables.dim() != 2:
+        raise ValueError("seq_lens [S], query_start_loc [S+1], block_tables [S, maxb] expected")
+    S = seq_lens.shape[0]
+    if query_start_loc.shape[0] != S + 1 or block_tables.shape[0] != S:
+        raise ValueError("seq_lens [S], query_start_loc [S+1], block_tables [S, maxb] disagree")
+    if out is not None and tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must have q's shape")
+    return T, nq, d, nb, bs, nkv, S
+
+
+def _new_rows_shapes(k, v, nkv, d, slot_mapping, name="k"):
+    """k, v [T, n_kv, d] and slot_mapping [T] against a cache's n_kv, d."""
+    if tuple(v.shape) != tuple(k.shape) or k.dim() != 3 or tuple(k.shape[1:]) != (nkv, d):
+        raise ValueError(f"{name} / v{name[1:]} must be [T, n_kv, d] matching the cache")
+    if slot_mapping.dim() != 1 or slot_mapping.shape[0] != k.shape[0]:
+        raise ValueError(f"slot_mapping must be [T] with T = {name}.shape[0]")
+
+
+def _need_workspace(workspace: torch.Tensor) -> None:
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA uint8 tensor")
+
+
+def _need_pairs(pairs: torch.Tensor) -> None:
+    _need(pairs, "src_dst_pairs", torch.int32, 2)
+    if pairs.shape[1] != 2:
+        raise ValueError("src_dst_pairs must be [n, 2]")
+
+
 def version() -> int:
     return int(_load().pa_version())
 
@@ -161,11 +203,10 @@ def reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
     _need(k_cache, "k_cache", torch.bfloat16, 4)
     _need(v_cache, "v_cache", torch.bfloat16, 4)
     _need(slot_mapping, "slot_mapping", torch.int32, 1)
-    if v.shape != k.shape or v_cache.shape != k_cache.shape:
-        raise ValueError("k/v and k_cache/v_cache shapes must match")
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache shapes must match")
     nb, bs, nkv, d = k_cache.shape
-    if k.shape[1:] != (nkv, d) or slot_mapping.shape[0] != k.shape[0]:
-        raise ValueError("k [T, n_kv, d] / slot_mapping [T] do not match the cache")
+    _new_rows_shapes(k, v, nkv, d, slot_mapping)
     _check(L.pa_reshape_and_cache(k.data_ptr(), v.data_ptr(), k.shape[0], k_cache.data_ptr(),
                                   v_cache.data_ptr(), nb, bs, nkv, d, slot_mapping.data_ptr(),
                                   _stream(stream)))
@@ -218,22 +259,14 @@ def paged_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
     _need(block_tables, "block_tables", torch.int32, 2)
     _need(seq_lens, "seq_lens", torch.int32, 1)
     _need(query_start_loc, "query_start_loc", torch.int32, 1)
-    T, nq, d = q.shape
-    nb, bs, nkv, d2 = k_cache.shape
-    if d2 != d or v_cache.shape != k_cache.shape:
-        raise ValueError("q / k_cache / v_cache head_dim or shapes disagree")
-    S = seq_lens.shape[0]
-    if query_start_loc.shape[0] != S + 1 or block_tables.shape[0] != S:
-        raise ValueError("seq_lens [S], query_start_loc [S+1], block_tables [S, maxb] disagree")
+    T, nq, d, nb, bs, nkv, S = _attention_shapes(q, k_cache, v_cache, block_tables, seq_lens,
+                                                 query_start_loc, out)
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", torch.bfloat16, 3)
-    if out.shape != q.shape:
-        raise ValueError("out must have q's shape")
     if workspace is None:
         workspace = alloc_workspace(S, T, nq, nkv, d, max_q_len, max_seq_len, q.device)
-    if workspace.dtype != torch.uint8 or not workspace.is_cuda or not workspace.is_contiguous():
-        raise ValueError("workspace must be a contiguous CUDA uint8 tensor")
+    _need_workspace(workspace)
     if min_q_len >= 2:
         _check(L.pa_paged_attention_qrange(
             q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, nq, nkv, d,
@@ -265,13 +298,17 @@ def decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
     for name, t in (("block_tables", block_tables), ("seq_lens", seq_lens),
                     ("query_start_loc", query_start_loc), ("slot_mapping", slot_mapping)):
         _need(t, name, torch.int32)
-    T, nq, d = q.shape
-    nb, bs, nkv, _ = k_cache.shape
-    S = seq_lens.shape[0]
+    T, nq, d, nb, bs, nkv, S = _attention_shapes(q, k_cache, v_cache, block_tables, seq_lens,
+                                                 query_start_loc, out)
+    _new_rows_shapes(k_new, v_new, nkv, d, slot_mapping, name="k_new")
+    if k_new.shape[0] != T:
+        raise ValueError("k_new / v_new must have one row per query token")
     if out is None:
         out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 3)
     if workspace is None:
         workspace = alloc_workspace(S, T, nq, nkv, d, 1, max_seq_len, q.device)
+    _need_workspace(workspace)
     _check(L.pa_decode_step(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
                             k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, nq, nkv, d,
                             block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),
@@ -287,9 +324,9 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs: tor
     L = _load()
     _need(k_cache, "k_cache", torch.bfloat16, 4)
     _need(v_cache, "v_cache", torch.bfloat16, 4)
-    _need(src_dst_pairs, "src_dst_pairs", torch.int32, 2)
-    if src_dst_pairs.shape[1] != 2:
-        raise ValueError("src_dst_pairs must be [n, 2]")
+    _need_pairs(src_dst_pairs)
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache shapes must match")
     nb, bs, nkv, d = k_cache.shape
     _check(L.pa_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, nkv, d,
                             src_dst_pairs.data_ptr(), src_dst_pairs.shape[0], _stream(stream)))
@@ -370,6 +407,7 @@ def reshape_and_cache_fp8(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tenso
     _need_fp8(k_cache, v_cache, k_scale, v_scale)
     _need(slot_mapping, "slot_mapping", torch.int32, 1)
     nb, bs, nkv, d = k_cache.shape
+    _new_rows_shapes(k, v, nkv, d, slot_mapping)
     _check(L.pa_reshape_and_cache_fp8(k.data_ptr(), v.data_ptr(), k.shape[0], k_cache.data_ptr(),
                                       v_cache.data_ptr(), k_scale.data_ptr(), v_scale.data_ptr(),
                                       nb, bs, nkv, d, slot_mapping.data_ptr(), _stream(stream)))
@@ -387,13 +425,14 @@ def paged_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.T
     for name, t in (("block_tables", block_tables), ("seq_lens", seq_lens),
                     ("query_start_loc", query_start_loc)):
         _need(t, name, torch.int32)
-    T, nq, d = q.shape
-    nb, bs, nkv, _ = k_cache.shape
-    S = seq_lens.shape[0]
+    T, nq, d, nb, bs, nkv, S = _attention_shapes(q, k_cache, v_cache, block_tables, seq_lens,
+                                                 query_start_loc, out)
     if out is None:
         out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 3)
     if workspace is None:
         workspace = alloc_workspace(S, T, nq, nkv, d, max_q_len, max_seq_len, q.device)
+    _need_workspace(workspace)
     _check(L.pa_paged_attention_fp8(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                                     k_scale.data_ptr(), v_scale.data_ptr(), nb, bs, nq, nkv, d,
                                     block_tables.data_ptr(), block_tables.shape[1],
@@ -409,7 +448,7 @@ def copy_blocks_fp8(k_cache, v_cache, k_scale, v_scale, src_dst_pairs: torch.Ten
     """Copy-on-write on the 8-bit cache: codes and scales of block dst <- src."""
     L = _load()
     _need_fp8(k_cache, v_cache, k_scale, v_scale)
-    _need(src_dst_pairs, "src_dst_pairs", torch.int32, 2)
+    _need_pairs(src_dst_pairs)
     nb, bs, nkv, d = k_cache.shape
     _check(L.pa_copy_blocks_fp8(k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(),
                                 v_scale.data_ptr(), nb, bs, nkv, d, src_dst_pairs.data_ptr(),
