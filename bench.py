@@ -152,6 +152,17 @@ def reduce_max(values, dist, device):
     return [float(x) for x in t.cpu()]
 
 
+def _config(b, world):
+    """The workload as the JSON line names it (both arms use the same)."""
+    from paged_kv_cache_174_gb300 import workloads as W
+    return {"workload": b.name, "description": W.WORKLOADS[b.name].description,
+            "num_seqs": b.num_seqs, "num_tokens": b.num_tokens,
+            "kv_tokens": int(b.seq_lens.sum()), "block_size": b.block_size,
+            "algorithmic_bytes_per_step": W.algorithmic_bytes(b)["total"],
+            "l2": "inputs larger than L2 (KV read per step >> 129 MB); no flush",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 def _make(workload: str, rank: int):
     from paged_kv_cache_174_gb300 import workloads as W
     b = W.by_name(workload, poison=False)
@@ -304,6 +315,26 @@ def _time_prefill(b, d, steps, warmup, stream, ops):
     flops = W.causal_flops(sub)
     return {"ms": round(ms, 5), "flops": flops, "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
             "tokens": sub.num_tokens}
+
+
+def _mixed_bounds(b, peaks):
+    """Per-kernel roofline times (ms) of one step of batch b: the scatter and
+    the decode rows against the HBM peak, the chunk's causal FLOPs against
+    the bf16 tensor peak (burst: the step is short)."""
+    from paged_kv_cache_174_gb300 import workloads as W
+    kv_row = b.num_kv_heads * b.head_dim * 2
+    dec = b.q_lens == 1
+    dec_bytes = int(b.seq_lens[dec].astype(np.int64).sum()) * 2 * kv_row
+    dec_bytes += 2 * int(dec.sum()) * b.num_q_heads * b.head_dim * 2
+    dec_bytes += sum(-(-int(L) // b.block_size) for L in b.seq_lens[dec]) * 4
+    flops = W.causal_flops(b)
+    scatter = W.algorithmic_bytes(b)["scatter"]
+    t_dec = dec_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3
+    t_pre = flops / (peaks["bf16_tflops"] * 1e12) * 1e3
+    t_sc = scatter / (peaks["hbm_gbs"] * 1e9) * 1e3
+    return {"decode_bytes": dec_bytes, "chunk_flops": flops, "scatter_bytes": scatter,
+            "decode_bound_ms": round(t_dec, 5), "chunk_bound_ms": round(t_pre, 5),
+            "scatter_bound_ms": round(t_sc, 5), "sum_bound_ms": round(t_dec + t_pre + t_sc, 5)}
 
 
 def _run_trace(dev, stream, ops, warmup):
@@ -506,7 +537,7 @@ def _fp8(args, dev, stream, ops, peaks, bf16_attn_ms):
             "attention_speedup_vs_bf16": round(bf16_attn_ms / attn_ms, 3)}
 
 
-def _other_decodes(args, dev, stream, ops, peaks):
+def _other_decodes(args, dev, stream, ops, peaks, host_batches=None):
     """The tiny decode (latency only), the long-context decode (8 x 32768
     tokens, HBM-bound) and the decode batch at group 8 (64 q / 8 kv heads,
     the same cache), timed like the main line."""
@@ -518,6 +549,8 @@ def _other_decodes(args, dev, stream, ops, peaks):
             b = W.decode_batch(poison=False, num_q_heads=64)
         else:
             b = W.by_name(name, poison=False)
+            if host_batches is not None:
+                host_batches[name] = b
         d = W.to_device(b, dev)
         ws = ops.alloc_workspace(b.num_seqs, b.num_tokens, b.num_q_heads, b.num_kv_heads,
                                  b.head_dim, b.max_q_len, b.max_seq_len, dev)
@@ -580,6 +613,37 @@ def _block32(args, dev, stream, ops, peaks):
     return res
 
 
+def _summary(line):
+    """The headline numbers again, compact, last in the line."""
+    out = {"decode_batch_GBps": line.get("value"),
+           "decode_attention_frac_hbm": _dig(line, ("roofline", "frac")),
+           "e2e_GBps": _dig(line, ("e2e", "value")),
+           "mixed_graph_tokens_per_s": _dig(line, ("mixed_batch", "graph_tokens_per_s")),
+           "mixed_roofline_frac": _dig(line, ("mixed_batch", "roofline", "frac")),
+           "prefill_frac_bf16": _dig(line, ("roofline_prefill", "frac")),
+           "prefill_TFLOPs": _dig(line, ("roofline_prefill", "achieved")),
+           "trace_graph_tokens_per_s": _dig(line, ("trace", "step_graph", "tokens_per_s")),
+           "fp8_decode_frac_hbm": _dig(line, ("fp8_cache", "roofline", "frac")),
+           "long_decode_frac_hbm": _dig(line, ("other_decodes", "long_decode",
+                                               "attention_frac_of_hbm")),
+           "group8_decode_frac_hbm": _dig(line, ("other_decodes", "group8_decode",
+                                                 "attention_frac_of_hbm"))}
+    cb = line.get("cpu_baselines")
+    if cb:
+        out["oracle_all_cores"] = {k: [v["value"], v["unit"]] for k, v in cb.items()}
+        out["oracle_one_core"] = {k: v["one_core_value"] for k, v in cb.items()}
+        out["oracle_cores"] = next(iter(cb.values()))["cores"]
+    return out
+
+
+def _dig(d, keys):
+    for k in keys:
+        if not isinstance(d, dict) or k not in d:
+            return None
+        d = d[k]
+    return d
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -596,6 +660,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     b = _make(args.workload, rank)
+    host_batches = {b.name: b}  # the CPU baseline times the oracle on these
     d = W.to_device(b, dev)
     alg = W.algorithmic_bytes(b)
     step_bytes = alg["total"]
@@ -684,12 +749,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16, shuffled physical blocks)",
-        "config": {"workload": b.name, "description": W.WORKLOADS[b.name].description,
-                   "num_seqs": b.num_seqs, "num_tokens": b.num_tokens,
-                   "kv_tokens": int(b.seq_lens.sum()), "block_size": b.block_size,
-                   "algorithmic_bytes_per_step": step_bytes,
-                   "l2": "inputs larger than L2 (KV read per step >> 129 MB); no flush",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": _config(b, world),
         "tokens_per_s": round(b.num_tokens * world / (ms * 1e-3), 1),
         "pct_of_hbm_peak": round(100.0 * gbs / world / peaks["hbm_gbs"], 2),
         "roofline": {"bound": "hbm", "kernel": "pa_paged_attention (split-KV decode + merge)",
@@ -726,13 +786,23 @@ def run_ours(args):
         if not torch.equal(mgout[:mb.num_tokens].view(torch.int16), mout.view(torch.int16)):
             raise RuntimeError("the mixed step's graph output differs from separate launches'")
         pre = _time_prefill(mb, md, args.steps, args.warmup, stream, ops)
+        bounds = _mixed_bounds(mb, peaks)
         line["mixed_batch"] = {
             "workload": mb.name, "description": W.WORKLOADS[mb.name].description,
             "tokens_per_s": round(mb.num_tokens * world / (mms * 1e-3), 1),
             "ms_per_step": round(mms, 5), "attention_ms": round(mattn, 5),
             "graph_tokens_per_s": round(mb.num_tokens * world / (mgms * 1e-3), 1),
             "graph_ms_per_step": round(mgms, 5),
-            "gpu_launches": _launch_count(mb) * args.steps}
+            "gpu_launches": _launch_count(mb) * args.steps,
+            "roofline": {"bound": "mixed (hbm + tensor)",
+                         "frac": round(bounds["sum_bound_ms"] / mgms, 4),
+                         "frac_separate_launches": round(bounds["sum_bound_ms"] / mms, 4),
+                         "definition": "sum over the step's kernels of their roofline time "
+                                       "(decode and scatter bytes / HBM peak, chunk causal "
+                                       "FLOPs / bf16 burst peak) / measured step time "
+                                       "(one graph launch per step)",
+                         **bounds}}
+        host_batches["mixed_step"] = mb
         if pre:
             line["roofline_prefill"] = {
                 "bound": "tensor", "kernel": "prefill chunk alone (tcgen05)",
@@ -749,11 +819,18 @@ def run_ours(args):
     if not args.no_block32:
         line["block_size_32"] = _block32(args, dev, stream, ops, peaks)
     if not args.no_other_decodes:
-        line["other_decodes"] = _other_decodes(args, dev, stream, ops, peaks)
+        line["other_decodes"] = _other_decodes(args, dev, stream, ops, peaks, host_batches)
     if not args.no_fp8:
         line["fp8_cache"] = _fp8(args, dev, stream, ops, peaks, attn_ms)
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(b, args.cpu_seconds)
+        cb = cpu_baselines(host_batches, trace_rows_full=args.cpu_full)
+        main = cb.get(b.name)
+        line["cpu_baseline"] = {"value": main["value"], "unit": main["unit"],
+                                "cores": main["cores"], "kind": "oracle",
+                                "single_thread_value": main["one_core_value"],
+                                "sample": main["sample"]}
+        line["cpu_baselines"] = cb
+    line["summary"] = _summary(line)
     if world > 1:
         dist.destroy_process_group()
     if rank == 0:
@@ -785,31 +862,184 @@ def _oracle_sample_step(b, n_seqs, rng, threads=0):
     return dt, W.algorithmic_bytes(sub)["total"], len(idx)
 
 
-def cpu_baseline(b, seconds: float):
-    """The oracle, as it stands, on the host cores: repeated passes over
-    random samples of the batch's requests until ~`seconds` of CPU time."""
+def _oracle_full_step(b, threads=0):
+    """One oracle pass over the whole batch b: scatter of the new tokens, then
+    attention of every row.  Returns seconds."""
     import oracle
-    rng = np.random.default_rng(0)
-    n_seqs = max(1, min(b.num_seqs, 8))
-    total_t, total_b, passes = 0.0, 0, 0
-    while total_t < seconds and passes < 1000:
-        dt, nb, _ = _oracle_sample_step(b, n_seqs, rng)
-        total_t += dt
-        total_b += nb
-        passes += 1
-    # the same on one thread, for a bounded ~2 s
-    t1, b1, p1 = 0.0, 0, 0
-    while t1 < min(2.0, seconds) and p1 < 100:
-        dt, nb, _ = _oracle_sample_step(b, n_seqs, rng, threads=1)
-        t1 += dt
-        b1 += nb
-        p1 += 1
-    return {"value": round(total_b / total_t / 1e9, 4), "unit": "GB/s",
-            "cores": oracle.num_threads(), "kind": "oracle",
-            "single_thread_value": round(b1 / t1 / 1e9, 4),
-            "sample": f"{passes} passes, each over {n_seqs} random requests of the batch "
-                      f"(scatter + attention), {total_t:.1f} s total; one thread: {p1} "
-                      f"passes, {t1:.1f} s"}
+    kc, vc = b.k_cache, b.v_cache
+    t = time.perf_counter()
+    oracle.reshape_and_cache(b.k_new, b.v_new, kc, vc, b.slot_mapping)
+    oracle.paged_attention(b.q, kc, vc, b.block_tables, b.seq_lens, b.query_start_loc,
+                           b.scale, threads=threads)
+    return time.perf_counter() - t
+
+
+def _oracle_rows(b, samples, threads=0):
+    """The oracle on the given (sequence, row, q head) samples of batch b
+    (its cache already holds the step's new tokens).  Returns seconds."""
+    import oracle
+    t = time.perf_counter()
+    oracle.paged_attention_rows(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens,
+                                b.query_start_loc, b.scale, samples, threads=threads)
+    return time.perf_counter() - t
+
+
+def _all_rows(b, seqs, every=1, rng=None):
+    """(sequence, row, q head) triples of the given sequences; with every > 1
+    one row in `every` of each sequence (a random offset), all q heads."""
+    out = []
+    for s in seqs:
+        n = int(b.q_lens[s])
+        start = int(rng.integers(0, every)) if (rng is not None and every > 1) else 0
+        for i in range(min(start, max(n - 1, 0)), n, every):
+            out.extend((s, i, h) for h in range(b.num_q_heads))
+    return np.array(out, np.int32).reshape(-1, 3)
+
+
+def _cpu_decode(b, unit_bytes, one_core_frac=1.0):
+    """A decode batch (C1-C3): the oracle over the whole batch on all cores;
+    on one core the whole batch, or a random fraction of its requests (the
+    unit is bytes per second, so a sample gives the rate directly)."""
+    from paged_kv_cache_174_gb300 import workloads as W
+    import oracle
+    t_all = _oracle_full_step(b)
+    reps = 1
+    while t_all < 0.5 and reps < 1000:  # small batches: repeat for a stable time
+        t_all += _oracle_full_step(b)
+        reps += 1
+    alg = W.algorithmic_bytes(b)["total"]
+    rng = np.random.default_rng(3)
+    if one_core_frac >= 1.0:
+        t1 = _oracle_full_step(b, threads=1)
+        b1, what1 = alg, "the whole batch"
+    else:
+        n = max(1, int(round(b.num_seqs * one_core_frac)))
+        dt, b1, _ = _oracle_sample_step(b, n, rng, threads=1)
+        t1, what1 = dt, f"{n} random requests of {b.num_seqs}"
+    return {"unit": unit_bytes, "cores": oracle.num_threads(),
+            "value": round(alg * reps / t_all / 1e9, 4),
+            "seconds": round(t_all / reps, 4),
+            "one_core_value": round(b1 / t1 / 1e9, 4),
+            "sample": f"all cores: the whole batch (scatter + attention), {reps} pass(es); "
+                      f"one core: {what1}"}
+
+
+def _cpu_mixed(b):
+    """The mixed step (C4): the whole step on all cores; on one core every
+    decode row and one chunk row in 16 (all q heads), the chunk's time scaled
+    by the rows it stands for."""
+    import oracle
+    t_all = _oracle_full_step(b)
+    rng = np.random.default_rng(4)
+    dec = [s for s in range(b.num_seqs) if b.q_lens[s] == 1]
+    pre = [s for s in range(b.num_seqs) if b.q_lens[s] >= 2]
+    t_dec = _oracle_rows(b, _all_rows(b, dec), threads=1)
+    smp = _all_rows(b, pre, every=16, rng=rng)
+    t_pre = _oracle_rows(b, smp, threads=1)
+    n_pre = int(sum(b.q_lens[s] for s in pre)) * b.num_q_heads
+    t1 = t_dec + t_pre * n_pre / max(len(smp), 1)
+    return {"unit": "tokens/s", "cores": oracle.num_threads(),
+            "value": round(b.num_tokens / t_all, 2), "seconds": round(t_all, 4),
+            "one_core_value": round(b.num_tokens / t1, 3),
+            "one_core_seconds_estimated": round(t1, 3),
+            "sample": "all cores: the whole step (scatter + attention of all 640 rows); one "
+                      "core: all decode rows, and 1 in 16 chunk rows (all q heads) with the "
+                      "chunk's time scaled by 16"}
+
+
+def _cpu_trace(every=10, full_rows=True):
+    """The continuous-batching trace (C5): every step's copy-on-write copies
+    and scatter replayed in the oracle, attention of every `every`-th step
+    timed (all its rows on all cores, or 1 in 8 chunk rows when full_rows is
+    False); on one core the attention of one timed step in 10, 1 in 16 chunk
+    rows, scaled.  The q / k / v values are drawn with torch's CPU generator
+    (the oracle's time does not depend on them)."""
+    import oracle
+    import torch
+    from paged_kv_cache_174_gb300 import workloads as W
+    from paged_kv_cache_174_gb300.host import CONTINUOUS_BATCHING_TRACE, ContinuousBatchingTrace
+
+    cfg = CONTINUOUS_BATCHING_TRACE
+    tr = ContinuousBatchingTrace(cfg)
+    plans = [tr.step() for _ in range(cfg.steps)]
+    kc, vc = W.trace_initial_cache(cfg, tr.prefix_blocks, poison=False)
+    gen = torch.Generator().manual_seed(cfg.seed)
+
+    def bits(*shape):
+        return torch.randn(*shape, generator=gen).bfloat16().view(torch.int16).numpy().view(
+            np.uint16)
+
+    rng = np.random.default_rng(5)
+    scale = 1.0 / np.sqrt(cfg.head_dim)
+    t_all = t_one = 0.0
+    toks = toks_one = timed = 0
+    for p in plans:
+        if p.num_tokens == 0:
+            continue
+        T = p.num_tokens
+        k, v = bits(T, cfg.num_kv_heads, cfg.head_dim), bits(T, cfg.num_kv_heads, cfg.head_dim)
+        take = p.index % every == 0
+        t0 = time.perf_counter()
+        if len(p.copy_pairs):
+            oracle.copy_blocks(kc, vc, p.copy_pairs)
+        oracle.reshape_and_cache(k, v, kc, vc, p.slot_mapping)
+        t_io = time.perf_counter() - t0
+        if not take:
+            continue
+        q = bits(T, cfg.num_q_heads, cfg.head_dim)
+        b = W.PagedBatch(name="trace", q=q, k_new=k, v_new=v, k_cache=kc, v_cache=vc,
+                         block_tables=p.block_tables, seq_lens=p.seq_lens,
+                         query_start_loc=p.query_start_loc, slot_mapping=p.slot_mapping,
+                         scale=scale, block_size=cfg.block_size, seed=cfg.seed)
+        ql = b.q_lens
+        if full_rows:
+            t0 = time.perf_counter()
+            oracle.paged_attention(q, kc, vc, p.block_tables, p.seq_lens, p.query_start_loc,
+                                   scale)
+            t_all += t_io + time.perf_counter() - t0
+        else:
+            dec = [s for s in range(b.num_seqs) if ql[s] == 1]
+            pre = [s for s in range(b.num_seqs) if ql[s] >= 2]
+            t_d = _oracle_rows(b, _all_rows(b, dec))
+            smp = _all_rows(b, pre, every=8, rng=rng)
+            t_p = _oracle_rows(b, smp) if len(smp) else 0.0
+            n_pre = int(sum(ql[s] for s in pre)) * b.num_q_heads
+            t_all += t_io + t_d + t_p * n_pre / max(len(smp), 1)
+        toks += T
+        if timed % 10 == 0:
+            dec = [s for s in range(b.num_seqs) if ql[s] == 1]
+            pre = [s for s in range(b.num_seqs) if ql[s] >= 2]
+            t_d = _oracle_rows(b, _all_rows(b, dec), threads=1)
+            smp = _all_rows(b, pre, every=16, rng=rng)
+            t_p = _oracle_rows(b, smp, threads=1) if len(smp) else 0.0
+            n_pre = int(sum(ql[s] for s in pre)) * b.num_q_heads
+            t_one += t_io + t_d + t_p * n_pre / max(len(smp), 1)
+            toks_one += T
+        timed += 1
+    rows = "all rows" if full_rows else "all decode rows and 1 in 8 chunk rows (scaled)"
+    return {"unit": "tokens/s", "cores": oracle.num_threads(),
+            "value": round(toks / t_all, 2), "seconds": round(t_all, 3),
+            "one_core_value": round(toks_one / t_one, 3),
+            "sample": f"all cores: {timed} steps (every {every}th of 200), {rows}, plus "
+                      f"their copies and scatter (the other steps' copies and scatter "
+                      f"replayed untimed); one core: one timed step in 10, all decode rows "
+                      f"and 1 in 16 chunk rows with the chunk's time scaled by 16"}
+
+
+def cpu_baselines(host_batches, trace_rows_full):
+    """The oracle on every workload, on all host cores and on one core."""
+    res = {}
+    if "tiny_decode" in host_batches:
+        res["tiny_decode"] = _cpu_decode(host_batches["tiny_decode"], "GB/s")
+    if "decode_batch" in host_batches:
+        res["decode_batch"] = _cpu_decode(host_batches["decode_batch"], "GB/s")
+    if "long_decode" in host_batches:
+        res["long_decode"] = _cpu_decode(host_batches["long_decode"], "GB/s",
+                                         one_core_frac=0.25)
+    if "mixed_step" in host_batches:
+        res["mixed_step"] = _cpu_mixed(host_batches["mixed_step"])
+    res["trace"] = _cpu_trace(full_rows=trace_rows_full)
+    return res
 
 
 def run_reference(args):
@@ -837,11 +1067,11 @@ def run_reference(args):
         "ms_per_step": round(1e3 * sum(ts) / len(ts), 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) bf16, shuffled physical blocks)",
-        "config": {"workload": b.name, "description": W.WORKLOADS[b.name].description,
-                   "sample_requests_per_step": n_seqs},
+        "config": _config(b, world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
                          "kind": "oracle",
-                         "sample": f"each step: {n_seqs} random requests of the batch"},
+                         "sample": f"each step: {n_seqs} random requests of the batch "
+                                   f"(scatter + attention)"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -856,7 +1086,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_batch",
                     choices=["tiny_decode", "decode_batch", "long_decode", "mixed_step"])
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-full", action="store_true",
+                    help="time the oracle on every row of the trace's sampled steps "
+                         "(default: all decode rows and 1 in 8 chunk rows)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-mixed", action="store_true",
                     help="skip the mixed chunked-prefill step measurement")

@@ -331,9 +331,13 @@ int pa_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
  * (pa_noalloc_scratch_bytes() bytes, 8 MiB, held on every device that loads
  * the library until the process exits).  A call needing more scratch than
  * that (see pa_workspace_size) returns PA_ERR_WORKSPACE.  Allocates nothing.
- * The first call on a device looks up the array's device address (make it
- * before any stream capture).  Calls share the array, so calls whose
- * executions overlap on the GPU race and must be serialised by the caller.
+ * The first call on a device looks up the array's device address and keeps
+ * it for the life of the process: make that first call before any stream
+ * capture (a call with num_seqs = 0 and a valid cache geometry does only
+ * this set-up and launches nothing), and do not use the library across a
+ * cudaDeviceReset, after which the kept address is stale.  Calls share the
+ * array, so calls whose executions overlap on the GPU race and must be
+ * serialised by the caller.
  */
 size_t pa_noalloc_scratch_bytes(void);
 

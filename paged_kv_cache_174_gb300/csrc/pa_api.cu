@@ -114,6 +114,7 @@ int pa_reshape_and_cache(const pa_bf16* k, const pa_bf16* v, int32_t num_tokens,
   unsigned* err = nullptr;
   st = device_state(&err, nullptr);
   if (st) return st;
+  pa::NvtxRange range("pa_reshape_and_cache (slot scatter)");
   cudaError_t e = pa::launch_reshape_and_cache(
       k, v, num_tokens, k_cache, v_cache, (int64_t)num_blocks * block_size,
       num_kv_heads * head_dim, slot_mapping, err, stream);
@@ -136,6 +137,7 @@ int pa_copy_blocks(pa_bf16* k_cache, pa_bf16* v_cache, int32_t num_blocks, int32
   unsigned* err = nullptr;
   st = device_state(&err, nullptr);
   if (st) return st;
+  pa::NvtxRange range("pa_copy_blocks (copy-on-write)");
   cudaError_t e = pa::launch_copy_blocks(k_cache, v_cache, num_blocks,
                                          (int64_t)block_size * num_kv_heads * head_dim,
                                          src_dst_pairs, num_pairs, err, stream);
@@ -161,6 +163,7 @@ int pa_reshape_and_cache_fp8(const pa_bf16* k, const pa_bf16* v, int32_t num_tok
   unsigned* err = nullptr;
   st = device_state(&err, nullptr);
   if (st) return st;
+  pa::NvtxRange range("pa_reshape_and_cache_fp8 (quantising slot scatter)");
   cudaError_t e = pa::launch_reshape_and_cache_fp8(
       k, v, num_tokens, k_cache, v_cache, k_scale, v_scale, (int64_t)num_blocks * block_size,
       num_kv_heads, head_dim, slot_mapping, err, stream);
@@ -189,6 +192,7 @@ int pa_copy_blocks_fp8(uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float
   unsigned* err = nullptr;
   st = device_state(&err, nullptr);
   if (st) return st;
+  pa::NvtxRange range("pa_copy_blocks_fp8 (copy-on-write)");
   // the copy kernel moves 16-byte vectors; sizes are given in 2-byte units
   cudaError_t e = pa::launch_copy_blocks(reinterpret_cast<uint16_t*>(k_cache),
                                          reinterpret_cast<uint16_t*>(v_cache), num_blocks,
@@ -227,6 +231,7 @@ int swap_blocks(pa_bf16* k_cache, pa_bf16* v_cache, int32_t num_blocks, int32_t 
   unsigned* err = nullptr;
   st = device_state(&err, nullptr);
   if (st) return st;
+  pa::NvtxRange range(out ? "pa_swap_out" : "pa_swap_in");
   cudaError_t e = pa::launch_swap(k_cache, v_cache, num_blocks,
                                   (int64_t)block_size * num_kv_heads * head_dim, block_ids, n,
                                   staging, host_k, host_v, out, err, stream);
@@ -481,6 +486,8 @@ int paged_attention_impl(const pa_bf16* q, KvCache kv,
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   if (max_q_len >= 2) {
+    pa::NvtxRange range(plan.nsplit > 1 ? "prefill (tcgen05) + key-piece merge"
+                                        : "prefill (tcgen05)");
     cudaError_t e = pa::launch_prefill(a, plan, ws + need_decode, sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     // with key pieces the merge kernel comes last and must not be overtaken
@@ -488,6 +495,9 @@ int paged_attention_impl(const pa_bf16* q, KvCache kv,
   }
   if (a.no_decode) return PA_OK;  // no request has a single query row
   pa::DecodeWorkspace dws = pa::decode_workspace(ws, ctas, num_seqs, num_q_heads, head_dim);
+  pa::NvtxRange range(fuse    ? "decode step (scatter + split-KV decode) + merge"
+                      : kv.fp8 ? "8-bit split-KV decode + merge"
+                               : "split-KV decode + merge");
   cudaError_t e = pa::launch_decode(a, dws, ctas, stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return PA_OK;
@@ -544,8 +554,11 @@ int pa_check_device_errors(cudaStream_t stream) {
 // every GPU that loads the library holds it until the process exits.
 //
 // Its device address is looked up once per device, on the first call made on
-// that device (with the device current); make that first call before any
-// stream capture begins.  All calls share the array and it keeps whatever the
+// that device (with the device current), and kept for the life of the
+// process, like the error word's: after a cudaDeviceReset both are stale, so
+// the library must not be used across one.  Make that first call before any
+// stream capture begins; a call with no requests does the look-up and
+// launches nothing.  All calls share the array and it keeps whatever the
 // last call left there: nothing in it needs to start at zero, but calls whose
 // executions overlap on the GPU (different streams, or different threads on
 // one device) race on it and must be serialised by the caller.

@@ -141,6 +141,7 @@ int pa_step_graph_launch(pa_step_graph* g, cudaStream_t stream) {
   if (dev != g->device)
     return pa::api_fail(PA_ERR_INVALID_ARG, "graph was built on device %d, current is %d",
                         g->device, dev);
+  pa::NvtxRange range("pa_step_graph_launch");
   cudaError_t e = cudaGraphLaunch(g->exec, stream);
   if (e != cudaSuccess) return graph_fail(e, "cudaGraphLaunch");
   return PA_OK;

@@ -5,8 +5,20 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 namespace pa {
+
+// A named NVTX range over a scope of host code (the launches of one call), so
+// that a profiler groups each kernel under the library call that issued it.
+// NVTX is header-only: with no tool attached a push or pop is a test of a
+// function pointer and nothing else.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Bits of the device error word (read back by pa_check_device_errors).
 enum : unsigned {

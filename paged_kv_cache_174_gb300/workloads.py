@@ -391,10 +391,13 @@ def trace_initial_cache(cfg, prefix_blocks, poison: bool = True):
     """Pool for the trace: the shared prefix's K/V written into its blocks,
     every other slot poisoned (or zero)."""
     rng = np.random.default_rng(cfg.seed + 1)
-    fill = BF16_NAN if poison else np.uint16(0)
     shape = (cfg.num_blocks, cfg.block_size, cfg.num_kv_heads, cfg.head_dim)
-    kc = np.full(shape, fill, dtype=np.uint16)
-    vc = np.full(shape, fill, dtype=np.uint16)
+    if poison:
+        kc = np.full(shape, BF16_NAN, dtype=np.uint16)
+        vc = np.full(shape, BF16_NAN, dtype=np.uint16)
+    else:  # zero pages are mapped lazily: only the slots a run writes cost memory
+        kc = np.zeros(shape, dtype=np.uint16)
+        vc = np.zeros(shape, dtype=np.uint16)
     kf = kc.reshape(-1, cfg.num_kv_heads, cfg.head_dim)
     vf = vc.reshape(-1, cfg.num_kv_heads, cfg.head_dim)
     pos = np.arange(cfg.prefix)
