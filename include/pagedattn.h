@@ -194,6 +194,36 @@ int pa_decode_step(const pa_bf16 *q, const pa_bf16 *k_new, const pa_bf16 *v_new,
                    void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * One serving step's slot scatter and attention, for any mix of decode rows
+ * and chunked-prefill rows ("PagedAttention 显存分页与连续批处理(Continuous
+ * Batching)实战", Chunked Prefill section: each iteration mixes prompt
+ * slices with the running decodes), without a separate scatter kernel:
+ * pa_reshape_and_cache followed by pa_paged_attention, in the attention
+ * kernels themselves.  The tensor-core kernel takes a prefill request's new
+ * key and value rows (tokens query_start_loc[s] ..) from k_new / v_new rather
+ * than from the cache, and stores them to their slots while it runs; the
+ * decode kernel does the same for decode rows (as pa_decode_step).  Outputs
+ * and the cache afterwards are bit-identical to the two separate calls.
+ * Precondition: slot_mapping[t] of query row i of request s is the slot of
+ * its position seq_lens[s] - q_len + i (its block table entry).  A prefill
+ * row with any other slot is not stored and flags PA_ERR_DEVICE_BOUNDS (its
+ * attention still uses its k_new / v_new row); a decode row follows
+ * pa_decode_step (a negative slot reads the cache's row, any other slot
+ * flags).  Tokens outside every request are not written.  bf16 cache only;
+ * arguments, workspace and errors otherwise as pa_reshape_and_cache and
+ * pa_paged_attention.
+ */
+int pa_paged_attention_step(const pa_bf16 *q, const pa_bf16 *k_new, const pa_bf16 *v_new,
+                            pa_bf16 *k_cache, pa_bf16 *v_cache, int32_t num_blocks,
+                            int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads,
+                            int32_t head_dim, const int32_t *block_tables, int32_t max_blocks,
+                            const int32_t *seq_lens, const int32_t *query_start_loc,
+                            int32_t num_seqs, int32_t num_tokens, int32_t max_q_len,
+                            int32_t max_seq_len, const int32_t *slot_mapping, float scale,
+                            pa_bf16 *out, void *workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+
+/*
  * Copy-on-write block copy: for each pair i, physical block
  * src_dst_pairs[2i+1] of both caches becomes a bit copy of block
  * src_dst_pairs[2i] ("PagedAttention 显存分页与连续批处理实战", comparison
@@ -368,8 +398,9 @@ int pa_paged_attention_noalloc(const pa_bf16 *q, const pa_bf16 *k_cache,
  *   - copy pairs i >= the step's count: copy_pairs[2i] = -1 (skipped).
  * A step's sizes must stay within the maxima (max_q_len and max_seq_len
  * included: a request beyond them flags PA_ERR_DEVICE_BOUNDS at run time).
- * With max_q_len 1 the graph runs scatter + attention as pa_decode_step (one
- * kernel; its slot precondition applies).
+ * The graph runs scatter + attention as pa_decode_step (max_q_len 1) or
+ * pa_paged_attention_step (no scatter kernel); their slot precondition
+ * applies.
  * Rows of out that belong to no request are left as they were.
  *
  * If host_meta is not NULL, every launch first copies meta_bytes from

@@ -313,7 +313,8 @@ int paged_attention_impl(const pa_bf16* q, KvCache kv,
                          pa_bf16* out, void* workspace, size_t workspace_bytes, size_t split_cap,
                          cudaStream_t stream, const pa_bf16* fuse_k_new = nullptr,
                          const pa_bf16* fuse_v_new = nullptr,
-                         const int32_t* fuse_slot_mapping = nullptr);
+                         const int32_t* fuse_slot_mapping = nullptr,
+                         bool fuse_any_q_len = false);
 
 }  // namespace
 
@@ -364,6 +365,24 @@ int pa_decode_step(const pa_bf16* q, const pa_bf16* k_new, const pa_bf16* v_new,
                               stream, k_new, v_new, slot_mapping);
 }
 
+int pa_paged_attention_step(const pa_bf16* q, const pa_bf16* k_new, const pa_bf16* v_new,
+                            pa_bf16* k_cache, pa_bf16* v_cache, int32_t num_blocks,
+                            int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads,
+                            int32_t head_dim, const int32_t* block_tables, int32_t max_blocks,
+                            const int32_t* seq_lens, const int32_t* query_start_loc,
+                            int32_t num_seqs, int32_t num_tokens, int32_t max_q_len,
+                            int32_t max_seq_len, const int32_t* slot_mapping, float scale,
+                            pa_bf16* out, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  if (!slot_mapping && num_tokens > 0)
+    return fail(PA_ERR_INVALID_ARG, "null pointer argument (slot_mapping)");
+  return paged_attention_impl(q, KvCache{k_cache, v_cache, nullptr, nullptr, false}, num_blocks,
+                              block_size, num_q_heads, num_kv_heads, head_dim, block_tables,
+                              max_blocks, seq_lens, query_start_loc, num_seqs, num_tokens, 0,
+                              max_q_len, max_seq_len, scale, out, workspace, workspace_bytes,
+                              ~size_t(0), stream, k_new, v_new, slot_mapping, true);
+}
+
 int pa_paged_attention_fp8(const pa_bf16* q, const uint8_t* k_cache, const uint8_t* v_cache,
                            const float* k_scale, const float* v_scale, int32_t num_blocks,
                            int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads,
@@ -392,7 +411,7 @@ int paged_attention_impl(const pa_bf16* q, KvCache kv,
                          pa_bf16* out, void* workspace, size_t workspace_bytes, size_t split_cap,
                          cudaStream_t stream, const pa_bf16* fuse_k_new,
                          const pa_bf16* fuse_v_new,
-                         const int32_t* fuse_slot_mapping) {
+                         const int32_t* fuse_slot_mapping, bool fuse_any_q_len) {
   const bool fuse = fuse_slot_mapping != nullptr;  // pa_decode_step
   int st = check_cache_geometry(num_blocks, block_size, num_kv_heads, head_dim);
   if (st) return st;
@@ -431,7 +450,7 @@ int paged_attention_impl(const pa_bf16* q, KvCache kv,
                 max_blocks, max_seq_len);
   if (max_q_len >= 2 && kv.fp8)
     return fail(PA_ERR_UNSUPPORTED, "rows with q_len >= 2 over the 8-bit cache (decode only)");
-  if (fuse && max_q_len > 1)
+  if (fuse && max_q_len > 1 && !fuse_any_q_len)
     return fail(PA_ERR_INVALID_ARG, "pa_decode_step takes decode rows only (max_q_len %d)",
                 max_q_len);
   if (max_q_len >= 2 && !pa::prefill_supported(head_dim, group, num_kv_heads))

@@ -51,15 +51,13 @@ int record_step(const pa_step_buffers& b, cudaStream_t s) {
                         b.slot_mapping, b.scale, b.out, b.workspace, b.workspace_bytes, s);
     if (st) return st;
   } else {
-    st = pa_reshape_and_cache(b.k_new, b.v_new, b.max_tokens, b.k_cache, b.v_cache,
-                              b.num_blocks, b.block_size, b.num_kv_heads, b.head_dim,
-                              b.slot_mapping, s);
-    if (st) return st;
-    st = pa_paged_attention(b.q, b.k_cache, b.v_cache, b.num_blocks, b.block_size,
-                            b.num_q_heads, b.num_kv_heads, b.head_dim, b.block_tables,
-                            b.max_blocks, b.seq_lens, b.query_start_loc, b.max_seqs,
-                            b.max_tokens, b.max_q_len, b.max_seq_len, b.scale, b.out,
-                            b.workspace, b.workspace_bytes, s);
+    // mixed rows: the scatter runs inside the attention kernels
+    st = pa_paged_attention_step(b.q, b.k_new, b.v_new, b.k_cache, b.v_cache, b.num_blocks,
+                                 b.block_size, b.num_q_heads, b.num_kv_heads, b.head_dim,
+                                 b.block_tables, b.max_blocks, b.seq_lens, b.query_start_loc,
+                                 b.max_seqs, b.max_tokens, b.max_q_len, b.max_seq_len,
+                                 b.slot_mapping, b.scale, b.out, b.workspace, b.workspace_bytes,
+                                 s);
     if (st) return st;
   }
   if (b.host_out) {

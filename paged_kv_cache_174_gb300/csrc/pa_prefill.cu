@@ -35,6 +35,15 @@
 //    are split over several units; each writes (O / l, m, l) per row and a
 //    merge kernel combines the pieces with log-sum-exp weights.
 //  * Persistent CTAs (at most one per SM) walk the unit list.
+//  * Fused step (pa_paged_attention_step): the step's new key and value rows
+//    are not in the cache yet.  The producers take pages of new positions
+//    straight from k_new / v_new (their own tensor maps: a request's new
+//    tokens are consecutive rows there), and the one page that holds both
+//    cached and new positions is loaded from the cache and has its new rows
+//    copied over in shared memory before it is handed to the products.  The
+//    unit of each query tile's last key piece stores that tile's new rows
+//    (its kv head) to their slots; no other unit reads them from the cache,
+//    so the stores need no ordering within the kernel.
 #include <algorithm>
 #include <cstdint>
 #include <mutex>
@@ -65,6 +74,13 @@ constexpr int kMaxSplit = 4;
 constexpr int kMaxListed = 1024;   // prefill requests the shared-memory unit list holds
 
 struct PrefillParams {
+  // fused step (the kernel's FUSE instance): new rows [num_tokens, n_kv, D]
+  // and their slots, and the caches they are stored to
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  const int32_t* slot_mapping;
+  uint16_t* k_cache;
+  uint16_t* v_cache;
   const int32_t* block_tables;
   const int32_t* seq_lens;
   const int32_t* qsl;
@@ -108,6 +124,8 @@ __device__ __forceinline__ int prefill_tiles(const PrefillParams& p, int s, bool
 // Geometry of one unit.
 struct Unit {
   int s, g, ks;
+  int a;        // first query token of the request
+  int c0;       // first new position of the request (seq_len - q_len)
   int q0;       // first query token of the tile
   int ntok;     // valid query tokens of the tile
   int p_first;  // position of token q0
@@ -159,6 +177,8 @@ struct UnitCursor {
     const int ql = b - a;
     const int first = (int)(tile - base) * TM;
     U.s = s;
+    U.a = a;
+    U.c0 = L - ql;
     U.g = rem / p.nsplit;
     U.ks = rem % p.nsplit;
     U.q0 = a + first;
@@ -179,6 +199,7 @@ struct PrefillShared {
   uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
   uint64_t o_full, o_empty;
   uint64_t s_done, pv_done_all;  // each issuer's last products, before TMEM is freed
+  uint64_t patch[kThreads / 32];  // per producer warp: a page to patch has landed
   uint32_t tmem_slot;
   int abort_flag;
   long long total_units;
@@ -261,11 +282,27 @@ __device__ __forceinline__ void issue_pv_mma(uint32_t o_tmem, uint32_t p_tmem, t
                                    (kk * V_PAGE) >> 4, IDESC_O);
 }
 
-template <int D, int G>
+// Whether token t's slot is the slot of position pos of request U (the fused
+// step's precondition), as a 64-bit slot or -1.
+__device__ __forceinline__ int64_t fused_slot(const PrefillParams& p, const int32_t* table,
+                                              int t, int pos) {
+  const int64_t slot = __ldg(p.slot_mapping + t);
+  const int lp = pos / kBlock;
+  const int b = __ldg(table + (lp >> p.block_shift));
+  const int64_t want =
+      ((int64_t)((b << p.block_shift) + (lp & ((1 << p.block_shift) - 1)))) * kBlock +
+      pos % kBlock;
+  if (b < 0 || b >= p.num_blocks || slot != want) return -1;
+  return slot;
+}
+
+template <int D, int G, bool FUSE>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
-                   const __grid_constant__ CUtensorMap vmap) {
+                   const __grid_constant__ CUtensorMap vmap,
+                   const __grid_constant__ CUtensorMap knmap,
+                   const __grid_constant__ CUtensorMap vnmap) {
   constexpr int TM = kRows / G;            // query tokens per tile
   constexpr int NH = D / 64;               // 64-element halves of head_dim
   constexpr uint32_t HALF = kRows * 128;   // bytes of one [128 rows][64] block
@@ -308,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_addr(&B.o_empty), kSoftmaxWarps);
     mbar_init(smem_addr(&B.s_done), 1);
     mbar_init(smem_addr(&B.pv_done_all), 1);
+    for (int w = 0; w < kThreads / 32; ++w) mbar_init(smem_addr(&B.patch[w]), 1);
     B.abort_flag = 0;
     fence_mbar_init();
   }
@@ -371,17 +409,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool v_warp = warp >= kWarpV0 && warp < kWarpV0 + kVWarps;
   if (k_warp || v_warp) {
     // ============================================================ producers
-    if (lane == 0) {
+    // (lane 0 issues and waits; in the fused step the whole warp runs along
+    // to patch pages and store the step's rows)
+    if (FUSE || lane == 0) {
       // K warp k and V warp k load pages 3k .. 3k+2 of each tile (the last
       // two): 96 rows of 128 bytes per warp and tile either way
       const int idx = k_warp ? (warp == 0 ? 0 : warp - kWarpK1 + 1) : warp - kWarpV0;
       const int pg_lo = 3 * idx;
       const int pg_hi = min(pg_lo + 3, kPagesPerTile);
       const CUtensorMap* map = k_warp ? &kmap : &vmap;
+      const CUtensorMap* nmap = k_warp ? &knmap : &vnmap;
+      const uint16_t* newrows = k_warp ? p.k_new : p.v_new;
       unsigned char* ring = k_warp ? k_s : v_s;
       uint64_t* full = k_warp ? B.k_full : B.v_full;
       uint64_t* empty = k_warp ? B.k_empty : B.v_empty;
       const uint32_t nst = k_warp ? kStagesK : kStagesV;
+      const uint32_t patch_bar = smem_addr(&B.patch[warp]);
+      uint32_t n_patch = 0;
       UnitCursor<TM> cur;
       cur.init(p, B.list_seq, B.list_base, B.listed);
       int n_out = 0, c = 0;
@@ -390,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         Unit U;
         if (!cur.locate(p, u, U)) break;
         if (U.kt0 == U.kt1) continue;
-        if (warp == 0) {
+        if (warp == 0 && lane == 0) {
           if (n_out > 0) mbar_wait(smem_addr(&B.q_empty), (n_out - 1) & 1, p.err, abort_flag);
           mbar_arrive_expect_tx(smem_addr(&B.q_full), Q_BYTES);
 #pragma unroll
@@ -402,51 +446,136 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pages = (U.kv_end + kBlock - 1) / kBlock;
         const int32_t* table = p.block_tables + (int64_t)U.s * p.max_blocks;
         for (int kt = U.kt0; kt < U.kt1; ++kt, ++c) {
-          int phys[4];  // 16-token page index in the pool (a 32-token block is two)
-          int nvalid = 0;
+          // per page: -1 (nothing to load), 0 (cached rows: the cache), 1
+          // (new rows only: k_new / v_new), 2 (both: the cache, then the new
+          // rows copied over)
+          int phys[4], kind[4];
+          uint32_t bytes = 0;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int lp = kt * kPagesPerTile + pg_lo + i;  // logical page
             phys[i] = -1;
+            kind[i] = -1;
             if (pg_lo + i < pg_hi && lp < pages) {
+              const int pos0 = lp * kBlock;
+              if (FUSE && pos0 >= U.c0) {
+                kind[i] = 1;
+                bytes += NH * (kBlock * 128);
+                continue;
+              }
               const int b = __ldg(table + (lp >> p.block_shift));
               if (b < 0 || b >= p.num_blocks) {
-                flag_error(p.err, DEVERR_BOUNDS);
+                if (lane == 0) flag_error(p.err, DEVERR_BOUNDS);
               } else {
                 phys[i] = (b << p.block_shift) + (lp & ((1 << p.block_shift) - 1));
-                ++nvalid;
+                kind[i] = (FUSE && pos0 + kBlock > U.c0) ? 2 : 0;
+                if (kind[i] == 0) bytes += NH * (kBlock * 128);
               }
             }
           }
           const uint32_t st = pos.stage;
-          if (c >= (int)nst) mbar_wait(smem_addr(&empty[st]), pos.phase ^ 1u, p.err, abort_flag);
-          mbar_arrive_expect_tx(smem_addr(&full[st]), (uint32_t)nvalid * NH * (kBlock * 128));
+          // the stage's last reader released it: one commit per use, and the
+          // next commit needs this load, so never two completions behind
+          if (lane == 0 && c >= (int)nst)
+            mbar_wait(smem_addr(&empty[st]), pos.phase ^ 1u, p.err, abort_flag);
+          if constexpr (FUSE) __syncwarp();
+          bool patch = false;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) patch |= FUSE && kind[i] == 2;
+          if (lane == 0) {
+            // with a page to patch, all of this warp's copies of the stage
+            // land on its own barrier, and its arrival on the stage's
+            // barrier waits until the new rows are in place
+            if (patch)
+              mbar_arrive_expect_tx(patch_bar, bytes + NH * (kBlock * 128));
+            else
+              mbar_arrive_expect_tx(smem_addr(&full[st]), bytes);
+          }
           unsigned char* stage = ring + st * KV_BYTES;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            if (phys[i] < 0) continue;
+            if (kind[i] < 0 || lane != 0) continue;
             const int pg = pg_lo + i;
+            const uint32_t bar = patch ? patch_bar : smem_addr(&full[st]);
+            // rows of the box: a cache page, or 16 new tokens of the request
+            const CUtensorMap* m = kind[i] == 1 ? nmap : map;
+            const int z = kind[i] == 1 ? U.a + (kt * kPagesPerTile + pg) * kBlock - U.c0
+                                       : phys[i] * kBlock;
             if (k_warp) {
 #pragma unroll
               for (int h = 0; h < NH; ++h)
-                tc::tma_load_3d(smem_addr(stage + h * HALF + pg * (kBlock * 128)), map, h * 64,
-                                U.g, phys[i] * kBlock, smem_addr(&full[st]));
+                tc::tma_load_3d(smem_addr(stage + h * HALF + pg * (kBlock * 128)), m, h * 64, U.g,
+                                z, bar);
             } else if (NH == 2) {
-              tma_load_4d(smem_addr(stage + pg * V_PAGE), map, 0, U.g, phys[i] * kBlock, 0,
-                          smem_addr(&full[st]));
+              tma_load_4d(smem_addr(stage + pg * V_PAGE), m, 0, U.g, z, 0, bar);
             } else {
-              tc::tma_load_3d(smem_addr(stage + pg * V_PAGE), map, 0, U.g, phys[i] * kBlock,
-                              smem_addr(&full[st]));
+              tc::tma_load_3d(smem_addr(stage + pg * V_PAGE), m, 0, U.g, z, bar);
             }
+          }
+          if (patch) {
+            // the page with both kinds of rows: wait for its cache rows,
+            // then copy its new rows over them (16-byte chunks, in the
+            // stage's 128-byte-swizzled layout), visible to the products
+            if (lane == 0) mbar_wait(patch_bar, n_patch & 1, p.err, abort_flag);
+            ++n_patch;
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if (kind[i] != 2) continue;
+              const int pg = pg_lo + i;
+              const int pos0 = (kt * kPagesPerTile + pg) * kBlock;
+              const int r0 = U.c0 - pos0;  // first new row of the page
+              // rows past the unit's keys are masked (and V rows cleared),
+              // and past the request's tokens there is no new row to copy
+              const int r1 = min(kBlock, U.kv_end - pos0);
+              const int nchunks = max(0, r1 - r0) * NH * 8;
+              for (int e = lane; e < nchunks; e += 32) {
+                const int r = r0 + e / (NH * 8), h = (e / 8) % NH, c8 = e % 8;
+                const int t = U.a + pos0 + r - U.c0;  // its token
+                const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+                    newrows + ((int64_t)t * p.n_kv + U.g) * D + h * 64 + c8 * 8));
+                unsigned char* dst =
+                    k_warp ? stage + h * HALF + sw128_chunk(pg * kBlock + r, c8)
+                           : stage + pg * V_PAGE + h * (kBlock * 128) + sw128_chunk(r, c8);
+                *reinterpret_cast<uint4*>(dst) = v;
+              }
+            }
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&full[st]));
           }
           pos.next(nst);
         }
+        // fused step: the unit of the tile's last key piece (never empty,
+        // unlike the first when a request has fewer key tiles than pieces)
+        // stores the tile's new rows of its kv head (K by the K warps, V by
+        // the V warps) to their slots; a token whose slot is not its
+        // position's slot is not stored and is flagged
+        if (FUSE && U.ks == p.nsplit - 1) {
+          const int nw = k_warp ? kKWarps : kVWarps;
+          uint16_t* cache = k_warp ? p.k_cache : p.v_cache;
+          const int per_tok = D / 8;  // 16-byte chunks of a row
+          for (int e = idx * 32 + lane; e < U.ntok * per_tok; e += nw * 32) {
+            const int i = e / per_tok, c8 = e % per_tok;
+            const int t = U.q0 + i;
+            const int64_t slot = fused_slot(p, table, t, U.p_first + i);
+            if (slot < 0) {
+              if (c8 == 0) flag_error(p.err, DEVERR_BOUNDS);
+              continue;
+            }
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+                newrows + ((int64_t)t * p.n_kv + U.g) * D + c8 * 8));
+            *reinterpret_cast<uint4*>(cache + (slot * p.n_kv + U.g) * D + c8 * 8) = v;
+          }
+        }
       }
       // never hand back shared memory with a TMA copy still landing in it
-      for (int i = max(0, c - (int)nst); i < c; ++i)
-        mbar_wait(smem_addr(&full[i % nst]), (i / nst) & 1, p.err, abort_flag);
-      if (warp == 0 && n_out > 0)
-        mbar_wait(smem_addr(&B.q_full), (n_out - 1) & 1, p.err, abort_flag);
+      if (lane == 0) {
+        for (int i = max(0, c - (int)nst); i < c; ++i)
+          mbar_wait(smem_addr(&full[i % nst]), (i / nst) & 1, p.err, abort_flag);
+        if (warp == 0 && n_out > 0)
+          mbar_wait(smem_addr(&B.q_full), (n_out - 1) & 1, p.err, abort_flag);
+      }
     }
   } else if (warp == 1 || warp == kWarpPV) {
     // ============================================================ MMA issuers
@@ -540,8 +669,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     UnitCursor<TM> cur;
     cur.init(p, B.list_seq, B.list_base, B.listed);
     int n_out = 0;
-    Ring sbr, prev, vr;  // S buffer of this tile and of the last one, V stage
-    uint32_t xpar = 0;   // exchange slot parity
+    Ring sbr, prev, prev2, vr;  // S buffer of this tile, the last one and the one
+                                // before; V stage of this tile
+    uint32_t xpar = 0;          // exchange slot parity
+    uint32_t nt = 0;            // tiles done by this CTA
     for (long long u = blockIdx.x; u < total_units; u += gridDim.x) {
       Unit U;
       if (!cur.locate(p, u, U)) break;
@@ -648,6 +779,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // clears half of the 16-byte chunks of V row 64 kh + r / 2.
         const int kv_local = U.kv_end - kt * kKeysPerTile;
         if (kv_local < kKeysPerTile) {
+          // A parity wait tells apart only two phases in a row: the stage's
+          // barrier must be at this tile's use or the one after, never still
+          // at the use two tiles back (its phase has this tile's parity, and
+          // the wait would pass before this tile's V landed).  These warps
+          // wait on V at tail tiles only, so nothing else keeps them from
+          // running two tiles ahead of the V copies; the P V product of the
+          // tile two back has read that use, so wait for it first.  (The V
+          // barrier cannot be past this tile's use: the next copy into the
+          // stage waits for this tile's P V, which waits for this tile's P.)
+          if (nt >= 2) mbar_wait(smem_addr(&B.pv_done[prev2.stage]), prev2.phase, p.err, abort_flag);
           mbar_wait(smem_addr(&B.v_full[vr.stage]), vr.phase, p.err, abort_flag);
           const int key = kh * 64 + (r >> 1);
           if (key >= kv_local) {
@@ -665,10 +806,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&B.p_full[sbr.stage]));
+        prev2 = prev;
         prev = sbr;
         sbr.next(kSBufs);
         vr.next(kStagesV);
         xpar ^= 1u;
+        ++nt;
       }
       // epilogue: each warp of the pair handles half of d
       const uint32_t upar = n_out & 1;
@@ -838,11 +981,16 @@ size_t split_bytes(int num_tokens, int num_q_heads, int head_dim, int nsplit) {
          ((rows * 2 * sizeof(float) + 255) & ~size_t(255));
 }
 
-template <int D, int G>
+template <int D, int G, bool FUSE>
 cudaError_t launch_prefill_t(const AttnArgs& a, const PrefillPlan& plan, void* ws, int sm_count,
                              cudaStream_t stream) {
   constexpr int TM = kRows / G;
   PrefillParams p;
+  p.k_new = a.fuse_k_new;
+  p.v_new = a.fuse_v_new;
+  p.slot_mapping = a.fuse_slot_mapping;
+  p.k_cache = static_cast<uint16_t*>(const_cast<void*>(a.k_cache));
+  p.v_cache = static_cast<uint16_t*>(const_cast<void*>(a.v_cache));
   p.block_tables = a.block_tables;
   p.seq_lens = a.seq_lens;
   p.qsl = a.query_start_loc;
@@ -869,7 +1017,7 @@ cudaError_t launch_prefill_t(const AttnArgs& a, const PrefillPlan& plan, void* w
   }
   const cuuint64_t nkv = (cuuint64_t)a.num_kv_heads;
   const cuuint64_t rows = ((cuuint64_t)a.num_blocks << a.block_shift) * kBlock;
-  CUtensorMap qm, km, vm;
+  CUtensorMap qm, km, vm, knm, vnm;
   {
     const cuuint64_t dims[3] = {D, (cuuint64_t)a.num_q_heads, (cuuint64_t)a.num_tokens};
     const cuuint64_t strides[2] = {D * 2, (cuuint64_t)a.num_q_heads * D * 2};
@@ -897,13 +1045,38 @@ cudaError_t launch_prefill_t(const AttnArgs& a, const PrefillPlan& plan, void* w
     cudaError_t e = make_map(&vm, a.v_cache, 4, dims, strides, box);
     if (e != cudaSuccess) return e;
   }
+  knm = km;
+  vnm = vm;
+  if (FUSE) {
+    // the step's new rows [num_tokens, n_kv, D], read with the caches' boxes:
+    // 16 consecutive tokens of one kv head
+    const cuuint64_t tok = (cuuint64_t)a.num_tokens;
+    {
+      const cuuint64_t dims[3] = {D, nkv, tok};
+      const cuuint64_t strides[2] = {D * 2, nkv * D * 2};
+      const cuuint32_t box[3] = {64, 1, kBlock};
+      cudaError_t e = make_map(&knm, a.fuse_k_new, 3, dims, strides, box);
+      if (e != cudaSuccess) return e;
+      if (D == 64) {
+        e = make_map(&vnm, a.fuse_v_new, 3, dims, strides, box);
+        if (e != cudaSuccess) return e;
+      }
+    }
+    if (D == 128) {
+      const cuuint64_t dims[4] = {64, nkv, tok, 2};
+      const cuuint64_t strides[3] = {D * 2, nkv * D * 2, 128};
+      const cuuint32_t box[4] = {64, 1, kBlock, 2};
+      cudaError_t e = make_map(&vnm, a.fuse_v_new, 4, dims, strides, box);
+      if (e != cudaSuccess) return e;
+    }
+  }
   // upper bound of the number of units; the kernel reads the exact count
   const long long tiles_bound = (long long)a.num_tokens / TM + a.num_seqs;
   const long long units_bound = tiles_bound * a.num_kv_heads * plan.nsplit;
   const int grid = (int)(units_bound < sm_count ? units_bound : sm_count);
   if (grid <= 0) return cudaSuccess;
   const size_t smem = prefill_smem_bytes<D, G>();
-  auto kern = prefill_kernel<D, G>;
+  auto kern = prefill_kernel<D, G, FUSE>;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -913,7 +1086,7 @@ cudaError_t launch_prefill_t(const AttnArgs& a, const PrefillPlan& plan, void* w
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  kern<<<grid, kThreads, smem, stream>>>(p, qm, km, vm);
+  kern<<<grid, kThreads, smem, stream>>>(p, qm, km, vm, knm, vnm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || plan.nsplit == 1) return e;
   // the merge may launch while the prefill grid runs; it waits for that grid
@@ -981,9 +1154,13 @@ size_t prefill_workspace_bound(int num_tokens, int num_q_heads, int num_kv_heads
 cudaError_t launch_prefill(const AttnArgs& a, const PrefillPlan& plan, void* ws, int sm_count,
                            cudaStream_t stream) {
   const int group = a.num_q_heads / a.num_kv_heads;
-#define PA_PREFILL_CASE(D_, G_)     \
-  if (a.head_dim == D_ && group == G_) \
-    return launch_prefill_t<D_, G_>(a, plan, ws, sm_count, stream);
+  // the fused step's instance loads new rows from k_new / v_new and stores
+  // them; the plain one reads the cache only
+  const bool fuse = a.fuse_slot_mapping != nullptr;
+#define PA_PREFILL_CASE(D_, G_)                                                  \
+  if (a.head_dim == D_ && group == G_)                                           \
+    return fuse ? launch_prefill_t<D_, G_, true>(a, plan, ws, sm_count, stream) \
+                : launch_prefill_t<D_, G_, false>(a, plan, ws, sm_count, stream);
   PA_PREFILL_CASE(128, 1)
   PA_PREFILL_CASE(128, 2)
   PA_PREFILL_CASE(128, 4)

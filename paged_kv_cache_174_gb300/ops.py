@@ -81,6 +81,9 @@ def _load() -> ctypes.CDLL:
     L.pa_decode_step.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, vp, vp,
                                  i32, i32, i32, vp, f32, vp, vp, sz, vp]
     L.pa_decode_step.restype = ctypes.c_int
+    L.pa_paged_attention_step.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, i32,
+                                          vp, vp, i32, i32, i32, i32, vp, f32, vp, vp, sz, vp]
+    L.pa_paged_attention_step.restype = ctypes.c_int
     L.pa_copy_blocks.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, vp]
     L.pa_swap_staging_bytes.argtypes = [i32, i32, i32, i32]
     L.pa_swap_staging_bytes.restype = sz
@@ -315,6 +318,43 @@ def decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                             query_start_loc.data_ptr(), S, T, int(max_seq_len),
                             slot_mapping.data_ptr(), float(scale), out.data_ptr(),
                             workspace.data_ptr(), workspace.numel(), _stream(stream)))
+    return out
+
+
+def attention_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                   k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                   seq_lens: torch.Tensor, query_start_loc: torch.Tensor,
+                   slot_mapping: torch.Tensor, scale: float, *, max_q_len: int, max_seq_len: int,
+                   out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                   stream=None) -> torch.Tensor:
+    """reshape_and_cache + paged_attention of a step with any mix of decode and
+    chunked-prefill rows, the scatter done inside the attention kernels
+    (pa_paged_attention_step).  Returns ``out``."""
+    L = _load()
+    for name, t, dim in (("q", q, 3), ("k_new", k_new, 3), ("v_new", v_new, 3),
+                         ("k_cache", k_cache, 4), ("v_cache", v_cache, 4)):
+        _need(t, name, torch.bfloat16, dim)
+    for name, t in (("block_tables", block_tables), ("seq_lens", seq_lens),
+                    ("query_start_loc", query_start_loc), ("slot_mapping", slot_mapping)):
+        _need(t, name, torch.int32)
+    T, nq, d, nb, bs, nkv, S = _attention_shapes(q, k_cache, v_cache, block_tables, seq_lens,
+                                                 query_start_loc, out)
+    _new_rows_shapes(k_new, v_new, nkv, d, slot_mapping, name="k_new")
+    if k_new.shape[0] != T:
+        raise ValueError("k_new / v_new must have one row per query token")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 3)
+    if workspace is None:
+        workspace = alloc_workspace(S, T, nq, nkv, d, max_q_len, max_seq_len, q.device)
+    _need_workspace(workspace)
+    _check(L.pa_paged_attention_step(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                     k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, nq, nkv, d,
+                                     block_tables.data_ptr(), block_tables.shape[1],
+                                     seq_lens.data_ptr(), query_start_loc.data_ptr(), S, T,
+                                     int(max_q_len), int(max_seq_len), slot_mapping.data_ptr(),
+                                     float(scale), out.data_ptr(), workspace.data_ptr(),
+                                     workspace.numel(), _stream(stream)))
     return out
 
 

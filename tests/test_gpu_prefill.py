@@ -45,6 +45,10 @@ def _batch(lens, q_lens, nq=32, nkv=8, d=128, seed=0, extra_blocks=9):
     ([4096, 100], [64, 100], 32, 8, 128),         # short request: pieces with no key tile
     ([1100], [1024], 8, 8, 128),                  # rows that see no key of a piece
     ([3000], [40], 8, 2, 64),                     # head_dim 64, keys in pieces
+    ([96], [32], 32, 8, 128),                     # one full tile, the second tile empty
+    ([600], [65], 32, 8, 128),                    # two row blocks, the last of 1 row
+    ([777], [230], 16, 2, 64),                    # group 8, head_dim 64
+    ([2000, 1500], [300, 700], 16, 8, 128),       # group 2: 128-token row blocks
 ])
 def test_prefill_edge_shapes(lens, q_lens, nq, nkv, d):
     b = _batch(lens, q_lens, nq, nkv, d, seed=sum(lens) % 97)
