@@ -653,6 +653,13 @@ __global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
       const bool seq_done = (cur.j + 1 == cur.np);
       const bool seg_end = seq_done || (i + 1 == n_pages);
       if (R == 1 || (i & 1) == rho) {
+        // Page i (phase-parity wait: the stage must be at page i or past
+        // it, never at page i - NST).  A stage's pages are i, i + NST, ...;
+        // with R == 1 this warp reads every one of them, with R == 2 they
+        // all have this warp's parity because NST is even (refused above
+        // otherwise), so this warp waited for page i - NST itself.  Page
+        // i + NST is copied only after every reader, this warp among them,
+        // released page i.
         mbar_wait(smem_addr(&S.full[st]), st_phase, p.err, abort_flag);
         const int ntok = min(kBlock, L - cur.j * kBlock);
         const int fslot = FUSE ? S.fused_slot[st] : -1;
@@ -935,7 +942,12 @@ __global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
     const unsigned char* stage = stages;
     for (int i = 0; i < n_pages; ++i) {
       const int b = i & 1;
+      // p buffer b freed by the PV warp after page i - 2: this warp waited
+      // for the release of page i - 4 on it, and the release of page i needs
+      // the p this warp writes next
       if (i >= 2) mbar_wait(smem_addr(&S.p_empty[g][b]), ((i >> 1) - 1) & 1, p.err, abort_flag);
+      // page i: every warp reads every page, so this warp waited for page
+      // i - NST of the stage; page i + NST is copied after all release page i
       mbar_wait(smem_addr(&S.full[st]), st_phase, p.err, abort_flag);
       const int ntok = min(kBlock, L - cur.j * kBlock);
       const int fslot = FUSE ? S.fused_slot[st] : -1;
@@ -1027,6 +1039,7 @@ __global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
     const unsigned char* stage = stages;
     for (int i = 0; i < n_pages; ++i) {
       const int b = i & 1;
+      // page i: as for the QK warps (every warp reads every page)
       mbar_wait(smem_addr(&S.full[st]), st_phase, p.err, abort_flag);
       const int ntok = min(kBlock, L - cur.j * kBlock);
       const int fslot = FUSE ? S.fused_slot[st] : -1;
@@ -1038,6 +1051,8 @@ __global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
         bulk_commit();
         stored = true;
       }
+      // p of page i: this warp waited for page i - 2's on buffer b, and the
+      // QK warp writes page i + 2's only after this warp frees b (p_empty)
       mbar_wait(smem_addr(&S.p_full[g][b]), (i >> 1) & 1, p.err, abort_flag);
       const PBuf<G>& pb = S.pb[g][b];
       const uint32_t pb_addr = smem_addr(&pb);
@@ -1140,7 +1155,9 @@ __global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
     if (FUSE && stored) bulk_wait_all();  // the stores are complete before the CTA exits
   }
   }
-  // never hand back shared memory with a copy still landing in it
+  // never hand back shared memory with a copy still landing in it: the
+  // last page copied into each stage (the one before it was read, and so
+  // complete, before this copy was issued; nothing is copied after it)
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int st = 0; st < NST; ++st) {

@@ -228,6 +228,15 @@ __device__ __forceinline__ uint32_t sw128_chunk(int r, int c) {
 
 // Position in a ring of pipeline stages: the stage and the parity of its
 // current use, which flips each time the ring wraps around.
+//
+// Every wait below is a phase-parity wait, which tells apart only the phase
+// it names and the one before it.  So each wait carries, beside it, why its
+// barrier is never still at the use before the one wanted (the wait would
+// pass at once) nor already past the wanted use (it would wait for a
+// completion that needs this thread).  The argument is the same shape each
+// time: the waiter saw the previous use complete, or a product it already
+// waited for needed it; and the next use needs something this thread does
+// after the wait.  Stage and buffer counts are compile-time constants.
 struct Ring {
   uint32_t stage = 0, phase = 0;
   __device__ __forceinline__ void next(uint32_t n) {
@@ -435,6 +444,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!cur.locate(p, u, U)) break;
         if (U.kt0 == U.kt1) continue;
         if (warp == 0 && lane == 0) {
+          // Q of the last unit released: this thread saw the release before
+          // that (it loaded the last Q after it), and the next release needs
+          // the S products of the Q loaded below
           if (n_out > 0) mbar_wait(smem_addr(&B.q_empty), (n_out - 1) & 1, p.err, abort_flag);
           mbar_arrive_expect_tx(smem_addr(&B.q_full), Q_BYTES);
 #pragma unroll
@@ -516,6 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the page with both kinds of rows: wait for its cache rows,
             // then copy its new rows over them (16-byte chunks, in the
             // stage's 128-byte-swizzled layout), visible to the products
+            // one use of this warp's own barrier at a time: armed above,
+            // completed here before it is armed again
             if (lane == 0) mbar_wait(patch_bar, n_patch & 1, p.err, abort_flag);
             ++n_patch;
             __syncwarp();
@@ -569,7 +583,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // never hand back shared memory with a TMA copy still landing in it
+      // never hand back shared memory with a TMA copy still landing in it:
+      // the last use of each stage (the one before it was released by the
+      // consumer that read it; no later use is ever issued)
       if (lane == 0) {
         for (int i = max(0, c - (int)nst); i < c; ++i)
           mbar_wait(smem_addr(&full[i % nst]), (i / nst) & 1, p.err, abort_flag);
@@ -599,9 +615,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           Unit U;
           if (!cur.locate(p, u, U)) break;
           if (U.kt0 == U.kt1) continue;
+          // this unit's Q: the last unit's load was waited for here, and
+          // the next load waits for q_empty, which this thread commits
           mbar_wait_spin(smem_addr(&B.q_full), n_out & 1, p.err, abort_flag);
           for (int kt = U.kt0; kt < U.kt1; ++kt, ++ntiles) {
+            // K tile kt: this thread waited for the stage's last use, and
+            // the stage's next copy waits for k_empty, committed below
             mbar_wait_spin(smem_addr(&B.k_full[kv.stage]), kv.phase, p.err, abort_flag);
+            // P V of the tile that last used this S buffer: the one before
+            // on the buffer was waited for here, and the next needs the P
+            // of the S about to be issued into it
             if (ntiles >= kSBufs)
               mbar_wait_spin(smem_addr(&B.pv_done[sb.stage]), sb.phase ^ 1u, p.err, abort_flag);
             tc::fence_after_sync();
@@ -616,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++n_out;
         }
         if (ntiles > 0) {
-          tc::commit(smem_addr(&B.s_done));
+          tc::commit(smem_addr(&B.s_done));  // its only use: phase 0
           mbar_wait_spin(smem_addr(&B.s_done), 0, p.err, abort_flag);
         }
       } else {
@@ -630,8 +653,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (U.kt0 == U.kt1) continue;
           for (int kt = U.kt0; kt < U.kt1; ++kt, ++ntiles) {
             const bool first = kt == U.kt0;
+            // P of this tile: the buffer's last P was waited for here, and
+            // its next P needs an S that waits for this P V (pv_done)
             mbar_wait_spin(smem_addr(&B.p_full[sb.stage]), sb.phase, p.err, abort_flag);
+            // V tile kt: the stage's last use was waited for here, and its
+            // next copy waits for v_empty, committed below
             mbar_wait_spin(smem_addr(&B.v_full[kv.stage]), kv.phase, p.err, abort_flag);
+            // the last unit's O read out: the release before was waited for
+            // here, and the next needs this unit's O (o_full)
             if (first && n_out > 0)
               mbar_wait_spin(smem_addr(&B.o_empty), (n_out - 1) & 1, p.err, abort_flag);
             tc::fence_after_sync();
@@ -646,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++n_out;
         }
         if (ntiles > 0) {
-          tc::commit(smem_addr(&B.pv_done_all));
+          tc::commit(smem_addr(&B.pv_done_all));  // its only use: phase 0
           mbar_wait_spin(smem_addr(&B.pv_done_all), 0, p.err, abort_flag);
         }
       }
@@ -689,6 +718,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_ref = kNegInf, l = 0.f;
       for (int kt = U.kt0; kt < U.kt1; ++kt) {
         const uint32_t s_cols = tmem + lane_addr + sbr.stage * kKeysPerTile + kh * 64;
+        // S of this tile: the buffer's last S was waited for here, and its
+        // next S waits for the P V of this tile, which needs this P
         mbar_wait(smem_addr(&B.s_full[sbr.stage]), sbr.phase, p.err, abort_flag);
         tc::fence_after_sync();
         uint32_t sr[64];
@@ -761,6 +792,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // rescale this half of the running output when the reference max moved
         // (rare); the P V product of the last tile must have landed first
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          // P V of the last tile: the buffer's use before (kSBufs tiles
+          // earlier) was waited for by the S issued into this tile's buffer,
+          // whose S these warps waited for; the next needs a later P
           mbar_wait(smem_addr(&B.pv_done[prev.stage]), prev.phase, p.err, abort_flag);
           tc::fence_after_sync();
 #pragma unroll
@@ -788,6 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // tile two back has read that use, so wait for it first.  (The V
           // barrier cannot be past this tile's use: the next copy into the
           // stage waits for this tile's P V, which waits for this tile's P.)
+          static_assert(kStagesV == 2 && kSBufs >= 3, "the P V two tiles back, on its own buffer");
           if (nt >= 2) mbar_wait(smem_addr(&B.pv_done[prev2.stage]), prev2.phase, p.err, abort_flag);
           mbar_wait(smem_addr(&B.v_full[vr.stage]), vr.phase, p.err, abort_flag);
           const int key = kh * 64 + (r >> 1);
@@ -819,6 +854,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_barrier(pair_bar, 64);
       const float ltot = l + B.xsum[upar][kh ^ 1][r];
       const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
+      // this unit's O: the last unit's was waited for here, and the next
+      // unit's first P V waits for o_empty, which these warps arrive on
       mbar_wait(smem_addr(&B.o_full), upar, p.err, abort_flag);
       tc::fence_after_sync();
 #pragma unroll
