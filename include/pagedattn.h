@@ -289,11 +289,15 @@ int pa_swap_in(pa_bf16 *k_cache, pa_bf16 *v_cache, int32_t num_blocks, int32_t b
  * A row x (head_dim bf16 values) is stored as scale = max |x| / 448 (1 when
  * the row is all zero) and codes e4m3(x_c / scale), rounding to nearest with
  * ties to even and saturating; both divisions are fp32, round to nearest.
- * Attention uses code * scale in place of each cached value; the decode
- * kernel runs q . k and p . V on the tensor cores with q * scale * log2(e)
- * and p * value scale * 2^9 rounded to f16 (codes convert to f16 exactly;
- * the 2^9 is removed exactly).  head_dim is 64 or 128.  Only decode rows (q_len 1) are implemented for this cache:
- * pa_paged_attention_fp8 with max_q_len >= 2 returns PA_ERR_UNSUPPORTED.
+ * Attention uses code * scale in place of each cached value.  The decode
+ * kernel (q_len 1) runs q . k and p . V on the tensor cores with
+ * q * scale * log2(e) and p * value scale * 2^9 rounded to f16 (codes
+ * convert to f16 exactly; the 2^9 is removed exactly).  The prefill kernel
+ * (q_len >= 2, the chunked-prefill rows) turns each cached row into
+ * f16(code * f16(scale)) in shared memory (codes exact in f16, one rounding
+ * of the scale and one of the product), and runs
+ * its tcgen05 products on f16 operands: q * scale * log2(e) and p rounded
+ * to f16.  head_dim is 64 or 128; the same shapes as the bf16 cache.
  *
  * pa_reshape_and_cache_fp8: pa_reshape_and_cache, quantising each new row
  * (codes and scale written to the new token's slot).  Alignment: k, v and
@@ -307,7 +311,8 @@ int pa_reshape_and_cache_fp8(const pa_bf16 *k, const pa_bf16 *v, int32_t num_tok
 /*
  * pa_paged_attention over the 8-bit cache (same arguments, meaning, errors
  * and workspace as pa_paged_attention, plus the two scale arrays, which must
- * be 16-byte aligned).  Decode rows only (see above).
+ * be 16-byte aligned).  Decode and prefill rows, mixed in one call, as
+ * pa_paged_attention (see above for the arithmetic).
  */
 int pa_paged_attention_fp8(const pa_bf16 *q, const uint8_t *k_cache, const uint8_t *v_cache,
                            const float *k_scale, const float *v_scale, int32_t num_blocks,

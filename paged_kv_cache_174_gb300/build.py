@@ -23,7 +23,7 @@ LIB_NAME = "libpagedattn.so"
 LIB = os.path.join(OUT_DIR, LIB_NAME)
 
 SOURCES = ["pa_api.cu", "pa_cache.cu", "pa_decode.cu", "pa_decode_fp8.cu", "pa_decode_fused.cu",
-           "pa_prefill.cu", "pa_graph.cu"]
+           "pa_prefill.cu", "pa_prefill_fp8.cu", "pa_graph.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -448,8 +448,6 @@ int paged_attention_impl(const pa_bf16* q, KvCache kv,
   if ((int64_t)max_blocks * block_size < max_seq_len)
     return fail(PA_ERR_INVALID_ARG, "max_blocks %d * block_size cannot hold max_seq_len %d",
                 max_blocks, max_seq_len);
-  if (max_q_len >= 2 && kv.fp8)
-    return fail(PA_ERR_UNSUPPORTED, "rows with q_len >= 2 over the 8-bit cache (decode only)");
   if (fuse && max_q_len > 1 && !fuse_any_q_len)
     return fail(PA_ERR_INVALID_ARG, "pa_decode_step takes decode rows only (max_q_len %d)",
                 max_q_len);

@@ -1,5 +1,5 @@
 // pa_common.cuh -- device helpers shared by the kernels of libpagedattn:
-// bfloat16 unpacking, mbarrier waits with a time limit, bulk async copies and
+// bfloat16 / f16 / E4M3 conversions, mbarrier waits with a time limit, bulk async copies and
 // the device error word.  sm_103a only.
 #pragma once
 
@@ -42,6 +42,22 @@ __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t w) {
       : "=f"(lo), "=f"(hi)
       : "r"(w));
   return make_float2(lo, hi);
+}
+
+// Two floats -> a half pair (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t f16x2_from_floats(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Four E4M3 codes -> two f16 pairs (exact: every E4M3 value is an f16
+// value): lo gets codes 0, 1 (bytes 0, 1 of w), hi codes 2, 3.
+__device__ __forceinline__ void f16x2x2_from_e4m3x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 // Two floats -> two E4M3 codes (lo in the low byte): nearest, ties to even,

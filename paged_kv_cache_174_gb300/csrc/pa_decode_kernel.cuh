@@ -292,19 +292,6 @@ __device__ __forceinline__ void qk_scores(const unsigned char* kb, int ntok,
 // every k-step: k-step s holds elements t * D/4 + 4s .. + 3, which is one
 // 32-bit word of codes per token -- two f16x2 B registers -- and the same
 // elements of q in its A registers.  E4M3 values are exact in f16.
-__device__ __forceinline__ uint32_t f16x2_from_floats(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-// Four E4M3 codes -> two f16 pairs: lo gets codes 0, 1 (bytes 0, 1 of w),
-// hi codes 2, 3.
-__device__ __forceinline__ void f16x2x2_from_e4m3x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(w));
-}
 __device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32_t a2,
                                               uint32_t b0, uint32_t b1) {
   asm volatile(

@@ -96,11 +96,16 @@ __device__ __forceinline__ Desc sw128_desc_pair(uint32_t addr, uint32_t lbo, uin
 }
 
 // Instruction descriptor of kind::f16 with bf16 A and B and an fp32
-// accumulator: D format F32 (1) at [4,6), A format BF16 (1) at [7,10),
+// accumulator (A and B of one product always share their type): D format F32 (1) at [4,6), A format BF16 (1) at [7,10),
 // B format BF16 (1) at [10,13), A / B major (0 = K, 1 = MN) at bits 15 / 16,
 // N >> 3 at [17,23), M >> 4 at [24,29).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// The same with f16 A and B (format 0 in both fields).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 

@@ -458,7 +458,7 @@ def paged_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.T
                         seq_lens: torch.Tensor, query_start_loc: torch.Tensor, scale: float, *,
                         max_q_len: int, max_seq_len: int, out: Optional[torch.Tensor] = None,
                         workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """paged_attention over the 8-bit cache (decode rows only)."""
+    """paged_attention over the 8-bit cache (decode and prefill rows)."""
     L = _load()
     _need(q, "q", torch.bfloat16, 3)
     _need_fp8(k_cache, v_cache, k_scale, v_scale)

@@ -1,7 +1,7 @@
 """The 8-bit (FP8 E4M3) KV cache on the GPU against the oracle: the
-quantising scatter bit for bit (codes and scales), decode attention over the
-8-bit cache against the oracle's attention over code * scale, the block copy
-of codes and scales, and the calls it rejects."""
+quantising scatter bit for bit (codes and scales), decode and chunked-prefill
+attention over the 8-bit cache against the oracle's attention over
+code * scale, and the block copy of codes and scales."""
 import numpy as np
 import pytest
 import torch
@@ -30,13 +30,20 @@ def _context_slots(b):
     return slots, rows_k, rows_v
 
 
-def fp8_step(b):
+def fp8_step(b, poison=False):
     """Quantise the batch's context and its new tokens into an 8-bit cache on
     both sides (GPU scatter and oracle scatter, compared bit for bit), then
-    run decode attention on both.  Returns (gpu out, oracle out)."""
+    run attention (decode and prefill rows) on both.  With poison, every GPU
+    slot that is not written holds NaN codes and NaN scales, which no output
+    may see.  Returns (gpu out, oracle out)."""
     nb, bs, nkv, d = b.k_cache.shape
     slots, rk, rv = _context_slots(b)
     dk8, dv8, dks, dvs = ops.empty_fp8_cache(nb, bs, nkv, d)
+    if poison:
+        for t in (dk8, dv8):
+            t.fill_(0x7F)  # E4M3 NaN
+        for t in (dks, dvs):
+            t.fill_(float("nan"))
     ok8, ov8, oks, ovs = oracle.fp8_cache(nb, bs, nkv, d, fill_code=0)
     oks[:] = 0
     ovs[:] = 0
@@ -47,18 +54,23 @@ def fp8_step(b):
                                   dv8, dks, dvs, W.int32_tensor(sl, "cuda"))
         oracle.reshape_and_cache_fp8(ks_, vs_, ok8, ov8, oks, ovs, sl)
     ops.check_device_errors()
-    assert np.array_equal(dk8.cpu().numpy(), ok8) and np.array_equal(dv8.cpu().numpy(), ov8), \
-        "codes differ from the oracle"
-    assert np.array_equal(dks.cpu().numpy().view(np.uint32), oks.view(np.uint32)) and \
-        np.array_equal(dvs.cpu().numpy().view(np.uint32), ovs.view(np.uint32)), \
-        "scales differ from the oracle"
+    written = np.zeros(nb * bs, bool)
+    written[slots] = True
+    written[b.slot_mapping[b.slot_mapping >= 0]] = True
+    for dev_t, ref, what in ((dk8, ok8, "K codes"), (dv8, ov8, "V codes"),
+                             (dks, oks, "K scales"), (dvs, ovs, "V scales")):
+        got = dev_t.cpu().numpy()
+        if got.dtype == np.float32:
+            got, ref = got.view(np.uint32), ref.view(np.uint32)
+        got = got.reshape(nb * bs, -1)[written]
+        assert np.array_equal(got, ref.reshape(nb * bs, -1)[written]), f"{what} differ"
     out = torch.full((b.num_tokens, b.num_q_heads, d), float("nan"), dtype=torch.bfloat16,
                      device="cuda")
     ops.paged_attention_fp8(W.bf16_tensor(b.q, "cuda"), dk8, dv8, dks, dvs,
                             W.int32_tensor(b.block_tables, "cuda"),
                             W.int32_tensor(b.seq_lens, "cuda"),
-                            W.int32_tensor(b.query_start_loc, "cuda"), b.scale, max_q_len=1,
-                            max_seq_len=b.max_seq_len, out=out)
+                            W.int32_tensor(b.query_start_loc, "cuda"), b.scale,
+                            max_q_len=b.max_q_len, max_seq_len=b.max_seq_len, out=out)
     ops.check_device_errors()
     ref = oracle.paged_attention_fp8(b.q, ok8, ov8, oks, ovs, b.block_tables, b.seq_lens,
                                      b.query_start_loc, b.scale)
@@ -145,14 +157,57 @@ def test_fp8_copy_blocks_moves_codes_and_scales(bs):
         assert np.array_equal(dev_t.cpu().numpy(), host)
 
 
-def test_fp8_rejects_prefill_rows():
-    b = W.make_batch("fp8", [40], [4], num_q_heads=8, num_kv_heads=2, head_dim=64,
-                     block_size=16, num_blocks=4, seed=1)
-    dk8, dv8, dks, dvs = ops.empty_fp8_cache(4, 16, 2, 64)
-    with pytest.raises(ops.PagedAttnError) as ei:
-        ops.paged_attention_fp8(W.bf16_tensor(b.q, "cuda"), dk8, dv8, dks, dvs,
-                                W.int32_tensor(b.block_tables, "cuda"),
-                                W.int32_tensor(b.seq_lens, "cuda"),
-                                W.int32_tensor(b.query_start_loc, "cuda"), b.scale, max_q_len=4,
-                                max_seq_len=40)
-    assert ei.value.code == 2
+def _mixed(lens, q_lens, nq=32, nkv=8, d=128, seed=0, bs=16):
+    nb = sum(-(-L // bs) for L in lens) + 5
+    return W.make_batch("fp8", lens, q_lens, num_q_heads=nq, num_kv_heads=nkv, head_dim=d,
+                        block_size=bs, num_blocks=nb, seed=seed)
+
+
+@pytest.mark.parametrize("lens,q_lens,nq,nkv,d,bs", [
+    ([2], [2], 32, 8, 128, 16),                    # smallest prefill
+    ([37], [37], 32, 8, 128, 16),                  # fresh prompt, one ragged tile
+    ([300], [77], 32, 8, 128, 16),                 # chunk at an offset, ragged tiles
+    ([1000, 50, 700], [512, 1, 40], 32, 8, 128, 16),  # prefill + decode rows
+    ([513], [513], 8, 8, 128, 16),                 # group 1
+    ([600], [200], 64, 8, 128, 16),                # group 8
+    ([333, 41], [150, 41], 8, 2, 64, 16),          # head_dim 64
+    ([250], [250], 4, 1, 64, 16),                  # multi-query, head_dim 64
+    ([4096], [64], 32, 8, 128, 16),                # keys in 4 pieces + merge
+    ([3000], [40], 8, 2, 64, 16),                  # head_dim 64, keys in pieces
+    ([600], [65], 32, 8, 128, 16),                 # two row blocks, the last of 1 row
+    ([777, 90], [230, 1], 16, 2, 64, 16),          # group 8, head_dim 64, + a decode row
+    ([700, 47], [300, 1], 32, 8, 128, 32),         # 32-token blocks
+])
+def test_fp8_prefill_edge_shapes(lens, q_lens, nq, nkv, d, bs):
+    """Chunked-prefill rows over the 8-bit cache (the tcgen05 kernel on
+    f16(code * scale)) against the oracle, with every unwritten slot of the
+    pool holding NaN codes and scales."""
+    b = _mixed(lens, q_lens, nq, nkv, d, seed=sum(lens) % 89, bs=bs)
+    got, ref = fp8_step(b, poison=True)
+    assert_attn_close(got, ref, f"fp8 prefill lens={lens} q_lens={q_lens} nq={nq} nkv={nkv} "
+                                f"d={d} bs={bs}")
+
+
+def test_fp8_mixed_step_workload():
+    """The mixed chunked-prefill step (a 512-token chunk over 3,584 cached
+    tokens plus 128 decode rows, 32/8 heads, d 128) over the 8-bit cache."""
+    got, ref = fp8_step(W.mixed_step(poison=False), poison=True)
+    assert_attn_close(got, ref, "fp8 mixed step")
+
+
+@pytest.mark.parametrize("mag", [1e-2, 3e3])
+def test_fp8_prefill_small_and_large_values(mag):
+    """Keys and values far from unit size through the prefill kernel's f16
+    operands: f16(code * scale) must neither flush small rows nor overflow
+    large ones.  Compared after dividing by mag.  Every row sees at least 130
+    keys, so the outputs stay near unit size: a row of one or two keys can
+    reach |out| ~ 5, where the bf16 output's own rounding (2^-9 relative) is
+    already 1e-2."""
+    b = _mixed([700, 230], [300, 100], seed=23)
+    for name in ("k_cache", "k_new", "v_cache", "v_new"):
+        a = W.f32_from_bf16(getattr(b, name)) * np.float32(mag)
+        setattr(b, name, W.bf16_from_f32(a.astype(np.float32)))
+    # the scores keep unit size: the keys are scaled by mag, the queries by 1 / mag
+    b.q = W.bf16_from_f32((W.f32_from_bf16(b.q) / np.float32(mag)).astype(np.float32))
+    got, ref = fp8_step(b)
+    assert_attn_close(got / mag, ref / mag, f"fp8 prefill values x {mag}")

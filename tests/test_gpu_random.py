@@ -64,10 +64,12 @@ def test_random_step_against_oracle(seed):
         assert torch.equal(d1.k_cache.view(torch.int16), d2.k_cache.view(torch.int16)), desc
 
 
-@pytest.mark.parametrize("seed", range(12))
-def test_random_fp8_decode_against_oracle(seed):
-    """The same sweep over the 8-bit cache (decode rows only; the oracle's
-    attention runs on code x scale)."""
+@pytest.mark.parametrize("seed", range(16))
+def test_random_fp8_against_oracle(seed):
+    """The same sweep over the 8-bit cache (the oracle's attention runs on
+    code x scale): even seeds decode rows only, odd seeds a mix of decode
+    rows, chunks at an offset and fresh prompts; the pool's unwritten slots
+    hold NaN codes and scales."""
     from test_gpu_fp8 import fp8_step
     rng = np.random.default_rng(3000 + seed)
     d = int(rng.choice([64, 128]))
@@ -75,9 +77,17 @@ def test_random_fp8_decode_against_oracle(seed):
     nkv = int(rng.choice([1, 2, 4, 8]))
     bs = int(rng.choice([16, 32]))
     lens = [int(x) for x in rng.integers(1, 1500, size=int(rng.integers(1, 10)))]
+    q_lens = [1] * len(lens)
+    if seed % 2:
+        for i, L in enumerate(lens):
+            kind = rng.random()
+            if kind < 0.3 or L < 2:
+                continue
+            q_lens[i] = int(rng.integers(2, min(L, 300) + 1)) if kind < 0.8 else L
     nb = sum(-(-L // bs) for L in lens) + 3
-    b = W.make_batch("random-fp8", lens, [1] * len(lens), num_q_heads=g * nkv,
+    b = W.make_batch("random-fp8", lens, q_lens, num_q_heads=g * nkv,
                      num_kv_heads=nkv, head_dim=d, block_size=bs, num_blocks=nb,
                      seed=4000 + seed)
-    got, ref = fp8_step(b)
-    assert_attn_close(got, ref, f"random fp8 d={d} g={g} nkv={nkv} bs={bs} lens={lens}")
+    got, ref = fp8_step(b, poison=True)
+    assert_attn_close(got, ref, f"random fp8 d={d} g={g} nkv={nkv} bs={bs} lens={lens} "
+                                f"q_lens={q_lens}")
