@@ -188,10 +188,10 @@ def _launch_count(b) -> int:
 
 
 def _graph_launch_count(b) -> int:
-    """Kernels one ops.StepGraph launch runs: the slot scatter happens inside
-    the attention kernels (pa_decode_step for decode rows only,
-    pa_paged_attention_step for mixed rows), so no scatter launch."""
-    return _launch_count(b) - (1 if b.num_tokens else 0)
+    """Kernels one ops.StepGraph launch runs: a decode-only step does its
+    slot scatter inside the decode kernel (pa_decode_step), a step with
+    prefill rows launches the scatter kernel first."""
+    return _launch_count(b) - (1 if b.num_tokens and b.max_q_len <= 1 else 0)
 
 
 def _time_steps(b, d, ws, out, steps, warmup, stream, ops):
@@ -464,8 +464,9 @@ def _run_trace(dev, stream, ops, warmup):
              "step_ms_p99": round(float(np.percentile(gms, 99)), 5),
              "graph_launches": len(gres),
              # every replay runs the kernels captured at the maxima: the CoW
-             # copy, the prefill (+ its key-piece merge), decode + merge
-             "gpu_launches": len(gres) * (4 + (ops.prefill_splits(
+             # copy, the scatter, the prefill (+ its key-piece merge), decode
+             # + merge
+             "gpu_launches": len(gres) * (5 + (ops.prefill_splits(
                  cfg.budget, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.chunk,
                  max(pl.max_seq_len for pl in plans)) > 1)),
              "maxima": {"tokens": cfg.budget, "seqs": cfg.max_num_seqs, "q_len": cfg.chunk}}
@@ -780,8 +781,8 @@ def run_ours(args):
                         "inputs from pinned host memory (side stream), scatter + attention, "
                         "one copy of out back to pinned memory (side stream); the copies "
                         "of one step overlap the kernels of its neighbours"},
-        # the timed value path: a graph launch per step, whose steps run the
-        # scatter inside the attention kernels
+        # the timed value path: a graph launch per step (a decode-only step
+        # scatters inside the decode kernel)
         "gpu_launches": _graph_launch_count(b) * args.steps,
         "clocks": clk,
     }

@@ -211,7 +211,10 @@ int pa_decode_step(const pa_bf16 *q, const pa_bf16 *k_new, const pa_bf16 *v_new,
  * pa_decode_step (a negative slot reads the cache's row, any other slot
  * flags).  Tokens outside every request are not written.  bf16 cache only;
  * arguments, workspace and errors otherwise as pa_reshape_and_cache and
- * pa_paged_attention.
+ * pa_paged_attention.  Cost: every later query tile of a chunk reads the
+ * chunk's new rows from k_new / v_new, and on a GB300 that measured slower
+ * than one scatter launch (a 512-token chunk with 128 decode rows: 150 us
+ * against 141 us for the two calls), so the step graph does not use it.
  */
 int pa_paged_attention_step(const pa_bf16 *q, const pa_bf16 *k_new, const pa_bf16 *v_new,
                             pa_bf16 *k_cache, pa_bf16 *v_cache, int32_t num_blocks,
@@ -403,9 +406,9 @@ int pa_paged_attention_noalloc(const pa_bf16 *q, const pa_bf16 *k_cache,
  *   - copy pairs i >= the step's count: copy_pairs[2i] = -1 (skipped).
  * A step's sizes must stay within the maxima (max_q_len and max_seq_len
  * included: a request beyond them flags PA_ERR_DEVICE_BOUNDS at run time).
- * The graph runs scatter + attention as pa_decode_step (max_q_len 1) or
- * pa_paged_attention_step (no scatter kernel); their slot precondition
- * applies.
+ * The graph runs scatter + attention as pa_decode_step (max_q_len 1: one
+ * kernel, whose slot precondition applies) or as pa_reshape_and_cache then
+ * pa_paged_attention.
  * Rows of out that belong to no request are left as they were.
  *
  * If host_meta is not NULL, every launch first copies meta_bytes from

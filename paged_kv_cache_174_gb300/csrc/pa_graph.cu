@@ -9,7 +9,8 @@
 // and the per-step metadata can ride in with one host-to-device copy node.
 // The captured calls are the library's own public entry points, so the graph
 // checks and computes exactly what those calls do; a graph whose steps have
-// decode rows only (max_q_len 1) runs scatter + attention as pa_decode_step.
+// decode rows only (max_q_len 1) runs scatter + attention as pa_decode_step,
+// one with prefill rows runs pa_reshape_and_cache, then pa_paged_attention.
 #include <cuda_runtime.h>
 
 #include <new>
@@ -51,13 +52,18 @@ int record_step(const pa_step_buffers& b, cudaStream_t s) {
                         b.slot_mapping, b.scale, b.out, b.workspace, b.workspace_bytes, s);
     if (st) return st;
   } else {
-    // mixed rows: the scatter runs inside the attention kernels
-    st = pa_paged_attention_step(b.q, b.k_new, b.v_new, b.k_cache, b.v_cache, b.num_blocks,
-                                 b.block_size, b.num_q_heads, b.num_kv_heads, b.head_dim,
-                                 b.block_tables, b.max_blocks, b.seq_lens, b.query_start_loc,
-                                 b.max_seqs, b.max_tokens, b.max_q_len, b.max_seq_len,
-                                 b.slot_mapping, b.scale, b.out, b.workspace, b.workspace_bytes,
-                                 s);
+    // mixed rows: scatter, then attention.  (pa_paged_attention_step does
+    // both in the attention kernels, but every later query tile of a chunk
+    // then reads the chunk's new rows from k_new / v_new instead of the
+    // cache, and on the chunked-prefill step and the serving trace that
+    // measured slower than one scatter launch.)
+    st = pa_reshape_and_cache(b.k_new, b.v_new, b.max_tokens, b.k_cache, b.v_cache, b.num_blocks,
+                              b.block_size, b.num_kv_heads, b.head_dim, b.slot_mapping, s);
+    if (st) return st;
+    st = pa_paged_attention(b.q, b.k_cache, b.v_cache, b.num_blocks, b.block_size, b.num_q_heads,
+                            b.num_kv_heads, b.head_dim, b.block_tables, b.max_blocks, b.seq_lens,
+                            b.query_start_loc, b.max_seqs, b.max_tokens, b.max_q_len,
+                            b.max_seq_len, b.scale, b.out, b.workspace, b.workspace_bytes, s);
     if (st) return st;
   }
   if (b.host_out) {

@@ -70,8 +70,9 @@ constexpr int kBlock = 16;         // tokens per physical block
 constexpr int kKeysPerTile = 128;  // keys per K/V tile (8 blocks)
 constexpr int kPagesPerTile = kKeysPerTile / kBlock;
 constexpr int kRows = 128;         // MMA rows of a query tile
-constexpr int kStagesK = 3;        // K tile stages
-constexpr int kStagesV = 2;        // V tile stages
+constexpr int kStagesK = 3;        // K tile stages (bf16 cache)
+constexpr int kStagesV = 2;        // V tile stages (bf16 cache)
+constexpr int kStagesMax = 3;      // the most stages of one kind in any instance
 constexpr int kSBufs = 3;          // S / P buffers in TMEM
 constexpr int kSoftmaxWarps = 8;   // two per TMEM lane quarter
 constexpr int kKWarps = 3;         // warp 0 (which also loads Q) and warps 10-11
@@ -218,8 +219,8 @@ struct UnitCursor {
 struct PrefillShared {
   uint64_t q_full, q_empty;
   uint64_t q_land;  // 8-bit cache: the bf16 query tile has landed (then rewritten)
-  uint64_t k_full[kStagesK], k_empty[kStagesK];
-  uint64_t v_full[kStagesV], v_empty[kStagesV];
+  uint64_t k_full[kStagesMax], k_empty[kStagesMax];
+  uint64_t v_full[kStagesMax], v_empty[kStagesMax];
   uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
   uint64_t o_full, o_empty;
   uint64_t s_done, pv_done_all;  // each issuer's last products, before TMEM is freed
@@ -357,6 +358,50 @@ __device__ __forceinline__ int64_t fused_slot(const PrefillParams& p, const int3
   return slot;
 }
 
+// Fused step: store the new rows of kv head U.g of the unit's query tile
+// (tokens q0 .. q0 + ntok - 1) from newrows to their slots in cache; warp
+// idx of the nw warps doing it.  Eight 16-byte chunks per lane at a time,
+// all their loads (row, slot, block-table entry) issued before any store,
+// so one round trip covers a batch.  A token whose slot is not its
+// position's slot is not stored and is flagged.
+template <int D>
+__device__ __forceinline__ void fused_store_rows(const PrefillParams& p, const Unit& U,
+                                                 const int32_t* table, const uint16_t* newrows,
+                                                 uint16_t* cache, int idx, int nw, int lane) {
+  constexpr int PER_TOK = D / 8;  // 16-byte chunks of a row
+  constexpr int NB = 8;
+  const int n = U.ntok * PER_TOK;
+  const int step = nw * 32;
+  for (int e0 = idx * 32 + lane; e0 < n; e0 += NB * step) {
+    uint4 v[NB];
+    int64_t slot[NB];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const int e = e0 + j * step;
+      slot[j] = -1;
+      v[j] = make_uint4(0u, 0u, 0u, 0u);
+      if (e < n) {
+        const int i = e / PER_TOK, c8 = e % PER_TOK;
+        const int t = U.q0 + i;
+        slot[j] = fused_slot(p, table, t, U.p_first + i);
+        v[j] = __ldg(reinterpret_cast<const uint4*>(newrows + ((int64_t)t * p.n_kv + U.g) * D +
+                                                    c8 * 8));
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const int e = e0 + j * step;
+      if (e >= n) continue;
+      const int c8 = e % PER_TOK;
+      if (slot[j] < 0) {
+        if (c8 == 0) flag_error(p.err, DEVERR_BOUNDS);
+        continue;
+      }
+      *reinterpret_cast<uint4*>(cache + (slot[j] * p.n_kv + U.g) * D + c8 * 8) = v[j];
+    }
+  }
+}
+
 template <int D, int G, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap qmap,
@@ -366,6 +411,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap vnmap) {
   constexpr bool FUSE = KIND == kKindFused;
   constexpr bool F8 = KIND == kKindFp8;
+  // Stages: the 8-bit instance's V copies wait for a product two tiles
+  // earlier with two V stages, and its producers take longer per page (code
+  // conversion), so it trades a K stage for a V stage (same shared memory).
+  constexpr int SK = F8 ? 2 : kStagesK;
+  constexpr int SV = F8 ? 3 : kStagesV;
+  static_assert(SK + SV == kStagesK + kStagesV && SK <= kStagesMax && SV <= kStagesMax,
+                "shared memory holds kStagesK + kStagesV tiles");
   constexpr int TM = kRows / G;            // query tokens per tile
   constexpr int NH = D / 64;               // 64-element halves of head_dim
   constexpr uint32_t HALF = kRows * 128;   // bytes of one [128 rows][64] block
@@ -381,22 +433,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   unsigned char* q_s = base;
   unsigned char* k_s = q_s + Q_BYTES;
-  unsigned char* v_s = k_s + kStagesK * KV_BYTES;
-  PrefillShared& B = *reinterpret_cast<PrefillShared*>(v_s + kStagesV * KV_BYTES);
+  unsigned char* v_s = k_s + SK * KV_BYTES;
+  PrefillShared& B = *reinterpret_cast<PrefillShared*>(v_s + SV * KV_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the merge grid of split keys may start launching now
   asm volatile("griddepcontrol.launch_dependents;");
+  // fetch the tensor maps this instance uses ahead of their first copy
+  if (threadIdx.x == 32) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&qmap)) : "memory");
+    if constexpr (!F8) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
+    }
+    if constexpr (FUSE) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&knmap)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vnmap)) : "memory");
+    }
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(smem_addr(&B.q_full), 1);
     mbar_init(smem_addr(&B.q_land), 1);
     mbar_init(smem_addr(&B.q_empty), 1);
-    for (int i = 0; i < kStagesK; ++i) {
+    for (int i = 0; i < SK; ++i) {
       mbar_init(smem_addr(&B.k_full[i]), kKWarps);
       mbar_init(smem_addr(&B.k_empty[i]), 1);
     }
-    for (int i = 0; i < kStagesV; ++i) {
+    for (int i = 0; i < SV; ++i) {
       mbar_init(smem_addr(&B.v_full[i]), kVWarps);
       mbar_init(smem_addr(&B.v_empty[i]), 1);
     }
@@ -487,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       unsigned char* ring = k_warp ? k_s : v_s;
       uint64_t* full = k_warp ? B.k_full : B.v_full;
       uint64_t* empty = k_warp ? B.k_empty : B.v_empty;
-      const uint32_t nst = k_warp ? kStagesK : kStagesV;
+      const uint32_t nst = k_warp ? SK : SV;
       const uint32_t patch_bar = smem_addr(&B.patch[warp]);
       uint32_t n_patch = 0;
       UnitCursor<TM> cur;
@@ -695,28 +759,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           pos.next(nst);
         }
-        // fused step: the unit of the tile's last key piece (never empty,
-        // unlike the first when a request has fewer key tiles than pieces)
-        // stores the tile's new rows of its kv head (K by the K warps, V by
-        // the V warps) to their slots; a token whose slot is not its
-        // position's slot is not stored and is flagged
-        if (FUSE && U.ks == p.nsplit - 1) {
-          const int nw = k_warp ? kKWarps : kVWarps;
-          uint16_t* cache = k_warp ? p.k_cache : p.v_cache;
-          const int per_tok = D / 8;  // 16-byte chunks of a row
-          for (int e = idx * 32 + lane; e < U.ntok * per_tok; e += nw * 32) {
-            const int i = e / per_tok, c8 = e % per_tok;
-            const int t = U.q0 + i;
-            const int64_t slot = fused_slot(p, table, t, U.p_first + i);
-            if (slot < 0) {
-              if (c8 == 0) flag_error(p.err, DEVERR_BOUNDS);
-              continue;
-            }
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-                newrows + ((int64_t)t * p.n_kv + U.g) * D + c8 * 8));
-            *reinterpret_cast<uint4*>(cache + (slot * p.n_kv + U.g) * D + c8 * 8) = v;
-          }
-        }
+        // fused step: the unit of the query tile's last key piece (never
+        // empty, unlike the first when a request has fewer key tiles than
+        // pieces) stores the tile's new rows of its kv head (K by the K
+        // warps, V by the V warps) to their slots.  No unit reads these rows
+        // from the cache, so the stores need no place in the pipeline: after
+        // the unit's last copies are issued, the products of the stages in
+        // flight cover them
+        if (FUSE && U.ks == p.nsplit - 1)
+          fused_store_rows<D>(p, U, table, newrows, k_warp ? p.k_cache : p.v_cache, idx,
+                              k_warp ? kKWarps : kVWarps, lane);
       }
       // never hand back shared memory with a TMA copy still landing in it:
       // the last use of each stage (the one before it was released by the
@@ -733,7 +785,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (waits spin without the suspend hint: these threads' latency is the
     // tensor pipe's)
     if (lane == 0) {
-      static_assert(kStagesK == 3 && kStagesV == 2, "descriptor selection below");
       UnitCursor<TM> cur;
       cur.init(p, B.list_seq, B.list_base, B.listed);
       int n_out = 0;
@@ -743,9 +794,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S = Q K^T into the S buffer at sb, which held P three tiles back:
         // the P V of that tile must have run
         const tc::Desc qd = tc::sw128_desc_pair(smem_addr(q_s), 16, 1024);
+        // stage i's descriptor: the start address (16-byte units, low word)
+        // advanced by i tiles
         const tc::Desc kd0 = tc::sw128_desc_pair(smem_addr(k_s), 16, 1024);
-        const tc::Desc kd1 = tc::sw128_desc_pair(smem_addr(k_s + KV_BYTES), 16, 1024);
-        const tc::Desc kd2 = tc::sw128_desc_pair(smem_addr(k_s + 2 * KV_BYTES), 16, 1024);
         for (long long u = blockIdx.x; u < total_units; u += gridDim.x) {
           Unit U;
           if (!cur.locate(p, u, U)) break;
@@ -764,11 +815,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_wait_spin(smem_addr(&B.pv_done[sb.stage]), sb.phase ^ 1u, p.err, abort_flag);
             tc::fence_after_sync();
             issue_s_mma<D, F8>(tmem + sb.stage * kKeysPerTile, qd,
-                           kv.stage == 0 ? kd0 : (kv.stage == 1 ? kd1 : kd2));
+                           tc::Desc{kd0.lo + kv.stage * (KV_BYTES >> 4), kd0.hi});
             tc::commit(smem_addr(&B.s_full[sb.stage]));
             tc::commit(smem_addr(&B.k_empty[kv.stage]));
             if (kt == U.kt1 - 1) tc::commit(smem_addr(&B.q_empty));
-            kv.next(kStagesK);
+            kv.next(SK);
             sb.next(kSBufs);
           }
           ++n_out;
@@ -781,7 +832,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O += P V with P in the S buffer at sb and V at kv; the first tile of
         // a unit overwrites O once the previous unit's epilogue has read it
         const tc::Desc vd0 = tc::sw128_desc_pair(smem_addr(v_s), kBlock * 128, 1024);
-        const tc::Desc vd1 = tc::sw128_desc_pair(smem_addr(v_s + KV_BYTES), kBlock * 128, 1024);
         for (long long u = blockIdx.x; u < total_units; u += gridDim.x) {
           Unit U;
           if (!cur.locate(p, u, U)) break;
@@ -799,11 +849,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (first && n_out > 0)
               mbar_wait_spin(smem_addr(&B.o_empty), (n_out - 1) & 1, p.err, abort_flag);
             tc::fence_after_sync();
-            issue_pv_mma<D, F8>(tmem + O_COL, tmem + sb.stage * kKeysPerTile, kv.stage ? vd1 : vd0,
+            issue_pv_mma<D, F8>(tmem + O_COL, tmem + sb.stage * kKeysPerTile,
+                                tc::Desc{vd0.lo + kv.stage * (KV_BYTES >> 4), vd0.hi},
                             first);
             tc::commit(smem_addr(&B.v_empty[kv.stage]));
             tc::commit(smem_addr(&B.pv_done[sb.stage]));
-            kv.next(kStagesV);
+            kv.next(SV);
             sb.next(kSBufs);
           }
           tc::commit(smem_addr(&B.o_full));
@@ -956,15 +1007,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kv_local < kKeysPerTile) {
           // A parity wait tells apart only two phases in a row: the stage's
           // barrier must be at this tile's use or the one after, never still
-          // at the use two tiles back (its phase has this tile's parity, and
+          // at the use SV tiles back (its phase has this tile's parity, and
           // the wait would pass before this tile's V landed).  These warps
           // wait on V at tail tiles only, so nothing else keeps them from
-          // running two tiles ahead of the V copies; the P V product of the
-          // tile two back has read that use, so wait for it first.  (The V
-          // barrier cannot be past this tile's use: the next copy into the
-          // stage waits for this tile's P V, which waits for this tile's P.)
-          static_assert(kStagesV == 2 && kSBufs >= 3, "the P V two tiles back, on its own buffer");
-          if (nt >= 2) mbar_wait(smem_addr(&B.pv_done[prev2.stage]), prev2.phase, p.err, abort_flag);
+          // running ahead of the V copies.  The P V product of that earlier
+          // tile has read its use: with SV >= kSBufs the S of this tile
+          // waited for it already (its buffer's last P V); with SV == 2 wait
+          // for it here.  (The V barrier cannot be past this tile's use: the
+          // next copy into the stage waits for this tile's P V, which waits
+          // for this tile's P.)
+          static_assert(SV >= kSBufs || (SV == 2 && kSBufs >= 3), "the P V SV tiles back");
+          if constexpr (SV < kSBufs) {
+            if (nt >= 2)
+              mbar_wait(smem_addr(&B.pv_done[prev2.stage]), prev2.phase, p.err, abort_flag);
+          }
           mbar_wait(smem_addr(&B.v_full[vr.stage]), vr.phase, p.err, abort_flag);
           const int key = kh * 64 + (r >> 1);
           if (key >= kv_local) {
@@ -985,7 +1041,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prev2 = prev;
         prev = sbr;
         sbr.next(kSBufs);
-        vr.next(kStagesV);
+        vr.next(SV);
         xpar ^= 1u;
         ++nt;
       }
