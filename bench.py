@@ -489,7 +489,8 @@ def _fp8(args, dev, stream, ops, peaks, bf16_attn_ms):
     """The decode batch over the 8-bit cache (E4M3 codes + one fp32 scale per
     cached row): the context is quantised once on the device, then each step
     quantises the new tokens and runs decode attention, timed like the main
-    line."""
+    line.  Then the mixed chunked-prefill step over the 8-bit cache, and its
+    chunk alone."""
     import torch
     from paged_kv_cache_174_gb300 import workloads as W
 
@@ -536,6 +537,7 @@ def _fp8(args, dev, stream, ops, peaks, bf16_attn_ms):
     attn_ms = statistics.mean(a.elapsed_time(c) for a, c in evs)
     alg = W.algorithmic_bytes_fp8(b)
     gbs = alg["attention"] / (attn_ms * 1e-3) / 1e9
+    mixed = None if args.no_mixed else _fp8_mixed(args, dev, stream, ops, peaks)
     return {"workload": "decode_batch, 8-bit cache (E4M3 codes + fp32 scale per row)",
             "ms_per_step": round(ms, 5), "attention_ms": round(attn_ms, 5),
             "tokens_per_s": round(b.num_tokens / (ms * 1e-3), 1),
@@ -547,7 +549,70 @@ def _fp8(args, dev, stream, ops, peaks, bf16_attn_ms):
                              "decode_kernel_fp8_decode_batch.md",
                              ["pa_decode_kernel.cuh", "pa_decode_fp8.cu", "pa_common.cuh"],
                              "decode_batch", "decode_batch")},
-            "attention_speedup_vs_bf16": round(bf16_attn_ms / attn_ms, 3)}
+            "attention_speedup_vs_bf16": round(bf16_attn_ms / attn_ms, 3),
+            "mixed_step": mixed}
+
+
+def _fp8_mixed(args, dev, stream, ops, peaks):
+    """The mixed step (128 decode rows + a 512-token chunk at offset 3584)
+    over the 8-bit cache: each step quantises the 640 new rows and runs
+    attention over codes and scales; then the chunk's rows alone (its call
+    also launches the empty decode grid: the 8-bit entry point takes no
+    min_q_len)."""
+    import types
+    import torch
+    from paged_kv_cache_174_gb300 import workloads as W
+
+    b = W.mixed_step(poison=False)
+    nb, bs, nkv, d = b.k_cache.shape
+    k8, v8, ks, vs = ops.empty_fp8_cache(nb, bs, nkv, d, dev)
+    slots = W.context_slots(b)
+    rows = b.k_cache.reshape(-1, nkv, d)
+    ops.reshape_and_cache_fp8(W.bf16_tensor(rows[slots], dev),
+                              W.bf16_tensor(b.v_cache.reshape(-1, nkv, d)[slots], dev),
+                              k8, v8, ks, vs, W.int32_tensor(slots, dev))
+    q = W.bf16_tensor(b.q, dev)
+    kn, vn = W.bf16_tensor(b.k_new, dev), W.bf16_tensor(b.v_new, dev)
+    meta = {k: W.int32_tensor(getattr(b, k), dev)
+            for k in ("slot_mapping", "block_tables", "seq_lens", "query_start_loc")}
+    ws = ops.alloc_workspace(b.num_seqs, b.num_tokens, b.num_q_heads, nkv, d, b.max_q_len,
+                             b.max_seq_len, dev)
+    out = torch.empty_like(q)
+    sub, t = _prefill_only(b, types.SimpleNamespace(q=q))
+    sout = torch.empty_like(t["q"])
+
+    def step():
+        ops.reshape_and_cache_fp8(kn, vn, k8, v8, ks, vs, meta["slot_mapping"])
+        ops.paged_attention_fp8(q, k8, v8, ks, vs, meta["block_tables"], meta["seq_lens"],
+                                meta["query_start_loc"], b.scale, max_q_len=b.max_q_len,
+                                max_seq_len=b.max_seq_len, out=out, workspace=ws)
+
+    def chunk():
+        ops.paged_attention_fp8(t["q"], k8, v8, ks, vs, t["block_tables"], t["seq_lens"],
+                                t["query_start_loc"], sub.scale, max_q_len=sub.max_q_len,
+                                max_seq_len=sub.max_seq_len, out=sout, workspace=ws)
+
+    res = {}
+    for name, fn in (("step", step), ("chunk", chunk)):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ops.check_device_errors()
+        res[name] = e0.elapsed_time(e1) / args.steps
+    flops = W.causal_flops(sub)
+    tflops = flops / (res["chunk"] * 1e-3) / 1e12
+    return {"workload": "mixed_step over the 8-bit cache",
+            "ms_per_step": round(res["step"], 5),
+            "tokens_per_s": round(b.num_tokens / (res["step"] * 1e-3), 1),
+            "chunk_ms": round(res["chunk"], 5),
+            "chunk_tflops": round(tflops, 2),
+            "chunk_frac_of_bf16_peak": round(tflops / peaks["bf16_tflops"], 4)}
 
 
 def _other_decodes(args, dev, stream, ops, peaks, host_batches=None):
@@ -637,6 +702,9 @@ def _summary(line):
            "prefill_TFLOPs": _dig(line, ("roofline_prefill", "achieved")),
            "trace_graph_tokens_per_s": _dig(line, ("trace", "step_graph", "tokens_per_s")),
            "fp8_decode_frac_hbm": _dig(line, ("fp8_cache", "roofline", "frac")),
+           "fp8_mixed_tokens_per_s": _dig(line, ("fp8_cache", "mixed_step", "tokens_per_s")),
+           "fp8_chunk_frac_bf16": _dig(line, ("fp8_cache", "mixed_step",
+                                              "chunk_frac_of_bf16_peak")),
            "long_decode_frac_hbm": _dig(line, ("other_decodes", "long_decode",
                                                "attention_frac_of_hbm")),
            "group8_decode_frac_hbm": _dig(line, ("other_decodes", "group8_decode",
@@ -823,8 +891,9 @@ def run_ours(args):
                 "frac": round(pre["tflops"] / peaks["bf16_tflops"], 4),
                 "peak_source": peaks["source"] + " (bf16_tflops, burst)",
                 "traffic": _profiled_traffic("prefill_kernel_mixed_step.md",
-                                             ["pa_prefill.cu", "pa_common.cuh",
-                                              "pa_tcgen05.cuh"], mb.name, "mixed_step"),
+                                             ["pa_prefill_kernel.cuh", "pa_prefill.cu",
+                                              "pa_common.cuh", "pa_tcgen05.cuh"],
+                                             mb.name, "mixed_step"),
                 "algorithmic_flops_per_launch": pre["flops"], "avg_launch_ms": pre["ms"]}
         del md, mws, mout
     if not args.no_trace:
