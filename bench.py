@@ -8,7 +8,11 @@ the slot scatter of the step's new K/V, then paged attention over every
 request (split-KV decode kernel + merge, and the tensor-core prefill kernel
 for chunked-prefill rows), through the C ABI.  Inputs are synthetic and
 seeded; the KV cache (hundreds of MB to GB) is far larger than the 129 MB L2,
-so no explicit L2 flush is done between steps.
+so no explicit L2 flush is done between steps.  The kernel durations behind
+the roofline figures come from CUDA graphs of back-to-back calls (no idle
+time from the host's per-call work); where a call's inputs fit in L2 (the
+prefill chunk alone, the tiny decode), a 256 MB write evicts L2 before each
+call and the time of those writes alone is subtracted.
 
 Prints one JSON line (rank 0).  With N > 1 (torchrun, one process per GPU)
 every rank runs its own replica of the batch and `value` is the bytes all
@@ -194,10 +198,84 @@ def _graph_launch_count(b) -> int:
     return _launch_count(b) - (1 if b.num_tokens and b.max_q_len <= 1 else 0)
 
 
-def _time_steps(b, d, ws, out, steps, warmup, stream, ops):
-    """Device-resident steps (scatter + attention); returns per-step and
-    per-attention-call milliseconds (CUDA events on the launching stream)."""
+L2_FLUSH_BYTES = 256 << 20  # a write of this many bytes evicts the 129 MB L2
+_FLUSH = {}
+
+
+def _flush_buffer(dev):
     import torch
+    if dev not in _FLUSH:
+        _FLUSH[dev] = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    return _FLUSH[dev]
+
+
+def _flush_if_small(b, dev):
+    """The flush buffer when batch b's attention inputs would stay in L2
+    between calls (the tiny decode), else None (they are larger than L2)."""
+    from paged_kv_cache_174_gb300 import workloads as W
+    if W.algorithmic_bytes(b)["attention"] < L2_FLUSH_BYTES:
+        return _flush_buffer(dev)
+    return None
+
+
+def _device_ms(call, steps, warmup, stream, flush_buf=None, reps=5):
+    """Device milliseconds per call of `call`: CUDA events on `stream` around
+    the replay of a CUDA graph holding `steps` back-to-back calls (median of
+    `reps` replays), so the host's per-call work (Python, argument checks)
+    leaves no idle GPU time inside the measurement.  With flush_buf (larger
+    than L2), every call in the graph follows a write of the whole buffer and
+    the replay time of a graph of those writes alone is subtracted: each call
+    then starts with its inputs out of L2."""
+    import torch
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+
+    def replay_ms(body):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(steps):
+                body()
+        times = []
+        with torch.cuda.stream(stream):
+            g.replay()
+            for _ in range(reps):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+        del g
+        return statistics.median(times)
+
+    if flush_buf is None:
+        return replay_ms(call) / steps
+
+    def flush():
+        flush_buf.fill_(1)
+
+    def flush_then_call():
+        flush()
+        call()
+
+    return (replay_ms(flush_then_call) - replay_ms(flush)) / steps
+
+
+def _time_steps(b, d, ws, out, steps, warmup, stream, ops, flush_buf=None):
+    """Device-resident steps (scatter + attention) launched one call at a time
+    from Python; returns per-step milliseconds, the mean of CUDA events around
+    each attention call in that loop (host gaps included), and the attention
+    call's device time from back-to-back launches (`_device_ms`, the roofline
+    figure)."""
+    import torch
+
+    def attention():
+        ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens,
+                            d.query_start_loc, b.scale, max_q_len=b.max_q_len,
+                            max_seq_len=b.max_seq_len, out=out, workspace=ws)
 
     def step(ev=None):
         if d.copy_pairs.numel():
@@ -205,9 +283,7 @@ def _time_steps(b, d, ws, out, steps, warmup, stream, ops):
         ops.reshape_and_cache(d.k_new, d.v_new, d.k_cache, d.v_cache, d.slot_mapping)
         if ev is not None:
             ev[0].record(stream)
-        ops.paged_attention(d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens,
-                            d.query_start_loc, b.scale, max_q_len=b.max_q_len,
-                            max_seq_len=b.max_seq_len, out=out, workspace=ws)
+        attention()
         if ev is not None:
             ev[1].record(stream)
 
@@ -224,8 +300,10 @@ def _time_steps(b, d, ws, out, steps, warmup, stream, ops):
     t1.record(stream)
     torch.cuda.synchronize()
     ops.check_device_errors()
+    dev_ms = _device_ms(attention, steps, warmup, stream, flush_buf)
+    ops.check_device_errors()
     return (t0.elapsed_time(t1) / steps,
-            statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs))
+            statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs), dev_ms)
 
 
 def _time_graph_steps(b, d, steps, warmup, stream, ops):
@@ -290,7 +368,10 @@ def _prefill_only(b, d):
                      query_start_loc=W.int32_tensor(qsl, dev))
 
 
-def _time_prefill(b, d, steps, warmup, stream, ops):
+def _time_prefill(b, d, steps, warmup, stream, ops, flush_buf):
+    """The batch's prefill rows alone (one prefill launch, plus the key-split
+    merge when the plan splits): device time per call with L2 flushed before
+    every call (`_device_ms`)."""
     import torch
     from paged_kv_cache_174_gb300 import workloads as W
     po = _prefill_only(b, d)
@@ -308,17 +389,8 @@ def _time_prefill(b, d, steps, warmup, stream, ops):
                             max_seq_len=sub.max_seq_len, out=out, workspace=ws,
                             min_q_len=int(sub.q_lens.min()))
 
-    for _ in range(warmup):
-        call()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        call()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    ms = _device_ms(call, steps, warmup, stream, flush_buf)
     ops.check_device_errors()
-    ms = e0.elapsed_time(e1) / steps
     flops = W.causal_flops(sub)
     return {"ms": round(ms, 5), "flops": flops, "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
             "tokens": sub.num_tokens}
@@ -510,13 +582,16 @@ def _fp8(args, dev, stream, ops, peaks, bf16_attn_ms):
                              b.max_seq_len, dev)
     out = torch.empty_like(q)
 
+    def attention():
+        ops.paged_attention_fp8(q, k8, v8, ks, vs, meta["block_tables"], meta["seq_lens"],
+                                meta["query_start_loc"], b.scale, max_q_len=1,
+                                max_seq_len=b.max_seq_len, out=out, workspace=ws)
+
     def step(ev=None):
         ops.reshape_and_cache_fp8(kn, vn, k8, v8, ks, vs, meta["slot_mapping"])
         if ev is not None:
             ev[0].record(stream)
-        ops.paged_attention_fp8(q, k8, v8, ks, vs, meta["block_tables"], meta["seq_lens"],
-                                meta["query_start_loc"], b.scale, max_q_len=1,
-                                max_seq_len=b.max_seq_len, out=out, workspace=ws)
+        attention()
         if ev is not None:
             ev[1].record(stream)
 
@@ -534,12 +609,16 @@ def _fp8(args, dev, stream, ops, peaks, bf16_attn_ms):
     torch.cuda.synchronize()
     ops.check_device_errors()
     ms = t0.elapsed_time(t1) / args.steps
-    attn_ms = statistics.mean(a.elapsed_time(c) for a, c in evs)
+    loop_attn_ms = statistics.mean(a.elapsed_time(c) for a, c in evs)
+    # the roofline's duration: back-to-back launches (inputs larger than L2)
+    attn_ms = _device_ms(attention, args.steps, args.warmup, stream)
+    ops.check_device_errors()
     alg = W.algorithmic_bytes_fp8(b)
     gbs = alg["attention"] / (attn_ms * 1e-3) / 1e9
     mixed = None if args.no_mixed else _fp8_mixed(args, dev, stream, ops, peaks)
     return {"workload": "decode_batch, 8-bit cache (E4M3 codes + fp32 scale per row)",
             "ms_per_step": round(ms, 5), "attention_ms": round(attn_ms, 5),
+            "attention_ms_host_loop": round(loop_attn_ms, 5),
             "tokens_per_s": round(b.num_tokens / (ms * 1e-3), 1),
             "kv_tokens_per_s": round(int(b.seq_lens.sum()) / (attn_ms * 1e-3), 1),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
@@ -592,19 +671,11 @@ def _fp8_mixed(args, dev, stream, ops, peaks):
                                 t["query_start_loc"], sub.scale, max_q_len=sub.max_q_len,
                                 max_seq_len=sub.max_seq_len, out=sout, workspace=ws)
 
-    res = {}
-    for name, fn in (("step", step), ("chunk", chunk)):
-        for _ in range(args.warmup):
-            fn()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ops.check_device_errors()
-        res[name] = e0.elapsed_time(e1) / args.steps
+    # device time per call (`_device_ms`): the step's inputs are larger than
+    # L2; the chunk's K/V are not, so L2 is flushed before each chunk call
+    res = {"step": _device_ms(step, args.steps, args.warmup, stream),
+           "chunk": _device_ms(chunk, args.steps, args.warmup, stream, _flush_buffer(dev))}
+    ops.check_device_errors()
     flops = W.causal_flops(sub)
     tflops = flops / (res["chunk"] * 1e-3) / 1e12
     return {"workload": "mixed_step over the 8-bit cache",
@@ -633,7 +704,8 @@ def _other_decodes(args, dev, stream, ops, peaks, host_batches=None):
         ws = ops.alloc_workspace(b.num_seqs, b.num_tokens, b.num_q_heads, b.num_kv_heads,
                                  b.head_dim, b.max_q_len, b.max_seq_len, dev)
         out = torch.empty_like(d.q)
-        ms, attn_ms = _time_steps(b, d, ws, out, args.steps, args.warmup, stream, ops)
+        ms, loop_ms, attn_ms = _time_steps(b, d, ws, out, args.steps, args.warmup, stream, ops,
+                                           _flush_if_small(b, dev))
         # the same step as one graph launch (decode-only: the decode kernel
         # does the scatter), which shows the device latency of a small step
         # without the host's per-call overhead
@@ -644,6 +716,7 @@ def _other_decodes(args, dev, stream, ops, peaks, host_batches=None):
                 "decode batch of 64 requests (lens U[128, 4096]) at 64 q / 8 kv heads, d 128")
         res[name] = {"description": desc,
                      "ms_per_step": round(ms, 5), "attention_ms": round(attn_ms, 5),
+                     "attention_ms_host_loop": round(loop_ms, 5),
                      "graph_ms_per_step": round(graph_ms, 5),
                      "attention_GB_per_s": round(gbs, 1),
                      "attention_frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
@@ -668,7 +741,7 @@ def _block32(args, dev, stream, ops, peaks):
         ws = ops.alloc_workspace(b.num_seqs, b.num_tokens, b.num_q_heads, b.num_kv_heads,
                                  b.head_dim, b.max_q_len, b.max_seq_len, dev)
         out = torch.empty_like(d.q)
-        ms, attn_ms = _time_steps(b, d, ws, out, args.steps, args.warmup, stream, ops)
+        ms, _, attn_ms = _time_steps(b, d, ws, out, args.steps, args.warmup, stream, ops)
         alg = W.algorithmic_bytes(b)
         res[name] = {"ms_per_step": round(ms, 5), "attention_ms": round(attn_ms, 5),
                      "GB_per_s": round(alg["total"] / (ms * 1e-3) / 1e9, 1),
@@ -756,8 +829,9 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    # separate launches per step (events around the attention call: roofline)
-    ms_sep, attn_ms = _time_steps(b, d, ws, out, args.steps, args.warmup, stream, ops)
+    # separate launches per step; the attention call's device time (roofline)
+    ms_sep, loop_attn_ms, attn_ms = _time_steps(b, d, ws, out, args.steps, args.warmup, stream,
+                                                ops, _flush_if_small(b, dev))
     if world > 1:
         dist.barrier()
     # the step as one graph launch (the value)
@@ -767,7 +841,8 @@ def run_ours(args):
     clk = clocks.stop()
     if not torch.equal(gout[:b.num_tokens].view(torch.int16), out.view(torch.int16)):
         raise RuntimeError("the graph step's output differs from the separate launches'")
-    ms, ms_sep, attn_ms = reduce_max([ms, ms_sep, attn_ms], dist if world > 1 else None, dev)
+    ms, ms_sep, attn_ms, loop_attn_ms = reduce_max([ms, ms_sep, attn_ms, loop_attn_ms],
+                                                   dist if world > 1 else None, dev)
 
     # ---- end to end through the public API from pinned host memory: the
     # step captured as a graph (ops.StepGraph, host_io) whose launch copies
@@ -841,7 +916,10 @@ def run_ours(args):
                                                   ["pa_decode_kernel.cuh", "pa_decode.cu",
                                                    "pa_common.cuh"], b.name, "decode_batch"),
                      "algorithmic_bytes_per_launch": alg["attention"],
-                     "avg_launch_ms": round(attn_ms, 5)},
+                     "avg_launch_ms": round(attn_ms, 5),
+                     "timing": "CUDA events around a CUDA graph of back-to-back attention "
+                               "calls (median of 5 replays); inputs larger than L2",
+                     "avg_launch_ms_host_loop": round(loop_attn_ms, 5)},
         "e2e": {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
@@ -861,11 +939,11 @@ def run_ours(args):
         mws = ops.alloc_workspace(mb.num_seqs, mb.num_tokens, mb.num_q_heads, mb.num_kv_heads,
                                   mb.head_dim, mb.max_q_len, mb.max_seq_len, dev)
         mout = torch.empty_like(md.q)
-        mms, mattn = _time_steps(mb, md, mws, mout, args.steps, args.warmup, stream, ops)
+        mms, _, mattn = _time_steps(mb, md, mws, mout, args.steps, args.warmup, stream, ops)
         mgms, mgout = _time_graph_steps(mb, md, args.steps, args.warmup, stream, ops)
         if not torch.equal(mgout[:mb.num_tokens].view(torch.int16), mout.view(torch.int16)):
             raise RuntimeError("the mixed step's graph output differs from separate launches'")
-        pre = _time_prefill(mb, md, args.steps, args.warmup, stream, ops)
+        pre = _time_prefill(mb, md, args.steps, args.warmup, stream, ops, _flush_buffer(dev))
         bounds = _mixed_bounds(mb, peaks)
         line["mixed_batch"] = {
             "workload": mb.name, "description": W.WORKLOADS[mb.name].description,
@@ -894,7 +972,10 @@ def run_ours(args):
                                              ["pa_prefill_kernel.cuh", "pa_prefill.cu",
                                               "pa_common.cuh", "pa_tcgen05.cuh"],
                                              mb.name, "mixed_step"),
-                "algorithmic_flops_per_launch": pre["flops"], "avg_launch_ms": pre["ms"]}
+                "algorithmic_flops_per_launch": pre["flops"], "avg_launch_ms": pre["ms"],
+                "timing": "CUDA events around a CUDA graph of back-to-back calls, each after "
+                          "a 256 MB write that evicts L2, minus a graph of the writes alone "
+                          "(median of 5 replays)"}
         del md, mws, mout
     if not args.no_trace:
         line["trace"] = _run_trace(dev, stream, ops, args.warmup)
