@@ -144,6 +144,22 @@ struct PageCursor {
   }
 };
 
+// L2 policy for data read once per call (evicted before other lines), and a
+// bulk copy that carries it.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst_smem, const void* src, uint32_t bytes,
+                                              uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(dst_smem),
+      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
+}
+
 // Issue the bulk copies of page (c.s, c.j) into a stage.  *fused_slot gets the
 // slot the stage's last row must be stored to (fused scatter), or -1.
 template <bool FUSE>
@@ -165,6 +181,10 @@ __device__ __forceinline__ void fetch_page(const DecodeParams& p, const PageCurs
   // 16-token page index in the pool: a block of 32 tokens is two pages
   const size_t page = ((size_t)phys << p.block_shift) + (c.j & ((1 << p.block_shift) - 1));
   const size_t off = page * p.page_bytes;
+  // the pages are read once per call: evict-first keeps them from pushing
+  // the call's reused data (tables, q, partial results) out of L2 (decode
+  // batch on GB300: 91.3 against 93.6 us per call)
+  const uint64_t pol = l2_evict_first_policy();
   if (FUSE && c.j == c.np - 1) {
     // the request's new token (position L - 1, last row of this page) comes
     // from k_new / v_new instead of the cache, which does not hold it yet
@@ -174,10 +194,11 @@ __device__ __forceinline__ void fetch_page(const DecodeParams& p, const PageCurs
     if (slot == want) {
       const uint32_t head = (uint32_t)(ntok - 1) * p.row_bytes;  // rows before the new one
       if (head) {
-        bulk_g2s(stage_smem, reinterpret_cast<const unsigned char*>(p.k_cache) + off, head,
-                 full_bar);
-        bulk_g2s(stage_smem + p.page_bytes,
-                 reinterpret_cast<const unsigned char*>(p.v_cache) + off, head, full_bar);
+        bulk_g2s_hint(stage_smem, reinterpret_cast<const unsigned char*>(p.k_cache) + off, head,
+                      full_bar, pol);
+        bulk_g2s_hint(stage_smem + p.page_bytes,
+                      reinterpret_cast<const unsigned char*>(p.v_cache) + off, head, full_bar,
+                      pol);
       }
       bulk_g2s(stage_smem + head, p.k_new + (int64_t)a * (p.row_bytes / 2), p.row_bytes,
                full_bar);
@@ -190,9 +211,10 @@ __device__ __forceinline__ void fetch_page(const DecodeParams& p, const PageCurs
     // as with a separate scatter; any other slot breaks the precondition
     if (slot >= 0) flag_error(p.err, DEVERR_BOUNDS);
   }
-  bulk_g2s(stage_smem, reinterpret_cast<const unsigned char*>(p.k_cache) + off, bytes, full_bar);
-  bulk_g2s(stage_smem + p.page_bytes, reinterpret_cast<const unsigned char*>(p.v_cache) + off,
-           bytes, full_bar);
+  bulk_g2s_hint(stage_smem, reinterpret_cast<const unsigned char*>(p.k_cache) + off, bytes,
+                full_bar, pol);
+  bulk_g2s_hint(stage_smem + p.page_bytes, reinterpret_cast<const unsigned char*>(p.v_cache) + off,
+                bytes, full_bar, pol);
   if (p.scale_bytes) {  // the whole page's scales (rows past ntok are never read)
     const size_t soff = page * p.scale_bytes;
     bulk_g2s(stage_smem + 2 * p.page_bytes,
