@@ -568,12 +568,12 @@ def _fp8(args, dev, stream, ops, peaks, bf16_attn_ms):
 
     b = W.decode_batch(poison=False)
     nb, bs, nkv, d = b.k_cache.shape
-    k8, v8, ks, vs = ops.empty_fp8_cache(nb, bs, nkv, d, dev)
+    k8, v8 = ops.empty_fp8_cache(nb, bs, nkv, d, dev)
     slots = W.context_slots(b)
     rows = b.k_cache.reshape(-1, nkv, d)
     ops.reshape_and_cache_fp8(W.bf16_tensor(rows[slots], dev),
                               W.bf16_tensor(b.v_cache.reshape(-1, nkv, d)[slots], dev),
-                              k8, v8, ks, vs, W.int32_tensor(slots, dev))
+                              k8, v8, W.int32_tensor(slots, dev))
     q = W.bf16_tensor(b.q, dev)
     kn, vn = W.bf16_tensor(b.k_new, dev), W.bf16_tensor(b.v_new, dev)
     meta = {k: W.int32_tensor(getattr(b, k), dev)
@@ -583,12 +583,12 @@ def _fp8(args, dev, stream, ops, peaks, bf16_attn_ms):
     out = torch.empty_like(q)
 
     def attention():
-        ops.paged_attention_fp8(q, k8, v8, ks, vs, meta["block_tables"], meta["seq_lens"],
+        ops.paged_attention_fp8(q, k8, v8, meta["block_tables"], meta["seq_lens"],
                                 meta["query_start_loc"], b.scale, max_q_len=1,
                                 max_seq_len=b.max_seq_len, out=out, workspace=ws)
 
     def step(ev=None):
-        ops.reshape_and_cache_fp8(kn, vn, k8, v8, ks, vs, meta["slot_mapping"])
+        ops.reshape_and_cache_fp8(kn, vn, k8, v8, meta["slot_mapping"])
         if ev is not None:
             ev[0].record(stream)
         attention()
@@ -644,12 +644,12 @@ def _fp8_mixed(args, dev, stream, ops, peaks):
 
     b = W.mixed_step(poison=False)
     nb, bs, nkv, d = b.k_cache.shape
-    k8, v8, ks, vs = ops.empty_fp8_cache(nb, bs, nkv, d, dev)
+    k8, v8 = ops.empty_fp8_cache(nb, bs, nkv, d, dev)
     slots = W.context_slots(b)
     rows = b.k_cache.reshape(-1, nkv, d)
     ops.reshape_and_cache_fp8(W.bf16_tensor(rows[slots], dev),
                               W.bf16_tensor(b.v_cache.reshape(-1, nkv, d)[slots], dev),
-                              k8, v8, ks, vs, W.int32_tensor(slots, dev))
+                              k8, v8, W.int32_tensor(slots, dev))
     q = W.bf16_tensor(b.q, dev)
     kn, vn = W.bf16_tensor(b.k_new, dev), W.bf16_tensor(b.v_new, dev)
     meta = {k: W.int32_tensor(getattr(b, k), dev)
@@ -661,13 +661,13 @@ def _fp8_mixed(args, dev, stream, ops, peaks):
     sout = torch.empty_like(t["q"])
 
     def step():
-        ops.reshape_and_cache_fp8(kn, vn, k8, v8, ks, vs, meta["slot_mapping"])
-        ops.paged_attention_fp8(q, k8, v8, ks, vs, meta["block_tables"], meta["seq_lens"],
+        ops.reshape_and_cache_fp8(kn, vn, k8, v8, meta["slot_mapping"])
+        ops.paged_attention_fp8(q, k8, v8, meta["block_tables"], meta["seq_lens"],
                                 meta["query_start_loc"], b.scale, max_q_len=b.max_q_len,
                                 max_seq_len=b.max_seq_len, out=out, workspace=ws)
 
     def chunk():
-        ops.paged_attention_fp8(t["q"], k8, v8, ks, vs, t["block_tables"], t["seq_lens"],
+        ops.paged_attention_fp8(t["q"], k8, v8, t["block_tables"], t["seq_lens"],
                                 t["query_start_loc"], sub.scale, max_q_len=sub.max_q_len,
                                 max_seq_len=sub.max_seq_len, out=sout, workspace=ws)
 

@@ -281,13 +281,20 @@ int pa_swap_in(pa_bf16 *k_cache, pa_bf16 *v_cache, int32_t num_blocks, int32_t b
 
 /*
  * 8-bit KV cache.  The pages have no counterpart: every cache they describe
- * holds the model's own precision.  This variant stores the same layout with
- * FP8 E4M3 codes (1 sign, 4 exponent bits of bias 7, 3 mantissa bits, no
- * infinities, largest magnitude 448) and one fp32 scale per cached
- * (token, kv head) row, so decode attention reads about half the bytes:
+ * holds the model's own precision.  This variant stores FP8 E4M3 codes (1
+ * sign, 4 exponent bits of bias 7, 3 mantissa bits, no infinities, largest
+ * magnitude 448) and one fp32 scale per cached (token, kv head) row, so
+ * decode attention reads about half the bytes.  Each 16-token page of a
+ * block holds its codes, then their scales, so one copy brings both:
  *
- *   k_cache, v_cache  [num_blocks, block_size, num_kv_heads, head_dim] uint8
- *   k_scale, v_scale  [num_blocks, block_size, num_kv_heads] fp32
+ *   page               [16, num_kv_heads, head_dim] uint8 codes, then
+ *                      [16, num_kv_heads] fp32 scales:
+ *                      pa_fp8_page_bytes(num_kv_heads, head_dim)
+ *                      = 16 * num_kv_heads * (head_dim + 4) bytes
+ *   k_cache, v_cache   [num_blocks, block_size / 16] pages
+ *
+ * The slot of token row r of page p of block b is b * block_size + 16 p + r.
+ * block_size is a multiple of 16 (16 or 32 for attention).
  *
  * A row x (head_dim bf16 values) is stored as scale = max |x| / 448 (1 when
  * the row is all zero) and codes e4m3(x_c / scale), rounding to nearest with
@@ -304,39 +311,37 @@ int pa_swap_in(pa_bf16 *k_cache, pa_bf16 *v_cache, int32_t num_blocks, int32_t b
  *
  * pa_reshape_and_cache_fp8: pa_reshape_and_cache, quantising each new row
  * (codes and scale written to the new token's slot).  Alignment: k, v and
- * the code arrays 16 bytes, scales and slot_mapping 4 bytes.
+ * both caches 16 bytes, slot_mapping 4 bytes.
  */
+size_t pa_fp8_page_bytes(int32_t num_kv_heads, int32_t head_dim);
+
 int pa_reshape_and_cache_fp8(const pa_bf16 *k, const pa_bf16 *v, int32_t num_tokens,
-                             uint8_t *k_cache, uint8_t *v_cache, float *k_scale, float *v_scale,
-                             int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
-                             int32_t head_dim, const int32_t *slot_mapping, cudaStream_t stream);
+                             uint8_t *k_cache, uint8_t *v_cache, int32_t num_blocks,
+                             int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                             const int32_t *slot_mapping, cudaStream_t stream);
 
 /*
  * pa_paged_attention over the 8-bit cache (same arguments, meaning, errors
- * and workspace as pa_paged_attention, plus the two scale arrays, which must
- * be 16-byte aligned).  Decode and prefill rows, mixed in one call, as
+ * and workspace as pa_paged_attention, with the caches in the page format
+ * above).  Decode and prefill rows, mixed in one call, as
  * pa_paged_attention (see above for the arithmetic).
  */
 int pa_paged_attention_fp8(const pa_bf16 *q, const uint8_t *k_cache, const uint8_t *v_cache,
-                           const float *k_scale, const float *v_scale, int32_t num_blocks,
-                           int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads,
-                           int32_t head_dim, const int32_t *block_tables, int32_t max_blocks,
-                           const int32_t *seq_lens, const int32_t *query_start_loc,
-                           int32_t num_seqs, int32_t num_tokens, int32_t max_q_len,
-                           int32_t max_seq_len, float scale, pa_bf16 *out, void *workspace,
-                           size_t workspace_bytes, cudaStream_t stream);
+                           int32_t num_blocks, int32_t block_size, int32_t num_q_heads,
+                           int32_t num_kv_heads, int32_t head_dim, const int32_t *block_tables,
+                           int32_t max_blocks, const int32_t *seq_lens,
+                           const int32_t *query_start_loc, int32_t num_seqs, int32_t num_tokens,
+                           int32_t max_q_len, int32_t max_seq_len, float scale, pa_bf16 *out,
+                           void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * pa_copy_blocks over the 8-bit cache: each pair copies the destination
- * block's codes and scales from the source block (same pair rules, padding
- * and errors).  A block's codes and its scales must each be a multiple of 16
- * bytes (block_size * num_kv_heads a multiple of 4); all four arrays 16-byte
- * aligned.
+ * block's pages (codes and scales) from the source block (same pair rules,
+ * padding and errors).  Both caches 16-byte aligned.
  */
-int pa_copy_blocks_fp8(uint8_t *k_cache, uint8_t *v_cache, float *k_scale, float *v_scale,
-                       int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
-                       int32_t head_dim, const int32_t *src_dst_pairs, int32_t num_pairs,
-                       cudaStream_t stream);
+int pa_copy_blocks_fp8(uint8_t *k_cache, uint8_t *v_cache, int32_t num_blocks,
+                       int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                       const int32_t *src_dst_pairs, int32_t num_pairs, cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device error word that

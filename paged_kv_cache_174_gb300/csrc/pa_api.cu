@@ -145,49 +145,57 @@ int pa_copy_blocks(pa_bf16* k_cache, pa_bf16* v_cache, int32_t num_blocks, int32
   return PA_OK;
 }
 
+size_t pa_fp8_page_bytes(int32_t num_kv_heads, int32_t head_dim) {
+  if (num_kv_heads <= 0 || head_dim <= 0) return 0;
+  return (size_t)pa::fp8_page_bytes(num_kv_heads, head_dim);
+}
+
 int pa_reshape_and_cache_fp8(const pa_bf16* k, const pa_bf16* v, int32_t num_tokens,
-                             uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float* v_scale,
-                             int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
-                             int32_t head_dim, const int32_t* slot_mapping, cudaStream_t stream) {
+                             uint8_t* k_cache, uint8_t* v_cache, int32_t num_blocks,
+                             int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                             const int32_t* slot_mapping, cudaStream_t stream) {
   if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens %d < 0", num_tokens);
   int st = check_cache_geometry(num_blocks, block_size, num_kv_heads, head_dim);
   if (st) return st;
   if (head_dim != 64 && head_dim != 128)
     return fail(PA_ERR_UNSUPPORTED, "8-bit cache with head_dim %d (64 or 128)", head_dim);
+  if (block_size % pa::kFp8PageTokens)
+    return fail(PA_ERR_UNSUPPORTED, "8-bit cache with block_size %d (a multiple of 16)",
+                block_size);
   if (num_tokens == 0) return PA_OK;
-  if (!k || !v || !k_cache || !v_cache || !k_scale || !v_scale || !slot_mapping)
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping)
     return fail(PA_ERR_INVALID_ARG, "null pointer argument");
   if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-      !aligned(k_scale, 4) || !aligned(v_scale, 4) || !aligned(slot_mapping, 4))
-    return fail(PA_ERR_INVALID_ARG, "k, v and the code arrays must be 16-byte aligned");
+      !aligned(slot_mapping, 4))
+    return fail(PA_ERR_INVALID_ARG, "k, v and the caches must be 16-byte aligned");
   unsigned* err = nullptr;
   st = device_state(&err, nullptr);
   if (st) return st;
   pa::NvtxRange range("pa_reshape_and_cache_fp8 (quantising slot scatter)");
   cudaError_t e = pa::launch_reshape_and_cache_fp8(
-      k, v, num_tokens, k_cache, v_cache, k_scale, v_scale, (int64_t)num_blocks * block_size,
-      num_kv_heads, head_dim, slot_mapping, err, stream);
+      k, v, num_tokens, k_cache, v_cache, (int64_t)num_blocks * block_size, num_kv_heads,
+      head_dim, slot_mapping, err, stream);
   if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache_fp8 launch");
   return PA_OK;
 }
 
-int pa_copy_blocks_fp8(uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float* v_scale,
-                       int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
-                       int32_t head_dim, const int32_t* src_dst_pairs, int32_t num_pairs,
-                       cudaStream_t stream) {
+int pa_copy_blocks_fp8(uint8_t* k_cache, uint8_t* v_cache, int32_t num_blocks,
+                       int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                       const int32_t* src_dst_pairs, int32_t num_pairs, cudaStream_t stream) {
   if (num_pairs < 0) return fail(PA_ERR_INVALID_ARG, "num_pairs %d < 0", num_pairs);
   int st = check_cache_geometry(num_blocks, block_size, num_kv_heads, head_dim);
   if (st) return st;
-  const int64_t code_bytes = (int64_t)block_size * num_kv_heads * head_dim;
-  const int64_t scale_bytes = (int64_t)block_size * num_kv_heads * 4;
-  if (code_bytes % 16 || scale_bytes % 16)
-    return fail(PA_ERR_UNSUPPORTED, "a block's codes and scales must be multiples of 16 bytes");
+  if (block_size % pa::kFp8PageTokens)
+    return fail(PA_ERR_UNSUPPORTED, "8-bit cache with block_size %d (a multiple of 16)",
+                block_size);
+  // whole 16-token pages, codes and scales together (a multiple of 16 bytes)
+  const int64_t block_bytes =
+      (int64_t)(block_size / pa::kFp8PageTokens) * pa::fp8_page_bytes(num_kv_heads, head_dim);
   if (num_pairs == 0) return PA_OK;
-  if (!k_cache || !v_cache || !k_scale || !v_scale || !src_dst_pairs)
+  if (!k_cache || !v_cache || !src_dst_pairs)
     return fail(PA_ERR_INVALID_ARG, "null pointer argument");
-  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_scale, 16) ||
-      !aligned(v_scale, 16) || !aligned(src_dst_pairs, 4))
-    return fail(PA_ERR_INVALID_ARG, "codes and scales must be 16-byte aligned, pairs 4-byte");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(src_dst_pairs, 4))
+    return fail(PA_ERR_INVALID_ARG, "the caches must be 16-byte aligned, pairs 4-byte");
   if (num_pairs > 0x7fffffff / 2) return fail(PA_ERR_INVALID_ARG, "too many pairs");
   unsigned* err = nullptr;
   st = device_state(&err, nullptr);
@@ -196,11 +204,7 @@ int pa_copy_blocks_fp8(uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float
   // the copy kernel moves 16-byte vectors; sizes are given in 2-byte units
   cudaError_t e = pa::launch_copy_blocks(reinterpret_cast<uint16_t*>(k_cache),
                                          reinterpret_cast<uint16_t*>(v_cache), num_blocks,
-                                         code_bytes / 2, src_dst_pairs, num_pairs, err, stream);
-  if (e == cudaSuccess)
-    e = pa::launch_copy_blocks(reinterpret_cast<uint16_t*>(k_scale),
-                               reinterpret_cast<uint16_t*>(v_scale), num_blocks,
-                               scale_bytes / 2, src_dst_pairs, num_pairs, err, stream);
+                                         block_bytes / 2, src_dst_pairs, num_pairs, err, stream);
   if (e != cudaSuccess) return cuda_fail(e, "copy_blocks_fp8 launch");
   return PA_OK;
 }
@@ -294,13 +298,11 @@ namespace {
 
 // pa_paged_attention with a cap on the workspace the prefill key split may
 // take (the allocation-free entry point has a fixed array).
-// The cache an attention call reads: bf16 values, or E4M3 codes with one
-// fp32 scale per (slot, kv head).
+// The cache an attention call reads: bf16 values, or pages of E4M3 codes
+// and their fp32 row scales.
 struct KvCache {
   const void* k;
   const void* v;
-  const float* k_scale;
-  const float* v_scale;
   bool fp8;
 };
 
@@ -327,7 +329,7 @@ int pa_paged_attention(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* 
                        const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens,
                        int32_t max_q_len, int32_t max_seq_len, float scale, pa_bf16* out,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  return paged_attention_impl(q, KvCache{k_cache, v_cache, nullptr, nullptr, false}, num_blocks,
+  return paged_attention_impl(q, KvCache{k_cache, v_cache, false}, num_blocks,
                               block_size, num_q_heads, num_kv_heads, head_dim, block_tables,
                               max_blocks, seq_lens, query_start_loc, num_seqs, num_tokens, 0,
                               max_q_len, max_seq_len, scale, out, workspace, workspace_bytes,
@@ -342,7 +344,7 @@ int pa_paged_attention_qrange(const pa_bf16* q, const pa_bf16* k_cache, const pa
                               int32_t num_tokens, int32_t min_q_len, int32_t max_q_len,
                               int32_t max_seq_len, float scale, pa_bf16* out, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream) {
-  return paged_attention_impl(q, KvCache{k_cache, v_cache, nullptr, nullptr, false}, num_blocks,
+  return paged_attention_impl(q, KvCache{k_cache, v_cache, false}, num_blocks,
                               block_size, num_q_heads, num_kv_heads, head_dim, block_tables,
                               max_blocks, seq_lens, query_start_loc, num_seqs, num_tokens,
                               min_q_len, max_q_len, max_seq_len, scale, out, workspace,
@@ -358,7 +360,7 @@ int pa_decode_step(const pa_bf16* q, const pa_bf16* k_new, const pa_bf16* v_new,
                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (!slot_mapping && num_tokens > 0)
     return fail(PA_ERR_INVALID_ARG, "null pointer argument (slot_mapping)");
-  return paged_attention_impl(q, KvCache{k_cache, v_cache, nullptr, nullptr, false}, num_blocks,
+  return paged_attention_impl(q, KvCache{k_cache, v_cache, false}, num_blocks,
                               block_size, num_q_heads, num_kv_heads, head_dim, block_tables,
                               max_blocks, seq_lens, query_start_loc, num_seqs, num_tokens, 0, 1,
                               max_seq_len, scale, out, workspace, workspace_bytes, ~size_t(0),
@@ -376,7 +378,7 @@ int pa_paged_attention_step(const pa_bf16* q, const pa_bf16* k_new, const pa_bf1
                             cudaStream_t stream) {
   if (!slot_mapping && num_tokens > 0)
     return fail(PA_ERR_INVALID_ARG, "null pointer argument (slot_mapping)");
-  return paged_attention_impl(q, KvCache{k_cache, v_cache, nullptr, nullptr, false}, num_blocks,
+  return paged_attention_impl(q, KvCache{k_cache, v_cache, false}, num_blocks,
                               block_size, num_q_heads, num_kv_heads, head_dim, block_tables,
                               max_blocks, seq_lens, query_start_loc, num_seqs, num_tokens, 0,
                               max_q_len, max_seq_len, scale, out, workspace, workspace_bytes,
@@ -384,14 +386,13 @@ int pa_paged_attention_step(const pa_bf16* q, const pa_bf16* k_new, const pa_bf1
 }
 
 int pa_paged_attention_fp8(const pa_bf16* q, const uint8_t* k_cache, const uint8_t* v_cache,
-                           const float* k_scale, const float* v_scale, int32_t num_blocks,
-                           int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads,
-                           int32_t head_dim, const int32_t* block_tables, int32_t max_blocks,
-                           const int32_t* seq_lens, const int32_t* query_start_loc,
-                           int32_t num_seqs, int32_t num_tokens, int32_t max_q_len,
-                           int32_t max_seq_len, float scale, pa_bf16* out, void* workspace,
-                           size_t workspace_bytes, cudaStream_t stream) {
-  return paged_attention_impl(q, KvCache{k_cache, v_cache, k_scale, v_scale, true}, num_blocks,
+                           int32_t num_blocks, int32_t block_size, int32_t num_q_heads,
+                           int32_t num_kv_heads, int32_t head_dim, const int32_t* block_tables,
+                           int32_t max_blocks, const int32_t* seq_lens,
+                           const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens,
+                           int32_t max_q_len, int32_t max_seq_len, float scale, pa_bf16* out,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return paged_attention_impl(q, KvCache{k_cache, v_cache, true}, num_blocks,
                               block_size, num_q_heads, num_kv_heads, head_dim, block_tables,
                               max_blocks, seq_lens, query_start_loc, num_seqs, num_tokens, 0,
                               max_q_len, max_seq_len, scale, out, workspace, workspace_bytes,
@@ -434,11 +435,8 @@ int paged_attention_impl(const pa_bf16* q, KvCache kv,
     return fail(PA_ERR_UNSUPPORTED, "shape head_dim=%d group=%d num_kv_heads=%d", head_dim,
                 group, num_kv_heads);
   if (num_seqs == 0 || num_tokens == 0 || max_seq_len == 0) return PA_OK;
-  if (!q || !kv.k || !kv.v || !block_tables || !seq_lens || !query_start_loc || !out ||
-      (kv.fp8 && (!kv.k_scale || !kv.v_scale)))
+  if (!q || !kv.k || !kv.v || !block_tables || !seq_lens || !query_start_loc || !out)
     return fail(PA_ERR_INVALID_ARG, "null pointer argument");
-  if (kv.fp8 && (!aligned(kv.k_scale, 16) || !aligned(kv.v_scale, 16)))
-    return fail(PA_ERR_INVALID_ARG, "scale arrays must be 16-byte aligned");
   if (fuse && (!fuse_k_new || !fuse_v_new || !aligned(fuse_k_new, 16) ||
                !aligned(fuse_v_new, 16) || !aligned(fuse_slot_mapping, 4)))
     return fail(PA_ERR_INVALID_ARG, "k_new / v_new must be 16-byte aligned, slot_mapping 4-byte");
@@ -476,8 +474,6 @@ int paged_attention_impl(const pa_bf16* q, KvCache kv,
   a.q = q;
   a.k_cache = kv.k;
   a.v_cache = kv.v;
-  a.k_scale = kv.k_scale;
-  a.v_scale = kv.v_scale;
   a.fp8 = kv.fp8;
   a.fuse_k_new = fuse_k_new;
   a.fuse_v_new = fuse_v_new;
@@ -630,7 +626,7 @@ int pa_paged_attention_noalloc(const pa_bf16* q, const pa_bf16* k_cache,
   void* scratch = nullptr;
   int st = noalloc_scratch(&scratch);
   if (st) return st;
-  return paged_attention_impl(q, KvCache{k_cache, v_cache, nullptr, nullptr, false}, num_blocks,
+  return paged_attention_impl(q, KvCache{k_cache, v_cache, false}, num_blocks,
                               block_size, num_q_heads, num_kv_heads, head_dim, block_tables,
                               max_blocks, seq_lens, query_start_loc, num_seqs, num_tokens, 0,
                               max_q_len, max_seq_len, scale, out, scratch, kNoAllocScratchBytes,

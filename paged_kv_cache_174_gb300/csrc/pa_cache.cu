@@ -16,8 +16,9 @@
 //   packs the listed blocks into a staging buffer (or unpacks them), so the
 //   host transfer is two large copies rather than one per block.
 // 8-bit cache scatter: each (token, kv head) row is quantised to E4M3 codes
-//   with one fp32 scale (row max / 448); the block copy of that cache moves
-//   the codes and the scales with the same copy kernel.
+//   with one fp32 scale (row max / 448), written into the slot's 16-token
+//   page (codes first, then the page's scales); the block copy of that cache
+//   moves whole pages.
 #include <cstdint>
 
 #include "pa_common.cuh"
@@ -64,9 +65,8 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
 template <int LPH>
 __global__ void __launch_bounds__(kScatterWarps * 32)
     reshape_and_cache_fp8_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
-                                 int32_t num_tokens, uint2* __restrict__ k_cache,
-                                 uint2* __restrict__ v_cache, float* __restrict__ k_scale,
-                                 float* __restrict__ v_scale, int64_t num_slots,
+                                 int32_t num_tokens, unsigned char* __restrict__ k_cache,
+                                 unsigned char* __restrict__ v_cache, int64_t num_slots,
                                  int32_t num_kv_heads, const int32_t* __restrict__ slot_mapping,
                                  unsigned* err) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -79,8 +79,13 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
     return;
   }
   constexpr int HPP = 32 / LPH;  // kv heads per pass of the warp
+  constexpr int D = LPH * 8;
   const int sub = lane % LPH;
   const int row_vec = num_kv_heads * LPH;  // 8-element vectors per token row
+  // the slot's page and row: codes at row * n_kv + h, scales after the codes
+  const int64_t page_off = (slot / kFp8PageTokens) * fp8_page_bytes(num_kv_heads, D);
+  const int r = (int)(slot % kFp8PageTokens);
+  const int64_t scales_off = page_off + fp8_scales_offset(num_kv_heads, D);
   for (int h0 = 0; h0 < num_kv_heads; h0 += HPP) {
     const int h = h0 + lane / LPH;
     const bool on = h < num_kv_heads;
@@ -103,9 +108,11 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
       codes.y = (uint32_t)e4m3x2_from_floats(__fdiv_rn(x2.x, sc), __fdiv_rn(x2.y, sc)) |
                 ((uint32_t)e4m3x2_from_floats(__fdiv_rn(x3.x, sc), __fdiv_rn(x3.y, sc)) << 16);
       if (on) {
-        uint2* dst = which ? v_cache : k_cache;
-        dst[slot * row_vec + h * LPH + sub] = codes;
-        if (sub == 0) (which ? v_scale : k_scale)[slot * num_kv_heads + h] = sc;
+        unsigned char* cache = which ? v_cache : k_cache;
+        *reinterpret_cast<uint2*>(cache + page_off + ((int64_t)r * row_vec + h * LPH + sub) * 8) =
+            codes;
+        if (sub == 0)
+          *reinterpret_cast<float*>(cache + scales_off + ((int64_t)r * num_kv_heads + h) * 4) = sc;
       }
     }
   }
@@ -227,17 +234,15 @@ cudaError_t launch_reshape_and_cache(const uint16_t* k, const uint16_t* v, int32
 
 cudaError_t launch_reshape_and_cache_fp8(const uint16_t* k, const uint16_t* v,
                                          int32_t num_tokens, uint8_t* k_cache, uint8_t* v_cache,
-                                         float* k_scale, float* v_scale, int64_t num_slots,
-                                         int32_t num_kv_heads, int32_t head_dim,
-                                         const int32_t* slot_mapping, unsigned* err,
-                                         cudaStream_t stream) {
+                                         int64_t num_slots, int32_t num_kv_heads,
+                                         int32_t head_dim, const int32_t* slot_mapping,
+                                         unsigned* err, cudaStream_t stream) {
   if (num_tokens == 0) return cudaSuccess;
   const int grid = (num_tokens + kScatterWarps - 1) / kScatterWarps;
   auto args = [&](auto kern) {
     kern<<<grid, kScatterWarps * 32, 0, stream>>>(
         reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v), num_tokens,
-        reinterpret_cast<uint2*>(k_cache), reinterpret_cast<uint2*>(v_cache), k_scale, v_scale,
-        num_slots, num_kv_heads, slot_mapping, err);
+        k_cache, v_cache, num_slots, num_kv_heads, slot_mapping, err);
     return cudaGetLastError();
   };
   if (head_dim == 128) return args(reshape_and_cache_fp8_kernel<16>);

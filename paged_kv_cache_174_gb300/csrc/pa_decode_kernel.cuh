@@ -21,8 +21,10 @@
 //    bulk asynchronous copy each into a ring of shared-memory stages, tracked
 //    by mbarriers (the last warp to release a stage refills it): several
 //    pages per SM are in flight at once, which is what keeps HBM busy.
-//  * 8-bit cache (F8): the page holds E4M3 codes and each (token, kv head)
-//    row has one fp32 scale; the page's scales come with two more bulk copies.
+//  * 8-bit cache (F8): the page holds E4M3 codes and, after all 16 rows, one
+//    fp32 scale per (token, kv head) row, so one copy per K or V page brings
+//    both (two small scale copies per page beside the codes cost 4 us more
+//    on the 8-bit decode batch).
 //    A key row's score is (q . codes) * scale; a value row is codes * scale.
 //  * Each consumer warp owns one kv head (and a slice of the page's tokens)
 //    and all q heads of its GQA group, so every K/V byte is read from HBM
@@ -47,10 +49,8 @@ constexpr float kNegInf = -INFINITY;
 
 struct DecodeParams {
   const uint16_t* q;
-  const void* k_cache;     // bf16 values, or E4M3 codes (F8)
+  const void* k_cache;     // bf16 values, or (F8) pages of E4M3 codes and row scales
   const void* v_cache;
-  const float* k_scale;    // F8: [num_blocks * block_size, n_kv] row scales
-  const float* v_scale;
   // Fused scatter (bf16 cache, decode-only steps): the new token of a decode
   // request comes from k_new / v_new into its page in shared memory and is
   // stored from there to its slot slot_mapping[t], which must be the slot of
@@ -71,10 +71,10 @@ struct DecodeParams {
   float scale_log2;
   int32_t nstages;
   int32_t ctas;
-  uint32_t stage_bytes;  // K page + V page (+ their scales, F8)
-  uint32_t page_bytes;   // one K (or V) page of 16 tokens: 16 * n_kv * head_dim * elem
+  uint32_t stage_bytes;  // K page + V page
+  uint32_t page_bytes;   // one K (or V) page of 16 tokens: 16 * n_kv * head_dim * elem,
+                         // F8: the codes, then their 16 * n_kv fp32 scales
   uint32_t row_bytes;    // one token row of one cache: n_kv * head_dim * elem
-  uint32_t scale_bytes;  // F8: one page's scales of one cache (16 * n_kv * 4), else 0
 };
 
 // Pages this kernel processes for request s (0 if it is not a decode request
@@ -162,7 +162,7 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst_smem, const void* src
 
 // Issue the bulk copies of page (c.s, c.j) into a stage.  *fused_slot gets the
 // slot the stage's last row must be stored to (fused scatter), or -1.
-template <bool FUSE>
+template <bool FUSE, bool F8>
 __device__ __forceinline__ void fetch_page(const DecodeParams& p, const PageCursor& c,
                                            uint32_t stage_smem, uint32_t full_bar,
                                            int* fused_slot) {
@@ -176,8 +176,10 @@ __device__ __forceinline__ void fetch_page(const DecodeParams& p, const PageCurs
     mbar_arrive_expect_tx(full_bar, 0);  // completes the phase with no data
     return;
   }
-  const uint32_t bytes = (uint32_t)ntok * p.row_bytes;
-  mbar_arrive_expect_tx(full_bar, 2 * bytes + 2 * p.scale_bytes);
+  // the page's rows (F8: the whole page, whose scales follow all 16 rows;
+  // rows past ntok are never used)
+  const uint32_t bytes = F8 ? p.page_bytes : (uint32_t)ntok * p.row_bytes;
+  mbar_arrive_expect_tx(full_bar, 2 * bytes);
   // 16-token page index in the pool: a block of 32 tokens is two pages
   const size_t page = ((size_t)phys << p.block_shift) + (c.j & ((1 << p.block_shift) - 1));
   const size_t off = page * p.page_bytes;
@@ -215,13 +217,6 @@ __device__ __forceinline__ void fetch_page(const DecodeParams& p, const PageCurs
                 full_bar, pol);
   bulk_g2s_hint(stage_smem + p.page_bytes, reinterpret_cast<const unsigned char*>(p.v_cache) + off,
                 bytes, full_bar, pol);
-  if (p.scale_bytes) {  // the whole page's scales (rows past ntok are never read)
-    const size_t soff = page * p.scale_bytes;
-    bulk_g2s(stage_smem + 2 * p.page_bytes,
-             reinterpret_cast<const unsigned char*>(p.k_scale) + soff, p.scale_bytes, full_bar);
-    bulk_g2s(stage_smem + 2 * p.page_bytes + p.scale_bytes,
-             reinterpret_cast<const unsigned char*>(p.v_scale) + soff, p.scale_bytes, full_bar);
-  }
 }
 
 template <int N>
@@ -580,7 +575,7 @@ __global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
       if (found_s >= 0) {
         PageCursor fc{found_s, found_j, decode_pages(p, found_s, false)};
         for (int i = 0; i < NST && i < n_pages; ++i) {
-          fetch_page<FUSE>(p, fc, smem_addr(stages + (size_t)i * p.stage_bytes),
+          fetch_page<FUSE, F8>(p, fc, smem_addr(stages + (size_t)i * p.stage_bytes),
                      smem_addr(&S.full[i]), &S.fused_slot[i]);
           S.last_issued[i] = i;
           fc.next(p);
@@ -693,7 +688,7 @@ __global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
         float sc4[4];
         if constexpr (F8)
           qk_scores_mma<D, NKV, ROW>(
-              stage + g * D, reinterpret_cast<const float*>(stage + 2 * p.page_bytes + g * 4),
+              stage + g * D, reinterpret_cast<const float*>(stage + kBlock * ROW + g * 4),
               ntok, qa, sc4, lane);
         else
           qk_scores_mma_bf16<D, ROW>(stage + g * D * ES, ntok, qa, p.scale_log2, sc4, lane);
@@ -709,7 +704,7 @@ __global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
         {
           const unsigned char* vb = stage + p.page_bytes + (g * D + r * (D / 8)) * ES;
           const float* vsc =
-              reinterpret_cast<const float*>(stage + 2 * p.page_bytes + p.scale_bytes + g * 4);
+              reinterpret_cast<const float*>(stage + p.page_bytes + kBlock * ROW + g * 4);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int tok = 2 * t + (k & 1) + 8 * (k >> 1);
@@ -805,7 +800,7 @@ __global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
           if (atomicAdd(&S.released[st], 1) == NKV - 1) {
             S.released[st] = 0;
             if (i + NST < n_pages && !*abort_flag) {
-              fetch_page<FUSE>(p, fc, smem_addr(stage), smem_addr(&S.full[st]),
+              fetch_page<FUSE, F8>(p, fc, smem_addr(stage), smem_addr(&S.full[st]),
                                &S.fused_slot[st]);
               S.last_issued[st] = i + NST;
             }
@@ -1014,7 +1009,7 @@ __global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
         if (atomicAdd(&S.released[st], 1) == NW - 1) {
           S.released[st] = 0;
           if (i + NST < n_pages && !*abort_flag) {
-            fetch_page<FUSE>(p, fc, smem_addr(stage), smem_addr(&S.full[st]),
+            fetch_page<FUSE, F8>(p, fc, smem_addr(stage), smem_addr(&S.full[st]),
                              &S.fused_slot[st]);
             S.last_issued[st] = i + NST;
           }
@@ -1092,7 +1087,7 @@ __global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
         if (atomicAdd(&S.released[st], 1) == NW - 1) {
           S.released[st] = 0;
           if (i + NST < n_pages && !*abort_flag) {
-            fetch_page<FUSE>(p, fc, smem_addr(stage), smem_addr(&S.full[st]),
+            fetch_page<FUSE, F8>(p, fc, smem_addr(stage), smem_addr(&S.full[st]),
                              &S.fused_slot[st]);
             S.last_issued[st] = i + NST;
           }
@@ -1306,8 +1301,6 @@ cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ct
   p.q = a.q;
   p.k_cache = a.k_cache;
   p.v_cache = a.v_cache;
-  p.k_scale = a.k_scale;
-  p.v_scale = a.v_scale;
   p.k_new = a.fuse_k_new;
   p.v_new = a.fuse_v_new;
   p.slot_mapping = a.fuse_slot_mapping;
@@ -1330,9 +1323,8 @@ cudaError_t launch_decode_t(const AttnArgs& a, const DecodeWorkspace& ws, int ct
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.ctas = ctas;
   p.row_bytes = (uint32_t)NKV * D * (F8 ? 1 : 2);
-  p.page_bytes = kBlock * p.row_bytes;
-  p.scale_bytes = F8 ? (uint32_t)(kBlock * NKV * sizeof(float)) : 0u;
-  p.stage_bytes = 2 * p.page_bytes + 2 * p.scale_bytes;
+  p.page_bytes = F8 ? (uint32_t)fp8_page_bytes(NKV, D) : kBlock * p.row_bytes;
+  p.stage_bytes = 2 * p.page_bytes;
   // the 8-bit kernel also holds the per-kv-head merge buffers, and takes
   // the shared memory up to the opt-in limit to keep six stages
   const size_t fixed =

@@ -26,13 +26,21 @@ enum : unsigned {
   DEVERR_TIMEOUT = 2u,  // a bounded wait gave up
 };
 
+// 8-bit cache page: the codes of 16 token rows ([16, n_kv, head_dim] bytes),
+// then their fp32 scales ([16, n_kv]); a block holds block_size / 16 pages.
+constexpr int kFp8PageTokens = 16;
+__host__ __device__ constexpr int64_t fp8_page_bytes(int n_kv, int head_dim) {
+  return (int64_t)kFp8PageTokens * n_kv * (head_dim + 4);
+}
+__host__ __device__ constexpr int64_t fp8_scales_offset(int n_kv, int head_dim) {
+  return (int64_t)kFp8PageTokens * n_kv * head_dim;
+}
+
 // Geometry and pointers of one paged-attention call, already validated.
 struct AttnArgs {
   const uint16_t* q;
-  const void* k_cache;     // bf16 values, or E4M3 codes when fp8
+  const void* k_cache;     // bf16 values, or (fp8) pages of E4M3 codes and row scales
   const void* v_cache;
-  const float* k_scale;    // fp8: one scale per (slot, kv head); else null
-  const float* v_scale;
   bool fp8;
   // Fused scatter (decode-only steps over the bf16 cache): the decode kernel
   // takes each decode request's new row from these and stores it to its
@@ -114,10 +122,9 @@ cudaError_t launch_reshape_and_cache(const uint16_t* k, const uint16_t* v, int32
 
 cudaError_t launch_reshape_and_cache_fp8(const uint16_t* k, const uint16_t* v,
                                          int32_t num_tokens, uint8_t* k_cache, uint8_t* v_cache,
-                                         float* k_scale, float* v_scale, int64_t num_slots,
-                                         int32_t num_kv_heads, int32_t head_dim,
-                                         const int32_t* slot_mapping, unsigned* err,
-                                         cudaStream_t stream);
+                                         int64_t num_slots, int32_t num_kv_heads,
+                                         int32_t head_dim, const int32_t* slot_mapping,
+                                         unsigned* err, cudaStream_t stream);
 cudaError_t launch_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, int32_t num_blocks,
                                int64_t block_elems, const int32_t* pairs, int32_t num_pairs,
                                unsigned* err, cudaStream_t stream);

@@ -98,12 +98,11 @@ struct PrefillParams {
   const int32_t* slot_mapping;
   uint16_t* k_cache;
   uint16_t* v_cache;
-  // 8-bit cache: codes [num_blocks * 16, n_kv, D], scales [num_blocks * 16,
-  // n_kv]; the query tile is scaled by q_mul (scale * log2 e) into f16
+  // 8-bit cache: 16-token pages of codes [16, n_kv, D], then their scales
+  // [16, n_kv] (fp32); the query tile is scaled by q_mul (scale * log2 e)
+  // into f16
   const uint8_t* k_codes;
   const uint8_t* v_codes;
-  const float* k_scale;
-  const float* v_scale;
   float q_mul;
   const int32_t* block_tables;
   const int32_t* seq_lens;
@@ -632,8 +631,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // overlaps the wait); lane j-th chunk: 16 codes of one row
             constexpr int CPR = D / 16;                  // chunks per row
             constexpr int NJ = 3 * kBlock * CPR / 32;    // chunks per lane
-            const uint8_t* codes = k_warp ? p.k_codes : p.v_codes;
-            const float* scales = k_warp ? p.k_scale : p.v_scale;
+            const uint8_t* pages = k_warp ? p.k_codes : p.v_codes;
+            const int64_t page_bytes = fp8_page_bytes(p.n_kv, D);
+            const int64_t scales_at = fp8_scales_offset(p.n_kv, D);
             uint4 w8[NJ];
             float sc[NJ];
 #pragma unroll
@@ -643,10 +643,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               w8[j] = make_uint4(0u, 0u, 0u, 0u);
               sc[j] = 0.f;
               if (phys[pi] >= 0) {
-                const int64_t row =
-                    ((int64_t)phys[pi] * kBlock + rem / CPR) * p.n_kv + U.g;  // (slot, head)
-                w8[j] = __ldg(reinterpret_cast<const uint4*>(codes + row * D) + rem % CPR);
-                sc[j] = __ldg(scales + row);
+                const uint8_t* page = pages + (int64_t)phys[pi] * page_bytes;
+                const int row = (rem / CPR) * p.n_kv + U.g;  // (token row, head) in the page
+                w8[j] = __ldg(reinterpret_cast<const uint4*>(page + (int64_t)row * D) + rem % CPR);
+                sc[j] = __ldg(reinterpret_cast<const float*>(page + scales_at) + row);
               }
             }
             // the stage's last reader released it (as below)
@@ -1229,8 +1229,6 @@ cudaError_t launch_prefill_t(const AttnArgs& a, const PrefillPlan& plan, void* w
   p.v_cache = F8 ? nullptr : static_cast<uint16_t*>(const_cast<void*>(a.v_cache));
   p.k_codes = F8 ? static_cast<const uint8_t*>(a.k_cache) : nullptr;
   p.v_codes = F8 ? static_cast<const uint8_t*>(a.v_cache) : nullptr;
-  p.k_scale = F8 ? a.k_scale : nullptr;
-  p.v_scale = F8 ? a.v_scale : nullptr;
   p.block_tables = a.block_tables;
   p.seq_lens = a.seq_lens;
   p.qsl = a.query_start_loc;

@@ -94,13 +94,14 @@ def _load() -> ctypes.CDLL:
     L.pa_selftest_wait_timeout.restype = ctypes.c_int
     L.pa_check_device_errors.argtypes = [vp]
     L.pa_check_device_errors.restype = ctypes.c_int
-    L.pa_reshape_and_cache_fp8.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp,
-                                           vp]
+    L.pa_fp8_page_bytes.argtypes = [i32, i32]
+    L.pa_fp8_page_bytes.restype = sz
+    L.pa_reshape_and_cache_fp8.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, i32, vp, vp]
     L.pa_reshape_and_cache_fp8.restype = ctypes.c_int
-    L.pa_paged_attention_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, i32,
+    L.pa_paged_attention_fp8.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, i32,
                                          vp, vp, i32, i32, i32, i32, f32, vp, vp, sz, vp]
     L.pa_paged_attention_fp8.restype = ctypes.c_int
-    L.pa_copy_blocks_fp8.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, i32, vp]
+    L.pa_copy_blocks_fp8.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, vp]
     L.pa_copy_blocks_fp8.restype = ctypes.c_int
     L.pa_step_graph_create.argtypes = [ctypes.POINTER(StepBuffers), ctypes.POINTER(vp)]
     L.pa_step_graph_create.restype = ctypes.c_int
@@ -412,87 +413,122 @@ def swap_in(k_cache: torch.Tensor, v_cache: torch.Tensor, block_ids: torch.Tenso
 
 
 # ---------------------------------------------------------------------------
-# 8-bit (FP8 E4M3) cache: uint8 codes [num_blocks, block_size, n_kv, d] and
-# fp32 scales [num_blocks, block_size, n_kv], one per cached row.
+# 8-bit (FP8 E4M3) cache: uint8 [num_blocks, block_size // 16, page bytes],
+# each 16-token page its codes [16, n_kv, d], then their fp32 scales
+# [16, n_kv] (one per cached row).
 # ---------------------------------------------------------------------------
+
+FP8_PAGE_TOKENS = 16
+
+
+def fp8_page_bytes(num_kv_heads: int, head_dim: int) -> int:
+    """Bytes of one 16-token page of the 8-bit cache (codes, then scales)."""
+    return FP8_PAGE_TOKENS * num_kv_heads * (head_dim + 4)
+
 
 def empty_fp8_cache(num_blocks: int, block_size: int, num_kv_heads: int, head_dim: int,
                     device=None):
-    """(k codes, v codes, k scales, v scales), zero-filled, on the device."""
+    """(k cache, v cache): uint8 [num_blocks, block_size // 16, page bytes],
+    zero-filled, on the device."""
+    if block_size % FP8_PAGE_TOKENS:
+        raise ValueError(f"block_size {block_size} is not a multiple of {FP8_PAGE_TOKENS}")
     dev = device or "cuda"
-    codes = (num_blocks, block_size, num_kv_heads, head_dim)
-    return (torch.zeros(codes, dtype=torch.uint8, device=dev),
-            torch.zeros(codes, dtype=torch.uint8, device=dev),
-            torch.zeros(codes[:3], dtype=torch.float32, device=dev),
-            torch.zeros(codes[:3], dtype=torch.float32, device=dev))
+    shape = (num_blocks, block_size // FP8_PAGE_TOKENS, fp8_page_bytes(num_kv_heads, head_dim))
+    return (torch.zeros(shape, dtype=torch.uint8, device=dev),
+            torch.zeros(shape, dtype=torch.uint8, device=dev))
 
 
-def _need_fp8(k_cache, v_cache, k_scale, v_scale):
-    _need(k_cache, "k_cache", torch.uint8, 4)
-    _need(v_cache, "v_cache", torch.uint8, 4)
-    _need(k_scale, "k_scale", torch.float32, 3)
-    _need(v_scale, "v_scale", torch.float32, 3)
-    if v_cache.shape != k_cache.shape or k_scale.shape != k_cache.shape[:3] or \
-            v_scale.shape != k_scale.shape:
-        raise ValueError("codes must be [nb, bs, n_kv, d] and scales [nb, bs, n_kv], alike")
+def fp8_cache_views(cache: torch.Tensor, num_kv_heads: int, head_dim: int):
+    """(codes, scales) views of an 8-bit cache: codes uint8 [num_blocks,
+    block_size // 16, 16, n_kv, d] and scales fp32 [num_blocks,
+    block_size // 16, 16, n_kv]; token row r of page p of block b is slot
+    b * block_size + 16 p + r."""
+    nb, npg, pb = cache.shape
+    if pb != fp8_page_bytes(num_kv_heads, head_dim):
+        raise ValueError(f"page of {pb} bytes is not one of n_kv {num_kv_heads}, d {head_dim}")
+    cb = FP8_PAGE_TOKENS * num_kv_heads * head_dim
+    codes = cache[:, :, :cb].view(nb, npg, FP8_PAGE_TOKENS, num_kv_heads, head_dim)
+    scales = cache[:, :, cb:].view(torch.float32).view(nb, npg, FP8_PAGE_TOKENS, num_kv_heads)
+    return codes, scales
+
+
+def _fp8_geometry(k_cache, v_cache, num_kv_heads: int, head_dim: int):
+    """(num_blocks, block_size) of a pair of 8-bit caches."""
+    _need(k_cache, "k_cache", torch.uint8, 3)
+    _need(v_cache, "v_cache", torch.uint8, 3)
+    if v_cache.shape != k_cache.shape or \
+            k_cache.shape[2] != fp8_page_bytes(num_kv_heads, head_dim):
+        raise ValueError("caches must be alike, uint8 [num_blocks, block_size // 16, "
+                         f"{fp8_page_bytes(num_kv_heads, head_dim)}] for n_kv {num_kv_heads}, "
+                         f"d {head_dim}")
+    return k_cache.shape[0], k_cache.shape[1] * FP8_PAGE_TOKENS
 
 
 def reshape_and_cache_fp8(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
-                          v_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
-                          slot_mapping: torch.Tensor, stream=None) -> None:
+                          v_cache: torch.Tensor, slot_mapping: torch.Tensor, stream=None) -> None:
     """Quantise each new (token, kv head) row of k / v into its slot."""
     L = _load()
     _need(k, "k", torch.bfloat16, 3)
     _need(v, "v", torch.bfloat16, 3)
-    _need_fp8(k_cache, v_cache, k_scale, v_scale)
     _need(slot_mapping, "slot_mapping", torch.int32, 1)
-    nb, bs, nkv, d = k_cache.shape
+    nkv, d = k.shape[1], k.shape[2]
+    nb, bs = _fp8_geometry(k_cache, v_cache, nkv, d)
     _new_rows_shapes(k, v, nkv, d, slot_mapping)
     _check(L.pa_reshape_and_cache_fp8(k.data_ptr(), v.data_ptr(), k.shape[0], k_cache.data_ptr(),
-                                      v_cache.data_ptr(), k_scale.data_ptr(), v_scale.data_ptr(),
-                                      nb, bs, nkv, d, slot_mapping.data_ptr(), _stream(stream)))
+                                      v_cache.data_ptr(), nb, bs, nkv, d,
+                                      slot_mapping.data_ptr(), _stream(stream)))
 
 
 def paged_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
-                        k_scale: torch.Tensor, v_scale: torch.Tensor, block_tables: torch.Tensor,
-                        seq_lens: torch.Tensor, query_start_loc: torch.Tensor, scale: float, *,
-                        max_q_len: int, max_seq_len: int, out: Optional[torch.Tensor] = None,
+                        block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                        query_start_loc: torch.Tensor, scale: float, *, max_q_len: int,
+                        max_seq_len: int, out: Optional[torch.Tensor] = None,
                         workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """paged_attention over the 8-bit cache (decode and prefill rows)."""
+    """paged_attention over the 8-bit cache (decode and prefill rows); n_kv
+    follows from the page size and q's head_dim."""
     L = _load()
     _need(q, "q", torch.bfloat16, 3)
-    _need_fp8(k_cache, v_cache, k_scale, v_scale)
+    T, nq, d = q.shape
+    _need(k_cache, "k_cache", torch.uint8, 3)
+    nkv = k_cache.shape[2] // fp8_page_bytes(1, d)
+    nb, bs = _fp8_geometry(k_cache, v_cache, nkv, d)
+    if nkv <= 0 or nq % nkv != 0:
+        raise ValueError(f"num_q_heads {nq} must be a multiple of num_kv_heads {nkv}")
     for name, t in (("block_tables", block_tables), ("seq_lens", seq_lens),
                     ("query_start_loc", query_start_loc)):
         _need(t, name, torch.int32)
-    T, nq, d, nb, bs, nkv, S = _attention_shapes(q, k_cache, v_cache, block_tables, seq_lens,
-                                                 query_start_loc, out)
+    if block_tables.dim() != 2 or seq_lens.dim() != 1 or query_start_loc.dim() != 1:
+        raise ValueError("block_tables must be 2-D, seq_lens and query_start_loc 1-D")
+    S = seq_lens.shape[0]
+    if block_tables.shape[0] != S or query_start_loc.shape[0] != S + 1:
+        raise ValueError("block_tables [S, max_blocks], seq_lens [S], query_start_loc [S + 1]")
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", torch.bfloat16, 3)
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
     if workspace is None:
         workspace = alloc_workspace(S, T, nq, nkv, d, max_q_len, max_seq_len, q.device)
     _need_workspace(workspace)
     _check(L.pa_paged_attention_fp8(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                                    k_scale.data_ptr(), v_scale.data_ptr(), nb, bs, nq, nkv, d,
-                                    block_tables.data_ptr(), block_tables.shape[1],
-                                    seq_lens.data_ptr(), query_start_loc.data_ptr(), S, T,
-                                    int(max_q_len), int(max_seq_len), float(scale),
-                                    out.data_ptr(), workspace.data_ptr(), workspace.numel(),
-                                    _stream(stream)))
+                                    nb, bs, nq, nkv, d, block_tables.data_ptr(),
+                                    block_tables.shape[1], seq_lens.data_ptr(),
+                                    query_start_loc.data_ptr(), S, T, int(max_q_len),
+                                    int(max_seq_len), float(scale), out.data_ptr(),
+                                    workspace.data_ptr(), workspace.numel(), _stream(stream)))
     return out
 
 
-def copy_blocks_fp8(k_cache, v_cache, k_scale, v_scale, src_dst_pairs: torch.Tensor,
-                    stream=None) -> None:
-    """Copy-on-write on the 8-bit cache: codes and scales of block dst <- src."""
+def copy_blocks_fp8(k_cache, v_cache, src_dst_pairs: torch.Tensor, *, num_kv_heads: int,
+                    head_dim: int, stream=None) -> None:
+    """Copy-on-write on the 8-bit cache: the pages (codes and scales) of block
+    dst <- block src."""
     L = _load()
-    _need_fp8(k_cache, v_cache, k_scale, v_scale)
+    nb, bs = _fp8_geometry(k_cache, v_cache, num_kv_heads, head_dim)
     _need_pairs(src_dst_pairs)
-    nb, bs, nkv, d = k_cache.shape
-    _check(L.pa_copy_blocks_fp8(k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(),
-                                v_scale.data_ptr(), nb, bs, nkv, d, src_dst_pairs.data_ptr(),
-                                src_dst_pairs.shape[0], _stream(stream)))
+    _check(L.pa_copy_blocks_fp8(k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, num_kv_heads,
+                                head_dim, src_dst_pairs.data_ptr(), src_dst_pairs.shape[0],
+                                _stream(stream)))
 
 
 def selftest_wait_timeout(limit_ns: int = 5_000_000, stream=None) -> None:

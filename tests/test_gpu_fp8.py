@@ -30,6 +30,13 @@ def _context_slots(b):
     return slots, rows_k, rows_v
 
 
+def fp8_slot_arrays(cache, nkv, d):
+    """(codes [slots, n_kv, d], scales [slots, n_kv]) of a device 8-bit cache,
+    in slot order, on the host."""
+    codes, scales = ops.fp8_cache_views(cache, nkv, d)
+    return (codes.cpu().numpy().reshape(-1, nkv, d), scales.cpu().numpy().reshape(-1, nkv))
+
+
 def fp8_step(b, poison=False):
     """Quantise the batch's context and its new tokens into an 8-bit cache on
     both sides (GPU scatter and oracle scatter, compared bit for bit), then
@@ -38,12 +45,12 @@ def fp8_step(b, poison=False):
     may see.  Returns (gpu out, oracle out)."""
     nb, bs, nkv, d = b.k_cache.shape
     slots, rk, rv = _context_slots(b)
-    dk8, dv8, dks, dvs = ops.empty_fp8_cache(nb, bs, nkv, d)
+    dk8, dv8 = ops.empty_fp8_cache(nb, bs, nkv, d)
     if poison:
         for t in (dk8, dv8):
-            t.fill_(0x7F)  # E4M3 NaN
-        for t in (dks, dvs):
-            t.fill_(float("nan"))
+            codes, scales = ops.fp8_cache_views(t, nkv, d)
+            codes.fill_(0x7F)  # E4M3 NaN
+            scales.fill_(float("nan"))
     ok8, ov8, oks, ovs = oracle.fp8_cache(nb, bs, nkv, d, fill_code=0)
     oks[:] = 0
     ovs[:] = 0
@@ -51,22 +58,22 @@ def fp8_step(b, poison=False):
         if len(sl) == 0:
             continue
         ops.reshape_and_cache_fp8(W.bf16_tensor(ks_, "cuda"), W.bf16_tensor(vs_, "cuda"), dk8,
-                                  dv8, dks, dvs, W.int32_tensor(sl, "cuda"))
+                                  dv8, W.int32_tensor(sl, "cuda"))
         oracle.reshape_and_cache_fp8(ks_, vs_, ok8, ov8, oks, ovs, sl)
     ops.check_device_errors()
     written = np.zeros(nb * bs, bool)
     written[slots] = True
     written[b.slot_mapping[b.slot_mapping >= 0]] = True
-    for dev_t, ref, what in ((dk8, ok8, "K codes"), (dv8, ov8, "V codes"),
-                             (dks, oks, "K scales"), (dvs, ovs, "V scales")):
-        got = dev_t.cpu().numpy()
+    dks_, dvs_ = fp8_slot_arrays(dk8, nkv, d), fp8_slot_arrays(dv8, nkv, d)
+    for got, ref, what in ((dks_[0], ok8, "K codes"), (dvs_[0], ov8, "V codes"),
+                           (dks_[1], oks, "K scales"), (dvs_[1], ovs, "V scales")):
         if got.dtype == np.float32:
             got, ref = got.view(np.uint32), ref.view(np.uint32)
         got = got.reshape(nb * bs, -1)[written]
         assert np.array_equal(got, ref.reshape(nb * bs, -1)[written]), f"{what} differ"
     out = torch.full((b.num_tokens, b.num_q_heads, d), float("nan"), dtype=torch.bfloat16,
                      device="cuda")
-    ops.paged_attention_fp8(W.bf16_tensor(b.q, "cuda"), dk8, dv8, dks, dvs,
+    ops.paged_attention_fp8(W.bf16_tensor(b.q, "cuda"), dk8, dv8,
                             W.int32_tensor(b.block_tables, "cuda"),
                             W.int32_tensor(b.seq_lens, "cuda"),
                             W.int32_tensor(b.query_start_loc, "cuda"), b.scale,
@@ -127,31 +134,66 @@ def test_fp8_quantises_zero_and_large_rows():
     big = (W.f32_from_bf16(k[7]) * np.float32(3e37)).astype(np.float32)
     k[7] = W.bf16_from_f32(big)
     slots = rng.permutation(64)[:24].astype(np.int32)
-    dk8, dv8, dks, dvs = ops.empty_fp8_cache(4, 16, 8, 128)
+    dk8, dv8 = ops.empty_fp8_cache(4, 16, 8, 128)
     ok8, ov8, oks, ovs = oracle.fp8_cache(4, 16, 8, 128, fill_code=0)
     oks[:] = 0
     ovs[:] = 0
-    ops.reshape_and_cache_fp8(W.bf16_tensor(k, "cuda"), W.bf16_tensor(v, "cuda"), dk8, dv8, dks,
-                              dvs, W.int32_tensor(slots, "cuda"))
+    ops.reshape_and_cache_fp8(W.bf16_tensor(k, "cuda"), W.bf16_tensor(v, "cuda"), dk8, dv8,
+                              W.int32_tensor(slots, "cuda"))
     ops.check_device_errors()
     oracle.reshape_and_cache_fp8(k, v, ok8, ov8, oks, ovs, slots)
-    assert np.array_equal(dk8.cpu().numpy(), ok8) and np.array_equal(dv8.cpu().numpy(), ov8)
-    assert np.array_equal(dks.cpu().numpy().view(np.uint32), oks.view(np.uint32))
-    assert np.array_equal(dvs.cpu().numpy().view(np.uint32), ovs.view(np.uint32))
+    (kc, ks), (vc, vs) = fp8_slot_arrays(dk8, 8, 128), fp8_slot_arrays(dv8, 8, 128)
+    assert np.array_equal(kc, ok8.reshape(64, 8, 128))
+    assert np.array_equal(vc, ov8.reshape(64, 8, 128))
+    assert np.array_equal(ks.view(np.uint32), oks.reshape(64, 8).view(np.uint32))
+    assert np.array_equal(vs.view(np.uint32), ovs.reshape(64, 8).view(np.uint32))
+
+
+def test_fp8_page_format():
+    """The page format: a 16-token page holds its codes, then its scales, and
+    the slot of row r of page p of block b is b * block_size + 16 p + r."""
+    nkv, d, bs = 2, 64, 32
+    assert ops.fp8_page_bytes(nkv, d) == 16 * nkv * (d + 4)
+    assert int(ops._load().pa_fp8_page_bytes(nkv, d)) == ops.fp8_page_bytes(nkv, d)
+    rng = np.random.default_rng(5)
+    k = W.randn_bf16(rng, (3, nkv, d))
+    slots = np.array([0, 17, 2 * bs + 31], np.int32)  # block 0 page 0 row 0; page 1 row 1; ...
+    dk8, dv8 = ops.empty_fp8_cache(3, bs, nkv, d)
+    ops.reshape_and_cache_fp8(W.bf16_tensor(k, "cuda"), W.bf16_tensor(k, "cuda"), dk8, dv8,
+                              W.int32_tensor(slots, "cuda"))
+    ops.check_device_errors()
+    ok8, _, oks, _ = oracle.fp8_cache(3, bs, nkv, d, fill_code=0)
+    oks[:] = 0
+    oracle.reshape_and_cache_fp8(k, k, ok8, ok8.copy(), oks, oks.copy(), slots)
+    raw = dk8.cpu().numpy()  # [blocks, pages, bytes]
+    cb = 16 * nkv * d
+    for t, slot in enumerate(slots):
+        blk, p, r = slot // bs, (slot % bs) // 16, slot % 16
+        page = raw[blk, p]
+        codes = page[(r * nkv) * d:(r * nkv + nkv) * d].reshape(nkv, d)
+        scales = page[cb + r * nkv * 4:cb + (r + 1) * nkv * 4].view(np.float32)
+        assert np.array_equal(codes, ok8.reshape(-1, nkv, d)[slot])
+        assert np.array_equal(scales.view(np.uint32), oks.reshape(-1, nkv)[slot].view(np.uint32))
+    # nothing else was written
+    mask = np.ones(raw.shape, bool)
+    for slot in slots:
+        blk, p, r = slot // bs, (slot % bs) // 16, slot % 16
+        mask[blk, p, (r * nkv) * d:(r * nkv + nkv) * d] = False
+        mask[blk, p, cb + r * nkv * 4:cb + (r + 1) * nkv * 4] = False
+    assert not raw[mask].any()
 
 
 @pytest.mark.parametrize("bs", [16, 32])
 def test_fp8_copy_blocks_moves_codes_and_scales(bs):
     rng = np.random.default_rng(8)
-    dk8 = torch.from_numpy(rng.integers(0, 256, (10, bs, 8, 128), dtype=np.uint8)).cuda()
-    dv8 = torch.from_numpy(rng.integers(0, 256, (10, bs, 8, 128), dtype=np.uint8)).cuda()
-    dks = torch.from_numpy(rng.standard_normal((10, bs, 8)).astype(np.float32)).cuda()
-    dvs = torch.from_numpy(rng.standard_normal((10, bs, 8)).astype(np.float32)).cuda()
-    before = [t.cpu().numpy().copy() for t in (dk8, dv8, dks, dvs)]
+    dk8, dv8 = ops.empty_fp8_cache(10, bs, 8, 128)
+    for t in (dk8, dv8):
+        t.copy_(torch.from_numpy(rng.integers(0, 256, tuple(t.shape), dtype=np.uint8)))
+    before = [t.cpu().numpy().copy() for t in (dk8, dv8)]
     pairs = np.array([[1, 4], [-1, -1], [6, 2]], np.int32)
-    ops.copy_blocks_fp8(dk8, dv8, dks, dvs, W.int32_tensor(pairs, "cuda"))
+    ops.copy_blocks_fp8(dk8, dv8, W.int32_tensor(pairs, "cuda"), num_kv_heads=8, head_dim=128)
     ops.check_device_errors()
-    for dev_t, host in zip((dk8, dv8, dks, dvs), before):
+    for dev_t, host in zip((dk8, dv8), before):
         host[4] = host[1]
         host[2] = host[6]
         assert np.array_equal(dev_t.cpu().numpy(), host)
