@@ -1191,6 +1191,10 @@ __global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
 // dependent of the decode kernel: it may start while the decode grid drains
 // and waits for it before reading partials.
 constexpr int kMergeWarps = 4;
+// Up to this many sequences the merge finds a request's pieces from the
+// call's inputs before waiting for the decode grid (each warp reads them all,
+// eight per lane); past it, it reads the record the decode kernel wrote.
+constexpr int kMergeScanMax = 256;
 
 template <int D, bool SPLIT>
 __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const DecodeParams p) {
@@ -1203,14 +1207,51 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
   // the request's shape and output row come from the call's inputs, which
   // are complete before the decode grid starts: read them before waiting for
   // it (with SPLIT every early return below is the same for the whole CTA)
-  if (decode_pages(p, s, false) == 0) return;  // not a (valid) decode request
+  const int np_s = decode_pages(p, s, false);
+  if (np_s == 0) return;  // not a (valid) decode request
   const int a_row = __ldg(p.qsl + s);
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int4 rec = p.seq_rec[s];
   const int C = p.ctas;
-  const int c_first = rec.x, c_last = rec.y, first_slot = rec.z;
-  const int64_t F = rec.w;
-  if (c_first == c_last) return;  // written directly by the decode kernel
+  int c_first, c_last, first_slot;
+  int64_t F;
+  if (p.num_seqs <= kMergeScanMax) {
+    // where the request's pieces are follows from the same inputs: its pages
+    // are flat pages fa .. fa + np_s - 1 of the F pages the decode grid cuts
+    // into slices, so they are known before the wait, and a request whole in
+    // one slice leaves without waiting at all
+    long long tot = 0, before = 0;
+#pragma unroll
+    for (int i = 0; i < kMergeScanMax / 32; ++i) {  // all loads in flight at once
+      const int s2 = lane + 32 * i;
+      const int n = s2 < p.num_seqs ? decode_pages(p, s2, false) : 0;
+      tot += n;
+      if (s2 < s) before += n;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      before += __shfl_xor_sync(0xffffffffu, before, o);
+    }
+    F = tot;
+    const int64_t fa = before, fb = before + np_s - 1;
+    // the CTA whose slice holds flat page f: the last c with slice_begin(c) <= f
+    auto owner = [&](int64_t f) {
+      const int64_t c = ((f + 1) * C + F - 1) / F - 1;
+      return (int)(c < C - 1 ? c : C - 1);
+    };
+    c_first = owner(fa);
+    c_last = owner(fb);
+    // the first CTA wrote its piece to its first slot when its slice starts
+    // with this request, else to its second (as the decode kernel chooses)
+    first_slot = 2 * c_first + (slice_begin(c_first, F, C) == fa ? 0 : 1);
+    if (c_first == c_last) return;  // written directly by the decode kernel
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+  } else {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int4 rec = p.seq_rec[s];
+    c_first = rec.x, c_last = rec.y, first_slot = rec.z;
+    F = rec.w;
+    if (c_first == c_last) return;  // written directly by the decode kernel
+  }
   if (c_first < 0 || c_last >= C || c_first > c_last || first_slot < 0 || first_slot >= 2 * C ||
       F <= 0) {
     if (threadIdx.x == 0) flag_error(p.err, DEVERR_BOUNDS);
