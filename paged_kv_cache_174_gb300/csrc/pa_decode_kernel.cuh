@@ -572,15 +572,16 @@ __global__ void __launch_bounds__(decode_threads<NKV, F8, MW>(), 1)
           mbar_init(smem_addr(&S.p_empty[g][b]), 1);
         }
       fence_mbar_init();
-      if (found_s >= 0) {
-        PageCursor fc{found_s, found_j, decode_pages(p, found_s, false)};
-        for (int i = 0; i < NST && i < n_pages; ++i) {
-          fetch_page<FUSE, F8>(p, fc, smem_addr(stages + (size_t)i * p.stage_bytes),
-                     smem_addr(&S.full[i]), &S.fused_slot[i]);
-          S.last_issued[i] = i;
-          fc.next(p);
-        }
-      }
+    }
+    __syncwarp();
+    // the slice's first NST pages, one lane each: each copy waits for two
+    // dependent table loads, which then overlap instead of queueing
+    if (found_s >= 0 && lane < NST && lane < n_pages) {
+      PageCursor fc{found_s, found_j, decode_pages(p, found_s, false)};
+      for (int i = 0; i < lane; ++i) fc.next(p);
+      fetch_page<FUSE, F8>(p, fc, smem_addr(stages + (size_t)lane * p.stage_bytes),
+                           smem_addr(&S.full[lane]), &S.fused_slot[lane]);
+      S.last_issued[lane] = lane;
     }
   }
   __syncthreads();
