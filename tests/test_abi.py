@@ -117,3 +117,57 @@ def test_step_graph_argument_checks_without_gpu():
                                     None, None, 4, 4, 48, None, ctypes.c_float(0.125), None,
                                     None, 0, None)) == "PA_ERR_INVALID_ARG"
     assert _status(L.pa_selftest_wait_timeout(2_000_000_000, None)) == "PA_ERR_INVALID_ARG"
+
+
+def test_fp8_page_format_host_checks(lib):
+    """The 8-bit cache's page size, and the host-side checks of its calls
+    (block_size a multiple of 16, head_dim 64 or 128), without a GPU."""
+    L = lib
+    assert L.pa_fp8_page_bytes(8, 128) == 16 * 8 * (128 + 4)
+    assert L.pa_fp8_page_bytes(2, 64) == 16 * 2 * 68
+    assert L.pa_fp8_page_bytes(0, 64) == 0 and L.pa_fp8_page_bytes(2, -1) == 0
+    # a page is a whole number of 16-byte vectors for every shape
+    for nkv in (1, 2, 3, 8):
+        for d in (64, 128):
+            assert L.pa_fp8_page_bytes(nkv, d) % 16 == 0
+    assert _status(L.pa_reshape_and_cache_fp8(None, None, 1, None, None, 4, 8, 2, 64, None,
+                                              None)) == "PA_ERR_UNSUPPORTED"  # block_size 8
+    assert _status(L.pa_reshape_and_cache_fp8(None, None, 1, None, None, 4, 16, 2, 96, None,
+                                              None)) == "PA_ERR_UNSUPPORTED"  # head_dim 96
+    assert L.pa_reshape_and_cache_fp8(None, None, 0, None, None, 4, 16, 2, 64, None, None) == 0
+    assert _status(L.pa_reshape_and_cache_fp8(None, None, 1, None, None, 4, 16, 2, 64, None,
+                                              None)) == "PA_ERR_INVALID_ARG"  # null pointers
+    assert _status(L.pa_copy_blocks_fp8(None, None, 4, 24, 2, 64, None, 1, None)) \
+        == "PA_ERR_UNSUPPORTED"  # block_size 24
+    assert L.pa_copy_blocks_fp8(None, None, 4, 48, 2, 64, None, 0, None) == 0
+    assert _status(L.pa_copy_blocks_fp8(None, None, 4, 48, 2, 64, None, 1, None)) \
+        == "PA_ERR_INVALID_ARG"
+
+
+def test_fp8_cache_views_follow_the_page_format():
+    """ops.fp8_cache_views reads a cache as the header lays it out: token row
+    r of page p of block b is slot b * block_size + 16 p + r; its codes sit at
+    (r * n_kv + h) * d in the page and its scales after all 16 rows' codes."""
+    import numpy as np
+    import torch
+    nb, bs, nkv, d = 3, 32, 2, 64
+    pb = ops.fp8_page_bytes(nkv, d)
+    assert pb == 16 * nkv * (d + 4)
+    raw = np.zeros((nb, bs // 16, pb), np.uint8)
+    cb = 16 * nkv * d
+    rng = np.random.default_rng(3)
+    want_codes = rng.integers(0, 256, (nb * bs, nkv, d), dtype=np.uint8)
+    want_scales = rng.standard_normal((nb * bs, nkv)).astype(np.float32)
+    for slot in range(nb * bs):
+        b, p, r = slot // bs, (slot % bs) // 16, slot % 16
+        for h in range(nkv):
+            raw[b, p, (r * nkv + h) * d:(r * nkv + h + 1) * d] = want_codes[slot, h]
+            raw[b, p, cb + (r * nkv + h) * 4:cb + (r * nkv + h + 1) * 4] = \
+                want_scales[slot, h:h + 1].view(np.uint8)
+    codes, scales = ops.fp8_cache_views(torch.from_numpy(raw), nkv, d)
+    assert tuple(codes.shape) == (nb, bs // 16, 16, nkv, d)
+    assert tuple(scales.shape) == (nb, bs // 16, 16, nkv)
+    assert np.array_equal(codes.numpy().reshape(-1, nkv, d), want_codes)
+    assert np.array_equal(scales.numpy().reshape(-1, nkv), want_scales)
+    with pytest.raises(ValueError):
+        ops.fp8_cache_views(torch.from_numpy(raw), nkv + 1, d)  # another page size
