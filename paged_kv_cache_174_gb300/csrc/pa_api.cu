@@ -94,7 +94,7 @@ int api_warm_device() { return device_state(nullptr, nullptr); }
 
 extern "C" {
 
-int pa_version(void) { return 100; }
+int pa_version(void) { return 200; }  // 0.2.0: the 8-bit cache in pages of codes, then scales
 
 const char* pa_get_last_error(void) { return t_last_error.c_str(); }
 
