@@ -309,6 +309,8 @@ int pa_swap_in(pa_bf16 *k_cache, pa_bf16 *v_cache, int32_t num_blocks, int32_t b
  * its tcgen05 products on f16 operands: q * scale * log2(e) and p rounded
  * to f16.  head_dim is 64 or 128; the same shapes as the bf16 cache.
  *
+ * pa_fp8_page_bytes: the page size above (0 for a non-positive argument).
+ *
  * pa_reshape_and_cache_fp8: pa_reshape_and_cache, quantising each new row
  * (codes and scale written to the new token's slot).  Alignment: k, v and
  * both caches 16 bytes, slot_mapping 4 bytes.
